@@ -1,0 +1,318 @@
+"""Pins of the CPU oracle against things other than itself.
+
+Each test checks the oracle against what the pages or the mathematics fix:
+the worked paging example (Ultralytics glossary "PagedAttention", section
+"How paging works"), library routines (torch fp64 scaled_dot_product_attention
+and softmax, numpy cumulative max, torch's bf16 rounding), closed forms
+(softmax rows sum to one, equal keys), and brute force on tiny inputs.
+"""
+import itertools
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from oracle import flow
+from synth import bf16_bits, bf16_to_f64, tiny
+
+RNG = np.random.default_rng(1234)
+
+
+def _sdpa(q, k, v, causal=True):
+    """torch fp64 SDPA on [n, H, d] arrays; GQA by repeating each KV head over
+    its contiguous group of query heads."""
+    h_q, h_kv = q.shape[1], k.shape[1]
+    tq = torch.from_numpy(q).permute(1, 0, 2)
+    tk = torch.from_numpy(k).permute(1, 0, 2).repeat_interleave(h_q // h_kv, dim=0)
+    tv = torch.from_numpy(v).permute(1, 0, 2).repeat_interleave(h_q // h_kv, dim=0)
+    if causal:
+        o = F.scaled_dot_product_attention(tq, tk, tv, is_causal=True)
+    else:
+        o = F.scaled_dot_product_attention(tq, tk, tv)
+    return o.permute(1, 0, 2).numpy()
+
+
+def _sdpa_probs(q, k):
+    """Causal attention probability matrices [H_q, n, n] via SDPA with V = I."""
+    n, h_q, _ = q.shape
+    eye = np.broadcast_to(np.eye(n)[:, None, :], (n, k.shape[1], n)).copy()
+    return _sdpa(q, k, eye).transpose(1, 0, 2)
+
+
+# ---------------------------------------------------------------------------
+# paging: the worked example
+# ---------------------------------------------------------------------------
+def test_paging_worked_example(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "paging_worked_example.json")))
+    pool = oracle.BlockPool(g["pool_blocks"], free=g["free_list"])
+    n, bs, d = g["n_tokens"], g["block_size"], g["head_dim"]
+    nb = oracle.blocks_for(n, bs)
+    assert nb == g["expected_blocks"]
+    table = [pool.alloc() for _ in range(nb)]
+    assert table == g["expected_table"]
+    keys = RNG.standard_normal((n, 1, d))
+    pk = np.zeros((g["pool_blocks"], 1, bs, d))
+    pv = np.zeros_like(pk)
+    oracle.compact(keys, keys, np.arange(n)[None, :], table, pk, pv, block=bs)
+    back = oracle.gather_rows(pk, table, n, 0, block=bs)
+    assert np.array_equal(back, keys[:, 0]) == g["expected_keys_intact"]
+    assert nb * bs - n == g["expected_unused_slots_paged"]
+    assert g["reservation_tokens"] - n == g["expected_unused_slots_reserved"]
+    # the two blocks left are still at the head of the free list, in order
+    assert pool.free == g["free_list"][nb:]
+
+
+def test_pool_fifo_refcount_cow():
+    pool = oracle.BlockPool(6)
+    a, b, c = pool.alloc(), pool.alloc(), pool.alloc()
+    assert (a, b, c) == (0, 1, 2)
+    pool.decref(b)                       # returns to the tail
+    assert pool.free == [3, 4, 5, 1]
+    pool.incref(a)
+    assert pool.ref[a] == 2
+    nb, copied = pool.cow(a)             # shared -> copy into the head block
+    assert copied and nb == 3 and pool.ref[a] == 1 and pool.ref[nb] == 1
+    same, copied = pool.cow(a)           # sole owner -> in place
+    assert not copied and same == a
+    for blk in (a, c, nb):
+        pool.decref(blk)
+    assert sorted(pool.free) == list(range(6))
+    with pytest.raises(ValueError):
+        pool.decref(a)
+    small = oracle.BlockPool(1)
+    small.alloc()
+    with pytest.raises(oracle.OutOfBlocks):
+        small.alloc()
+
+
+def test_pool_conservation_random_trace():
+    pool = oracle.BlockPool(40, free=RNG.permutation(40))
+    owned = []
+    for _ in range(2000):
+        op = RNG.integers(0, 4)
+        if op == 0 and pool.num_free():
+            owned.append(pool.alloc())
+        elif op == 1 and owned:
+            blk = owned[RNG.integers(len(owned))]
+            pool.incref(blk)
+            owned.append(blk)
+        elif op == 2 and owned:
+            pool.decref(owned.pop(RNG.integers(len(owned))))
+        elif op == 3 and owned and pool.num_free():
+            i = RNG.integers(len(owned))
+            owned[i], _ = pool.cow(owned[i])
+        in_use = {b for b in range(40) if pool.ref[b] > 0}
+        assert pool.num_free() + len(in_use) == 40
+        assert sorted(owned) == sorted(b for b in range(40) for _ in range(pool.ref[b]))
+
+
+# ---------------------------------------------------------------------------
+# prefill rows: O, m, l
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("n,h_q,h_kv,d", [(67, 4, 2, 16), (33, 6, 3, 8), (20, 2, 2, 32)])
+def test_prefill_O_equals_sdpa(n, h_q, h_kv, d):
+    q = RNG.standard_normal((n, h_q, d))
+    k = RNG.standard_normal((n, h_kv, d))
+    v = RNG.standard_normal((n, h_kv, d))
+    o, m, l = oracle.prefill_rows(q, k, v, 1 / np.sqrt(d))
+    np.testing.assert_allclose(o, _sdpa(q, k, v), atol=1e-12, rtol=0)
+
+
+def test_prefill_l_is_inverse_max_probability():
+    n, h_q, h_kv, d = 45, 4, 2, 16
+    q = RNG.standard_normal((n, h_q, d)) * 2
+    k = RNG.standard_normal((n, h_kv, d))
+    _, _, l = oracle.prefill_rows(q, k, k, 1 / np.sqrt(d))
+    p = _sdpa_probs(q, k)                       # [H_q, n, n]
+    # the maximal logit contributes exp(0) = 1 to l, so max_i p = 1 / l
+    np.testing.assert_allclose(l, 1.0 / p.max(axis=2), rtol=1e-12)
+
+
+def test_prefill_m_one_hot_queries():
+    n, h_q, h_kv, d = 50, 4, 2, 16
+    k = RNG.standard_normal((n, h_kv, d))
+    q = np.zeros((n, h_q, d))
+    t = 3.0
+    for g in range(h_q):
+        q[:, g, g % d] = t
+    scale = 1 / np.sqrt(d)
+    _, m, _ = oracle.prefill_rows(q, k, k, scale)
+    for g in range(h_q):
+        h = g // (h_q // h_kv)
+        expect = scale * t * np.maximum.accumulate(k[:, h, g % d])
+        np.testing.assert_allclose(m[g], expect, rtol=1e-13, atol=1e-13)
+
+
+def test_prefill_equal_keys_closed_form():
+    n, h_q, h_kv, d = 40, 2, 1, 8
+    k0 = RNG.standard_normal(d)
+    k = np.broadcast_to(k0, (n, h_kv, d)).copy()
+    q = RNG.standard_normal((n, h_q, d))
+    v = RNG.standard_normal((n, h_kv, d))
+    scale = 1 / np.sqrt(d)
+    o, m, l = oracle.prefill_rows(q, k, v, scale)
+    counts = np.arange(1, n + 1)
+    for g in range(h_q):
+        np.testing.assert_allclose(l[g], counts, rtol=1e-13)           # every logit equal
+        np.testing.assert_allclose(m[g], scale * (q[:, g] @ k0), rtol=1e-13)
+        np.testing.assert_allclose(o[:, g], np.cumsum(v[:, 0], axis=0) / counts[:, None],
+                                   rtol=1e-11, atol=1e-12)
+
+
+def test_prefill_row_subset_matches_full():
+    n, h_q, h_kv, d = 70, 4, 2, 16
+    q, k, v = (RNG.standard_normal((n, h, d)) for h in (h_q, h_kv, h_kv))
+    o, m, l = oracle.prefill_rows(q, k, v, 0.3)
+    rows = np.array([0, 5, 69, 33])
+    o2, m2, l2 = oracle.prefill_rows(q, k, v, 0.3, rows)
+    np.testing.assert_array_equal(o2, o[rows])
+    np.testing.assert_array_equal(m2, m[:, rows])
+    np.testing.assert_array_equal(l2, l[:, rows])
+
+
+# ---------------------------------------------------------------------------
+# window scores
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("n,h_q,h_kv,d,alpha", [(50, 4, 2, 16, 7), (33, 2, 1, 8, 33), (64, 8, 2, 16, 1)])
+def test_window_scores_sum_to_alpha_times_group(n, h_q, h_kv, d, alpha):
+    q, k = RNG.standard_normal((n, h_q, d)) * 1.5, RNG.standard_normal((n, h_kv, d))
+    win = np.arange(n - alpha, n)
+    _, m, l = oracle.prefill_rows(q, k, k, 1 / np.sqrt(d), win)
+    S = oracle.window_scores(q, k, m, l, alpha, 1 / np.sqrt(d))
+    # each causal softmax row sums to one: sum_i S[h][i] = alpha * G
+    np.testing.assert_allclose(S.sum(axis=1), alpha * (h_q // h_kv), rtol=1e-12)
+    assert (S >= 0).all()
+
+
+def test_window_scores_equal_sdpa_probability_column_sums():
+    n, h_q, h_kv, d, alpha = 48, 4, 2, 16, 9
+    q, k = RNG.standard_normal((n, h_q, d)), RNG.standard_normal((n, h_kv, d))
+    scale = 1 / np.sqrt(d)
+    win = np.arange(n - alpha, n)
+    _, m, l = oracle.prefill_rows(q, k, k, scale, win)
+    S = oracle.window_scores(q, k, m, l, alpha, scale)
+    p = _sdpa_probs(q, k)
+    G = h_q // h_kv
+    expect = np.stack([p[h * G:(h + 1) * G, n - alpha:, :].sum(axis=(0, 1)) for h in range(h_kv)])
+    np.testing.assert_allclose(S, expect, rtol=1e-11, atol=1e-14)
+
+
+def test_window_work_matches_article_estimate():
+    # the article's example: n = 5000, window 256 -> ~5000*256 instead of
+    # 5000*5000 (query, key) pairs.  Count the causal pairs inside the window.
+    n, alpha = 5000, 256
+    pairs = sum(q + 1 for q in range(n - alpha, n))
+    assert pairs == alpha * n - alpha * (alpha - 1) // 2
+    assert pairs <= n * alpha and pairs > 0.97 * n * alpha
+
+
+# ---------------------------------------------------------------------------
+# selection
+# ---------------------------------------------------------------------------
+def _brute_force_select(scores, n, k, r):
+    cand = list(range(n - r))
+    winners = []
+    for sub in itertools.combinations(cand, k - r):
+        rest = [i for i in cand if i not in sub]
+        # every chosen key precedes every other one in (score desc, position asc)
+        if all((scores[a] > scores[b]) or (scores[a] == scores[b] and a < b)
+               for a in sub for b in rest):
+            winners.append(sub)
+    assert len(winners) == 1
+    return sorted(list(winners[0]) + list(range(n - r, n)))
+
+
+@pytest.mark.parametrize("trial", range(12))
+def test_selection_brute_force(trial):
+    n = int(RNG.integers(4, 11))
+    scores = RNG.integers(0, 4, size=n).astype(np.float32)   # frequent ties
+    for r in range(0, 3):
+        for k in range(r, n + 2):
+            got = oracle.select_kept(scores, n, k, r)
+            if k >= n:
+                assert got.tolist() == list(range(n))
+            else:
+                assert got.tolist() == _brute_force_select(scores, n, k, r)
+
+
+def test_selection_all_equal_keeps_lowest_positions_and_recent():
+    n, k, r = 100, 20, 5
+    got = oracle.select_kept(np.ones(n, np.float32), n, k, r)
+    assert got.tolist() == list(range(15)) + list(range(95, 100))
+
+
+def test_selection_rejects_nan_and_oversized_recent():
+    s = np.zeros(10, np.float32)
+    s[3] = np.nan
+    with pytest.raises(ValueError):
+        oracle.select_kept(s, 10, 5, 2)
+    with pytest.raises(ValueError):
+        oracle.select_kept(np.zeros(10), 10, 3, 4)
+
+
+# ---------------------------------------------------------------------------
+# decode over the paged cache
+# ---------------------------------------------------------------------------
+def test_decode_full_cache_equals_dense_attention():
+    """k_l >= n keeps every token, so paged decode must equal dense attention
+    of each new query over prompt + appended tokens (itself included)."""
+    w = tiny()
+    n, steps = 37, 20
+    qb, kb, vb = (bf16_bits(RNG.standard_normal(s).astype(np.float32))
+                  for s in ((n, w.h_q, w.d), (n, w.h_kv, w.d), (n, w.h_kv, w.d)))
+    dq, dk, dv = (bf16_bits(RNG.standard_normal(s).astype(np.float32))
+                  for s in ((steps, w.h_q, w.d), (steps, w.h_kv, w.d), (steps, w.h_kv, w.d)))
+    pool = oracle.BlockPool(16, free=RNG.permutation(16))
+    pk = np.zeros((16, w.h_kv, 16, w.d), np.uint16)
+    pv = np.zeros_like(pk)
+    rec = flow.sparsify_layer(w, 1, qb, kb, vb)          # budget 64 >= n -> identity
+    assert not rec.budgeted and rec.k_eff == n
+    flow.place_layer(rec, pool, kb, vb, pk, pv)
+    st = flow.new_stream([rec])
+    allk, allv = bf16_to_f64(kb), bf16_to_f64(vb)
+    for t in range(steps):
+        flow.prepare_append(pool, st, 0, pk, pv)
+        out = flow.append_and_attend(w, st, 0, dq[t], dk[t], dv[t], pk, pv)
+        allk = np.concatenate([allk, bf16_to_f64(dk[t])[None]])
+        allv = np.concatenate([allv, bf16_to_f64(dv[t])[None]])
+        ref = _sdpa(bf16_to_f64(dq[t])[None], allk, allv, causal=False)[0]
+        np.testing.assert_allclose(out, ref, atol=1e-12)
+    assert st.lens[0] == n + steps
+    assert len(st.tables[0]) == oracle.blocks_for(n + steps)
+
+
+def test_copy_on_write_for_three_samples():
+    w = tiny()
+    n = 21                                              # partial last block
+    qb, kb, vb = (bf16_bits(RNG.standard_normal(s).astype(np.float32))
+                  for s in ((n, w.h_q, w.d), (n, w.h_kv, w.d), (n, w.h_kv, w.d)))
+    pool = oracle.BlockPool(12)
+    pk = np.zeros((12, w.h_kv, 16, w.d), np.uint16)
+    pv = np.zeros_like(pk)
+    rec = flow.sparsify_layer(w, 0, qb, kb, vb)
+    flow.place_layer(rec, pool, kb, vb, pk, pv)
+    s0 = flow.new_stream([rec])
+    s1, s2 = flow.share_stream(pool, s0), flow.share_stream(pool, s0)
+    assert pool.ref[s0.tables[0][1]] == 3
+    copies = [flow.prepare_append(pool, s, 0, pk, pv) for s in (s0, s1, s2)]
+    # the first two samples copy the shared partial block, the third writes in place
+    assert copies[0] is not None and copies[1] is not None and copies[2] is None
+    assert s2.tables[0][1] == rec.table[1]
+    assert pool.ref[rec.table[0]] == 3                 # full prompt block still shared
+    for s in (s0, s1, s2):
+        np.testing.assert_array_equal(pk[s.tables[0][1], :, :5], pk[rec.table[1], :, :5])
+
+
+# ---------------------------------------------------------------------------
+# the generator's bf16 rounding against torch's
+# ---------------------------------------------------------------------------
+def test_bf16_rounding_matches_torch():
+    x = np.concatenate([RNG.standard_normal(100000).astype(np.float32) * 7,
+                        np.array([1.00390625, 1.01171875, -2.00781250, 0.0, -0.0], np.float32)])
+    ours = bf16_bits(x)
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(ours, ref)
