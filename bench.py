@@ -1,0 +1,454 @@
+"""Benchmark of the layer-wise KV sparsification hot path on one GB300.
+
+Workload: Llama-3-8B attention shapes, one request of 4000 prompt tokens and
+500 generated tokens (32 layers, 32 query / 8 KV heads, d = 128, bf16;
+layers 0-2 full cache, layers 3-31 budgets 2048 .. 256 incl. the 32 most
+recent tokens, window alpha = 32), seeded synthetic inputs.
+
+One bench step = one request through the whole hot path:
+  prefill+sparsify  per layer prefill attention (+ m, l) and window scores,
+                    one selection launch, host block allocation + table upload,
+                    one compaction launch;
+  decode            500 steps, each: host block preparation, one paged-decode
+                    launch over the 32 (request, layer) items;
+then the request's blocks are returned to the pool.
+
+Reported: value = prefill+sparsify tokens/s (device time, inputs resident),
+decode tokens/s beside it, a roofline object for the dominant kernel
+(prefill attention, tensor-bound) and one for the decode kernel (HBM-bound),
+the same metrics end to end through host buffers, the CPU oracle timed on a
+bounded sample, and the SM clocks sampled during the timed region.
+
+L2: the inputs of one request (1.57 GB of Q/K/V) exceed L2; a 512 MB buffer
+is written between decode steps and between bench steps (outside the timed
+events) so every decode step starts from a cold L2.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+os.environ.setdefault("OMP_NUM_THREADS", "1")
+os.environ.setdefault("MKL_NUM_THREADS", "1")
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "prefill+sparsify tok/s & decode tok/s (1 GB300, 4000/500); % of roofline"
+WORKLOAD = "llama3-8b attention shapes, 1 x 4000-token prompt, 500 decode steps, 32 layers"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM bytes per launch from ncu captures (profiles/); None until captured for
+# the current kernel version.
+NCU_TRAFFIC = {"prefill_attn": None, "paged_decode": None}
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=2)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# workload
+# ---------------------------------------------------------------------------
+def make_inputs(w, n, steps, device):
+    import torch
+    from synth import decode_qkv, prefill_qkv
+    L = w.n_layers
+    q = torch.empty((L, n, w.h_q, w.d), dtype=torch.bfloat16, device=device)
+    k = torch.empty((L, n, w.h_kv, w.d), dtype=torch.bfloat16, device=device)
+    v = torch.empty_like(k)
+    dq = torch.empty((steps, L, w.h_q, w.d), dtype=torch.bfloat16, device=device)
+    dk = torch.empty((steps, L, w.h_kv, w.d), dtype=torch.bfloat16, device=device)
+    dv = torch.empty_like(dk)
+
+    def dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+    for l in range(L):
+        qb, kb, vb = prefill_qkv(w, 0, l, n)
+        q[l].copy_(dev(qb))
+        k[l].copy_(dev(kb))
+        v[l].copy_(dev(vb))
+        a, b, c = decode_qkv(w, 0, l, steps)
+        dq[:, l].copy_(dev(a))
+        dk[:, l].copy_(dev(b))
+        dv[:, l].copy_(dev(c))
+    return q, k, v, dq, dk, dv
+
+
+def prefill_flops(w, n):
+    """Causal attention work: QK^T and PV over the lower triangle incl. the
+    diagonal, all query heads, all layers: 2 * 2 * d * n(n+1)/2 per head."""
+    return 2.0 * w.h_q * w.d * n * (n + 1)
+
+
+def decode_bytes(w, lens):
+    """Algorithmic bytes of one decode launch: every cached K and V row of
+    every item read once (the new row included), q read, out written, the new
+    k/v rows written."""
+    kv = sum((L + 1) * w.h_kv * w.d * 2 * 2 for L in lens)
+    return kv + len(lens) * (w.h_q * w.d * 2 * 2 + w.h_kv * w.d * 2 * 2)
+
+
+def run_request(eng, dec, w, n, steps, q, k, v, dq, dk, dv, o_buf, ml_buf, flush, rec,
+                host=None):
+    """One request.  rec: dict collecting event pairs.  host: pinned host
+    buffers for the end-to-end variant (inputs copied in, outputs read back
+    inside the timed events)."""
+    import torch
+    L = w.n_layers
+    st = torch.cuda.current_stream()
+    budgets = [[w.budget(l, n) for l in range(L)]]
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    if host is not None:
+        q.copy_(host["q"], non_blocking=True)
+        k.copy_(host["k"], non_blocking=True)
+        v.copy_(host["v"], non_blocking=True)
+    res = eng.prefill_sparsify(list(q), list(k), list(v), [n], budgets, o_buf=o_buf,
+                               ml_buf=ml_buf, timing=rec.get("k1"))
+    if host is not None:
+        host["kept"][: res.kept_idx.numel()].copy_(res.kept_idx, non_blocking=True)
+    e1.record(st)
+    rec["prefill"].append((e0, e1))
+    dec.set_stream(0, res.tables[0], res.k_eff[0])
+    for t in range(steps):
+        flush()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        if host is not None:
+            dq[t].copy_(host["dq"][t], non_blocking=True)
+            dk[t].copy_(host["dk"][t], non_blocking=True)
+            dv[t].copy_(host["dv"][t], non_blocking=True)
+        out = dec.step(dq[t], dk[t], dv[t])
+        if host is not None:
+            host["out"][t].copy_(out, non_blocking=True)
+        b.record(st)
+        rec["decode"].append((a, b))
+    torch.cuda.synchronize()
+    eng.check_status()
+    for s in range(1):
+        dec.retire(s)
+    return res
+
+
+def bench_gpu(args):
+    import torch
+    import torch.distributed as dist
+    from synth import llama3_8b
+    from layer_wise_kv_gb300 import kvs
+    from layer_wise_kv_gb300.pipeline import DecodeBatch, Engine, Shape, blocks_for
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    kvs.library()
+
+    w = llama3_8b()
+    n, steps, L = w.prompt_lens[0], args.decode_steps, w.n_layers
+    q, k, v, dq, dk, dv = make_inputs(w, n, steps, dev)
+    shape = Shape(w.n_layers, w.h_q, w.h_kv, w.d, w.alpha, w.recent)
+    blocks = sum(blocks_for(w.k_eff(l, n) + steps) + 1 for l in range(L))
+    eng = Engine(shape, blocks + 64, device=dev)
+    o_buf = torch.empty((n, w.h_q, w.d), dtype=torch.bfloat16, device=dev)
+    ml_buf = (torch.empty((w.h_q, n), dtype=torch.float32, device=dev),
+              torch.empty((w.h_q, n), dtype=torch.float32, device=dev))
+    scrub = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    dec = DecodeBatch(eng, 1, n + steps)
+
+    def flush():
+        scrub.fill_(1)
+
+    def new_rec(k1=True):
+        return {"prefill": [], "decode": [], "k1": {"attn": [], "scores": []} if k1 else None}
+
+    # warm-up
+    for _ in range(args.warmup):
+        run_request(eng, dec, w, n, steps, q, k, v, dq, dk, dv, o_buf, ml_buf, flush,
+                    new_rec(False))
+    flush()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = ClockSampler(local)
+    clocks.start()
+    rec = new_rec()
+    t_wall = time.perf_counter()
+    for _ in range(args.steps):
+        flush()
+        run_request(eng, dec, w, n, steps, q, k, v, dq, dk, dv, o_buf, ml_buf, flush, rec)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    if world > 1:
+        dist.barrier()
+
+    pre_ms = [a.elapsed_time(b) for a, b in rec["prefill"]]
+    dec_ms = [a.elapsed_time(b) for a, b in rec["decode"]]
+    k1_ms = [a.elapsed_time(b) for a, b in rec["k1"]["attn"]]
+    k2_ms = [a.elapsed_time(b) for a, b in rec["k1"]["scores"]]
+    t_pre = sum(pre_ms) / args.steps            # ms per request
+    t_dec = sum(dec_ms) / args.steps
+    if world > 1:
+        tt = torch.tensor([t_pre, t_dec], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_pre, t_dec = tt.tolist()
+    prefill_tok_s = world * n / (t_pre / 1e3)
+    decode_tok_s = world * steps / (t_dec / 1e3)
+
+    peaks, peak_src = read_peaks()
+    k1_avg = sum(k1_ms) / len(k1_ms)
+    flops_launch = prefill_flops(w, n)
+    tflops = flops_launch / (k1_avg / 1e3) / 1e12
+    peak_t = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    dec_avg = sum(dec_ms) / len(dec_ms)
+    lens = [w.k_eff(l, n) + steps // 2 for l in range(L)]   # mean length over the request
+    gbs = decode_bytes(w, lens) / (dec_avg / 1e3) / 1e9
+
+    out = {
+        "metric": METRIC,
+        "value": round(prefill_tok_s, 1),
+        "unit": "tok/s",
+        "decode": {"value": round(decode_tok_s, 1), "unit": "tok/s",
+                   "ms_per_token": round(t_dec / steps, 4)},
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(t_pre + t_dec, 3),
+        "ms_prefill_sparsify": round(t_pre, 3),
+        "ms_decode_500": round(t_dec, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) Q/K/V with sink tokens; no weights)",
+        "config": {"workload": WORKLOAD, "prompt": n, "decode_steps": steps, "layers": L,
+                   "h_q": w.h_q, "h_kv": w.h_kv, "d": w.d, "alpha": w.alpha,
+                   "recent": w.recent, "budgets": "layers 0-2 full, 2048-64*(l-3)",
+                   "l2": "inputs 1.57 GB > L2; 512 MB written between decode steps",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"kernel": "prefill_attn (tcgen05)", "bound": "tensor",
+                     "achieved": round(tflops, 1), "peak": peak_t, "unit": "TFLOP/s",
+                     "frac": round(tflops / peak_t, 4), "traffic": NCU_TRAFFIC["prefill_attn"],
+                     "peak_source": f"{peak_src} bf16 sustained",
+                     "per_launch_ms": round(k1_avg, 4), "flops_per_launch": flops_launch},
+        "roofline_decode": {"kernel": "paged_decode", "bound": "hbm", "achieved": round(gbs, 1),
+                            "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                            "frac": round(gbs / peaks["hbm_gbs"], 4),
+                            "traffic": NCU_TRAFFIC["paged_decode"],
+                            "peak_source": f"{peak_src} copy bandwidth",
+                            "per_launch_ms": round(dec_avg, 4)},
+        "scores_ms_per_launch": round(sum(k2_ms) / max(1, len(k2_ms)), 4),
+        "gpu_launches": args.steps * (2 * L - 3 + 2 + steps),
+        "clocks": clk,
+        "wall_s": round(t_wall, 2),
+    }
+    if args.e2e:
+        out["e2e"] = bench_e2e(args, eng, dec, w, n, steps, q, k, v, dq, dk, dv, o_buf, ml_buf,
+                               flush, world, dist)
+    if rank == 0 and args.cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(args)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def bench_e2e(args, eng, dec, w, n, steps, q, k, v, dq, dk, dv, o_buf, ml_buf, flush, world,
+              dist):
+    """Same metric through host buffers: Q/K/V of the request and every decode
+    step's q/k/v copied in from pinned memory, the kept indices and every
+    decode output copied back, all inside the timed events."""
+    import torch
+    host = {"q": q.cpu().pin_memory(), "k": k.cpu().pin_memory(), "v": v.cpu().pin_memory(),
+            "dq": dq.cpu().pin_memory(), "dk": dk.cpu().pin_memory(), "dv": dv.cpu().pin_memory(),
+            "out": torch.empty((steps, w.n_layers, w.h_q, w.d), dtype=torch.bfloat16).pin_memory(),
+            "kept": torch.empty(n * w.n_layers * w.h_kv, dtype=torch.int32).pin_memory()}
+    rec = {"prefill": [], "decode": [], "k1": None}
+    reps = max(1, min(args.steps, 3))
+    for _ in range(reps):
+        flush()
+        run_request(eng, dec, w, n, steps, q, k, v, dq, dk, dv, o_buf, ml_buf, flush, rec,
+                    host=host)
+    t_pre = sum(a.elapsed_time(b) for a, b in rec["prefill"]) / reps
+    t_dec = sum(a.elapsed_time(b) for a, b in rec["decode"]) / reps
+    if world > 1:
+        tt = torch.tensor([t_pre, t_dec], dtype=torch.float64, device=q.device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_pre, t_dec = tt.tolist()
+    kept_bytes = sum(w.k_eff(l, n) for l in range(w.n_layers)) * w.h_kv * 4
+    h2d = (q.numel() + k.numel() + v.numel()) * 2 + (dq.numel() + dk.numel() + dv.numel()) * 2
+    d2h = kept_bytes + steps * w.n_layers * w.h_q * w.d * 2
+    return {"value": round(world * n / (t_pre / 1e3), 1), "unit": "tok/s",
+            "decode_tok_s": round(world * steps / (t_dec / 1e3), 1),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "steps": reps}
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle, timed on a bounded sample of the same workload
+# ---------------------------------------------------------------------------
+def cpu_baseline(args):
+    """The oracle (fp64 numpy, one thread) on the host cores: prefill rows,
+    window scores, selection and compaction of one budgeted layer (all 4000
+    rows), and the decode of one step over all 32 layers; scaled to the
+    request (x32 layers for prefill+sparsify, per token for decode)."""
+    import oracle
+    from oracle import flow
+    from synth import decode_qkv, llama3_8b, prefill_qkv
+    w = llama3_8b()
+    n, L = w.prompt_lens[0], w.n_layers
+    layer = 3
+    rows = np.arange(0, n, max(1, n // args.cpu_rows)) if args.cpu_rows < n else None
+    qb, kb, vb = prefill_qkv(w, 0, layer, n)
+    t0 = time.perf_counter()
+    rec = flow.sparsify_layer(w, layer, qb, kb, vb, rows=rows if rows is not None else np.arange(n))
+    pool = oracle.BlockPool(4096)
+    pk = np.zeros((4096, w.h_kv, 16, w.d), np.uint16)
+    pv = np.zeros_like(pk)
+    flow.place_layer(rec, pool, kb, vb, pk, pv)
+    t_layer = time.perf_counter() - t0
+    frac_rows = (len(rows) if rows is not None else n) / n
+    # prefill cost scales with the rows evaluated; the rest is per layer
+    t_req_prefill = t_layer / frac_rows * L
+    # decode: one step, all layers (caches gathered from the pool)
+    recs = []
+    for l in range(L):
+        k_eff = w.k_eff(l, n)
+        r2 = flow.LayerRecord(budgeted=False, k_eff=k_eff,
+                              idx=np.tile(np.arange(n - k_eff, n), (w.h_kv, 1)))
+        flow.place_layer(r2, pool, kb, vb, pk, pv)
+        recs.append(r2)
+    st = flow.new_stream(recs)
+    dq = [decode_qkv(w, 0, l, 1) for l in range(L)]
+    t0 = time.perf_counter()
+    for l in range(L):
+        flow.prepare_append(pool, st, l, pk, pv)
+        flow.append_and_attend(w, st, l, dq[l][0][0], dq[l][1][0], dq[l][2][0], pk, pv)
+    t_dec = time.perf_counter() - t0
+    return {"value": round(n / t_req_prefill, 3), "unit": "tok/s",
+            "decode_tok_s": round(1.0 / t_dec, 3), "cores": 1, "kind": "oracle",
+            "sample": (f"layer {layer} of {L}: prefill rows "
+                       f"{len(rows) if rows is not None else n}/{n} + scores + selection + "
+                       f"compaction, scaled to all rows and 32 layers; decode: one step over "
+                       f"32 layers"),
+            "host_cores_available": len(os.sched_getaffinity(0))}
+
+
+def bench_reference(args):
+    """--impl reference: the CPU oracle as the reference arm, on rank 0."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    t0 = time.perf_counter()
+    cb = cpu_baseline(args)
+    wall = time.perf_counter() - t0
+    out = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "tok/s",
+           "decode": {"value": cb["decode_tok_s"], "unit": "tok/s"},
+           "n_gpus": 1, "steps": 1, "warmup": 0, "higher_is_better": True,
+           "config": {"workload": WORKLOAD}, "dtype": "f64", "data": "synthetic",
+           "cpu_baseline": {"value": cb["value"], "unit": "tok/s", "cores": cb["cores"],
+                            "kind": "oracle", "sample": cb["sample"]},
+           "e2e": {"value": cb["value"], "unit": "tok/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0},
+           "wall_s": round(wall, 2)}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="kvs", choices=["kvs", "reference"])
+    ap.add_argument("--decode-steps", type=int, default=500)
+    ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--cpu-rows", type=int, default=400,
+                    help="prefill rows the CPU oracle evaluates (sample size)")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        bench_reference(args)
+        return
+    bench_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,266 @@
+/*
+ * kvs.h -- C ABI of the layer-wise KV-cache sparsification hot path over a
+ * paged KV cache, for one NVIDIA GB300 (sm_103a).
+ *
+ * The method (Novita AI, "How KV Sparsity achieves 1.5x acceleration for
+ * vLLM"; Ultralytics glossary, "PagedAttention"):
+ *   1. causal prefill attention that also returns each query row's maximum
+ *      logit m and softmax normaliser l          -> kvs_prefill_attn_lse
+ *   2. window scores S summed over the last alpha queries -> kvs_window_scores
+ *   3. per-(layer, KV head) top-k_l with a recent window  -> kvs_select_topk
+ *   4. compaction of the kept K/V into 16-token blocks    -> kvs_compact_blocks
+ *      tracked by a block allocator (free list, reference counts,
+ *      copy-on-write)                                   -> kvs_alloc_*, kvs_copy_blocks
+ *   5. decode attention gathering K/V through block tables -> kvs_paged_decode
+ *
+ * Conventions (all entry points)
+ *   - bf16 tensors are passed as raw 16-bit patterns (kvs_bf16).
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller unless the
+ *     argument says "host".  The library never allocates device memory; scratch
+ *     is a caller-provided workspace whose size a *_workspace_size call gives.
+ *   - Launching calls are asynchronous on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream).  Arguments are validated on the host before any
+ *     launch: a bad argument returns KVS_ERR_INVALID (or KVS_ERR_UNSUPPORTED
+ *     for a shape outside the supported set) and launches nothing.  A launch
+ *     failure returns KVS_ERR_CUDA.  Faults inside kernels surface at the
+ *     caller's next synchronisation.
+ *   - `status` (nullable device int32): kernels that meet a corrupt index
+ *     (block id outside the pool, kept index outside the sequence) skip that
+ *     access and store KVS_ERR_INVALID there; a kernel whose bounded wait on
+ *     an mbarrier gives up stores KVS_ERR_DEVICE_TIMEOUT and returns.  The
+ *     word is only ever set, never cleared, by the library.
+ *   - kvs_last_error() returns a thread-local message for the last failure.
+ *   - Supported: d in {64, 128}; h_q % h_kv == 0; G = h_q / h_kv <= 16;
+ *     block size fixed at 16 tokens.
+ *   - Layouts: prompt Q is [T][h_q][d], prompt K and V are [T][h_kv][d]
+ *     (token-major, sequences packed back to back, T = total tokens); the
+ *     paged pools are [num_blocks][h_kv][16][d].
+ */
+#ifndef KVS_H_
+#define KVS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t kvs_bf16;  /* raw bf16 bit pattern */
+typedef void* kvs_stream;   /* cudaStream_t */
+
+typedef enum {
+  KVS_OK = 0,
+  KVS_ERR_INVALID = 1,
+  KVS_ERR_OOM_BLOCKS = 2,
+  KVS_ERR_CUDA = 3,
+  KVS_ERR_UNSUPPORTED = 4,
+  KVS_ERR_DEVICE_TIMEOUT = 5
+} kvs_status;
+
+#define KVS_BLOCK_TOKENS 16
+
+/* Message describing the last failed call on this thread ("" if none). */
+const char* kvs_last_error(void);
+
+/* Library ABI version (major * 100 + minor). */
+int32_t kvs_version(void);
+
+/* ------------------------------------------------------------------------
+ * 1. Prefill attention with row max and normaliser.
+ * Source: Novita article, section "Key techniques 2: attention
+ * modification" -- FlashAttention-2 (Figure 7) already computes the running
+ * row maximum and l; the modification returns them.  Computes, per query
+ * head g (KV head g / G) and query row r of each sequence,
+ *     s_i = scale * q_r . k_i  for keys i <= r of the same sequence,
+ *     m = max_i s_i,  l = sum_i exp(s_i - m),  O_r = sum_i exp(s_i - m)/l v_i
+ *   q      [T][h_q][d] bf16, k/v [T][h_kv][d] bf16
+ *   o      [T][h_q][d] bf16 (output)
+ *   m, l   [h_q][T] fp32 (output; natural-exponent, scaled-logit domain)
+ *   cu_seqlens [batch + 1] int32 (device): sequence b owns tokens
+ *          cu_seqlens[b] .. cu_seqlens[b+1]-1; cu_seqlens[batch] == T.
+ *   max_n  host upper bound of the sequence lengths (sizes the grid).
+ * Row blocks of 128 queries run on the 5th-generation tensor cores
+ * (tcgen05, TMEM accumulators, TMA-fed shared memory).
+ * ---------------------------------------------------------------------- */
+kvs_status kvs_prefill_attn_lse(const kvs_bf16* q, const kvs_bf16* k, const kvs_bf16* v,
+                                kvs_bf16* o, float* m, float* l,
+                                const int32_t* cu_seqlens, int32_t batch, int32_t max_n,
+                                int32_t total_tokens, int32_t h_q, int32_t h_kv, int32_t d,
+                                float scale, int32_t* status, kvs_stream stream);
+
+/* ------------------------------------------------------------------------
+ * 2. Window scores.
+ * Source: Novita article, section "Key techniques 2" (PyramidKV-style score
+ * over the instruction window [n - alpha, n]; probabilities rebuilt as
+ * exp(k.q - rowmax)/l from the prefill's outputs; key-major loop order;
+ * only window query blocks visited).  For each sequence (length n, window
+ * w = min(alpha, n) rows n-w .. n-1) and KV head h:
+ *     S[h][i] = sum_{g in group(h)} sum_{q = n-w}^{n-1} [i <= q]
+ *               exp(scale * q_g . k_i - m[g][q]) / l[g][q]
+ *   q [T][h_q][d], k [T][h_kv][d] bf16; m, l [h_q][T] fp32 (only the window
+ *   rows are read); scores [h_kv][T] fp32 (output; every token of every
+ *   sequence is written).  alpha * G <= 256.
+ * ---------------------------------------------------------------------- */
+kvs_status kvs_window_scores(const kvs_bf16* q, const kvs_bf16* k, const float* m, const float* l,
+                             float* scores, const int32_t* cu_seqlens, int32_t batch,
+                             int32_t max_n, int32_t total_tokens, int32_t h_q, int32_t h_kv,
+                             int32_t d, int32_t alpha, float scale, int32_t* status,
+                             kvs_stream stream);
+
+/* ------------------------------------------------------------------------
+ * 3. Top-k_l selection.
+ * Source: Novita article, section "System model" (keep the higher-scoring and
+ * nearer KV pairs), section "Key techniques 1" (first three layers full,
+ * later layers evict the lowest scores), section "Key techniques 2" (per
+ * layer l and head h keep the k_l highest-scoring tokens; the rest is
+ * discarded for the whole generation).
+ * One item = one (sequence, layer).  For each item and KV head h the row
+ * scores[score_off + h * head_stride + i], i < n, is read and
+ *   k >= n : kept = 0 .. n-1 (identity)
+ *   else   : kept = {n-recent .. n-1} plus the (k - recent) highest scores of
+ *            positions 0 .. n-recent-1, ties to the lower position,
+ * written in ascending position order to
+ *   kept_idx[idx_off + h * min(k, n) + j], j < min(k, n).
+ * Scores are non-negative finite fp32 (compared as stored); recent <= k.
+ * items: device array of n_items descriptors.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  int64_t score_off; /* element offset of head 0's row in `scores` */
+  int32_t n;         /* prompt length */
+  int32_t k;         /* budget k_l (>= n means keep all) */
+  int64_t idx_off;   /* element offset of head 0's output in `kept_idx` */
+} kvs_select_item;
+
+kvs_status kvs_select_topk(const float* scores, int64_t head_stride, const kvs_select_item* items,
+                           int32_t n_items, int32_t h_kv, int32_t recent, int32_t* kept_idx,
+                           int32_t* status, kvs_stream stream);
+
+/* ------------------------------------------------------------------------
+ * 4. Compaction into 16-token blocks.
+ * Source: Ultralytics glossary "PagedAttention", section "How paging works"
+ * (slot p % 16 of block table[p / 16]); Novita article, section "Key
+ * techniques 1" (per-layer block-table strategies).
+ * One item = one (sequence, layer).  For each item, head h and kept slot
+ * j < k_eff, with p = kept_idx[idx_off + h * k_eff + j] and
+ * b = block_tables[table_off + j / 16]:
+ *     k_pool[b][h][j % 16][:] = k[src_tok + p][h][:]   (same for v)
+ * a bit-exact copy (rows are items' (j) slots; all h_kv heads of a slot are
+ * copied together).  row_off is the item's first row in the flattened
+ * (item, j) enumeration: row_off(i) = sum of k_eff over items before i;
+ * total_rows = sum of all k_eff.  items: device array.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  int64_t src_tok;   /* first token of the item's K/V in `k` / `v` */
+  int64_t idx_off;   /* element offset of head 0's kept indices */
+  int64_t row_off;   /* prefix sum of k_eff over earlier items */
+  int32_t n;         /* tokens of the item (kept indices must be < n) */
+  int32_t k_eff;     /* kept tokens per head */
+  int32_t table_off; /* element offset of the item's block table */
+  int32_t reserved;  /* 0 */
+} kvs_compact_item;
+
+kvs_status kvs_compact_blocks(const kvs_bf16* k, const kvs_bf16* v, const kvs_compact_item* items,
+                              int32_t n_items, int64_t total_rows, int32_t h_kv, int32_t d,
+                              const int32_t* kept_idx, const int32_t* block_tables,
+                              kvs_bf16* k_pool, kvs_bf16* v_pool, int32_t num_blocks,
+                              int32_t* status, kvs_stream stream);
+
+/* Copy whole blocks src[i] -> dst[i] in both pools (the copy of
+ * copy-on-write; Ultralytics glossary "PagedAttention", section "Block
+ * sharing between sequences").  src, dst: device int32 [count]. */
+kvs_status kvs_copy_blocks(const int32_t* src, const int32_t* dst, int32_t count,
+                           kvs_bf16* k_pool, kvs_bf16* v_pool, int32_t num_blocks, int32_t h_kv,
+                           int32_t d, int32_t* status, kvs_stream stream);
+
+/* ------------------------------------------------------------------------
+ * 5. Paged decode attention (split-K over 16-token blocks).
+ * Source: Ultralytics glossary "PagedAttention", section "How paging works"
+ * (the kernel follows the block table and gathers K/V block by block);
+ * Novita article, section "Key techniques 2" (PagedAttention on the decode
+ * side).  One item = one (stream, layer) with `lens[i]` tokens already in
+ * its table.  If k_new is not NULL the item's new k/v row is first written
+ * at slot lens[i] (block table[lens[i] / 16], slot lens[i] % 16) and
+ * attention runs over lens[i] + 1 tokens (the new token attends to itself);
+ * otherwise over lens[i] tokens.  Per query head g (KV head g / G):
+ *     out[i][g] = softmax_t(scale * q[i][g] . K_t) V
+ *   q, out [batch][h_q][d]; k_new, v_new [batch][h_kv][d] (nullable)
+ *   block_tables [batch][max_blocks] int32; lens [batch] int32
+ *   table_patch  [batch] int32, nullable: entry >= 0 replaces
+ *                block_tables[i][lens[i] / 16] before use and is written
+ *                back there (the host allocator's new or copied-on-write
+ *                last block); -1 = no change.
+ *   lens_next    [batch] int32, nullable: receives lens[i] + (k_new != NULL).
+ *   max_len      host upper bound of lens[i] + 1 over all items.
+ *   workspace    scratch of kvs_paged_decode_workspace_size(...) bytes; must
+ *                be zero-filled before its first use (kvs_workspace_zero);
+ *                each call leaves it ready for the next one.  Calls sharing
+ *                a workspace must not overlap in time.
+ * ---------------------------------------------------------------------- */
+size_t kvs_paged_decode_workspace_size(int32_t batch, int32_t h_q, int32_t h_kv, int32_t d,
+                                       int32_t max_len);
+
+kvs_status kvs_workspace_zero(void* workspace, size_t bytes, kvs_stream stream);
+
+kvs_status kvs_paged_decode(const kvs_bf16* q, const kvs_bf16* k_new, const kvs_bf16* v_new,
+                            kvs_bf16* k_pool, kvs_bf16* v_pool, int32_t num_blocks,
+                            int32_t* block_tables, int32_t max_blocks, const int32_t* table_patch,
+                            const int32_t* lens, int32_t* lens_next, int32_t batch,
+                            int32_t max_len, int32_t h_q, int32_t h_kv, int32_t d, float scale,
+                            kvs_bf16* out, void* workspace, size_t workspace_bytes,
+                            int32_t* status, kvs_stream stream);
+
+/* ------------------------------------------------------------------------
+ * Block allocator (host memory, single-threaded, not thread-safe).
+ * Source: Ultralytics glossary "PagedAttention": sections "How paging
+ * works" (a new block only when the last one is full, taken from wherever one
+ * is free; the worked example pops the front of the free list) and "Block
+ * sharing between sequences" (reference counts; copy before writing a block
+ * others still use).  The free list is FIFO: allocation pops the head, a block
+ * whose count reaches zero is appended to the tail.  All operations are O(1)
+ * except creation.
+ * ---------------------------------------------------------------------- */
+typedef struct kvs_allocator kvs_allocator;
+
+/* num_blocks physical blocks.  initial_free (host, nullable): the initial free
+ * list order, n_initial distinct ids in [0, num_blocks); blocks not listed are
+ * unmanaged (reference count 0, never handed out).  NULL = 0 .. num_blocks-1. */
+kvs_status kvs_alloc_create(int32_t num_blocks, const int32_t* initial_free, int32_t n_initial,
+                            kvs_allocator** out);
+void kvs_alloc_destroy(kvs_allocator* a);
+/* Pop the head of the free list; its count becomes 1.  KVS_ERR_OOM_BLOCKS if empty. */
+kvs_status kvs_alloc_block(kvs_allocator* a, int32_t* out);
+/* Pop `count` blocks into out (host); all or nothing. */
+kvs_status kvs_alloc_blocks(kvs_allocator* a, int32_t count, int32_t* out);
+kvs_status kvs_alloc_incref(kvs_allocator* a, int32_t block);
+kvs_status kvs_alloc_decref(kvs_allocator* a, int32_t block);
+/* If block is shared (count > 1): pop a new block, drop one reference to
+ * `block`, *out = new block, *copied = 1 (the caller copies the contents).
+ * Otherwise *out = block, *copied = 0. */
+kvs_status kvs_alloc_cow(kvs_allocator* a, int32_t block, int32_t* out, int32_t* copied);
+int32_t kvs_alloc_refcount(const kvs_allocator* a, int32_t block); /* -1 if out of range */
+int32_t kvs_alloc_num_free(const kvs_allocator* a);
+/* Copy up to cap free-list entries, head first, into buf (host); returns count. */
+int32_t kvs_alloc_free_list(const kvs_allocator* a, int32_t* buf, int32_t cap);
+
+/* Host-side step preparation for a batch of decode items (one per (stream,
+ * layer)), visited in order: for item i with length lens[i] (host) and table
+ * row tables[i * max_blocks ..] (host):
+ *   lens[i] % 16 == 0             -> pop a new block; patch[i] = it
+ *   last block shared (count > 1) -> copy-on-write; patch[i] = new block and
+ *                                    the pair (old, new) is appended to
+ *                                    cow_src / cow_dst
+ *   otherwise                     -> patch[i] = -1
+ * The host table row is updated in place.  *n_cow receives the number of
+ * copies (cow_src / cow_dst need room for n_items entries).  If the pool runs
+ * dry, returns KVS_ERR_OOM_BLOCKS with *n_done = items fully prepared. */
+kvs_status kvs_decode_prepare(kvs_allocator* a, int32_t* tables, int32_t max_blocks,
+                              const int32_t* lens, int32_t n_items, int32_t* patch,
+                              int32_t* cow_src, int32_t* cow_dst, int32_t* n_cow,
+                              int32_t* n_done);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVS_H_ */

@@ -1,0 +1,180 @@
+// Compaction of kept K/V rows into 16-token blocks, and whole-block copies.
+//
+// Compaction: Ultralytics glossary "PagedAttention", section "How paging
+// works" -- token slot j of a request lives at slot j % 16 of block
+// table[j / 16]; Novita article, section "Key techniques 1" (after the
+// sparsification step each layer keeps only its selected KV).  Block copies:
+// same glossary, section "Block sharing between sequences" (copy-on-write).
+//
+// Both kernels are pure data movement, bound by HBM bandwidth: every byte is
+// read once and written once with 16-byte vector accesses.  One warp moves one
+// kept slot j of one item: for each KV head it reads the 2*d-byte K and V rows
+// of the kept token (d=128: 256 B contiguous each) and writes them to the
+// pool.  Algorithmic bytes per slot: 2 (K,V) * h_kv * d * 2 B read + the same
+// written.
+#include <cuda_runtime.h>
+
+#include "host_common.h"
+#include "ptx.cuh"
+
+namespace kvs {
+namespace {
+
+constexpr int kWarpsPerCta = 8;
+
+__device__ __forceinline__ int find_item(const kvs_compact_item* items, int n_items,
+                                         int64_t row) {
+  // last item with row_off <= row
+  int lo = 0, hi = n_items - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (items[mid].row_off <= row) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+compact_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+               const kvs_compact_item* __restrict__ items, int n_items, int64_t total_rows,
+               int h_kv, int chunks_per_row /* d * 2 / 16 */,
+               const int32_t* __restrict__ kept_idx, const int32_t* __restrict__ tables,
+               uint4* __restrict__ k_pool, uint4* __restrict__ v_pool, int num_blocks,
+               int32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp_global = static_cast<int64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
+  const int64_t warp_stride = static_cast<int64_t>(gridDim.x) * kWarpsPerCta;
+  const int per_head = chunks_per_row;            // 16-byte chunks per (token, head) row
+  const int per_slot = 2 * h_kv * per_head;       // K and V, every head
+  for (int64_t row = warp_global; row < total_rows; row += warp_stride) {
+    const int it = find_item(items, n_items, row);
+    const kvs_compact_item item = items[it];
+    const int j = static_cast<int>(row - item.row_off);
+    if (j >= item.k_eff) continue;                // a row past a short item (cannot happen
+                                                  // with consistent row_off)
+    const int block = tables[item.table_off + j / KVS_BLOCK_TOKENS];
+    const bool block_ok = block >= 0 && block < num_blocks;
+    if (!block_ok) {
+      if (lane == 0) flag_status(status, KVS_ERR_INVALID);
+      continue;
+    }
+    const int slot = j % KVS_BLOCK_TOKENS;
+    for (int c = lane; c < per_slot; c += 32) {
+      const int is_v = c >= h_kv * per_head;
+      const int cc = is_v ? c - h_kv * per_head : c;
+      const int h = cc / per_head;
+      const int part = cc - h * per_head;
+      const int p = kept_idx[item.idx_off + static_cast<int64_t>(h) * item.k_eff + j];
+      if (p < 0 || p >= item.n) {
+        flag_status(status, KVS_ERR_INVALID);
+        continue;
+      }
+      const int64_t src = ((item.src_tok + p) * h_kv + h) * per_head + part;
+      const int64_t dst =
+          ((static_cast<int64_t>(block) * h_kv + h) * KVS_BLOCK_TOKENS + slot) * per_head + part;
+      if (is_v) v_pool[dst] = __ldg(v + src);
+      else k_pool[dst] = __ldg(k + src);
+    }
+  }
+}
+
+__global__ void copy_blocks_kernel(const int32_t* __restrict__ src, const int32_t* __restrict__ dst,
+                                   int count, uint4* __restrict__ k_pool,
+                                   uint4* __restrict__ v_pool, int num_blocks,
+                                   int64_t chunks_per_block, int32_t* status) {
+  const int64_t total = static_cast<int64_t>(count) * chunks_per_block * 2;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t per_pair = chunks_per_block * 2;
+    const int pair = static_cast<int>(i / per_pair);
+    int64_t off = i - pair * per_pair;
+    uint4* pool = k_pool;
+    if (off >= chunks_per_block) {
+      pool = v_pool;
+      off -= chunks_per_block;
+    }
+    const int s = src[pair], d = dst[pair];
+    if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) {
+      flag_status(status, KVS_ERR_INVALID);
+      continue;
+    }
+    pool[d * chunks_per_block + off] = pool[s * chunks_per_block + off];
+  }
+}
+
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace kvs
+
+extern "C" {
+
+kvs_status kvs_compact_blocks(const kvs_bf16* k, const kvs_bf16* v, const kvs_compact_item* items,
+                              int32_t n_items, int64_t total_rows, int32_t h_kv, int32_t d,
+                              const int32_t* kept_idx, const int32_t* block_tables,
+                              kvs_bf16* k_pool, kvs_bf16* v_pool, int32_t num_blocks,
+                              int32_t* status, kvs_stream stream) {
+  KVS_REQUIRE(n_items >= 0 && total_rows >= 0, "kvs_compact_blocks: negative sizes");
+  if (n_items == 0 || total_rows == 0) return KVS_OK;
+  KVS_REQUIRE(k && v && items && kept_idx && block_tables && k_pool && v_pool,
+              "kvs_compact_blocks: NULL pointer");
+  KVS_SUPPORTED(d == 64 || d == 128, "kvs_compact_blocks: d = %d (supported: 64, 128)", d);
+  KVS_REQUIRE(h_kv > 0 && num_blocks > 0, "kvs_compact_blocks: h_kv / num_blocks must be > 0");
+  KVS_REQUIRE(kvs::aligned16(k) && kvs::aligned16(v) && kvs::aligned16(k_pool) &&
+                  kvs::aligned16(v_pool),
+              "kvs_compact_blocks: K/V and pool pointers must be 16-byte aligned");
+  const int64_t warps = total_rows;
+  int64_t grid = (warps + kvs::kWarpsPerCta - 1) / kvs::kWarpsPerCta;
+  const int64_t cap = static_cast<int64_t>(kvs::sm_count()) * 8;
+  if (grid > cap) grid = cap;
+  kvs::compact_kernel<<<static_cast<unsigned>(grid), kvs::kWarpsPerCta * 32, 0,
+                        static_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<const uint4*>(k), reinterpret_cast<const uint4*>(v), items, n_items,
+      total_rows, h_kv, d * 2 / 16, kept_idx, block_tables, reinterpret_cast<uint4*>(k_pool),
+      reinterpret_cast<uint4*>(v_pool), num_blocks, status);
+  KVS_CHECK_LAUNCH("kvs_compact_blocks");
+  return KVS_OK;
+}
+
+kvs_status kvs_copy_blocks(const int32_t* src, const int32_t* dst, int32_t count,
+                           kvs_bf16* k_pool, kvs_bf16* v_pool, int32_t num_blocks, int32_t h_kv,
+                           int32_t d, int32_t* status, kvs_stream stream) {
+  KVS_REQUIRE(count >= 0, "kvs_copy_blocks: negative count");
+  if (count == 0) return KVS_OK;
+  KVS_REQUIRE(src && dst && k_pool && v_pool, "kvs_copy_blocks: NULL pointer");
+  KVS_SUPPORTED(d == 64 || d == 128, "kvs_copy_blocks: d = %d (supported: 64, 128)", d);
+  KVS_REQUIRE(h_kv > 0 && num_blocks > 0, "kvs_copy_blocks: h_kv / num_blocks must be > 0");
+  KVS_REQUIRE(kvs::aligned16(k_pool) && kvs::aligned16(v_pool),
+              "kvs_copy_blocks: pool pointers must be 16-byte aligned");
+  const int64_t chunks = static_cast<int64_t>(h_kv) * KVS_BLOCK_TOKENS * d * 2 / 16;
+  const int64_t total = chunks * 2 * count;
+  int64_t grid = (total + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(kvs::sm_count()) * 8;
+  if (grid > cap) grid = cap;
+  kvs::copy_blocks_kernel<<<static_cast<unsigned>(grid), 256, 0,
+                            static_cast<cudaStream_t>(stream)>>>(
+      src, dst, count, reinterpret_cast<uint4*>(k_pool), reinterpret_cast<uint4*>(v_pool),
+      num_blocks, chunks, status);
+  KVS_CHECK_LAUNCH("kvs_copy_blocks");
+  return KVS_OK;
+}
+
+kvs_status kvs_workspace_zero(void* workspace, size_t bytes, kvs_stream stream) {
+  if (bytes == 0) return KVS_OK;
+  KVS_REQUIRE(workspace != nullptr, "kvs_workspace_zero: NULL workspace");
+  KVS_CUDA(cudaMemsetAsync(workspace, 0, bytes, static_cast<cudaStream_t>(stream)),
+           "kvs_workspace_zero");
+  return KVS_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,330 @@
+"""The hot path as a sequence of kvs C-ABI calls: prefill+sparsify of a batch
+of prompts over all layers, then decode steps over the paged cache.
+
+Step orders (the same ones the CPU oracle uses):
+* prefill: for each layer, prefill attention (+ m, l) and, for layers with a
+  budget below the prompt length, the window scores; then one selection launch
+  over every (sequence, layer) item; then, sequence by sequence and layer by
+  layer, ceil(k_eff / 16) blocks from the allocator; then one compaction
+  launch over all items.
+* decode step: the host allocator prepares every (stream, layer) item in order
+  (new block when the length is a multiple of 16, copy-on-write of a shared
+  last block), the copies run, then one paged-decode launch covers all items.
+
+Sources: Novita AI, "How KV Sparsity achieves 1.5x acceleration for vLLM"
+(sections "Key techniques 1" and "Key techniques 2"); Ultralytics glossary
+"PagedAttention" (sections "How paging works", "Block sharing between
+sequences").
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+from typing import List, Optional, Sequence
+
+import numpy as np
+import torch
+
+from . import kvs
+
+BLOCK = kvs.BLOCK_TOKENS
+
+
+def blocks_for(tokens: int) -> int:
+    return -(-tokens // BLOCK)
+
+
+def _u8(arr: np.ndarray, device) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(arr).view(np.uint8).reshape(-1)).to(device)
+
+
+@dataclass
+class Shape:
+    n_layers: int
+    h_q: int
+    h_kv: int
+    d: int
+    alpha: int
+    recent: int
+
+    @property
+    def group(self):
+        return self.h_q // self.h_kv
+
+    @property
+    def scale(self):
+        return 1.0 / float(np.sqrt(self.d))
+
+
+@dataclass
+class PrefillResult:
+    """Per-sequence, per-layer block tables (host) and kept-token counts."""
+    tables: List[List[List[int]]]        # [seq][layer] -> block ids
+    k_eff: List[List[int]]               # [seq][layer]
+    kept_idx: torch.Tensor               # device int32, all items
+    idx_off: np.ndarray                  # [seq][layer] element offsets into kept_idx
+    scores: Optional[torch.Tensor] = None  # [L][h_kv][T] fp32 (budgeted layers filled)
+    m: Optional[List[torch.Tensor]] = None  # per layer [h_q][T] when kept
+    l: Optional[List[torch.Tensor]] = None
+    o: Optional[List[torch.Tensor]] = None
+
+
+class Engine:
+    """Device pools, the host block allocator and scratch for one workload."""
+
+    def __init__(self, shape: Shape, num_blocks: int, device="cuda", initial_free=None):
+        self.shape = shape
+        self.device = torch.device(device)
+        self.num_blocks = num_blocks
+        self.alloc = kvs.BlockAllocator(num_blocks, initial_free)
+        s = shape
+        self.k_pool = torch.empty((num_blocks, s.h_kv, BLOCK, s.d), dtype=torch.bfloat16,
+                                  device=self.device)
+        self.v_pool = torch.empty_like(self.k_pool)
+        self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+
+    # ------------------------------------------------------------------ checks
+    def check_status(self):
+        code = int(self.status.item())
+        if code != 0:
+            raise kvs.KvsError(code, "a kernel reported a device-side error")
+
+    # ------------------------------------------------------------------ prefill
+    def prefill_sparsify(self, q_layers: Sequence[torch.Tensor], k_layers: Sequence[torch.Tensor],
+                         v_layers: Sequence[torch.Tensor], seq_lens: Sequence[int],
+                         budgets: Sequence[Sequence[Optional[int]]], keep_outputs=False,
+                         o_buf=None, ml_buf=None, select_scores: Optional[torch.Tensor] = None,
+                         stream=None, timing=None) -> PrefillResult:
+        """q_layers[l]: [T][h_q][d] bf16, k/v_layers[l]: [T][h_kv][d] (T = sum of
+        seq_lens, sequences packed).  budgets[b][l]: k_l for sequence b (None =
+        full cache).  select_scores: optional [L][h_kv][T] scores to select on
+        instead of the ones computed here.  timing: optional dict of lists
+        "attn" / "scores" that receive a (start, end) CUDA event pair around
+        every prefill-attention / window-score launch."""
+        s = self.shape
+        dev = self.device
+        L = s.n_layers
+        lens = [int(x) for x in seq_lens]
+        B = len(lens)
+        T = int(sum(lens))
+        cu = np.zeros(B + 1, dtype=np.int32)
+        cu[1:] = np.cumsum(lens)
+        cu_d = torch.from_numpy(cu).to(dev, non_blocking=True)
+        max_n = max(lens)
+        keff = [[(n if budgets[b][l] is None else min(int(budgets[b][l]), n))
+                 for l in range(L)] for b, n in enumerate(lens)]
+        budgeted = [[budgets[b][l] is not None and budgets[b][l] < lens[b] for l in range(L)]
+                    for b in range(B)]
+        any_budget = [any(budgeted[b][l] for b in range(B)) for l in range(L)]
+
+        if o_buf is None:
+            o_buf = torch.empty((T, s.h_q, s.d), dtype=torch.bfloat16, device=dev)
+        scores = torch.zeros((L, s.h_kv, T), dtype=torch.float32, device=dev)
+        keep_m, keep_l, keep_o = [], [], []
+        for l in range(L):
+            if ml_buf is None or keep_outputs:
+                m = torch.empty((s.h_q, T), dtype=torch.float32, device=dev)
+                lsum = torch.empty_like(m)
+            else:
+                m, lsum = ml_buf
+            o = o_buf if not keep_outputs else torch.empty_like(o_buf)
+            ev = _events(timing, "attn", stream)
+            kvs.kvs_prefill_attn_lse(q_layers[l], k_layers[l], v_layers[l], o, m, lsum, cu_d, B,
+                                     max_n, T, s.h_q, s.h_kv, s.d, s.scale, self.status, stream)
+            _close(ev, stream)
+            if any_budget[l]:
+                ev = _events(timing, "scores", stream)
+                kvs.kvs_window_scores(q_layers[l], k_layers[l], m, lsum, scores[l], cu_d, B, max_n,
+                                      T, s.h_q, s.h_kv, s.d, s.alpha, s.scale, self.status, stream)
+                _close(ev, stream)
+            if keep_outputs:
+                keep_m.append(m)
+                keep_l.append(lsum)
+                keep_o.append(o)
+
+        # selection over every (sequence, layer) item
+        sel = np.zeros(B * L, dtype=kvs.SELECT_ITEM)
+        idx_off = np.zeros((B, L), dtype=np.int64)
+        off = 0
+        for b in range(B):
+            for l in range(L):
+                i = b * L + l
+                sel[i]["score_off"] = l * s.h_kv * T + cu[b]
+                sel[i]["n"] = lens[b]
+                sel[i]["k"] = lens[b] if not budgeted[b][l] else int(budgets[b][l])
+                sel[i]["idx_off"] = off
+                idx_off[b, l] = off
+                off += s.h_kv * keff[b][l]
+        kept = torch.empty(max(off, 1), dtype=torch.int32, device=dev)
+        src_scores = scores if select_scores is None else select_scores
+        kvs.kvs_select_topk(src_scores, T, _u8(sel, dev), B * L, s.h_kv, s.recent, kept,
+                            self.status, stream)
+
+        # host allocator: sequence by sequence, layer by layer
+        tables: List[List[List[int]]] = []
+        flat_tables = []
+        table_off = np.zeros((B, L), dtype=np.int64)
+        toff = 0
+        for b in range(B):
+            per_layer = []
+            for l in range(L):
+                ids = self.alloc.alloc_many(blocks_for(keff[b][l])).tolist()
+                per_layer.append(ids)
+                table_off[b, l] = toff
+                flat_tables.extend(ids)
+                toff += len(ids)
+            tables.append(per_layer)
+        tab_d = torch.tensor(flat_tables if flat_tables else [0], dtype=torch.int32).to(dev)
+
+        comp = np.zeros(B * L, dtype=kvs.COMPACT_ITEM)
+        row = 0
+        for b in range(B):
+            for l in range(L):
+                i = b * L + l
+                comp[i]["src_tok"] = l * T + cu[b]     # K/V of all layers viewed as [L*T][h][d]
+                comp[i]["idx_off"] = idx_off[b, l]
+                comp[i]["row_off"] = row
+                comp[i]["n"] = lens[b]
+                comp[i]["k_eff"] = keff[b][l]
+                comp[i]["table_off"] = table_off[b, l]
+                row += keff[b][l]
+        k_all = _stacked(k_layers)
+        v_all = _stacked(v_layers)
+        kvs.kvs_compact_blocks(k_all, v_all, _u8(comp, dev), B * L, row, s.h_kv, s.d, kept, tab_d,
+                               self.k_pool, self.v_pool, self.num_blocks, self.status, stream)
+        res = PrefillResult(tables=tables, k_eff=keff, kept_idx=kept, idx_off=idx_off,
+                            scores=scores)
+        if keep_outputs:
+            res.m, res.l, res.o = keep_m, keep_l, keep_o
+        return res
+
+
+def _events(timing, key, stream):
+    if timing is None:
+        return None
+    st = torch.cuda.current_stream() if stream is None else stream
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(st)
+    timing.setdefault(key, []).append((a, b))
+    return b
+
+
+def _close(ev, stream):
+    if ev is not None:
+        ev.record(torch.cuda.current_stream() if stream is None else stream)
+
+
+def _stacked(layers):
+    """View per-layer [T][h][d] tensors as one [L*T][h][d] tensor when they are
+    slices of one contiguous buffer; otherwise concatenate."""
+    first = layers[0]
+    T = first.shape[0]
+    n = len(layers)
+    base = first.data_ptr()
+    step = first.numel() * first.element_size()
+    if all(t.data_ptr() == base + i * step for i, t in enumerate(layers)) and first.is_contiguous():
+        return torch.as_strided(first, (n * T, *first.shape[1:]),
+                                (first.stride(0), first.stride(1), first.stride(2)))
+    return torch.cat(list(layers), dim=0)
+
+
+class DecodeBatch:
+    """Decode items (one per (stream, layer)) over an Engine's pools."""
+
+    def __init__(self, eng: Engine, n_streams: int, max_len: int):
+        s = eng.shape
+        self.eng = eng
+        self.n_streams = n_streams
+        self.n_items = n_streams * s.n_layers
+        self.max_len = max_len
+        self.max_blocks = blocks_for(max_len)
+        dev = eng.device
+        self.tables_h = np.full((self.n_items, self.max_blocks), -1, dtype=np.int32)
+        self.lens_h = np.zeros(self.n_items, dtype=np.int32)
+        self.tables_d = torch.zeros((self.n_items, self.max_blocks), dtype=torch.int32, device=dev)
+        self.lens_d = [torch.zeros(self.n_items, dtype=torch.int32, device=dev) for _ in range(2)]
+        self.cur = 0
+        # pinned staging for the per-step table patches and copy-on-write pairs:
+        # a ring, each slot guarded by an event so the host never rewrites a
+        # buffer whose upload has not run yet
+        self._ring = 4
+        self.patch_h = [torch.empty(self.n_items, dtype=torch.int32).pin_memory()
+                        for _ in range(self._ring)]
+        self.cow_h = [torch.empty(2 * self.n_items, dtype=torch.int32).pin_memory()
+                      for _ in range(self._ring)]
+        self._ev = [None] * self._ring
+        self._slot = 0
+        self.patch_d = torch.empty(self.n_items, dtype=torch.int32, device=dev)
+        self.cow_src = np.zeros(self.n_items, dtype=np.int32)
+        self.cow_dst = np.zeros(self.n_items, dtype=np.int32)
+        self.cow_d = torch.empty(2 * self.n_items, dtype=torch.int32, device=dev)
+        self.ws_bytes = kvs.kvs_paged_decode_workspace_size(self.n_items, s.h_q, s.h_kv, s.d,
+                                                            max_len)
+        self.ws = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
+        kvs.kvs_workspace_zero(self.ws, self.ws_bytes)
+        self.out = torch.empty((self.n_items, s.h_q, s.d), dtype=torch.bfloat16, device=dev)
+
+    def set_stream(self, slot: int, tables: List[List[int]], lens: List[int]):
+        """Install a stream's per-layer tables (host copy + device rows)."""
+        L = self.eng.shape.n_layers
+        for l in range(L):
+            i = slot * L + l
+            self.tables_h[i, :] = -1
+            self.tables_h[i, :len(tables[l])] = tables[l]
+            self.lens_h[i] = lens[l]
+        rows = slice(slot * L, (slot + 1) * L)
+        self.tables_d[rows] = torch.from_numpy(self.tables_h[rows]).to(self.eng.device)
+        self.lens_d[self.cur][rows] = torch.from_numpy(self.lens_h[rows]).to(self.eng.device)
+
+    def stream_tables(self, slot: int) -> List[List[int]]:
+        L = self.eng.shape.n_layers
+        out = []
+        for l in range(L):
+            i = slot * L + l
+            nb = blocks_for(int(self.lens_h[i]))
+            out.append(self.tables_h[i, :nb].tolist())
+        return out
+
+    def retire(self, slot: int):
+        for t in self.stream_tables(slot):
+            for b in t:
+                self.eng.alloc.decref(b)
+        L = self.eng.shape.n_layers
+        self.tables_h[slot * L:(slot + 1) * L] = -1
+        self.lens_h[slot * L:(slot + 1) * L] = 0
+
+    def step(self, q, k_new, v_new, stream=None):
+        """One decode step for every item: q [n_items][h_q][d], k_new/v_new
+        [n_items][h_kv][d] bf16 on the device.  Returns the output tensor."""
+        eng, s = self.eng, self.eng.shape
+        n = self.n_items
+        slot = self._slot
+        self._slot = (slot + 1) % self._ring
+        if self._ev[slot] is not None:
+            self._ev[slot].synchronize()
+        patch_t, cow_t = self.patch_h[slot], self.cow_h[slot]
+        patch = patch_t.numpy()
+        n_cow = eng.alloc.decode_prepare(self.tables_h, self.lens_h, patch, self.cow_src,
+                                         self.cow_dst)
+        cur_stream = torch.cuda.current_stream() if stream is None else stream
+        with torch.cuda.stream(cur_stream):
+            self.patch_d.copy_(patch_t, non_blocking=True)
+            if n_cow:
+                cow = cow_t.numpy()
+                cow[:n_cow] = self.cow_src[:n_cow]
+                cow[n_cow:2 * n_cow] = self.cow_dst[:n_cow]
+                self.cow_d[:2 * n_cow].copy_(cow_t[:2 * n_cow], non_blocking=True)
+                kvs.kvs_copy_blocks(self.cow_d[:n_cow], self.cow_d[n_cow:2 * n_cow], n_cow,
+                                    eng.k_pool, eng.v_pool, eng.num_blocks, s.h_kv, s.d,
+                                    eng.status, cur_stream)
+            ev = torch.cuda.Event()
+            ev.record(cur_stream)
+            self._ev[slot] = ev
+        nxt = 1 - self.cur
+        kvs.kvs_paged_decode(q, k_new, v_new, eng.k_pool, eng.v_pool, eng.num_blocks,
+                             self.tables_d, self.max_blocks, self.patch_d, self.lens_d[self.cur],
+                             self.lens_d[nxt], n, self.max_len, s.h_q, s.h_kv, s.d, s.scale,
+                             self.out, self.ws, self.ws_bytes, eng.status, cur_stream)
+        self.cur = nxt
+        self.lens_h += 1
+        return self.out

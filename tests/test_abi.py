@@ -1,0 +1,163 @@
+"""The C ABI library on the host: it loads without a GPU, exports every
+function include/kvs.h declares, and its block allocator (host code) agrees
+with the oracle's list-based pool on the worked example and on random traces.
+No compute call is made here."""
+import os
+import re
+import shutil
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import flow
+from synth import tiny
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def kvs():
+    from layer_wise_kv_gb300 import kvs as k
+    if shutil.which("nvcc") is not None or os.path.exists("/usr/local/cuda/bin/nvcc"):
+        from layer_wise_kv_gb300 import build
+        build.build()          # incremental: a no-op when the library is current
+    elif not os.path.exists(k.LIB_PATH):
+        pytest.skip("libkvs.so not built and nvcc unavailable")
+    k.library()
+    return k
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "kvs.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvs_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_symbols_exported(kvs):
+    lib = kvs.library()
+    names = _declared()
+    assert len(names) >= 20
+    for name in names:
+        assert hasattr(lib, name), name
+    # the binding wraps every declared function
+    assert sorted(names) == sorted(kvs.exported_symbols())
+
+
+def test_last_error_and_version(kvs):
+    assert kvs.library().kvs_version() >= 100
+    with pytest.raises(kvs.KvsError) as e:
+        kvs.BlockAllocator(0)
+    assert e.value.code == kvs.KVS_ERR_INVALID
+    assert "num_blocks" in kvs.last_error()
+
+
+def test_invalid_arguments_rejected_before_launch(kvs):
+    lib = kvs.library()
+    # NULL pointers and unsupported shapes return an error without touching a GPU
+    assert lib.kvs_compact_blocks(None, None, None, 1, 1, 8, 128, None, None, None, None, 4,
+                                  None, None) == kvs.KVS_ERR_INVALID
+    rc = lib.kvs_paged_decode(1, None, None, 1, 1, 4, 1, 4, None, 1, None, 1, 16, 8, 8, 96,
+                              0.1, 1, 1, 1 << 20, None, None)
+    assert rc == kvs.KVS_ERR_UNSUPPORTED and "d = 96" in kvs.last_error()
+    assert lib.kvs_window_scores(1, 1, 1, 1, 1, 1, 1, 64, 64, 32, 8, 128, 128, 0.1, None,
+                                 None) == kvs.KVS_ERR_UNSUPPORTED  # alpha * G > 256
+    assert lib.kvs_prefill_attn_lse(1, 1, 1, 1, 1, 1, 1, 1, 16, 16, 6, 4, 128, 0.1, None,
+                                    None) == kvs.KVS_ERR_INVALID  # 6 % 4 != 0
+    assert kvs.kvs_paged_decode_workspace_size(0, 32, 8, 128, 100) == 0
+
+
+def test_worked_example_allocator(kvs, golden_dir):
+    import json
+    g = json.load(open(os.path.join(golden_dir, "paging_worked_example.json")))
+    a = kvs.BlockAllocator(g["pool_blocks"], g["free_list"])
+    table = a.alloc_many(g["expected_blocks"]).tolist()
+    assert table == g["expected_table"]
+    assert a.free_list() == g["free_list"][len(table):]
+    a.close()
+
+
+def test_allocator_matches_oracle_random_trace(kvs):
+    rng = np.random.default_rng(7)
+    N = 50
+    order = rng.permutation(N)
+    a = kvs.BlockAllocator(N, order)
+    o = oracle.BlockPool(N, free=order)
+    owned = []
+    for step in range(5000):
+        op = rng.integers(0, 5)
+        if op == 0:
+            if o.num_free():
+                b1, b2 = a.alloc(), o.alloc()
+                assert b1 == b2
+                owned.append(b1)
+            else:
+                with pytest.raises(kvs.KvsError) as e:
+                    a.alloc()
+                assert e.value.code == kvs.KVS_ERR_OOM_BLOCKS
+        elif op == 1 and owned:
+            b = owned[rng.integers(len(owned))]
+            a.incref(b)
+            o.incref(b)
+            owned.append(b)
+        elif op == 2 and owned:
+            b = owned.pop(rng.integers(len(owned)))
+            a.decref(b)
+            o.decref(b)
+        elif op == 3 and owned and o.num_free():
+            i = rng.integers(len(owned))
+            r1 = a.cow(owned[i])
+            r2 = o.cow(owned[i])
+            assert r1 == r2
+            owned[i] = r1[0]
+        elif op == 4:
+            k = int(rng.integers(0, 4))
+            if k <= o.num_free():
+                got = a.alloc_many(k).tolist()
+                assert got == [o.alloc() for _ in range(k)]
+                owned.extend(got)
+        assert a.num_free() == o.num_free()
+        if step % 97 == 0:
+            assert a.free_list() == o.free
+            assert [a.refcount(b) for b in range(N)] == o.ref
+    a.close()
+
+
+def test_decode_prepare_matches_oracle_flow(kvs):
+    """kvs_decode_prepare (host) against the oracle's prepare_append, with
+    shared blocks so that copy-on-write happens."""
+    w = tiny()
+    rng = np.random.default_rng(3)
+    N = 64
+    a = kvs.BlockAllocator(N)
+    o = oracle.BlockPool(N)
+    # three streams of one layer sharing a prompt of 21 tokens (partial last block)
+    prompt = [o.alloc(), o.alloc()]
+    assert a.alloc_many(2).tolist() == prompt
+    streams = [flow.Stream(tables=[list(prompt)], lens=[21])]
+    for _ in range(2):
+        streams.append(flow.share_stream(o, streams[0]))
+        for b in prompt:
+            a.incref(b)
+    max_blocks = 8
+    tables = np.full((3, max_blocks), -1, dtype=np.int32)
+    tables[:, :2] = prompt
+    lens = np.full(3, 21, dtype=np.int32)
+    patch = np.zeros(3, dtype=np.int32)
+    cs, cd = np.zeros(3, dtype=np.int32), np.zeros(3, dtype=np.int32)
+    for step in range(40):
+        n_cow = a.decode_prepare(tables, lens, patch, cs, cd)
+        copies = []
+        for s in streams:
+            c = flow.prepare_append(o, s, 0)
+            copies.append(c)
+            s.lens[0] += 1
+        exp_pairs = [c for c in copies if c is not None]
+        assert n_cow == len(exp_pairs)
+        assert list(zip(cs[:n_cow].tolist(), cd[:n_cow].tolist())) == exp_pairs
+        for i, s in enumerate(streams):
+            assert tables[i, :len(s.tables[0])].tolist() == s.tables[0]
+        lens += 1
+        assert [a.refcount(b) for b in range(N)] == o.ref
+    assert step == 39
+    a.close()

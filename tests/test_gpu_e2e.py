@@ -1,0 +1,339 @@
+"""End-to-end parity of the hot path (prefill attention + m/l, window scores,
+selection, allocation + compaction, paged decode) against the oracle's flow,
+on the seeded workloads.  The GPU path runs through the C ABI via
+layer_wise_kv_gb300.pipeline; the oracle runs the same step orders on CPU."""
+import numpy as np
+import pytest
+
+import oracle
+from oracle import flow
+from synth import (bf16_to_f64, continuous_batching, decode_qkv, llama3_8b, prefill_qkv,
+                   shuffled_block_order, tiny)
+from gpu_helpers import (ABS_O, REL_ML, REL_S, ABS_S, bf16_f64, check_kept, check_m, check_rel,
+                         dev_bf16, host_bits, kvs_lib, torch)
+
+pytestmark = pytest.mark.gpu
+
+
+def _shape(w):
+    from layer_wise_kv_gb300.pipeline import Shape
+    return Shape(w.n_layers, w.h_q, w.h_kv, w.d, w.alpha, w.recent)
+
+
+def _layers_to_device(w, seqs, lens, layers=None):
+    """Per-layer Q/K/V of the packed sequences, as slices of one buffer each."""
+    layers = list(range(w.n_layers)) if layers is None else layers
+    T = sum(lens)
+    qd = torch.empty((len(layers), T, w.h_q, w.d), dtype=torch.bfloat16, device="cuda")
+    kd = torch.empty((len(layers), T, w.h_kv, w.d), dtype=torch.bfloat16, device="cuda")
+    vd = torch.empty_like(kd)
+    host = {}
+    for li, l in enumerate(layers):
+        tok = 0
+        for s, n in zip(seqs, lens):
+            qb, kb, vb = prefill_qkv(w, s, l, n)
+            host[(s, l)] = (qb, kb, vb)
+            qd[li, tok:tok + n] = dev_bf16(qb)
+            kd[li, tok:tok + n] = dev_bf16(kb)
+            vd[li, tok:tok + n] = dev_bf16(vb)
+            tok += n
+    return [qd[i] for i in range(len(layers))], [kd[i] for i in range(len(layers))], \
+        [vd[i] for i in range(len(layers))], host
+
+
+def _gpu_idx(res, b, l, h_kv, k_eff):
+    off = int(res.idx_off[b, l])
+    return res.kept_idx[off:off + h_kv * k_eff].cpu().numpy().reshape(h_kv, k_eff)
+
+
+# ---------------------------------------------------------------------------
+def test_tiny_workload_end_to_end():
+    kvs_lib()
+    from layer_wise_kv_gb300.pipeline import DecodeBatch, Engine
+    w = tiny()
+    n = w.prompt_lens[0]
+    L = w.n_layers
+    eng = Engine(_shape(w), 64)
+    ql, kl, vl, host = _layers_to_device(w, [0], [n])
+    budgets = [[w.budget(l, n) for l in range(L)]]
+    res = eng.prefill_sparsify(ql, kl, vl, [n], budgets, keep_outputs=True)
+    torch.cuda.synchronize()
+    eng.check_status()
+
+    pool = oracle.BlockPool(64)
+    opk = np.zeros((64, w.h_kv, 16, w.d), np.uint16)
+    opv = np.zeros_like(opk)
+    recs = []
+    for l in range(L):
+        qb, kb, vb = host[(0, l)]
+        rec = flow.sparsify_layer(w, l, qb, kb, vb, rows=np.arange(n))
+        recs.append(rec)
+        # prefill O, m, l on every row
+        assert np.abs(bf16_f64(res.o[l]) - rec.o_rows).max() <= ABS_O
+        check_m(res.m[l].cpu().numpy(), rec.m_rows)
+        check_rel(res.l[l].cpu().numpy(), rec.l_rows, REL_ML, what="l")
+        gidx = _gpu_idx(res, 0, l, w.h_kv, rec.k_eff)
+        if rec.budgeted:
+            S = res.scores[l].cpu().numpy().astype(np.float64)
+            check_rel(S, rec.scores, REL_S, ABS_S, what=f"S layer {l}")
+            for h in range(w.h_kv):
+                check_kept(gidx[h], rec.idx[h], rec.scores[h], n, w.budget(l, n), w.recent)
+        else:
+            np.testing.assert_array_equal(gidx, rec.idx)
+        # tables: same allocator order, bit-exact
+        rec.idx = gidx                               # compact what the GPU kept
+        flow.place_layer(rec, pool, kb, vb, opk, opv)
+        assert res.tables[0][l] == rec.table
+    # compacted bytes, valid slots only
+    gk, gv = host_bits(eng.k_pool), host_bits(eng.v_pool)
+    for l in range(L):
+        for j in range(recs[l].k_eff):
+            b, s = recs[l].table[j // 16], j % 16
+            np.testing.assert_array_equal(gk[b, :, s], opk[b, :, s])
+            np.testing.assert_array_equal(gv[b, :, s], opv[b, :, s])
+
+    # selection on the oracle's scores (cast to fp32): bit-exact
+    sel = torch.zeros_like(res.scores)
+    for l in range(L):
+        if recs[l].budgeted:
+            sel[l] = torch.from_numpy(recs[l].scores.astype(np.float32))
+    eng2 = Engine(_shape(w), 64)
+    res2 = eng2.prefill_sparsify(ql, kl, vl, [n], budgets, select_scores=sel)
+    torch.cuda.synchronize()
+    for l in range(L):
+        want = np.stack([oracle.select_kept(sel[l, h].cpu().numpy(), n, w.budget(l, n), w.recent)
+                         for h in range(w.h_kv)]) if recs[l].budgeted else recs[l].idx
+        np.testing.assert_array_equal(_gpu_idx(res2, 0, l, w.h_kv, recs[l].k_eff), want)
+
+    # decode steps over the paged cache
+    steps = w.decode_steps
+    dec = DecodeBatch(eng, 1, n + steps)
+    dec.set_stream(0, res.tables[0], res.k_eff[0])
+    st = flow.new_stream(recs)
+    dq = [decode_qkv(w, 0, l, steps) for l in range(L)]
+    for t in range(steps):
+        q = dev_bf16(np.stack([dq[l][0][t] for l in range(L)]))
+        k = dev_bf16(np.stack([dq[l][1][t] for l in range(L)]))
+        v = dev_bf16(np.stack([dq[l][2][t] for l in range(L)]))
+        out = bf16_f64(dec.step(q, k, v))
+        for l in range(L):
+            flow.prepare_append(pool, st, l, opk, opv)
+            ref = flow.append_and_attend(w, st, l, dq[l][0][t], dq[l][1][t], dq[l][2][t], opk, opv)
+            assert np.abs(out[l] - ref).max() <= ABS_O, (t, l)
+    torch.cuda.synchronize()
+    eng.check_status()
+    assert dec.stream_tables(0) == st.tables
+
+
+# ---------------------------------------------------------------------------
+def test_shared_prefix_copy_on_write():
+    """n = 3 parallel samples share a prompt's blocks; the partial last block
+    of a full-cache layer is copied on each sample's first write (the first
+    two samples copy, the third writes in place)."""
+    kvs_lib()
+    from layer_wise_kv_gb300.pipeline import DecodeBatch, Engine
+    w = tiny()
+    n = 100                                  # layer 0: 100 tokens (partial block); layer 1: 64
+    L = w.n_layers
+    N = 64
+    eng = Engine(_shape(w), N)
+    ql, kl, vl, host = _layers_to_device(w, [3], [n])
+    budgets = [[w.budget(l, n) for l in range(L)]]
+    res = eng.prefill_sparsify(ql, kl, vl, [n], budgets)
+    torch.cuda.synchronize()
+    pool = oracle.BlockPool(N)
+    opk = np.zeros((N, w.h_kv, 16, w.d), np.uint16)
+    opv = np.zeros_like(opk)
+    recs = []
+    for l in range(L):
+        qb, kb, vb = host[(3, l)]
+        rec = flow.sparsify_layer(w, l, qb, kb, vb)
+        rec.idx = _gpu_idx(res, 0, l, w.h_kv, rec.k_eff)
+        flow.place_layer(rec, pool, kb, vb, opk, opv)
+        assert res.tables[0][l] == rec.table
+        recs.append(rec)
+    S = 3
+    dec = DecodeBatch(eng, S, n + 40)
+    streams = [flow.new_stream(recs)]
+    dec.set_stream(0, res.tables[0], res.k_eff[0])
+    for s in range(1, S):
+        streams.append(flow.share_stream(pool, streams[0]))
+        for t in res.tables[0]:
+            for b in t:
+                eng.alloc.incref(b)
+        dec.set_stream(s, res.tables[0], res.k_eff[0])
+    assert eng.alloc.refcount(res.tables[0][0][-1]) == 3
+    steps = 20
+    dq = {(s, l): decode_qkv(w, 3, l, steps, sample=s) for s in range(S) for l in range(L)}
+    for t in range(steps):
+        q = dev_bf16(np.stack([dq[(s, l)][0][t] for s in range(S) for l in range(L)]))
+        k = dev_bf16(np.stack([dq[(s, l)][1][t] for s in range(S) for l in range(L)]))
+        v = dev_bf16(np.stack([dq[(s, l)][2][t] for s in range(S) for l in range(L)]))
+        out = bf16_f64(dec.step(q, k, v))
+        copies = 0
+        for s in range(S):
+            for l in range(L):
+                c = flow.prepare_append(pool, streams[s], l, opk, opv)
+                copies += c is not None
+                ref = flow.append_and_attend(w, streams[s], l, dq[(s, l)][0][t], dq[(s, l)][1][t],
+                                             dq[(s, l)][2][t], opk, opv)
+                assert np.abs(out[s * L + l] - ref).max() <= ABS_O, (t, s, l)
+        if t == 0:
+            assert copies == 2                        # samples 0 and 1 copy layer 0's block
+    torch.cuda.synchronize()
+    eng.check_status()
+    for s in range(S):
+        assert dec.stream_tables(s) == streams[s].tables
+    assert [eng.alloc.refcount(b) for b in range(N)] == pool.ref
+
+
+# ---------------------------------------------------------------------------
+def test_continuous_batching_small():
+    """Slots are refilled as sequences finish; finished sequences' blocks go
+    back to a seed-shuffled free pool.  Tables must match the oracle's pool
+    bit-exactly at every admission; outputs are checked on every step."""
+    kvs_lib()
+    from layer_wise_kv_gb300.pipeline import DecodeBatch, Engine
+    w = tiny()
+    L = w.n_layers
+    N = 96
+    order = shuffled_block_order(N, 1)
+    eng = Engine(_shape(w), N, initial_free=order)
+    pool = oracle.BlockPool(N, free=order)
+    opk = np.zeros((N, w.h_kv, 16, w.d), np.uint16)
+    opv = np.zeros_like(opk)
+    rng = np.random.default_rng(5)
+    prompt = [int(x) for x in rng.integers(40, 140, size=5)]
+    outs = [int(x) for x in rng.integers(3, 12, size=5)]
+    slots = 2
+    dec = DecodeBatch(eng, slots, 140 + 12)
+    live = {}                                  # slot -> (seq, produced, oracle stream)
+
+    def admit(slot, seq):
+        n = prompt[seq]
+        ql, kl, vl, host = _layers_to_device(w, [10 + seq], [n])
+        res = eng.prefill_sparsify(ql, kl, vl, [n], [[w.budget(l, n) for l in range(L)]])
+        recs = []
+        for l in range(L):
+            qb, kb, vb = host[(10 + seq, l)]
+            rec = flow.sparsify_layer(w, l, qb, kb, vb)
+            rec.idx = _gpu_idx(res, 0, l, w.h_kv, rec.k_eff)
+            flow.place_layer(rec, pool, kb, vb, opk, opv)
+            assert res.tables[0][l] == rec.table
+            recs.append(rec)
+        dec.set_stream(slot, res.tables[0], res.k_eff[0])
+        live[slot] = [seq, 0, flow.new_stream(recs)]
+
+    nxt = 0
+    for s in range(slots):
+        admit(s, nxt)
+        nxt += 1
+    step = 0
+    while live:
+        qs, ks, vs = [], [], []
+        for s in range(slots):
+            seq = live[s][0]
+            for l in range(L):
+                dq = decode_qkv(w, 50 + seq, l, step + 1)
+                qs.append(dq[0][step]), ks.append(dq[1][step]), vs.append(dq[2][step])
+        out = bf16_f64(dec.step(dev_bf16(np.stack(qs)), dev_bf16(np.stack(ks)),
+                                dev_bf16(np.stack(vs))))
+        for s in sorted(live):
+            seq, made, st = live[s]
+            for l in range(L):
+                flow.prepare_append(pool, st, l, opk, opv)
+                ref = flow.append_and_attend(w, st, l, qs[s * L + l], ks[s * L + l],
+                                             vs[s * L + l], opk, opv)
+                assert np.abs(out[s * L + l] - ref).max() <= ABS_O
+            live[s][1] += 1
+        step += 1
+        for s in sorted(live):
+            if live[s][1] >= outs[live[s][0]]:
+                flow.retire(pool, live[s][2])
+                dec.retire(s)
+                del live[s]
+                if nxt < len(prompt):
+                    admit(s, nxt)
+                    nxt += 1
+        if len(live) < slots and nxt >= len(prompt):
+            break                               # the batch drains with one slot idle
+    torch.cuda.synchronize()
+    eng.check_status()
+    assert eng.alloc.free_list() == pool.free
+    assert [eng.alloc.refcount(b) for b in range(N)] == pool.ref
+
+
+# ---------------------------------------------------------------------------
+def test_llama3_8b_full_size_sampled():
+    """The bench's launch configuration (32 layers, 32/8 heads, d=128, one 4000
+    token prompt): prefill O/m/l on sampled rows of four layers, every window
+    score, the kept sets of every budgeted layer, compacted bytes of every
+    layer and three decode steps over all 32 layers."""
+    kvs_lib()
+    from layer_wise_kv_gb300.pipeline import DecodeBatch, Engine
+    w = llama3_8b()
+    n = w.prompt_lens[0]
+    L = w.n_layers
+    N = 4096
+    eng = Engine(_shape(w), N)
+    ql, kl, vl, host = _layers_to_device(w, [0], [n])
+    budgets = [[w.budget(l, n) for l in range(L)]]
+    res = eng.prefill_sparsify(ql, kl, vl, [n], budgets, keep_outputs=True)
+    torch.cuda.synchronize()
+    eng.check_status()
+    rng = np.random.default_rng(8)
+    rows = np.unique(np.concatenate([np.arange(128), np.arange(n - 128, n),
+                                     rng.integers(0, n, 64)]))
+    pool = oracle.BlockPool(N)
+    swaps = 0
+    recs = []
+    for l in range(L):
+        qb, kb, vb = host[(0, l)]
+        sample = rows if l in (0, 3, 17, 31) else None
+        rec = flow.sparsify_layer(w, l, qb, kb, vb, rows=sample)
+        if sample is not None:
+            assert np.abs(bf16_f64(res.o[l])[rows] - rec.o_rows).max() <= ABS_O
+            check_m(res.m[l].cpu().numpy()[:, rows], rec.m_rows)
+            check_rel(res.l[l].cpu().numpy()[:, rows], rec.l_rows, REL_ML, what="l")
+        gidx = _gpu_idx(res, 0, l, w.h_kv, rec.k_eff)
+        if rec.budgeted:
+            check_m(res.m[l].cpu().numpy()[:, n - w.alpha:], rec.m_win)
+            check_rel(res.l[l].cpu().numpy()[:, n - w.alpha:], rec.l_win, REL_ML, what="l win")
+            check_rel(res.scores[l].cpu().numpy().astype(np.float64), rec.scores, REL_S, ABS_S,
+                      what=f"S layer {l}")
+            for h in range(w.h_kv):
+                swaps += check_kept(gidx[h], rec.idx[h], rec.scores[h], n, w.budget(l, n),
+                                    w.recent)
+        else:
+            np.testing.assert_array_equal(gidx, rec.idx)
+        rec.idx = gidx
+        flow.place_layer(rec, pool, kb, vb, None, None)
+        assert res.tables[0][l] == rec.table
+        recs.append(rec)
+    # compacted bytes: gather back through the tables equals K[idx], bit for bit
+    gk, gv = host_bits(eng.k_pool), host_bits(eng.v_pool)
+    for l in range(L):
+        _, kb, vb = host[(0, l)]
+        t = np.array(recs[l].table)
+        j = np.arange(recs[l].k_eff)
+        for h in range(w.h_kv):
+            np.testing.assert_array_equal(gk[t[j // 16], h, j % 16], kb[recs[l].idx[h], h])
+            np.testing.assert_array_equal(gv[t[j // 16], h, j % 16], vb[recs[l].idx[h], h])
+    # decode: three steps over all 32 layers in one launch per step
+    steps = 3
+    dec = DecodeBatch(eng, 1, n + w.decode_steps)
+    dec.set_stream(0, res.tables[0], res.k_eff[0])
+    opk, opv = gk.copy(), gv.copy()
+    st = flow.new_stream(recs)
+    dq = [decode_qkv(w, 0, l, steps) for l in range(L)]
+    for t in range(steps):
+        out = bf16_f64(dec.step(dev_bf16(np.stack([dq[l][0][t] for l in range(L)])),
+                                dev_bf16(np.stack([dq[l][1][t] for l in range(L)])),
+                                dev_bf16(np.stack([dq[l][2][t] for l in range(L)]))))
+        for l in range(L):
+            flow.prepare_append(pool, st, l, opk, opv)
+            ref = flow.append_and_attend(w, st, l, dq[l][0][t], dq[l][1][t], dq[l][2][t], opk, opv)
+            assert np.abs(out[l] - ref).max() <= ABS_O, (t, l)
+    torch.cuda.synchronize()
+    eng.check_status()
+    print(f"kept-set swaps within the 1e-3 band: {swaps}")
