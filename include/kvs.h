@@ -185,30 +185,30 @@ kvs_status kvs_copy_blocks(const int32_t* src, const int32_t* dst, int32_t count
  * otherwise over lens[i] tokens.  Per query head g (KV head g / G):
  *     out[i][g] = softmax_t(scale * q[i][g] . K_t) V
  *   q, out [batch][h_q][d]; k_new, v_new [batch][h_kv][d] (nullable)
- *   block_tables [batch][max_blocks] int32; lens [batch] int32
+ *   block_tables [batch][max_blocks] int32; lens [batch] int32 (batch <= 4096)
  *   table_patch  [batch] int32, nullable: entry >= 0 replaces
  *                block_tables[i][lens[i] / 16] before use and is written
  *                back there (the host allocator's new or copied-on-write
  *                last block); -1 = no change.
- *   lens_next    [batch] int32, nullable: receives lens[i] + (k_new != NULL).
- *   max_len      host upper bound of lens[i] + 1 over all items.
- *   workspace    scratch of kvs_paged_decode_workspace_size(...) bytes; must
- *                be zero-filled before its first use (kvs_workspace_zero);
- *                each call leaves it ready for the next one.  Calls sharing
- *                a workspace must not overlap in time.
+ *   lens_next    [batch] int32, nullable, must not alias lens: receives
+ *                lens[i] + (k_new != NULL).
+ *   workspace    scratch of kvs_paged_decode_workspace_size(batch, h_q, h_kv,
+ *                d) bytes; must be zero-filled before its first use
+ *                (kvs_workspace_zero); each call leaves it ready for the next.
+ *                Calls sharing a workspace must not overlap in time.
+ * An item with zero tokens to attend (lens[i] == 0 and no append) gets no
+ * output row.
  * ---------------------------------------------------------------------- */
-size_t kvs_paged_decode_workspace_size(int32_t batch, int32_t h_q, int32_t h_kv, int32_t d,
-                                       int32_t max_len);
+size_t kvs_paged_decode_workspace_size(int32_t batch, int32_t h_q, int32_t h_kv, int32_t d);
 
 kvs_status kvs_workspace_zero(void* workspace, size_t bytes, kvs_stream stream);
 
 kvs_status kvs_paged_decode(const kvs_bf16* q, const kvs_bf16* k_new, const kvs_bf16* v_new,
                             kvs_bf16* k_pool, kvs_bf16* v_pool, int32_t num_blocks,
                             int32_t* block_tables, int32_t max_blocks, const int32_t* table_patch,
-                            const int32_t* lens, int32_t* lens_next, int32_t batch,
-                            int32_t max_len, int32_t h_q, int32_t h_kv, int32_t d, float scale,
-                            kvs_bf16* out, void* workspace, size_t workspace_bytes,
-                            int32_t* status, kvs_stream stream);
+                            const int32_t* lens, int32_t* lens_next, int32_t batch, int32_t h_q,
+                            int32_t h_kv, int32_t d, float scale, kvs_bf16* out, void* workspace,
+                            size_t workspace_bytes, int32_t* status, kvs_stream stream);
 
 /* ------------------------------------------------------------------------
  * Block allocator (host memory, single-threaded, not thread-safe).
@@ -252,12 +252,14 @@ int32_t kvs_alloc_free_list(const kvs_allocator* a, int32_t* buf, int32_t cap);
  *                                    cow_src / cow_dst
  *   otherwise                     -> patch[i] = -1
  * The host table row is updated in place.  *n_cow receives the number of
- * copies (cow_src / cow_dst need room for n_items entries).  If the pool runs
+ * copies (cow_src / cow_dst need room for n_items entries); *n_patch
+ * (nullable) the number of entries of `patch` that are >= 0, so that a step
+ * with none can pass table_patch = NULL to kvs_paged_decode.  If the pool runs
  * dry, returns KVS_ERR_OOM_BLOCKS with *n_done = items fully prepared. */
 kvs_status kvs_decode_prepare(kvs_allocator* a, int32_t* tables, int32_t max_blocks,
                               const int32_t* lens, int32_t n_items, int32_t* patch,
                               int32_t* cow_src, int32_t* cow_dst, int32_t* n_cow,
-                              int32_t* n_done);
+                              int32_t* n_patch, int32_t* n_done);
 
 #ifdef __cplusplus
 }

@@ -9,24 +9,30 @@
 // cache).
 //
 // Design (HBM-bound: ~4 flop per byte of K/V):
-// * A unit is (item, KV head, split of 256 tokens = 16 blocks).  Persistent
-//   CTAs walk units round-robin; each CTA has one producer warp and eight
-//   consumer warps.  Per-CTA unit lists come from a prefix sum over the
-//   items' split counts, computed from `lens` in shared memory, so the launch
+// * The work is the sequence of (item, KV head) segments, each a run of
+//   16-token blocks.  Persistent CTAs (one per SM, twelve warps) split the
+//   concatenated block sequence into equal contiguous ranges, one per warp
+//   (stream-K): every warp streams the same number of bytes, whatever the mix
+//   of lengths, and a segment is cut into at most a few pieces.  Segment
+//   offsets come from a prefix sum over `lens` in shared memory, so the launch
 //   needs no host knowledge of the lengths.
-// * The producer streams each block's K and V rows for the head (16 x d bf16
-//   each, contiguous in the pool) into a 16-stage shared-memory ring with 2-D
-//   TMA loads (128-byte swizzle), mbarrier-tracked.
-// * Consumer warp w takes blocks w, w+8 of the unit.  The G query rows of the
-//   KV head form the M=16 side of mma.sync m16n8k16 (bf16 in, fp32 out): S =
-//   q K^T (K fragments by ldmatrix), online softmax in registers (log2
-//   domain), O += P V (V fragments by ldmatrix.trans).  The tensor pipe only
-//   takes the instruction count off the issue slots; the bound is HBM.
-// * Warps merge through shared memory at the end of a unit; an item with one
-//   split writes `out` directly, otherwise the unit writes an unnormalised
-//   partial (m, l, o) to the workspace and the last unit of (item, head) to
-//   finish (an atomic counter, no waiting) merges all partials and resets the
-//   counter.
+// * A warp runs its range with no CTA-wide barrier: its own 2- or 3-stage
+//   shared-memory ring (as shared memory allows), refilled by its lane 0 with 2-D TMA loads (128-byte
+//   swizzle) of each block's K and V rows for the head (16 x d bf16 each,
+//   contiguous in the pool) plus, with a piece's first block, a linear bulk
+//   copy of the group's q rows.  Block-table entries are fetched 32 at a time,
+//   one chunk ahead.
+// * Per 16-token block the products run transposed on mma.sync m16n8k16
+//   (bf16 in, fp32 out), with the block's tokens as the M=16 side and the G
+//   query heads of the KV head as the N side (8 per n-tile): S^T = K q^T (K
+//   fragments by ldmatrix), online softmax per head in registers (log2
+//   domain), P^T turned into a B fragment with movmatrix, O^T += V^T P^T (V
+//   fragments by ldmatrix.trans).  The tensor pipe only takes the instruction
+//   count off the issue slots; the bound is HBM.
+// * A segment covered by one piece writes `out` directly; otherwise each piece
+//   writes an unnormalised partial (m, l, o) to its workspace slot (warp index
+//   + segment index, unique), and the last piece of the segment to finish (an
+//   atomic counter, no waiting) merges them and resets the counter.
 #include <cuda_runtime.h>
 
 #include "host_common.h"
@@ -36,12 +42,11 @@
 namespace kvs {
 namespace {
 
-constexpr int kConsumers = 8;
-constexpr int kDecThreads = (kConsumers + 1) * 32;
-constexpr int kStages = 16;
-constexpr int kSplitBlocks = 16;
-constexpr int kSplitTokens = kSplitBlocks * KVS_BLOCK_TOKENS;
+constexpr int kWarps = 12;
+constexpr int kDecThreads = kWarps * 32;
+constexpr int kMaxGrid = 256;
 constexpr int kMaxG = 16;
+constexpr int kMaxBatch = 2048;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct DecodeParams {
@@ -58,23 +63,16 @@ struct DecodeParams {
   float* ws_part;
   int32_t* ws_count;
   int32_t* status;
-  int batch, max_blocks, num_blocks, h_q, h_kv, group, s_max, append;
+  int batch, max_blocks, num_blocks, h_q, h_kv, group, append, n_stages;
+  int q_bytes, q_stride, q_off, bar_off, scr_off, idx_off;
   float scale_log2;
 };
 
 template <int D>
-struct DecodeSmem {
-  static constexpr int kBoxBytes = KVS_BLOCK_TOKENS * 128;         // 16 rows x 64 bf16
-  static constexpr int kBlockBytes = KVS_BLOCK_TOKENS * D * 2;     // one head's K (or V) block
+struct DecodeLayout {
+  static constexpr int kBoxBytes = KVS_BLOCK_TOKENS * 128;       // 16 rows x 64 bf16
+  static constexpr int kBlockBytes = KVS_BLOCK_TOKENS * D * 2;   // one head's K (or V) block
   static constexpr int kStageBytes = 2 * kBlockBytes;
-  static constexpr int kRing = kStages * kStageBytes;
-  static constexpr int kScratchFloats = kConsumers * kMaxG * (D + 2);
-  // ring | full[kStages] | empty[kStages] | scratch | flags | prefix[batch+1]
-  static constexpr int kBarOff = kRing;
-  static constexpr int kScratchOff = kBarOff + 2 * kStages * 8;
-  static constexpr int kFlagOff = kScratchOff + kScratchFloats * 4;
-  static constexpr int kPrefixOff = kFlagOff + 16;
-  static size_t bytes(int batch) { return 1024 + kPrefixOff + 4 * (batch + 1); }
 };
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
@@ -100,6 +98,12 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+
 // byte offset of 16-byte chunk `c` (0 .. D/8-1) of row `r` in a block stored
 // as D/64 boxes of 16 rows x 128 B with the 128-byte swizzle
 __device__ __forceinline__ uint32_t sw_off(int r, int c) {
@@ -107,65 +111,104 @@ __device__ __forceinline__ uint32_t sw_off(int r, int c) {
                                (((c & 7) ^ (r & 7)) << 4));
 }
 
-struct Unit {
-  int item, h, split, ns, nblk, len, lens0;
+// owner warp of global block b when T blocks are split evenly over W warps
+// (warp w owns [w*T/W, (w+1)*T/W))
+__device__ __forceinline__ int owner_of(int64_t b, int64_t T, int W) {
+  const int64_t w = ((b + 1) * W - 1) / T;
+  return static_cast<int>(w < W - 1 ? w : W - 1);
+}
+
+struct Piece {
+  bool valid;
+  int item, h, seg, blk0, nblk, lens0, len, first_slot, npieces;
+  int64_t end;  // global block index just past the piece
 };
 
-__device__ __forceinline__ Unit decode_unit(int u, const int* prefix, int batch, int h_kv,
-                                            int append) {
-  int lo = 0, hi = batch - 1;  // last item with prefix[item] <= u
+// The piece of warp-range [pos, range_end) that starts at pos.
+__device__ __forceinline__ Piece piece_at(int64_t pos, int64_t range_end, int64_t T, int W,
+                                          const int* prefix, const int* lens_s,
+                                          const DecodeParams& p) {
+  Piece x;
+  x.valid = pos < range_end;
+  if (!x.valid) {
+    x.item = x.h = x.seg = x.blk0 = x.nblk = x.lens0 = x.len = x.first_slot = x.npieces = 0;
+    x.end = pos;
+    return x;
+  }
+  int lo = 0, hi = p.batch - 1;  // last item with prefix[item] <= pos
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (prefix[mid] <= u) lo = mid; else hi = mid - 1;
+    if (prefix[mid] <= pos) lo = mid; else hi = mid - 1;
   }
-  Unit x;
   x.item = lo;
-  const int units = prefix[lo + 1] - prefix[lo];
-  x.ns = units / h_kv;
-  const int local = u - prefix[lo];
-  x.h = local / x.ns;
-  x.split = local - x.h * x.ns;
+  x.lens0 = lens_s[lo];
+  x.len = x.lens0 + p.append;
+  const int nb = (x.len + KVS_BLOCK_TOKENS - 1) / KVS_BLOCK_TOKENS;  // blocks per head
+  const int local = static_cast<int>(pos - prefix[lo]);
+  x.h = local / nb;
+  x.blk0 = local - x.h * nb;
+  x.seg = lo * p.h_kv + x.h;
+  const int64_t seg_lo = prefix[lo] + static_cast<int64_t>(x.h) * nb;
+  const int64_t seg_hi = seg_lo + nb;
+  x.end = seg_hi < range_end ? seg_hi : range_end;
+  x.nblk = static_cast<int>(x.end - pos);
+  const int w_lo = owner_of(seg_lo, T, W);
+  x.npieces = owner_of(seg_hi - 1, T, W) - w_lo + 1;
+  x.first_slot = w_lo + x.seg;
   return x;
 }
 
-template <int D>
+// Physical block for block (base + lane) of the piece; 0 past its end.
+__device__ __forceinline__ int fetch_chunk(const Piece& x, int base, int lane,
+                                           const DecodeParams& p) {
+  const int j = base + lane;
+  if (!x.valid || j >= x.nblk) return 0;
+  const int lb = x.blk0 + j;
+  int pb;
+  if (p.append && p.patch != nullptr && lb == x.lens0 / KVS_BLOCK_TOKENS && p.patch[x.item] >= 0)
+    pb = p.patch[x.item];
+  else
+    pb = lb < p.max_blocks ? p.tables[static_cast<int64_t>(x.item) * p.max_blocks + lb] : -1;
+  if (pb < 0 || pb >= p.num_blocks) {
+    flag_status(p.status, KVS_ERR_INVALID);
+    pb = 0;
+  }
+  return pb;
+}
+
+template <int D, int NT>
 __global__ void __launch_bounds__(kDecThreads, 1)
 paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
                     const __grid_constant__ CUtensorMap v_map, const DecodeParams p) {
-  using L = DecodeSmem<D>;
+  using L = DecodeLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
-  uint64_t* empty = full + kStages;
-  float* scratch = reinterpret_cast<float*>(smem + L::kScratchOff);
-  volatile int* flags = reinterpret_cast<volatile int*>(smem + L::kFlagOff);  // [0] abort, [1] last
-  int* prefix = reinterpret_cast<int*>(smem + L::kPrefixOff);
-
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int NS = p.n_stages;
   const int G = p.group;
+  uint8_t* my_stages = smem + warp * NS * L::kStageBytes;
+  uint8_t* my_q = smem + p.q_off + warp * 2 * p.q_stride;
+  uint64_t* my_full = reinterpret_cast<uint64_t*>(smem + p.bar_off) + warp * NS;
+  float* my_scr = reinterpret_cast<float*>(smem + p.scr_off) + warp * 2 * kMaxG;
+  int* prefix = reinterpret_cast<int*>(smem + p.idx_off);  // [batch + 1], in blocks
+  int* lens_s = prefix + (p.batch + 1);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    flags[0] = 0;
-    flags[1] = 0;
+    for (int i = 0; i < kWarps * NS; ++i) mbar_init(reinterpret_cast<uint64_t*>(smem + p.bar_off) + i, 1);
     fence_mbar_init();
   }
-  // prefix over items of (splits x heads); one warp, each lane a contiguous range
+  for (int b = threadIdx.x; b < p.batch; b += kDecThreads) lens_s[b] = p.lens[b];
+  __syncthreads();
+  // prefix over items of (blocks x heads); one warp, each lane a contiguous range
   if (warp == 0) {
     const int per = (p.batch + 31) / 32;
     const int b0 = lane * per;
     const int b1 = min(p.batch, b0 + per);
     int sum = 0;
-    for (int b = b0; b < b1; ++b) {
-      const int len = p.lens[b] + p.append;
-      const int ns = len > 0 ? (len + kSplitTokens - 1) / kSplitTokens : 0;
-      sum += ns * p.h_kv;
-    }
+    for (int b = b0; b < b1; ++b)
+      sum += (lens_s[b] + p.append + KVS_BLOCK_TOKENS - 1) / KVS_BLOCK_TOKENS * p.h_kv;
     int incl = sum;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -175,328 +218,366 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
     int run = incl - sum;
     for (int b = b0; b < b1; ++b) {
       prefix[b] = run;
-      const int len = p.lens[b] + p.append;
-      const int ns = len > 0 ? (len + kSplitTokens - 1) / kSplitTokens : 0;
-      run += ns * p.h_kv;
+      run += (lens_s[b] + p.append + KVS_BLOCK_TOKENS - 1) / KVS_BLOCK_TOKENS * p.h_kv;
     }
     if (lane == 31) prefix[p.batch] = incl;
   }
   __syncthreads();
-  const int total_units = prefix[p.batch];
+  const int64_t T = prefix[p.batch];
+  // W warps take part, never more than there are blocks, so that every range
+  // holds at least one block (the piece counts below rely on it)
+  const int W = static_cast<int>(T < gridDim.x * kWarps ? T : gridDim.x * kWarps);
+  const int w = blockIdx.x * kWarps + warp;
+  if (w >= W) return;
+  const int64_t r_lo = T * w / W;
+  const int64_t r_hi = T * (w + 1) / W;
 
-  if (warp == kConsumers) {
-    // ------------------------------------------------------------ producer
-    int g = 0;
-    for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
-      if (flags[0]) break;
-      Unit x = decode_unit(u, prefix, p.batch, p.h_kv, p.append);
-      const int lens0 = p.lens[x.item];
-      const int len = lens0 + p.append;
-      const int tok0 = x.split * kSplitTokens;
-      const int nblk = min(kSplitBlocks, (len - tok0 + KVS_BLOCK_TOKENS - 1) / KVS_BLOCK_TOKENS);
-      // every lane fetches one table entry of the unit
-      int phys = 0;
-      if (lane < nblk) {
-        const int lb = x.split * kSplitBlocks + lane;
-        int patch = -1;
-        if (p.append && p.patch != nullptr && lb == lens0 / KVS_BLOCK_TOKENS) patch = p.patch[x.item];
-        phys = patch >= 0 ? patch : p.tables[static_cast<int64_t>(x.item) * p.max_blocks + lb];
-        if (phys < 0 || phys >= p.num_blocks || lb >= p.max_blocks) {
-          flag_status(p.status, KVS_ERR_INVALID);
-          phys = 0;
-        }
-      }
-      for (int j = 0; j < nblk; ++j) {
-        const int pb = __shfl_sync(0xffffffffu, phys, j);
-        const int s = g % kStages;
-        const uint32_t ph = (g / kStages) & 1;
-        bool ok = true;
-        if (lane == 0) {
-          ok = mbar_wait(&empty[s], ph ^ 1);
-          if (!ok) {
-            flag_status(p.status, KVS_ERR_DEVICE_TIMEOUT);
-            flags[0] = 1;
-          } else {
-            mbar_arrive_expect_tx(&full[s], L::kStageBytes);
-            uint8_t* st = smem + s * L::kStageBytes;
-            const int row = (pb * p.h_kv + x.h) * KVS_BLOCK_TOKENS;
-#pragma unroll
-            for (int b = 0; b < D / 64; ++b) {
-              tma_load_2d(st + b * L::kBoxBytes, &k_map, &full[s], b * 64, row);
-              tma_load_2d(st + L::kBlockBytes + b * L::kBoxBytes, &v_map, &full[s], b * 64, row);
-            }
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
-        ++g;
-      }
-    }
-    // make sure no load of ours is still landing in shared memory when we leave
+  Piece cur = piece_at(r_lo, r_hi, T, W, prefix, lens_s, p);
+  Piece nxt = piece_at(cur.end, r_hi, T, W, prefix, lens_s, p);
+  // issue-side table chunks: tb (current chunk of the issuing piece), tb_n
+  // (its next chunk), tb_q (first chunk of the piece after cur)
+  int tb = fetch_chunk(cur, 0, lane, p);
+  int tb_n = fetch_chunk(cur, 32, lane, p);
+  int tb_q = fetch_chunk(nxt, 0, lane, p);
+  int tb_base = 0;
+
+  const uint32_t stages_u32 = smem_u32(my_stages);
+  int g_iss = 0, g_cons = 0;
+  bool iss_next = false;  // issue pointer in nxt (else in cur)
+  int iss_j = 0;          // next block of the issuing piece
+  int k = 0;              // index of cur among this warp's pieces (q buffer parity)
+  bool aborted = false;
+
+  auto issue = [&](const Piece& x, int j, int pb, int qpar) {
     if (lane == 0) {
-      const int first = g > kStages ? g - kStages : 0;
-      for (int gg = first; gg < g; ++gg)
-        if (!mbar_wait(&full[gg % kStages], (gg / kStages) & 1)) break;
-    }
-    return;
-  }
-
-  // -------------------------------------------------------------- consumers
-  const int ra = lane >> 2;   // rows (query heads of the group) ra and ra + 8
-  const int rb = ra + 8;
-  const int cq = (lane & 3) * 2;
-  const uint32_t ring = smem_u32(smem);
-  int g_base = 0;
-  for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
-    Unit x = decode_unit(u, prefix, p.batch, p.h_kv, p.append);
-    const int lens0 = p.lens[x.item];
-    const int len = lens0 + p.append;
-    const int tok_split = x.split * kSplitTokens;
-    const int nblk = min(kSplitBlocks, (len - tok_split + KVS_BLOCK_TOKENS - 1) / KVS_BLOCK_TOKENS);
-
-    // q fragments of the group's query rows (rows >= G are zero)
-    uint32_t qa[D / 16][4];
-    {
-      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-          p.q + (static_cast<int64_t>(x.item) * p.h_q + x.h * G) * D);
+      const int s = g_iss % NS;
+      uint8_t* st = my_stages + s * L::kStageBytes;
+      mbar_arrive_expect_tx(&my_full[s], L::kStageBytes + (j == 0 ? p.q_bytes : 0));
+      const int row = (pb * p.h_kv + x.h) * KVS_BLOCK_TOKENS;
 #pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        const int c0 = (ks * 16 + cq) >> 1;
-        qa[ks][0] = ra < G ? __ldg(qrow + ra * (D / 2) + c0) : 0u;
-        qa[ks][1] = rb < G ? __ldg(qrow + rb * (D / 2) + c0) : 0u;
-        qa[ks][2] = ra < G ? __ldg(qrow + ra * (D / 2) + c0 + 4) : 0u;
-        qa[ks][3] = rb < G ? __ldg(qrow + rb * (D / 2) + c0 + 4) : 0u;
+      for (int b = 0; b < D / 64; ++b) {
+        tma_load_2d(st + b * L::kBoxBytes, &k_map, &my_full[s], b * 64, row);
+        tma_load_2d(st + L::kBlockBytes + b * L::kBoxBytes, &v_map, &my_full[s], b * 64, row);
       }
+      if (j == 0)
+        bulk_load(my_q + qpar * p.q_stride,
+                  p.q + (static_cast<int64_t>(x.item) * p.h_q + x.h * G) * D, p.q_bytes,
+                  &my_full[s]);
     }
-    float o[D / 8][4];
-#pragma unroll
-    for (int nt = 0; nt < D / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-    float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
+    ++g_iss;
+  };
+  auto top_up = [&]() {
+    while (g_iss < g_cons + NS) {
+      const Piece& x = iss_next ? nxt : cur;
+      if (iss_j >= x.nblk) {
+        if (iss_next || !nxt.valid) break;
+        iss_next = true;  // move the issue pointer into the next piece
+        iss_j = 0;
+        tb = tb_q;
+        tb_n = fetch_chunk(nxt, 32, lane, p);
+        tb_base = 0;
+        continue;
+      }
+      if (iss_j - tb_base >= 32) {
+        tb = tb_n;
+        tb_base += 32;
+        tb_n = fetch_chunk(x, tb_base + 32, lane, p);
+      }
+      const int pb = __shfl_sync(0xffffffffu, tb, iss_j - tb_base);
+      issue(x, iss_j, pb, (k + (iss_next ? 1 : 0)) & 1);
+      ++iss_j;
+    }
+  };
 
-    for (int j = warp; j < nblk; j += kConsumers) {
-      const int g = g_base + j;
-      const int s = g % kStages;
-      const uint32_t ph = (g / kStages) & 1;
-      if (!flags[0]) {
-        bool ok = true;
-        if (lane == 0) {
-          ok = mbar_wait(&full[s], ph);
-          if (!ok) {
-            flag_status(p.status, KVS_ERR_DEVICE_TIMEOUT);
-            flags[0] = 1;
+  while (cur.valid && !aborted) {
+    top_up();
+    // NT n-tiles of 8 query heads; per thread: heads hc = nt*8 + 2*(lane%4) + {0,1}
+    uint32_t qb[D / 16][NT][2];  // B fragments of q^T (k = d, n = head)
+    float o[D / 16][NT][4];      // O^T accumulators (m = d, n = head)
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) o[mt][nt][0] = o[mt][nt][1] = o[mt][nt][2] = o[mt][nt][3] = 0.f;
+    float m_h[NT][2], l_h[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      m_h[nt][0] = m_h[nt][1] = -INFINITY;
+      l_h[nt][0] = l_h[nt][1] = 0.f;
+    }
+
+    for (int j = 0; j < cur.nblk; ++j) {
+      const int s = g_cons % NS;
+      if (!__all_sync(0xffffffffu, mbar_wait(&my_full[s], (g_cons / NS) & 1))) {
+        flag_status(p.status, KVS_ERR_DEVICE_TIMEOUT);
+        aborted = true;
+        break;
+      }
+      if (j == 0) {  // the group's q rows arrived with the piece's first block
+        const uint8_t* qs = my_q + (k & 1) * p.q_stride;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const int hd = nt * 8 + (lane >> 2);
+            const int off = hd * D * 2 + (ks * 16 + (lane & 3) * 2) * 2;
+            qb[ks][nt][0] = hd < G ? *reinterpret_cast<const uint32_t*>(qs + off) : 0u;
+            qb[ks][nt][1] = hd < G ? *reinterpret_cast<const uint32_t*>(qs + off + 16) : 0u;
           }
-        }
-        __syncwarp();
       }
-      const bool aborted = flags[0] != 0;
-      const uint32_t kst = ring + s * L::kStageBytes;
+      const uint32_t kst = stages_u32 + s * L::kStageBytes;
       const uint32_t vst = kst + L::kBlockBytes;
-      const int tok0 = tok_split + j * KVS_BLOCK_TOKENS;
+      const int tok0 = (cur.blk0 + j) * KVS_BLOCK_TOKENS;
 
       // the block holding the appended token: put the new row into the stage
       // and into the pool
-      if (p.append && !aborted && lens0 >= tok0 && lens0 < tok0 + KVS_BLOCK_TOKENS) {
-        const int slot = lens0 - tok0;
-        const int lb = lens0 / KVS_BLOCK_TOKENS;
-        int pb = (p.patch != nullptr && p.patch[x.item] >= 0)
-                     ? p.patch[x.item]
-                     : p.tables[static_cast<int64_t>(x.item) * p.max_blocks + lb];
-        const bool pb_ok = pb >= 0 && pb < p.num_blocks;
+      if (p.append && cur.lens0 >= tok0 && cur.lens0 < tok0 + KVS_BLOCK_TOKENS) {
+        const int slot = cur.lens0 - tok0;
+        const int lb = cur.lens0 / KVS_BLOCK_TOKENS;
+        const int pb = (p.patch != nullptr && p.patch[cur.item] >= 0)
+                           ? p.patch[cur.item]
+                           : p.tables[static_cast<int64_t>(cur.item) * p.max_blocks + lb];
         const int per = D / 8;  // 16-byte chunks per row
         if (lane < 2 * per) {
           const bool is_v = lane >= per;
           const int c = is_v ? lane - per : lane;
           const uint4* src = reinterpret_cast<const uint4*>(
-              (is_v ? p.v_new : p.k_new) + (static_cast<int64_t>(x.item) * p.h_kv + x.h) * D);
+              (is_v ? p.v_new : p.k_new) + (static_cast<int64_t>(cur.item) * p.h_kv + cur.h) * D);
           const uint4 val = __ldg(src + c);
-          uint8_t* st = smem + s * L::kStageBytes + (is_v ? L::kBlockBytes : 0);
+          uint8_t* st = my_stages + s * L::kStageBytes + (is_v ? L::kBlockBytes : 0);
           *reinterpret_cast<uint4*>(st + sw_off(slot, c)) = val;
-          if (pb_ok) {
+          if (pb >= 0 && pb < p.num_blocks) {
             uint4* dst = reinterpret_cast<uint4*>(
                 (is_v ? p.v_pool : p.k_pool) +
-                ((static_cast<int64_t>(pb) * p.h_kv + x.h) * KVS_BLOCK_TOKENS + slot) * D);
+                ((static_cast<int64_t>(pb) * p.h_kv + cur.h) * KVS_BLOCK_TOKENS + slot) * D);
             dst[c] = val;
           }
+          fence_proxy_async_smem();  // before a later TMA refill of this stage
         }
-        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      // the last block: slots past the length hold undefined bytes (possibly
+      // NaN patterns); P is 0 there, but 0 * NaN is NaN, so zero those V rows
+      if (tok0 + KVS_BLOCK_TOKENS > cur.len) {
+        const int valid = cur.len - tok0;
+        const int per = D / 8;
+        uint8_t* vs = my_stages + s * L::kStageBytes + L::kBlockBytes;
+        for (int idx = lane; idx < (KVS_BLOCK_TOKENS - valid) * per; idx += 32) {
+          const int r = valid + idx / per;
+          *reinterpret_cast<uint4*>(vs + sw_off(r, idx % per)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();  // before a later TMA refill of this stage
         __syncwarp();
       }
 
-      // S = q K^T for the 16 tokens of the block
-      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      {
-        const int mi = lane >> 3, rr = lane & 7;
-        const int tok = (mi >> 1) * 8 + rr;
+      // S^T = K q^T: rows = tokens (lane/4, lane/4 + 8), columns = heads.
+      // Two accumulator chains (even / odd k-steps) halve the dependent MMA chain.
+      float sa[NT][4], sb[NT][4];
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(kst + sw_off(tok, ks * 2 + (mi & 1)), b0, b1, b2, b3);
-          mma16816(sc[0], qa[ks], b0, b1);
-          mma16816(sc[1], qa[ks], b2, b3);
-        }
-      }
-      // online softmax (log2 domain); rows ra, rb; columns cq, cq+1, 8+cq, 9+cq
-      float mx_a = -INFINITY, mx_b = -INFINITY;
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int t = tok0 + nt * 8 + cq + e;
-          const bool valid = t < len;
-          sc[nt][e] = valid ? sc[nt][e] * p.scale_log2 : -INFINITY;
-          sc[nt][2 + e] = valid ? sc[nt][2 + e] * p.scale_log2 : -INFINITY;
-          mx_a = fmaxf(mx_a, sc[nt][e]);
-          mx_b = fmaxf(mx_b, sc[nt][2 + e]);
-        }
-      }
-      mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
-      mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
-      mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
-      mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
-      const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
-      const float al_a = ex2(m_a - mn_a), al_b = ex2(m_b - mn_b);
-      m_a = mn_a;
-      m_b = mn_b;
-      float ps_a = 0.f, ps_b = 0.f;
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          sc[nt][e] = ex2(sc[nt][e] - mn_a);
-          sc[nt][2 + e] = ex2(sc[nt][2 + e] - mn_b);
-          ps_a += sc[nt][e];
-          ps_b += sc[nt][2 + e];
-        }
-      }
-      l_a = l_a * al_a + ps_a;
-      l_b = l_b * al_b + ps_b;
-#pragma unroll
-      for (int nt = 0; nt < D / 8; ++nt) {
-        o[nt][0] *= al_a;
-        o[nt][1] *= al_a;
-        o[nt][2] *= al_b;
-        o[nt][3] *= al_b;
-      }
-      uint32_t pa[4];
-      pa[0] = pack_bf16x2(sc[0][0], sc[0][1]);
-      pa[1] = pack_bf16x2(sc[0][2], sc[0][3]);
-      pa[2] = pack_bf16x2(sc[1][0], sc[1][1]);
-      pa[3] = pack_bf16x2(sc[1][2], sc[1][3]);
-      // O += P V
+        for (int e = 0; e < 4; ++e) sa[nt][e] = sb[nt][e] = 0.f;
       {
         const int mi = lane >> 3, rr = lane & 7;
         const int tok = (mi & 1) * 8 + rr;
 #pragma unroll
-        for (int np = 0; np < D / 16; ++np) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(vst + sw_off(tok, np * 2 + (mi >> 1)), b0, b1, b2, b3);
-          mma16816(o[2 * np], pa, b0, b1);
-          mma16816(o[2 * np + 1], pa, b2, b3);
+        for (int ks = 0; ks < D / 16; ++ks) {
+          uint32_t a[4];
+          ldsm_x4(kst + sw_off(tok, ks * 2 + (mi >> 1)), a[0], a[1], a[2], a[3]);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            if (ks & 1) mma16816(sb[nt], a, qb[ks][nt][0], qb[ks][nt][1]);
+            else mma16816(sa[nt], a, qb[ks][nt][0], qb[ks][nt][1]);
+          }
+        }
+      }
+      // online softmax per head (log2 domain): a head's 16 scores sit in the 8
+      // lanes with the same lane % 4 (rows lane/4 and lane/4 + 8)
+      const bool v0 = tok0 + (lane >> 2) < cur.len;
+      const bool v1 = tok0 + (lane >> 2) + 8 < cur.len;
+      uint32_t pb0[NT], pb1[NT];
+      bool rescale = false;
+      float al[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        float s0[2], s1[2], mx[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          s0[e] = v0 ? (sa[nt][e] + sb[nt][e]) * p.scale_log2 : -INFINITY;
+          s1[e] = v1 ? (sa[nt][2 + e] + sb[nt][2 + e]) * p.scale_log2 : -INFINITY;
+          mx[e] = fmaxf(s0[e], s1[e]);
+          mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 4));
+          mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 8));
+          mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 16));
+          const float mn = fmaxf(m_h[nt][e], mx[e]);
+          al[nt][e] = ex2(m_h[nt][e] - mn);
+          rescale |= mn != m_h[nt][e];
+          m_h[nt][e] = mn;
+          s0[e] = ex2(s0[e] - mn);
+          s1[e] = ex2(s1[e] - mn);
+          l_h[nt][e] = l_h[nt][e] * al[nt][e] + (s0[e] + s1[e]);
+        }
+        // P^T (tokens x heads) -> B fragments (k = tokens, n = heads)
+        pb0[nt] = movmatrix_t(pack_bf16x2(s0[0], s0[1]));
+        pb1[nt] = movmatrix_t(pack_bf16x2(s1[0], s1[1]));
+      }
+      if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            o[mt][nt][0] *= al[nt][0];
+            o[mt][nt][1] *= al[nt][1];
+            o[mt][nt][2] *= al[nt][0];
+            o[mt][nt][3] *= al[nt][1];
+          }
+      }
+      // O^T += V^T P^T: A = V^T (m = d, k = tokens) by ldmatrix.trans
+      {
+        const int mi = lane >> 3, rr = lane & 7;
+        const int tok = (mi >> 1) * 8 + rr;
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+          uint32_t a[4];
+          ldsm_x4_t(vst + sw_off(tok, mt * 2 + (mi & 1)), a[0], a[1], a[2], a[3]);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma16816(o[mt][nt], a, pb0[nt], pb1[nt]);
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
+      ++g_cons;
+      top_up();
     }
-    g_base += nblk;
+    if (aborted) break;
 
-    // ---- merge the consumer warps of this unit ----
-    l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
-    l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
-    l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
-    l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
-    float* wsc = scratch + warp * kMaxG * (D + 2);
-    if (ra < G) {
+    // ---- the piece's result ----
+    // per head: l summed over the 8 lanes sharing lane % 4
 #pragma unroll
-      for (int nt = 0; nt < D / 8; ++nt) {
-        wsc[ra * (D + 2) + nt * 8 + cq] = o[nt][0];
-        wsc[ra * (D + 2) + nt * 8 + cq + 1] = o[nt][1];
-      }
-      if ((lane & 3) == 0) {
-        wsc[ra * (D + 2) + D] = m_a;
-        wsc[ra * (D + 2) + D + 1] = l_a;
-      }
-    }
-    if (rb < G) {
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int nt = 0; nt < D / 8; ++nt) {
-        wsc[rb * (D + 2) + nt * 8 + cq] = o[nt][2];
-        wsc[rb * (D + 2) + nt * 8 + cq + 1] = o[nt][3];
+      for (int e = 0; e < 2; ++e) {
+        l_h[nt][e] += __shfl_xor_sync(0xffffffffu, l_h[nt][e], 4);
+        l_h[nt][e] += __shfl_xor_sync(0xffffffffu, l_h[nt][e], 8);
+        l_h[nt][e] += __shfl_xor_sync(0xffffffffu, l_h[nt][e], 16);
       }
-      if ((lane & 3) == 0) {
-        wsc[rb * (D + 2) + D] = m_b;
-        wsc[rb * (D + 2) + D + 1] = l_b;
-      }
-    }
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
-
-    const int out_row0 = x.item * p.h_q + x.h * G;
-    const int64_t part_slot = (static_cast<int64_t>(x.item) * p.h_kv + x.h) * p.s_max + x.split;
-    float* part = p.ws_part + part_slot * G * (D + 2);
-    for (int e = threadIdx.x; e < G * D; e += kConsumers * 32) {
-      const int r = e / D, c = e - r * D;
-      float M = -INFINITY;
+    const int64_t out_row0 = static_cast<int64_t>(cur.item) * p.h_q + cur.h * G;
+    const int dr = lane >> 2;  // d offset inside an m-tile (and + 8)
+    if (cur.npieces == 1) {
 #pragma unroll
-      for (int w = 0; w < kConsumers; ++w)
-        M = fmaxf(M, scratch[w * kMaxG * (D + 2) + r * (D + 2) + D]);
-      float Lsum = 0.f, O = 0.f;
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int w = 0; w < kConsumers; ++w) {
-        const float* ws = scratch + w * kMaxG * (D + 2) + r * (D + 2);
-        const float f = ex2(ws[D] - M);
-        Lsum += ws[D + 1] * f;
-        O += ws[c] * f;
-      }
-      if (x.ns == 1) {
-        const float val = O / Lsum;
-        const uint32_t b = pack_bf16x2(val, 0.f);
-        p.out[static_cast<int64_t>(out_row0 + r) * D + c] = static_cast<uint16_t>(b & 0xFFFFu);
-      } else {
-        part[r * D + c] = O;
-        if (c == 0) {
-          part[G * D + r] = M;
-          part[G * D + G + r] = Lsum;
-        }
-      }
-    }
-    if (x.ns > 1) {
-      __threadfence();
-      asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
-      if (threadIdx.x == 0) {
-        const int old = atomicAdd(p.ws_count + x.item * p.h_kv + x.h, 1);
-        flags[1] = (old == x.ns - 1) ? 1 : 0;
-      }
-      asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
-      if (flags[1]) {
-        __threadfence();
-        const float* base = p.ws_part + (static_cast<int64_t>(x.item) * p.h_kv + x.h) * p.s_max *
-                                            G * (D + 2);
-        for (int e = threadIdx.x; e < G * D; e += kConsumers * 32) {
-          const int r = e / D, c = e - r * D;
-          float M = -INFINITY;
-          for (int sp = 0; sp < x.ns; ++sp)
-            M = fmaxf(M, __ldcg(base + static_cast<int64_t>(sp) * G * (D + 2) + G * D + r));
-          float Lsum = 0.f, O = 0.f;
-          for (int sp = 0; sp < x.ns; ++sp) {
-            const float* pr = base + static_cast<int64_t>(sp) * G * (D + 2);
-            const float f = ex2(__ldcg(pr + G * D + r) - M);
-            Lsum += __ldcg(pr + G * D + G + r) * f;
-            O += __ldcg(pr + r * D + c) * f;
+        for (int e = 0; e < 2; ++e) {
+          const int hd = nt * 8 + (lane & 3) * 2 + e;
+          if (hd < G) {
+            const float il = 1.0f / l_h[nt][e];
+            uint16_t* orow = p.out + (out_row0 + hd) * D;
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+              orow[mt * 16 + dr] =
+                  static_cast<uint16_t>(pack_bf16x2(o[mt][nt][e] * il, 0.f) & 0xFFFFu);
+              orow[mt * 16 + dr + 8] =
+                  static_cast<uint16_t>(pack_bf16x2(o[mt][nt][2 + e] * il, 0.f) & 0xFFFFu);
+            }
           }
-          const uint32_t b = pack_bf16x2(O / Lsum, 0.f);
-          p.out[static_cast<int64_t>(out_row0 + r) * D + c] = static_cast<uint16_t>(b & 0xFFFFu);
         }
-        if (threadIdx.x == 0) p.ws_count[x.item * p.h_kv + x.h] = 0;
+    } else {
+      const int rec = G * (D + 2);
+      float* part = p.ws_part + static_cast<int64_t>(w + cur.seg) * rec;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int hd = nt * 8 + (lane & 3) * 2 + e;
+          if (hd < G) {
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+              part[hd * D + mt * 16 + dr] = o[mt][nt][e];
+              part[hd * D + mt * 16 + dr + 8] = o[mt][nt][2 + e];
+            }
+            if (lane < 4) {
+              part[G * D + hd] = m_h[nt][e];
+              part[G * D + G + hd] = l_h[nt][e];
+            }
+          }
+        }
+      __threadfence();
+      __syncwarp();
+      int last = 0;
+      if (lane == 0) last = atomicAdd(p.ws_count + cur.seg, 1) == cur.npieces - 1;
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (last) {
+        __threadfence();
+        const float* base = p.ws_part + static_cast<int64_t>(cur.first_slot) * rec;
+        const int np = cur.npieces;
+        // row maxima and normalisers over the pieces
+        for (int r = 0; r < G; ++r) {
+          float mx = -INFINITY;
+          for (int sp = lane; sp < np; sp += 32)
+            mx = fmaxf(mx, __ldcg(base + static_cast<int64_t>(sp) * rec + G * D + r));
+#pragma unroll
+          for (int o2 = 16; o2 > 0; o2 >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+          float sum = 0.f;
+          for (int sp = lane; sp < np; sp += 32) {
+            const float* pr = base + static_cast<int64_t>(sp) * rec;
+            sum += __ldcg(pr + G * D + G + r) * ex2(__ldcg(pr + G * D + r) - mx);
+          }
+#pragma unroll
+          for (int o2 = 16; o2 > 0; o2 >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o2);
+          if (lane == 0) {
+            my_scr[r] = mx;
+            my_scr[kMaxG + r] = sum;
+          }
+        }
+        __syncwarp();
+        for (int e4 = lane; e4 < G * D / 4; e4 += 32) {
+          const int r = (e4 * 4) / D;
+          const int c = e4 * 4 - r * D;
+          const float mx = my_scr[r];
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int sp = 0; sp < np; ++sp) {
+            const float* pr = base + static_cast<int64_t>(sp) * rec;
+            const float f = ex2(__ldcg(pr + G * D + r) - mx);
+            const float4 v4 = __ldcg(reinterpret_cast<const float4*>(pr + r * D + c));
+            acc.x += f * v4.x;
+            acc.y += f * v4.y;
+            acc.z += f * v4.z;
+            acc.w += f * v4.w;
+          }
+          const float il = 1.0f / my_scr[kMaxG + r];
+          uint2 w2;
+          w2.x = pack_bf16x2(acc.x * il, acc.y * il);
+          w2.y = pack_bf16x2(acc.z * il, acc.w * il);
+          *reinterpret_cast<uint2*>(p.out + (out_row0 + r) * D + c) = w2;
+        }
+        __syncwarp();
+        if (lane == 0) p.ws_count[cur.seg] = 0;
       }
     }
-    // table patch and length bookkeeping, once per item
-    if (threadIdx.x == 0 && x.split == 0 && x.h == 0) {
-      if (p.append && p.patch != nullptr && p.patch[x.item] >= 0)
-        p.tables[static_cast<int64_t>(x.item) * p.max_blocks + lens0 / KVS_BLOCK_TOKENS] =
-            p.patch[x.item];
-      if (p.lens_next != nullptr) p.lens_next[x.item] = len;
+    // table patch and length bookkeeping, once per item (its head-0 segment start)
+    if (lane == 0 && cur.blk0 == 0 && cur.h == 0) {
+      if (p.append && p.patch != nullptr && p.patch[cur.item] >= 0)
+        p.tables[static_cast<int64_t>(cur.item) * p.max_blocks + cur.lens0 / KVS_BLOCK_TOKENS] =
+            p.patch[cur.item];
+      if (p.lens_next != nullptr) p.lens_next[cur.item] = cur.len;
     }
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
+
+    // ---- next piece ----
+    ++k;
+    cur = nxt;
+    if (!iss_next) {  // nothing of the new cur was issued yet (cannot happen
+      iss_j = 0;      // while it is valid, kept for safety)
+      tb = tb_q;
+      tb_n = fetch_chunk(cur, 32, lane, p);
+      tb_base = 0;
+    }
+    iss_next = false;
+    nxt = piece_at(cur.end, r_hi, T, W, prefix, lens_s, p);
+    tb_q = fetch_chunk(nxt, 0, lane, p);
   }
+  // leave no load of ours landing in shared memory after we return
+  if (lane == 0)
+    for (int g = g_cons; g < g_iss; ++g)
+      if (!mbar_wait(&my_full[g % NS], (g / NS) & 1)) break;
+  __syncwarp();
 }
 
 struct MapCache {
@@ -522,7 +603,9 @@ bool pool_map(MapCache& c, const void* pool, int num_blocks, int h_kv, int d) {
   return true;
 }
 
-int s_max_for(int max_len) { return (max_len + kSplitTokens - 1) / kSplitTokens; }
+int64_t counter_bytes(int batch, int h_kv) {
+  return (static_cast<int64_t>(batch) * h_kv * 4 + 255) / 256 * 256;
+}
 
 int sm_count_dec() {
   static int n = 0;
@@ -535,18 +618,51 @@ int sm_count_dec() {
   return n;
 }
 
+constexpr int kSmemLimit = 232448;
+
+// Shared-memory plan for a launch; returns the bytes, 0 if it cannot fit.
 template <int D>
-kvs_status launch_decode(const DecodeParams& prm, const CUtensorMap& km, const CUtensorMap& vm,
-                         int grid, cudaStream_t stream) {
-  const size_t smem = DecodeSmem<D>::bytes(prm.batch);
+size_t plan_smem(DecodeParams& prm) {
+  using L = DecodeLayout<D>;
+  prm.q_bytes = prm.group * D * 2;
+  prm.q_stride = (prm.q_bytes + 127) / 128 * 128;
+  for (int ns = 3; ns >= 1; --ns) {
+    size_t off = static_cast<size_t>(kWarps) * ns * L::kStageBytes;
+    const size_t q_off = off;
+    off += static_cast<size_t>(kWarps) * 2 * prm.q_stride;
+    const size_t bar_off = off;
+    off += static_cast<size_t>(kWarps) * ns * 8;
+    const size_t scr_off = off;
+    off += static_cast<size_t>(kWarps) * 2 * kMaxG * 4;
+    const size_t idx_off = off;
+    off += static_cast<size_t>(2 * prm.batch + 1) * 4;
+    const size_t total = off + 1024;
+    if (total <= kSmemLimit) {
+      prm.n_stages = ns;
+      prm.q_off = static_cast<int>(q_off);
+      prm.bar_off = static_cast<int>(bar_off);
+      prm.scr_off = static_cast<int>(scr_off);
+      prm.idx_off = static_cast<int>(idx_off);
+      return total;
+    }
+  }
+  return 0;
+}
+
+template <int D, int NT>
+kvs_status launch_decode(DecodeParams& prm, const CUtensorMap& km, const CUtensorMap& vm,
+                         cudaStream_t stream) {
+  const size_t smem = plan_smem<D>(prm);
+  if (smem == 0) return fail(KVS_ERR_UNSUPPORTED, "kvs_paged_decode: shared-memory plan does not fit");
   static bool configured = false;
   if (!configured) {
-    KVS_CUDA(cudaFuncSetAttribute(paged_decode_kernel<D>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, 232448),
+    KVS_CUDA(cudaFuncSetAttribute(paged_decode_kernel<D, NT>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit),
              "kvs_paged_decode: raising the shared-memory limit");
     configured = true;
   }
-  paged_decode_kernel<D><<<grid, kDecThreads, smem, stream>>>(km, vm, prm);
+  const int grid = sm_count_dec() < kMaxGrid ? sm_count_dec() : kMaxGrid;
+  paged_decode_kernel<D, NT><<<grid, kDecThreads, smem, stream>>>(km, vm, prm);
   KVS_CHECK_LAUNCH("kvs_paged_decode");
   return KVS_OK;
 }
@@ -556,44 +672,46 @@ kvs_status launch_decode(const DecodeParams& prm, const CUtensorMap& km, const C
 
 extern "C" {
 
-size_t kvs_paged_decode_workspace_size(int32_t batch, int32_t h_q, int32_t h_kv, int32_t d,
-                                       int32_t max_len) {
-  if (batch <= 0 || h_kv <= 0 || h_q <= 0 || d <= 0 || max_len <= 0) return 0;
+size_t kvs_paged_decode_workspace_size(int32_t batch, int32_t h_q, int32_t h_kv, int32_t d) {
+  if (batch <= 0 || h_kv <= 0 || h_q <= 0 || d <= 0) return 0;
   const int64_t G = h_q / h_kv;
-  const int64_t counters = static_cast<int64_t>(batch) * h_kv;
-  const int64_t counter_bytes = (counters * 4 + 255) / 256 * 256;
-  const int64_t parts = counters * kvs::s_max_for(max_len) * G * (d + 2);
-  return static_cast<size_t>(counter_bytes + parts * 4);
+  // one partial slot per (warp, segment it touches): slot = warp + segment
+  const int64_t slots = static_cast<int64_t>(kvs::kMaxGrid) * kvs::kWarps +
+                        static_cast<int64_t>(batch) * h_kv;
+  return static_cast<size_t>(kvs::counter_bytes(batch, h_kv) + slots * G * (d + 2) * 4);
 }
 
 kvs_status kvs_paged_decode(const kvs_bf16* q, const kvs_bf16* k_new, const kvs_bf16* v_new,
                             kvs_bf16* k_pool, kvs_bf16* v_pool, int32_t num_blocks,
                             int32_t* block_tables, int32_t max_blocks, const int32_t* table_patch,
-                            const int32_t* lens, int32_t* lens_next, int32_t batch,
-                            int32_t max_len, int32_t h_q, int32_t h_kv, int32_t d, float scale,
-                            kvs_bf16* out, void* workspace, size_t workspace_bytes,
-                            int32_t* status, kvs_stream stream) {
+                            const int32_t* lens, int32_t* lens_next, int32_t batch, int32_t h_q,
+                            int32_t h_kv, int32_t d, float scale, kvs_bf16* out, void* workspace,
+                            size_t workspace_bytes, int32_t* status, kvs_stream stream) {
   KVS_REQUIRE(batch >= 0, "kvs_paged_decode: negative batch");
   if (batch == 0) return KVS_OK;
   KVS_REQUIRE(q && k_pool && v_pool && block_tables && lens && out && workspace,
               "kvs_paged_decode: NULL pointer");
   KVS_REQUIRE((k_new == nullptr) == (v_new == nullptr),
               "kvs_paged_decode: k_new and v_new must both be given or both be NULL");
+  KVS_REQUIRE(lens_next == nullptr || lens_next != lens,
+              "kvs_paged_decode: lens_next must not alias lens");
   KVS_SUPPORTED(d == 64 || d == 128, "kvs_paged_decode: d = %d (supported: 64, 128)", d);
   KVS_REQUIRE(h_kv > 0 && h_q > 0 && h_q % h_kv == 0, "kvs_paged_decode: bad head counts");
   KVS_SUPPORTED(h_q / h_kv <= kvs::kMaxG, "kvs_paged_decode: group size %d > %d", h_q / h_kv,
                 kvs::kMaxG);
-  KVS_REQUIRE(num_blocks > 0 && max_blocks > 0 && max_len > 0, "kvs_paged_decode: bad sizes");
+  KVS_SUPPORTED(batch <= kvs::kMaxBatch, "kvs_paged_decode: batch %d > %d", batch,
+                kvs::kMaxBatch);
+  KVS_REQUIRE(num_blocks > 0 && max_blocks > 0, "kvs_paged_decode: bad sizes");
   KVS_REQUIRE(static_cast<int64_t>(num_blocks) * h_kv * KVS_BLOCK_TOKENS < (1ll << 31),
               "kvs_paged_decode: pool too large for 32-bit TMA row coordinates");
-  KVS_REQUIRE(static_cast<int64_t>(max_blocks) * KVS_BLOCK_TOKENS >= max_len,
-              "kvs_paged_decode: max_len %d exceeds the table capacity", max_len);
   KVS_REQUIRE((reinterpret_cast<uintptr_t>(k_pool) & 15) == 0 &&
                   (reinterpret_cast<uintptr_t>(v_pool) & 15) == 0 &&
-                  (reinterpret_cast<uintptr_t>(q) & 15) == 0,
-              "kvs_paged_decode: q and pools must be 16-byte aligned");
-  KVS_REQUIRE(batch <= 8192, "kvs_paged_decode: batch %d > 8192", batch);
-  const size_t need = kvs_paged_decode_workspace_size(batch, h_q, h_kv, d, max_len);
+                  (reinterpret_cast<uintptr_t>(q) & 15) == 0 &&
+                  (reinterpret_cast<uintptr_t>(out) & 15) == 0,
+              "kvs_paged_decode: q, out and pools must be 16-byte aligned");
+  const int64_t G = h_q / h_kv;
+  const int64_t cbytes = kvs::counter_bytes(batch, h_kv);
+  const size_t need = kvs_paged_decode_workspace_size(batch, h_q, h_kv, d);
   KVS_REQUIRE(workspace_bytes >= need, "kvs_paged_decode: workspace %zu bytes < %zu needed",
               workspace_bytes, need);
   static thread_local kvs::MapCache kc, vc;
@@ -612,26 +730,24 @@ kvs_status kvs_paged_decode(const kvs_bf16* q, const kvs_bf16* k_new, const kvs_
   prm.lens = lens;
   prm.lens_next = lens_next;
   prm.out = out;
-  const int64_t counters = static_cast<int64_t>(batch) * h_kv;
-  const int64_t counter_bytes = (counters * 4 + 255) / 256 * 256;
   prm.ws_count = static_cast<int32_t*>(workspace);
-  prm.ws_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + counter_bytes);
+  prm.ws_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + cbytes);
   prm.status = status;
   prm.batch = batch;
   prm.max_blocks = max_blocks;
   prm.num_blocks = num_blocks;
   prm.h_q = h_q;
   prm.h_kv = h_kv;
-  prm.group = h_q / h_kv;
-  prm.s_max = kvs::s_max_for(max_len);
+  prm.group = static_cast<int>(G);
   prm.append = k_new != nullptr ? 1 : 0;
   prm.scale_log2 = scale * kvs::kLog2e;
-  // persistent grid: one CTA per SM, never more CTAs than units
-  const int64_t units_ub = counters * prm.s_max;
-  const int grid = static_cast<int>(units_ub < kvs::sm_count_dec() ? units_ub : kvs::sm_count_dec());
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (d == 128) return kvs::launch_decode<128>(prm, kc.map, vc.map, grid, st);
-  return kvs::launch_decode<64>(prm, kc.map, vc.map, grid, st);
+  if (G <= 8) {
+    if (d == 128) return kvs::launch_decode<128, 1>(prm, kc.map, vc.map, st);
+    return kvs::launch_decode<64, 1>(prm, kc.map, vc.map, st);
+  }
+  if (d == 128) return kvs::launch_decode<128, 2>(prm, kc.map, vc.map, st);
+  return kvs::launch_decode<64, 2>(prm, kc.map, vc.map, st);
 }
 
 }  // extern "C"

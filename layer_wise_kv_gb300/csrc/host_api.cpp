@@ -189,12 +189,13 @@ int32_t kvs_alloc_free_list(const kvs_allocator* a, int32_t* buf, int32_t cap) {
 kvs_status kvs_decode_prepare(kvs_allocator* a, int32_t* tables, int32_t max_blocks,
                               const int32_t* lens, int32_t n_items, int32_t* patch,
                               int32_t* cow_src, int32_t* cow_dst, int32_t* n_cow,
-                              int32_t* n_done) {
+                              int32_t* n_patch, int32_t* n_done) {
   KVS_REQUIRE(a != nullptr && tables != nullptr && lens != nullptr && patch != nullptr &&
                   cow_src != nullptr && cow_dst != nullptr && n_cow != nullptr,
               "kvs_decode_prepare: NULL argument");
   KVS_REQUIRE(n_items >= 0 && max_blocks > 0, "kvs_decode_prepare: bad sizes");
   *n_cow = 0;
+  if (n_patch) *n_patch = 0;
   if (n_done) *n_done = 0;
   for (int32_t i = 0; i < n_items; ++i) {
     const int32_t len = lens[i];
@@ -210,6 +211,7 @@ kvs_status kvs_decode_prepare(kvs_allocator* a, int32_t* tables, int32_t max_blo
       a->ref[b] = 1;
       row[slot] = b;
       patch[i] = b;
+      if (n_patch) ++*n_patch;
     } else {
       const int32_t last = row[slot];
       KVS_REQUIRE(a->valid(last) && a->ref[last] > 0,
@@ -223,6 +225,7 @@ kvs_status kvs_decode_prepare(kvs_allocator* a, int32_t* tables, int32_t max_blo
         --a->ref[last];
         row[slot] = nb;
         patch[i] = nb;
+        if (n_patch) ++*n_patch;
         cow_src[*n_cow] = last;
         cow_dst[*n_cow] = nb;
         ++*n_cow;

@@ -8,18 +8,23 @@
 // maximum and l (small outputs, slight cost) so the scoring pass can rebuild
 // softmax probabilities without a second attention pass.
 //
-// Kernel layout (one CTA per (query head, 128-query tile, sequence)):
-//   warp 4      TMA producer: Q tile once, then K_j / V_j tiles (128 keys x d,
-//               128-byte swizzle) into a 2-stage ring each.
-//   warp 5      MMA issuer (one thread): S_j = Q K_j^T into TMEM buffer j%2
-//               (M=128, N=128, K=d), and O += P_{j-1} V_{j-1} with P read from
-//               TMEM (the A operand) and V from shared memory (MN-major B).
-//   warps 0-3   softmax warpgroup, one thread per query row: load S_j from
-//               TMEM, causal mask on the diagonal tile, online max in the log2
-//               domain with lazy rescaling (O and l are rescaled only when the
-//               row maximum grows by more than 8, i.e. a factor of 256), P as
-//               bf16 written back over S_j in TMEM; finally O / l, m and l.
-// TMEM: S buffers at columns [0,128) and [128,256), O at [256, 256+d).
+// Kernel layout (one CTA per (query head, pair of 128-query tiles, sequence);
+// the lower tile A and the upper tile B share every K/V tile):
+//   warp 8      TMA producer: Q_A and Q_B once, then K_j / V_j tiles (128 keys
+//               x d, 128-byte swizzle) into 2-stage rings.
+//   warp 9      MMA issuer (one thread): S_t = Q_t K_j^T into TMEM (M=N=128,
+//               K=d) and O_t += P_t V_j with P_t read from TMEM as the A operand
+//               and V_j as an MN-major shared-memory B operand.  Issue order
+//               PV_A(j), S_A(j+1), PV_B(j), S_B(j+1): the tensor core works on
+//               one tile while the other tile's softmax runs.
+//   warps 0-3   softmax warpgroup of tile A, warps 4-7 of tile B; one thread
+//               per query row: two passes over its S row in TMEM (row maximum,
+//               then exponentials), causal mask on the diagonal tile, online
+//               maximum in the log2 domain with lazy rescaling (O and l are
+//               rescaled only when the row maximum grows by more than 8, a
+//               factor of 256), P as bf16 written back over S in TMEM; finally
+//               O / l, m and l.
+// TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
 // Every wait on an mbarrier is bounded; on a timeout the kernel records
 // KVS_ERR_DEVICE_TIMEOUT, drains its own copies and MMAs, frees TMEM and ends.
 #include <cuda_runtime.h>
@@ -31,10 +36,10 @@
 namespace kvs {
 namespace {
 
-constexpr int kBM = 128;
-constexpr int kBN = 128;
+constexpr int kBM = 128;            // rows per query tile
+constexpr int kBN = 128;            // keys per K/V tile
 constexpr int kStagesKV = 2;
-constexpr int kPrefillThreads = 192;
+constexpr int kPrefillThreads = 320;
 constexpr float kLog2eP = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -45,7 +50,7 @@ struct PrefillParams {
   float* l;
   const int32_t* cu_seqlens;
   int32_t* status;
-  int total, h_q, h_kv, group, n_qtiles_max;
+  int total, h_q, h_kv, group, n_pairs_max;
   float scale_log2;
 };
 
@@ -53,14 +58,14 @@ template <int D>
 struct PrefillSmem {
   static constexpr int kTile = kBN * D * 2;  // one 128 x D bf16 tile = D/64 chunks of 16 KB
   static constexpr int kChunk = 128 * 128;
-  // V ring first (see the note on descriptor reach), then K ring, then Q.
+  // V ring first (an MN-major descriptor reaches furthest), then K ring, Q_A, Q_B.
   static constexpr int kV = 0;
   static constexpr int kK = kV + kStagesKV * kTile;
   static constexpr int kQ = kK + kStagesKV * kTile;
-  static constexpr int kBar = kQ + kTile;
+  static constexpr int kBar = kQ + 2 * kTile;
   // barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2],
-  // p_full[2], o_done, drain
-  static constexpr int kNumBars = 1 + 2 * kStagesKV * 2 + 2 + 2 + 2;
+  // p_full[2], o_done[2], drain
+  static constexpr int kNumBars = 1 + 4 * kStagesKV + 2 + 2 + 2 + 1;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr size_t kBytes = 1024 + kMisc + 16;
 };
@@ -80,10 +85,10 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
   uint64_t* k_empty = k_full + kStagesKV;
   uint64_t* v_full = k_empty + kStagesKV;
   uint64_t* v_empty = v_full + kStagesKV;
-  uint64_t* s_full = v_empty + kStagesKV;
-  uint64_t* p_full = s_full + 2;
-  uint64_t* o_done = p_full + 2;
-  uint64_t* drain = o_done + 1;
+  uint64_t* s_full = v_empty + kStagesKV;  // [tile]
+  uint64_t* p_full = s_full + 2;           // [tile]
+  uint64_t* o_done = p_full + 2;           // [tile]
+  uint64_t* drain = o_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
 
@@ -91,11 +96,12 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
   const int b = blockIdx.z;   // sequence
   const int seq0 = p.cu_seqlens[b];
   const int n = p.cu_seqlens[b + 1] - seq0;
-  const int ntiles = (n + kBM - 1) / kBM;
-  const int qt = ntiles - 1 - static_cast<int>(blockIdx.y);  // longest tiles first
-  if (qt < 0) return;
-  const int q0 = qt * kBM;       // first query of the tile (within the sequence)
-  const int nkv = qt + 1;        // causal: key tiles 0 .. qt
+  const int npairs = (n + 2 * kBM - 1) / (2 * kBM);
+  const int pr = npairs - 1 - static_cast<int>(blockIdx.y);  // longest pairs first
+  if (pr < 0) return;
+  const int q0 = pr * 2 * kBM;   // first query of tile A (within the sequence)
+  const int nkv_a = 2 * pr + 1;  // causal: key tiles 0 .. 2pr for tile A
+  const int nkv_b = 2 * pr + 2;  //         key tiles 0 .. 2pr+1 for tile B
   const int hk = g / p.group;    // KV head
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -111,11 +117,11 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&s_full[s], 1);
-      mbar_init(&p_full[s], kBM);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], kBM);
+      mbar_init(&o_done[t], 1);
     }
-    mbar_init(o_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -124,22 +130,24 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_o = tmem + 256;
 
   auto fail_timeout = [&]() {
     flag_status(p.status, KVS_ERR_DEVICE_TIMEOUT);
     *abort_flag = 1;
   };
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int issued_k = 0, issued_v = 0;
-      mbar_arrive_expect_tx(q_full, L::kTile);
+      mbar_arrive_expect_tx(q_full, 2 * L::kTile);
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c)
-        tma_load_3d(smem + L::kQ + c * L::kChunk, &q_map, q_full, c * 64, g, seq0 + q0);
-      for (int j = 0; j < nkv && !*abort_flag; ++j) {
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(smem + L::kQ + t * L::kTile + c * L::kChunk, &q_map, q_full, c * 64, g,
+                      seq0 + q0 + t * kBM);
+      for (int j = 0; j < nkv_b && !*abort_flag; ++j) {
         const int s = j % kStagesKV;
         const uint32_t ph = (j / kStagesKV) & 1;
         const int tok = seq0 + j * kBN;
@@ -165,52 +173,78 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
       for (int j = issued_v > kStagesKV ? issued_v - kStagesKV : 0; j < issued_v; ++j)
         if (!mbar_wait(&v_full[j % kStagesKV], (j / kStagesKV) & 1)) break;
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, 0);
       const uint32_t idesc_o = idesc_bf16_f32(kBM, D, 1);
       const uint32_t qa = smem_u32(smem + L::kQ);
       bool ok = mbar_wait(q_full, 0);
-      if (!ok) fail_timeout();
-      auto issue_pv = [&](int jj) -> bool {
-        const int pb = jj & 1;
-        if (!mbar_wait(&p_full[pb], (jj >> 1) & 1)) return false;
-        const int sv = jj % kStagesKV;
-        if (!mbar_wait(&v_full[sv], (jj / kStagesKV) & 1)) return false;
-        tc_fence_after();
-        const uint32_t vb = smem_u32(smem + L::kV + sv * L::kTile);
+      auto issue_s = [&](int t, int j) {
+        const uint32_t kb = smem_u32(smem + L::kK + (j % kStagesKV) * L::kTile);
+        const uint32_t qt = qa + t * L::kTile;
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t adesc = smem_desc_sw128(qt + c * L::kChunk + kk * 32, 16, 1024);
+            const uint64_t bdesc = smem_desc_sw128(kb + c * L::kChunk + kk * 32, 16, 1024);
+            mma_ss(tmem + t * 128, adesc, bdesc, idesc_s, (c | kk) != 0 ? 1u : 0u);
+          }
+        }
+        mma_commit(&s_full[t]);
+      };
+      auto issue_pv = [&](int t, int j) {
+        const uint32_t vb = smem_u32(smem + L::kV + (j % kStagesKV) * L::kTile);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
           // B = V_j: MN-major, 64-column atoms kChunk bytes apart (LBO), 8-key
           // groups 1024 bytes apart (SBO); 16 keys per step = 2048 bytes
           const uint64_t bdesc = smem_desc_sw128(vb + kk * 2048, L::kChunk, 1024);
-          mma_ts(tmem_o, tmem + pb * 128 + kk * 8, bdesc, idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, bdesc, idesc_o,
+                 (j > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&v_empty[sv]);
-        mma_commit(o_done);
+        mma_commit(&o_done[t]);
+      };
+      auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        if (!ok || *abort_flag) return false;
+        if (!mbar_wait(bar, parity)) {
+          ok = false;
+          return false;
+        }
+        tc_fence_after();
         return true;
       };
-      for (int j = 0; j < nkv && ok && !*abort_flag; ++j) {
-        const int sk = j % kStagesKV;
-        if (!mbar_wait(&k_full[sk], (j / kStagesKV) & 1)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t kb = smem_u32(smem + L::kK + sk * L::kTile);
-        const uint32_t s_tmem = tmem + (j & 1) * 128;
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t adesc = smem_desc_sw128(qa + c * L::kChunk + kk * 32, 16, 1024);
-            const uint64_t bdesc = smem_desc_sw128(kb + c * L::kChunk + kk * 32, 16, 1024);
-            mma_ss(s_tmem, adesc, bdesc, idesc_s, (c | kk) != 0 ? 1u : 0u);
+      if (ok && wait(&k_full[0], 0)) {
+        issue_s(0, 0);
+        issue_s(1, 0);
+        mma_commit(&k_empty[0]);
+      }
+      for (int j = 0; j < nkv_b && ok && !*abort_flag; ++j) {
+        const int sv = j % kStagesKV;
+        const int sk1 = (j + 1) % kStagesKV;
+        const uint32_t ph_v = (j / kStagesKV) & 1;
+        const uint32_t ph_k1 = ((j + 1) / kStagesKV) & 1;
+        if (!wait(&v_full[sv], ph_v)) break;
+        bool k1_ready = false;
+        if (j < nkv_a) {
+          if (!wait(&p_full[0], j & 1)) break;
+          issue_pv(0, j);
+          if (j + 1 < nkv_a) {
+            if (!wait(&k_full[sk1], ph_k1)) break;
+            k1_ready = true;
+            issue_s(0, j + 1);
           }
         }
-        mma_commit(&s_full[j & 1]);
-        mma_commit(&k_empty[sk]);
-        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+        if (!wait(&p_full[1], j & 1)) break;
+        issue_pv(1, j);
+        mma_commit(&v_empty[sv]);
+        if (j + 1 < nkv_b) {
+          if (!k1_ready && !wait(&k_full[sk1], ph_k1)) break;
+          issue_s(1, j + 1);
+          mma_commit(&k_empty[sk1]);
+        }
       }
-      if (ok && !*abort_flag && !issue_pv(nkv - 1)) ok = false;
       if (!ok) fail_timeout();
       // drain: all MMAs we issued are complete before TMEM may be freed
       mma_commit(drain);
@@ -218,44 +252,95 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int r = tid;                    // row of the tile (TMEM lane)
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const int t = warp >> 2;              // 0: tile A, 1: tile B
+    const int r = tid & 127;              // row of the tile (TMEM lane)
+    const int nkv = t == 0 ? nkv_a : nkv_b;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t s_tm = tmem + lane_base + t * 128;
+    const uint32_t o_tm = tmem + lane_base + 256 + t * 128;
     float m_ref = -INFINITY;              // exponent reference (lazy)
-    float m_max = -INFINITY;              // true running maximum
+    float m_max = -INFINITY;              // true running maximum (log2 units)
     float l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
-      const int sb = j & 1;
       if (*abort_flag) { ok = false; break; }
-      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[sb], (j >> 1) & 1))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[t], j & 1))) {
         fail_timeout();
         ok = false;
         break;
       }
       tc_fence_after();
-      float s[kBN];
+      const bool diag = j == nkv - 1;     // key column c visible iff c <= r
+      // pass 1: the row maximum, 64 columns (two loads in flight) at a time;
+      // eight independent partial maxima keep the dependent chain short
+      float mx8[8];
 #pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) {
-        uint32_t rr[32];
-        tmem_ld32(tmem + lane_base + sb * 128 + c * 32, rr);
+      for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t sr[64];
+        tmem_ld32(s_tm + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(sr));
+        tmem_ld32(s_tm + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
         tmem_wait_ld();
+        if (diag) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(rr[e]) * p.scale_log2;
+          for (int c = 0; c < 64; ++c)
+            mx8[c & 7] = hf * 64 + c > r ? mx8[c & 7] : fmaxf(mx8[c & 7], __uint_as_float(sr[c]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; c += 16)
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              mx8[i] = fmax3(mx8[i], __uint_as_float(sr[c + i]), __uint_as_float(sr[c + 8 + i]));
+        }
       }
-      if (j == qt) {  // diagonal tile: key column c visible iff c <= r
-#pragma unroll
-        for (int c = 0; c < kBN; ++c) s[c] = c <= r ? s[c] : -INFINITY;
-      }
-      float mt = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < kBN; ++c) mt = fmaxf(mt, s[c]);
-      m_max = fmaxf(m_max, mt);
+      const float mt = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]),
+                             fmaxf(fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      m_max = fmaxf(m_max, mt * p.scale_log2);
       const bool need = m_max > m_ref + kRescaleThreshold;
       const float m_new = need ? m_max : m_ref;
       const float factor = ex2(m_ref - m_new);  // 1 when unchanged, 0 on the first tile
+      // pass 2: P = exp2(s * scale_log2 - m_new) as bf16 over the S columns;
+      // pairs of columns go through the packed fp32x2 pipe
+      const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
+      const uint64_t nm2 = f2_pack(-m_new, -m_new);
+      uint64_t acc2[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc2[i] = f2_pack(0.f, 0.f);
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t sr[64];
+        tmem_ld32(s_tm + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(sr));
+        tmem_ld32(s_tm + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+        tmem_wait_ld();
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int c0 = hf * 64 + 2 * e;
+          float t0, t1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])),
+                           sc2, nm2),
+                    t0, t1);
+          float p0 = ex2(t0);
+          float p1 = ex2(t1);
+          if (diag) {
+            p0 = c0 <= r ? p0 : 0.f;
+            p1 = c0 + 1 <= r ? p1 : 0.f;
+          }
+          acc2[e & 3] = f2_add(acc2[e & 3], f2_pack(p0, p1));
+          pk[e] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32(s_tm + hf * 32, pk);
+      }
+      float rs0, rs1;
+      f2_unpack(f2_add(f2_add(acc2[0], acc2[1]), f2_add(acc2[2], acc2[3])), rs0, rs1);
+      const float rs = rs0 + rs1;
+      l_run = l_run * factor + rs;
+      m_ref = m_new;
       if (__any_sync(0xffffffffu, need) && j > 0) {
-        // O holds PV of tiles < j; wait until PV_{j-1} has landed, then rescale
-        if (!__all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1))) {
+        // O holds PV of tiles < j; once PV(j-1) has landed, rescale it (PV(j)
+        // is issued only after p_full, below)
+        if (!__all_sync(0xffffffffu, mbar_wait(&o_done[t], (j - 1) & 1))) {
           fail_timeout();
           ok = false;
           break;
@@ -264,47 +349,30 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t rr[32];
-          tmem_ld32(tmem_o + lane_base + c * 32, rr);
+          tmem_ld32(o_tm + c * 32, rr);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * factor);
-          tmem_st32(tmem_o + lane_base + c * 32, rr);
+          tmem_st32(o_tm + c * 32, rr);
         }
-        tmem_wait_st();
       }
-      l_run *= factor;
-      m_ref = m_new;
-      float rs = 0.f;
-#pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2(s[c * 32 + 2 * e] - m_ref);
-          const float p1 = ex2(s[c * 32 + 2 * e + 1] - m_ref);
-          rs += p0 + p1;
-          pk[e] = pack_bf16x2(p0, p1);
-        }
-        tmem_st16(tmem + lane_base + sb * 128 + c * 16, pk);
-      }
-      l_run += rs;
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&p_full[sb]);
+      mbar_arrive(&p_full[t]);
     }
     // epilogue: O / l, m, l (tcgen05.ld is warp-collective: decide per warp)
     ok = __all_sync(0xffffffffu, ok && !*abort_flag);
-    const bool o_ready = ok && __all_sync(0xffffffffu, mbar_wait(o_done, (nkv - 1) & 1));
+    const bool o_ready = ok && __all_sync(0xffffffffu, mbar_wait(&o_done[t], (nkv - 1) & 1));
     if (o_ready) {
       tc_fence_after();
-      const int qi = q0 + r;
+      const int qi = q0 + t * kBM + r;
       const bool row_ok = qi < n;
       const float inv_l = 1.0f / l_run;
       uint16_t* orow = p.o + (static_cast<int64_t>(seq0 + qi) * p.h_q + g) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t rr[32];
-        tmem_ld32(tmem_o + lane_base + c * 32, rr);
+        tmem_ld32(o_tm + c * 32, rr);
         tmem_wait_ld();
         if (row_ok) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
@@ -361,7 +429,7 @@ kvs_status launch_prefill(const PrefillMaps& mp, const PrefillParams& prm, int b
              "kvs_prefill_attn_lse: raising the shared-memory limit");
     configured = true;
   }
-  dim3 grid(prm.h_q, prm.n_qtiles_max, batch);
+  dim3 grid(prm.h_q, prm.n_pairs_max, batch);
   prefill_attn_kernel<D><<<grid, kPrefillThreads, PrefillSmem<D>::kBytes, st>>>(mp.qm, mp.km,
                                                                                mp.vm, prm);
   KVS_CHECK_LAUNCH("kvs_prefill_attn_lse");
@@ -397,9 +465,9 @@ extern "C" kvs_status kvs_prefill_attn_lse(const kvs_bf16* q, const kvs_bf16* k,
   prm.h_q = h_q;
   prm.h_kv = h_kv;
   prm.group = h_q / h_kv;
-  prm.n_qtiles_max = (max_n + kvs::kBM - 1) / kvs::kBM;
+  prm.n_pairs_max = (max_n + 2 * kvs::kBM - 1) / (2 * kvs::kBM);
   prm.scale_log2 = scale * kvs::kLog2eP;
-  KVS_REQUIRE(prm.n_qtiles_max <= 65535, "kvs_prefill_attn_lse: max_n too large");
+  KVS_REQUIRE(prm.n_pairs_max <= 65535, "kvs_prefill_attn_lse: max_n too large");
 
   static thread_local kvs::PrefillMaps cache;
   if (cache.q != q || cache.k != k || cache.v != v || cache.total != total_tokens ||

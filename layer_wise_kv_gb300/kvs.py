@@ -53,10 +53,10 @@ _SIGS = {
     "kvs_compact_blocks": (_I32, [_VP, _VP, _VP, _I32, _I64, _I32, _I32, _VP, _VP, _VP, _VP,
                                   _I32, _VP, _VP]),
     "kvs_copy_blocks": (_I32, [_VP, _VP, _I32, _VP, _VP, _I32, _I32, _I32, _VP, _VP]),
-    "kvs_paged_decode_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32]),
+    "kvs_paged_decode_workspace_size": (_SZ, [_I32, _I32, _I32, _I32]),
     "kvs_workspace_zero": (_I32, [_VP, _SZ, _VP]),
     "kvs_paged_decode": (_I32, [_VP, _VP, _VP, _VP, _VP, _I32, _VP, _I32, _VP, _VP, _VP, _I32,
-                                _I32, _I32, _I32, _I32, _F32, _VP, _VP, _SZ, _VP, _VP]),
+                                _I32, _I32, _I32, _F32, _VP, _VP, _SZ, _VP, _VP]),
     "kvs_alloc_create": (_I32, [_I32, _VP, _I32, ctypes.POINTER(_VP)]),
     "kvs_alloc_destroy": (None, [_VP]),
     "kvs_alloc_block": (_I32, [_VP, _P32]),
@@ -67,7 +67,7 @@ _SIGS = {
     "kvs_alloc_refcount": (_I32, [_VP, _I32]),
     "kvs_alloc_num_free": (_I32, [_VP]),
     "kvs_alloc_free_list": (_I32, [_VP, _VP, _I32]),
-    "kvs_decode_prepare": (_I32, [_VP, _VP, _I32, _VP, _I32, _VP, _VP, _VP, _P32, _P32]),
+    "kvs_decode_prepare": (_I32, [_VP, _VP, _I32, _VP, _I32, _VP, _VP, _VP, _P32, _P32, _P32]),
 }
 
 _lib = None
@@ -180,8 +180,8 @@ def kvs_copy_blocks(src, dst, count, k_pool, v_pool, num_blocks, h_kv, d, status
         None if status is None else _dev(status, "i32", "status"), _stream(stream)))
 
 
-def kvs_paged_decode_workspace_size(batch, h_q, h_kv, d, max_len) -> int:
-    return int(library().kvs_paged_decode_workspace_size(batch, h_q, h_kv, d, max_len))
+def kvs_paged_decode_workspace_size(batch, h_q, h_kv, d) -> int:
+    return int(library().kvs_paged_decode_workspace_size(batch, h_q, h_kv, d))
 
 
 def kvs_workspace_zero(workspace, nbytes, stream=None):
@@ -190,7 +190,7 @@ def kvs_workspace_zero(workspace, nbytes, stream=None):
 
 
 def kvs_paged_decode(q, k_new, v_new, k_pool, v_pool, num_blocks, block_tables, max_blocks,
-                     table_patch, lens, lens_next, batch, max_len, h_q, h_kv, d, scale, out,
+                     table_patch, lens, lens_next, batch, h_q, h_kv, d, scale, out,
                      workspace, workspace_bytes, status=None, stream=None):
     _check(library().kvs_paged_decode(
         _dev(q, "bf16", "q"), None if k_new is None else _dev(k_new, "bf16", "k_new"),
@@ -199,7 +199,7 @@ def kvs_paged_decode(q, k_new, v_new, k_pool, v_pool, num_blocks, block_tables, 
         _dev(block_tables, "i32", "block_tables"), max_blocks,
         None if table_patch is None else _dev(table_patch, "i32", "table_patch"),
         _dev(lens, "i32", "lens"), None if lens_next is None else _dev(lens_next, "i32", "lens_next"),
-        batch, max_len, h_q, h_kv, d, float(scale), _dev(out, "bf16", "out"),
+        batch, h_q, h_kv, d, float(scale), _dev(out, "bf16", "out"),
         _dev(workspace, "u8", "workspace"), workspace_bytes,
         None if status is None else _dev(status, "i32", "status"), _stream(stream)))
 
@@ -267,14 +267,17 @@ class BlockAllocator:
         return buf[:got].tolist()
 
     def decode_prepare(self, tables: np.ndarray, lens: np.ndarray, patch: np.ndarray,
-                       cow_src: np.ndarray, cow_dst: np.ndarray) -> int:
+                       cow_src: np.ndarray, cow_dst: np.ndarray, with_patch_count=False):
         """kvs_decode_prepare on host int32 arrays (tables [n_items, max_blocks],
-        updated in place).  Returns the number of copy-on-write pairs."""
+        updated in place).  Returns the number of copy-on-write pairs (and the
+        number of patched table entries with with_patch_count)."""
         assert tables.dtype == np.int32 and tables.flags.c_contiguous
         n_items, max_blocks = tables.shape
-        n_cow, n_done = ctypes.c_int32(), ctypes.c_int32()
+        n_cow, n_patch, n_done = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
         _check(self._lib.kvs_decode_prepare(
             self._h, tables.ctypes.data, max_blocks, lens.ctypes.data, n_items,
             patch.ctypes.data, cow_src.ctypes.data, cow_dst.ctypes.data, ctypes.byref(n_cow),
-            ctypes.byref(n_done)))
+            ctypes.byref(n_patch), ctypes.byref(n_done)))
+        if with_patch_count:
+            return n_cow.value, n_patch.value
         return n_cow.value

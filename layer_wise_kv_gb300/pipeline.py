@@ -71,7 +71,10 @@ class PrefillResult:
 class Engine:
     """Device pools, the host block allocator and scratch for one workload."""
 
-    def __init__(self, shape: Shape, num_blocks: int, device="cuda", initial_free=None):
+    def __init__(self, shape: Shape, num_blocks: int, device="cuda", initial_free=None,
+                 poison=False):
+        """poison: fill the pools with bf16 NaN patterns (0xFFFF) so that any
+        read of an unwritten slot shows up in the outputs (tests)."""
         self.shape = shape
         self.device = torch.device(device)
         self.num_blocks = num_blocks
@@ -80,6 +83,9 @@ class Engine:
         self.k_pool = torch.empty((num_blocks, s.h_kv, BLOCK, s.d), dtype=torch.bfloat16,
                                   device=self.device)
         self.v_pool = torch.empty_like(self.k_pool)
+        if poison:
+            self.k_pool.view(torch.int16).fill_(-1)
+            self.v_pool.view(torch.int16).fill_(-1)
         self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
 
     # ------------------------------------------------------------------ checks
@@ -254,12 +260,13 @@ class DecodeBatch:
                       for _ in range(self._ring)]
         self._ev = [None] * self._ring
         self._slot = 0
+        self._patch_np = [t.numpy() for t in self.patch_h]
+        self._cow_np = [t.numpy() for t in self.cow_h]
         self.patch_d = torch.empty(self.n_items, dtype=torch.int32, device=dev)
         self.cow_src = np.zeros(self.n_items, dtype=np.int32)
         self.cow_dst = np.zeros(self.n_items, dtype=np.int32)
         self.cow_d = torch.empty(2 * self.n_items, dtype=torch.int32, device=dev)
-        self.ws_bytes = kvs.kvs_paged_decode_workspace_size(self.n_items, s.h_q, s.h_kv, s.d,
-                                                            max_len)
+        self.ws_bytes = kvs.kvs_paged_decode_workspace_size(self.n_items, s.h_q, s.h_kv, s.d)
         self.ws = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
         kvs.kvs_workspace_zero(self.ws, self.ws_bytes)
         self.out = torch.empty((self.n_items, s.h_q, s.d), dtype=torch.bfloat16, device=dev)
@@ -293,38 +300,50 @@ class DecodeBatch:
         self.tables_h[slot * L:(slot + 1) * L] = -1
         self.lens_h[slot * L:(slot + 1) * L] = 0
 
-    def step(self, q, k_new, v_new, stream=None):
+    def step(self, q, k_new, v_new, stream=None, timing=None):
         """One decode step for every item: q [n_items][h_q][d], k_new/v_new
-        [n_items][h_kv][d] bf16 on the device.  Returns the output tensor."""
+        [n_items][h_kv][d] bf16 on the device.  Returns the output tensor.
+        timing: optional list receiving a (start, end) event pair around the
+        decode kernel."""
         eng, s = self.eng, self.eng.shape
         n = self.n_items
         slot = self._slot
-        self._slot = (slot + 1) % self._ring
+        patch_t, cow_t = self.patch_h[slot], self.cow_h[slot]
         if self._ev[slot] is not None:
             self._ev[slot].synchronize()
-        patch_t, cow_t = self.patch_h[slot], self.cow_h[slot]
-        patch = patch_t.numpy()
-        n_cow = eng.alloc.decode_prepare(self.tables_h, self.lens_h, patch, self.cow_src,
-                                         self.cow_dst)
+        n_cow, n_patch = eng.alloc.decode_prepare(self.tables_h, self.lens_h, self._patch_np[slot],
+                                                  self.cow_src, self.cow_dst,
+                                                  with_patch_count=True)
         cur_stream = torch.cuda.current_stream() if stream is None else stream
-        with torch.cuda.stream(cur_stream):
-            self.patch_d.copy_(patch_t, non_blocking=True)
-            if n_cow:
-                cow = cow_t.numpy()
-                cow[:n_cow] = self.cow_src[:n_cow]
-                cow[n_cow:2 * n_cow] = self.cow_dst[:n_cow]
-                self.cow_d[:2 * n_cow].copy_(cow_t[:2 * n_cow], non_blocking=True)
-                kvs.kvs_copy_blocks(self.cow_d[:n_cow], self.cow_d[n_cow:2 * n_cow], n_cow,
-                                    eng.k_pool, eng.v_pool, eng.num_blocks, s.h_kv, s.d,
-                                    eng.status, cur_stream)
-            ev = torch.cuda.Event()
-            ev.record(cur_stream)
-            self._ev[slot] = ev
+        patch_arg = None
+        if n_patch or n_cow:
+            self._slot = (slot + 1) % self._ring
+            with torch.cuda.stream(cur_stream):
+                self.patch_d.copy_(patch_t, non_blocking=True)
+                patch_arg = self.patch_d
+                if n_cow:
+                    cow = self._cow_np[slot]
+                    cow[:n_cow] = self.cow_src[:n_cow]
+                    cow[n_cow:2 * n_cow] = self.cow_dst[:n_cow]
+                    self.cow_d[:2 * n_cow].copy_(cow_t[:2 * n_cow], non_blocking=True)
+                    kvs.kvs_copy_blocks(self.cow_d[:n_cow], self.cow_d[n_cow:2 * n_cow], n_cow,
+                                        eng.k_pool, eng.v_pool, eng.num_blocks, s.h_kv, s.d,
+                                        eng.status, cur_stream)
+                ev = torch.cuda.Event()
+                ev.record(cur_stream)
+                self._ev[slot] = ev
         nxt = 1 - self.cur
+        if timing is not None:
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(cur_stream)
         kvs.kvs_paged_decode(q, k_new, v_new, eng.k_pool, eng.v_pool, eng.num_blocks,
-                             self.tables_d, self.max_blocks, self.patch_d, self.lens_d[self.cur],
-                             self.lens_d[nxt], n, self.max_len, s.h_q, s.h_kv, s.d, s.scale,
+                             self.tables_d, self.max_blocks, patch_arg, self.lens_d[self.cur],
+                             self.lens_d[nxt], n, s.h_q, s.h_kv, s.d, s.scale,
                              self.out, self.ws, self.ws_bytes, eng.status, cur_stream)
+        if timing is not None:
+            b.record(cur_stream)
+            timing.append((a, b))
         self.cur = nxt
         self.lens_h += 1
         return self.out

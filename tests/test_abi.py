@@ -57,14 +57,14 @@ def test_invalid_arguments_rejected_before_launch(kvs):
     # NULL pointers and unsupported shapes return an error without touching a GPU
     assert lib.kvs_compact_blocks(None, None, None, 1, 1, 8, 128, None, None, None, None, 4,
                                   None, None) == kvs.KVS_ERR_INVALID
-    rc = lib.kvs_paged_decode(1, None, None, 1, 1, 4, 1, 4, None, 1, None, 1, 16, 8, 8, 96,
+    rc = lib.kvs_paged_decode(1, None, None, 1, 1, 4, 1, 4, None, 1, None, 1, 8, 8, 96,
                               0.1, 1, 1, 1 << 20, None, None)
     assert rc == kvs.KVS_ERR_UNSUPPORTED and "d = 96" in kvs.last_error()
     assert lib.kvs_window_scores(1, 1, 1, 1, 1, 1, 1, 64, 64, 32, 8, 128, 128, 0.1, None,
                                  None) == kvs.KVS_ERR_UNSUPPORTED  # alpha * G > 256
     assert lib.kvs_prefill_attn_lse(1, 1, 1, 1, 1, 1, 1, 1, 16, 16, 6, 4, 128, 0.1, None,
                                     None) == kvs.KVS_ERR_INVALID  # 6 % 4 != 0
-    assert kvs.kvs_paged_decode_workspace_size(0, 32, 8, 128, 100) == 0
+    assert kvs.kvs_paged_decode_workspace_size(0, 32, 8, 128) == 0
 
 
 def test_worked_example_allocator(kvs, golden_dir):
@@ -146,7 +146,8 @@ def test_decode_prepare_matches_oracle_flow(kvs):
     patch = np.zeros(3, dtype=np.int32)
     cs, cd = np.zeros(3, dtype=np.int32), np.zeros(3, dtype=np.int32)
     for step in range(40):
-        n_cow = a.decode_prepare(tables, lens, patch, cs, cd)
+        n_cow, n_patch = a.decode_prepare(tables, lens, patch, cs, cd, with_patch_count=True)
+        assert n_patch == int((patch >= 0).sum())
         copies = []
         for s in streams:
             c = flow.prepare_append(o, s, 0)

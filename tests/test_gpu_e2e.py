@@ -53,7 +53,7 @@ def test_tiny_workload_end_to_end():
     w = tiny()
     n = w.prompt_lens[0]
     L = w.n_layers
-    eng = Engine(_shape(w), 64)
+    eng = Engine(_shape(w), 64, poison=True)
     ql, kl, vl, host = _layers_to_device(w, [0], [n])
     budgets = [[w.budget(l, n) for l in range(L)]]
     res = eng.prefill_sparsify(ql, kl, vl, [n], budgets, keep_outputs=True)
@@ -97,7 +97,7 @@ def test_tiny_workload_end_to_end():
     for l in range(L):
         if recs[l].budgeted:
             sel[l] = torch.from_numpy(recs[l].scores.astype(np.float32))
-    eng2 = Engine(_shape(w), 64)
+    eng2 = Engine(_shape(w), 64, poison=True)
     res2 = eng2.prefill_sparsify(ql, kl, vl, [n], budgets, select_scores=sel)
     torch.cuda.synchronize()
     for l in range(L):
@@ -136,7 +136,7 @@ def test_shared_prefix_copy_on_write():
     n = 100                                  # layer 0: 100 tokens (partial block); layer 1: 64
     L = w.n_layers
     N = 64
-    eng = Engine(_shape(w), N)
+    eng = Engine(_shape(w), N, poison=True)
     ql, kl, vl, host = _layers_to_device(w, [3], [n])
     budgets = [[w.budget(l, n) for l in range(L)]]
     res = eng.prefill_sparsify(ql, kl, vl, [n], budgets)
@@ -198,7 +198,7 @@ def test_continuous_batching_small():
     L = w.n_layers
     N = 96
     order = shuffled_block_order(N, 1)
-    eng = Engine(_shape(w), N, initial_free=order)
+    eng = Engine(_shape(w), N, initial_free=order, poison=True)
     pool = oracle.BlockPool(N, free=order)
     opk = np.zeros((N, w.h_kv, 16, w.d), np.uint16)
     opv = np.zeros_like(opk)
@@ -275,7 +275,7 @@ def test_llama3_8b_full_size_sampled():
     n = w.prompt_lens[0]
     L = w.n_layers
     N = 4096
-    eng = Engine(_shape(w), N)
+    eng = Engine(_shape(w), N, poison=True)
     ql, kl, vl, host = _layers_to_device(w, [0], [n])
     budgets = [[w.budget(l, n) for l in range(L)]]
     res = eng.prefill_sparsify(ql, kl, vl, [n], budgets, keep_outputs=True)

@@ -236,18 +236,23 @@ def test_paged_decode_vs_oracle(h_q, h_kv, d):
     max_blocks = oracle.blocks_for(max_len)
     N = n_items * max_blocks + 8
     a = kvs.BlockAllocator(N, rng.permutation(N))
-    pk = _randn_bits(rng, (N, h_kv, 16, d))
-    pv = _randn_bits(rng, (N, h_kv, 16, d))
+    # every slot starts as a bf16 NaN pattern; only slots below each item's
+    # length hold data, so a read of an unwritten slot poisons the output
+    pk = np.full((N, h_kv, 16, d), 0xFFFF, np.uint16)
+    pv = pk.copy()
     tables = np.full((n_items, max_blocks), -1, np.int32)
     for i, L0 in enumerate(start_lens):
         ids = a.alloc_many(oracle.blocks_for(L0))
         tables[i, :len(ids)] = ids
+        for j in range(L0):
+            pk[ids[j // 16], :, j % 16] = _randn_bits(rng, (h_kv, d))
+            pv[ids[j // 16], :, j % 16] = _randn_bits(rng, (h_kv, d))
     k_pool, v_pool = dev_bf16(pk), dev_bf16(pv)
     tables_d = torch.from_numpy(tables).cuda()
     lens_h = np.array(start_lens, np.int32)
     lens_d = [torch.from_numpy(lens_h.copy()).cuda(), torch.zeros(n_items, dtype=torch.int32,
                                                                   device="cuda")]
-    ws_bytes = kvs.kvs_paged_decode_workspace_size(n_items, h_q, h_kv, d, max_len)
+    ws_bytes = kvs.kvs_paged_decode_workspace_size(n_items, h_q, h_kv, d)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     kvs.kvs_workspace_zero(ws, ws_bytes)
     out = torch.empty((n_items, h_q, d), dtype=torch.bfloat16, device="cuda")
@@ -263,7 +268,7 @@ def test_paged_decode_vs_oracle(h_q, h_kv, d):
         cur = step % 2
         kvs.kvs_paged_decode(dev_bf16(q), dev_bf16(kn), dev_bf16(vn), k_pool, v_pool, N,
                              tables_d, max_blocks, torch.from_numpy(patch).cuda(), lens_d[cur],
-                             lens_d[1 - cur], n_items, max_len, h_q, h_kv, d, 1 / np.sqrt(d), out,
+                             lens_d[1 - cur], n_items, h_q, h_kv, d, 1 / np.sqrt(d), out,
                              ws, ws_bytes, status)
         torch.cuda.synchronize()
         assert status.item() == 0
