@@ -321,7 +321,7 @@ def bench_gpu(args):
                             "per_launch_ms": round(dec_avg, 4),
                             "step_ms": round(sum(dec_ms) / len(dec_ms), 4)},
         "scores_ms_per_launch": round(sum(k2_ms) / max(1, len(k2_ms)), 4),
-        "gpu_launches": args.steps * (2 * L - 3 + 2 + steps),
+        "gpu_launches": args.steps * (2 * L - 3 + 2 + 2 * steps),
         "clocks": clk,
         "wall_s": round(t_wall, 2),
     }

@@ -193,14 +193,16 @@ kvs_status kvs_copy_blocks(const int32_t* src, const int32_t* dst, int32_t count
  *   lens_next    [batch] int32, nullable, must not alias lens: receives
  *                lens[i] + (k_new != NULL).
  *   workspace    scratch of kvs_paged_decode_workspace_size(batch, h_q, h_kv,
- *                d) bytes; must be zero-filled before its first use
- *                (kvs_workspace_zero); each call leaves it ready for the next.
- *                Calls sharing a workspace must not overlap in time.
+ *                d) bytes (split partials and their index); needs no
+ *                initialisation.  Calls sharing a workspace must not overlap in
+ *                time.
+ * Two launches on `stream`: the split decode, then a merge of the splits.
  * An item with zero tokens to attend (lens[i] == 0 and no append) gets no
  * output row.
  * ---------------------------------------------------------------------- */
 size_t kvs_paged_decode_workspace_size(int32_t batch, int32_t h_q, int32_t h_kv, int32_t d);
 
+/* Zero-fill a device buffer on `stream` (convenience for callers' scratch). */
 kvs_status kvs_workspace_zero(void* workspace, size_t bytes, kvs_stream stream);
 
 kvs_status kvs_paged_decode(const kvs_bf16* q, const kvs_bf16* k_new, const kvs_bf16* v_new,

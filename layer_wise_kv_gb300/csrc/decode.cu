@@ -31,8 +31,10 @@
 //   count off the issue slots; the bound is HBM.
 // * A segment covered by one piece writes `out` directly; otherwise each piece
 //   writes an unnormalised partial (m, l, o) to its workspace slot (warp index
-//   + segment index, unique), and the last piece of the segment to finish (an
-//   atomic counter, no waiting) merges them and resets the counter.
+//   + segment index, unique) and the segment's first piece records where its
+//   pieces lie.  A second, small kernel (one CTA per segment, every partial
+//   load in flight at once) merges them; the decode kernel itself needs no
+//   fence, atomic or wait between warps.
 #include <cuda_runtime.h>
 
 #include "host_common.h"
@@ -42,11 +44,15 @@
 namespace kvs {
 namespace {
 
-constexpr int kWarps = 12;
+#ifndef KVS_DECODE_WARPS
+#define KVS_DECODE_WARPS 12
+#endif
+constexpr int kWarps = KVS_DECODE_WARPS;
 constexpr int kDecThreads = kWarps * 32;
 constexpr int kMaxGrid = 256;
 constexpr int kMaxG = 16;
 constexpr int kMaxBatch = 2048;
+constexpr int kMaxStages = 8;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct DecodeParams {
@@ -61,10 +67,10 @@ struct DecodeParams {
   int32_t* lens_next;
   uint16_t* out;
   float* ws_part;
-  int32_t* ws_count;
+  int32_t* ws_seg;  // [segments][2]: first partial slot, number of pieces
   int32_t* status;
   int batch, max_blocks, num_blocks, h_q, h_kv, group, append, n_stages;
-  int q_bytes, q_stride, q_off, bar_off, scr_off, idx_off;
+  int q_bytes, q_stride, q_off, bar_off, idx_off;
   float scale_log2;
 };
 
@@ -191,11 +197,12 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
   uint8_t* my_stages = smem + warp * NS * L::kStageBytes;
   uint8_t* my_q = smem + p.q_off + warp * 2 * p.q_stride;
   uint64_t* my_full = reinterpret_cast<uint64_t*>(smem + p.bar_off) + warp * NS;
-  float* my_scr = reinterpret_cast<float*>(smem + p.scr_off) + warp * 2 * kMaxG;
   int* prefix = reinterpret_cast<int*>(smem + p.idx_off);  // [batch + 1], in blocks
   int* lens_s = prefix + (p.batch + 1);
 
   if (threadIdx.x == 0) {
+    tma_prefetch_desc(&k_map);
+    tma_prefetch_desc(&v_map);
     for (int i = 0; i < kWarps * NS; ++i) mbar_init(reinterpret_cast<uint64_t*>(smem + p.bar_off) + i, 1);
     fence_mbar_init();
   }
@@ -499,59 +506,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
             }
           }
         }
-      __threadfence();
-      __syncwarp();
-      int last = 0;
-      if (lane == 0) last = atomicAdd(p.ws_count + cur.seg, 1) == cur.npieces - 1;
-      last = __shfl_sync(0xffffffffu, last, 0);
-      if (last) {
-        __threadfence();
-        const float* base = p.ws_part + static_cast<int64_t>(cur.first_slot) * rec;
-        const int np = cur.npieces;
-        // row maxima and normalisers over the pieces
-        for (int r = 0; r < G; ++r) {
-          float mx = -INFINITY;
-          for (int sp = lane; sp < np; sp += 32)
-            mx = fmaxf(mx, __ldcg(base + static_cast<int64_t>(sp) * rec + G * D + r));
-#pragma unroll
-          for (int o2 = 16; o2 > 0; o2 >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
-          float sum = 0.f;
-          for (int sp = lane; sp < np; sp += 32) {
-            const float* pr = base + static_cast<int64_t>(sp) * rec;
-            sum += __ldcg(pr + G * D + G + r) * ex2(__ldcg(pr + G * D + r) - mx);
-          }
-#pragma unroll
-          for (int o2 = 16; o2 > 0; o2 >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o2);
-          if (lane == 0) {
-            my_scr[r] = mx;
-            my_scr[kMaxG + r] = sum;
-          }
-        }
-        __syncwarp();
-        for (int e4 = lane; e4 < G * D / 4; e4 += 32) {
-          const int r = (e4 * 4) / D;
-          const int c = e4 * 4 - r * D;
-          const float mx = my_scr[r];
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int sp = 0; sp < np; ++sp) {
-            const float* pr = base + static_cast<int64_t>(sp) * rec;
-            const float f = ex2(__ldcg(pr + G * D + r) - mx);
-            const float4 v4 = __ldcg(reinterpret_cast<const float4*>(pr + r * D + c));
-            acc.x += f * v4.x;
-            acc.y += f * v4.y;
-            acc.z += f * v4.z;
-            acc.w += f * v4.w;
-          }
-          const float il = 1.0f / my_scr[kMaxG + r];
-          uint2 w2;
-          w2.x = pack_bf16x2(acc.x * il, acc.y * il);
-          w2.y = pack_bf16x2(acc.z * il, acc.w * il);
-          *reinterpret_cast<uint2*>(p.out + (out_row0 + r) * D + c) = w2;
-        }
-        __syncwarp();
-        if (lane == 0) p.ws_count[cur.seg] = 0;
-      }
     }
+    // where the segment's pieces lie, for the merge kernel (its first piece)
+    if (lane == 0 && cur.blk0 == 0)
+      *reinterpret_cast<int2*>(p.ws_seg + 2 * cur.seg) = make_int2(cur.first_slot, cur.npieces);
     // table patch and length bookkeeping, once per item (its head-0 segment start)
     if (lane == 0 && cur.blk0 == 0 && cur.h == 0) {
       if (p.append && p.patch != nullptr && p.patch[cur.item] >= 0)
@@ -580,6 +538,73 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
   __syncwarp();
 }
 
+// Merge of the pieces of every split segment: one CTA per (item, KV head).
+// Pieces are combined as softmax partials: with M the largest piece maximum,
+// out = sum_p exp2(m_p - M) o_p / sum_p exp2(m_p - M) l_p.
+constexpr int kMergeThreads = 128;
+constexpr int kMergeWeights = 4096;
+
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads)
+decode_merge_kernel(const float* __restrict__ ws_part, const int32_t* __restrict__ ws_seg,
+                    const int32_t* __restrict__ lens, int append, int h_q, int h_kv, int G,
+                    uint16_t* __restrict__ out) {
+  __shared__ float wsm[kMergeWeights];
+  __shared__ float Ms[kMaxG], Ls[kMaxG];
+  const int seg = blockIdx.x;
+  const int item = seg / h_kv, h = seg - item * h_kv;
+  if (lens[item] + append <= 0) return;  // no tokens: no output row
+  const int2 info = *reinterpret_cast<const int2*>(ws_seg + 2 * seg);
+  const int np = info.y;
+  if (np <= 1) return;                   // written directly by its only piece
+  const int rec = G * (D + 2);
+  const float* base = ws_part + static_cast<int64_t>(info.x) * rec;
+  const bool cached = np * G <= kMergeWeights;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int r = warp; r < G; r += kMergeThreads / 32) {
+    float mx = -INFINITY;
+    for (int sp = lane; sp < np; sp += 32)
+      mx = fmaxf(mx, __ldcg(base + static_cast<int64_t>(sp) * rec + G * D + r));
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+    float sum = 0.f;
+    for (int sp = lane; sp < np; sp += 32) {
+      const float* pr = base + static_cast<int64_t>(sp) * rec;
+      const float wgt = ex2(__ldcg(pr + G * D + r) - mx);
+      if (cached) wsm[sp * G + r] = wgt;
+      sum += __ldcg(pr + G * D + G + r) * wgt;
+    }
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o2);
+    if (lane == 0) {
+      Ms[r] = mx;
+      Ls[r] = sum;
+    }
+  }
+  __syncthreads();
+  const int64_t out_row0 = static_cast<int64_t>(item) * h_q + h * G;
+  for (int e4 = threadIdx.x; e4 < G * D / 4; e4 += kMergeThreads) {
+    const int r = (e4 * 4) / D;
+    const int c = e4 * 4 - r * D;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+    for (int sp = 0; sp < np; ++sp) {
+      const float* pr = base + static_cast<int64_t>(sp) * rec;
+      const float wgt = cached ? wsm[sp * G + r] : ex2(__ldcg(pr + G * D + r) - Ms[r]);
+      const float4 v4 = __ldcg(reinterpret_cast<const float4*>(pr + r * D + c));
+      acc.x += wgt * v4.x;
+      acc.y += wgt * v4.y;
+      acc.z += wgt * v4.z;
+      acc.w += wgt * v4.w;
+    }
+    const float il = 1.0f / Ls[r];
+    uint2 w2;
+    w2.x = pack_bf16x2(acc.x * il, acc.y * il);
+    w2.y = pack_bf16x2(acc.z * il, acc.w * il);
+    *reinterpret_cast<uint2*>(out + (out_row0 + r) * D + c) = w2;
+  }
+}
+
 struct MapCache {
   const void* base = nullptr;
   int num_blocks = 0, h_kv = 0, d = 0;
@@ -603,8 +628,8 @@ bool pool_map(MapCache& c, const void* pool, int num_blocks, int h_kv, int d) {
   return true;
 }
 
-int64_t counter_bytes(int batch, int h_kv) {
-  return (static_cast<int64_t>(batch) * h_kv * 4 + 255) / 256 * 256;
+int64_t seg_bytes(int batch, int h_kv) {
+  return (static_cast<int64_t>(batch) * h_kv * 8 + 255) / 256 * 256;
 }
 
 int sm_count_dec() {
@@ -626,14 +651,12 @@ size_t plan_smem(DecodeParams& prm) {
   using L = DecodeLayout<D>;
   prm.q_bytes = prm.group * D * 2;
   prm.q_stride = (prm.q_bytes + 127) / 128 * 128;
-  for (int ns = 3; ns >= 1; --ns) {
+  for (int ns = kMaxStages; ns >= 1; --ns) {
     size_t off = static_cast<size_t>(kWarps) * ns * L::kStageBytes;
     const size_t q_off = off;
     off += static_cast<size_t>(kWarps) * 2 * prm.q_stride;
     const size_t bar_off = off;
     off += static_cast<size_t>(kWarps) * ns * 8;
-    const size_t scr_off = off;
-    off += static_cast<size_t>(kWarps) * 2 * kMaxG * 4;
     const size_t idx_off = off;
     off += static_cast<size_t>(2 * prm.batch + 1) * 4;
     const size_t total = off + 1024;
@@ -641,7 +664,6 @@ size_t plan_smem(DecodeParams& prm) {
       prm.n_stages = ns;
       prm.q_off = static_cast<int>(q_off);
       prm.bar_off = static_cast<int>(bar_off);
-      prm.scr_off = static_cast<int>(scr_off);
       prm.idx_off = static_cast<int>(idx_off);
       return total;
     }
@@ -664,6 +686,9 @@ kvs_status launch_decode(DecodeParams& prm, const CUtensorMap& km, const CUtenso
   const int grid = sm_count_dec() < kMaxGrid ? sm_count_dec() : kMaxGrid;
   paged_decode_kernel<D, NT><<<grid, kDecThreads, smem, stream>>>(km, vm, prm);
   KVS_CHECK_LAUNCH("kvs_paged_decode");
+  decode_merge_kernel<D><<<prm.batch * prm.h_kv, kMergeThreads, 0, stream>>>(
+      prm.ws_part, prm.ws_seg, prm.lens, prm.append, prm.h_q, prm.h_kv, prm.group, prm.out);
+  KVS_CHECK_LAUNCH("kvs_paged_decode (merge)");
   return KVS_OK;
 }
 
@@ -678,7 +703,7 @@ size_t kvs_paged_decode_workspace_size(int32_t batch, int32_t h_q, int32_t h_kv,
   // one partial slot per (warp, segment it touches): slot = warp + segment
   const int64_t slots = static_cast<int64_t>(kvs::kMaxGrid) * kvs::kWarps +
                         static_cast<int64_t>(batch) * h_kv;
-  return static_cast<size_t>(kvs::counter_bytes(batch, h_kv) + slots * G * (d + 2) * 4);
+  return static_cast<size_t>(kvs::seg_bytes(batch, h_kv) + slots * G * (d + 2) * 4);
 }
 
 kvs_status kvs_paged_decode(const kvs_bf16* q, const kvs_bf16* k_new, const kvs_bf16* v_new,
@@ -710,7 +735,7 @@ kvs_status kvs_paged_decode(const kvs_bf16* q, const kvs_bf16* k_new, const kvs_
                   (reinterpret_cast<uintptr_t>(out) & 15) == 0,
               "kvs_paged_decode: q, out and pools must be 16-byte aligned");
   const int64_t G = h_q / h_kv;
-  const int64_t cbytes = kvs::counter_bytes(batch, h_kv);
+  const int64_t cbytes = kvs::seg_bytes(batch, h_kv);
   const size_t need = kvs_paged_decode_workspace_size(batch, h_q, h_kv, d);
   KVS_REQUIRE(workspace_bytes >= need, "kvs_paged_decode: workspace %zu bytes < %zu needed",
               workspace_bytes, need);
@@ -730,7 +755,7 @@ kvs_status kvs_paged_decode(const kvs_bf16* q, const kvs_bf16* k_new, const kvs_
   prm.lens = lens;
   prm.lens_next = lens_next;
   prm.out = out;
-  prm.ws_count = static_cast<int32_t*>(workspace);
+  prm.ws_seg = static_cast<int32_t*>(workspace);
   prm.ws_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + cbytes);
   prm.status = status;
   prm.batch = batch;
