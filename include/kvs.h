@@ -213,6 +213,42 @@ kvs_status kvs_paged_decode(const kvs_bf16* q, const kvs_bf16* k_new, const kvs_
                             size_t workspace_bytes, int32_t* status, kvs_stream stream);
 
 /* ------------------------------------------------------------------------
+ * Paged decode that allocates nothing (no counterpart in the method's
+ * sources: this is a calling convention, not a step of the method).
+ *
+ * Some callers cannot hand the library a workspace: a serving process that
+ * reserved all device memory for its paged pool up front and allows no
+ * allocation on the decode path (an allocation there can fail under memory
+ * pressure, fragment the reserved pool, or synchronise the device), or a
+ * plain C host without a device allocator of its own.  This entry point takes
+ * the same arguments and computes the same result as kvs_paged_decode, but
+ * its split partials live in a device array built into the library, of
+ * KVS_DECODE_STATIC_SCRATCH_BYTES; every GPU that loads the library holds
+ * that array until the process exits.  It calls no cudaMalloc, cudaFree or
+ * allocating library routine.
+ *   - Sizes whose workspace (kvs_paged_decode_workspace_size) exceeds the
+ *     array are rejected with KVS_ERR_UNSUPPORTED before any launch.  With
+ *     h_q = 32, h_kv = 8, d = 128 the array serves up to 621 items (one
+ *     32-layer sequence is 32 items and needs about 7 MB).
+ *   - The first call on a device looks up the array's device address on that
+ *     device (the current one); make that first call before any stream
+ *     capture.
+ *   - All calls share the one array and it keeps the last call's contents;
+ *     nothing in it needs to start at zero (each call writes its split index
+ *     and partials before reading them).  Calls that overlap on the GPU (on
+ *     different streams, or from different threads) race on it.
+ * ---------------------------------------------------------------------- */
+#define KVS_DECODE_STATIC_SCRATCH_BYTES (16u << 20)
+
+kvs_status kvs_paged_decode_static(const kvs_bf16* q, const kvs_bf16* k_new,
+                                   const kvs_bf16* v_new, kvs_bf16* k_pool, kvs_bf16* v_pool,
+                                   int32_t num_blocks, int32_t* block_tables, int32_t max_blocks,
+                                   const int32_t* table_patch, const int32_t* lens,
+                                   int32_t* lens_next, int32_t batch, int32_t h_q, int32_t h_kv,
+                                   int32_t d, float scale, kvs_bf16* out, int32_t* status,
+                                   kvs_stream stream);
+
+/* ------------------------------------------------------------------------
  * Block allocator (host memory, single-threaded, not thread-safe).
  * Source: Ultralytics glossary "PagedAttention": sections "How paging
  * works" (a new block only when the last one is full, taken from wherever one

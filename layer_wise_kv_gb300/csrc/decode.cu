@@ -37,9 +37,16 @@
 //   fence, atomic or wait between warps.
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "host_common.h"
 #include "ptx.cuh"
 #include "tma_host.h"
+
+// Built-in scratch of kvs_paged_decode_static: the split index and partials
+// for callers that cannot provide a workspace.  Host code never uses the name
+// as an address; it looks the device address up per device (below).
+static __device__ __align__(256) unsigned char g_decode_static_scratch[KVS_DECODE_STATIC_SCRATCH_BYTES];
 
 namespace kvs {
 namespace {
@@ -776,3 +783,56 @@ kvs_status kvs_paged_decode(const kvs_bf16* q, const kvs_bf16* k_new, const kvs_
 }
 
 }  // extern "C"
+
+namespace {
+
+// Device address of the built-in scratch on the current device, looked up
+// once per device.  Returns nullptr (and records the error) on failure.
+void* static_scratch_address() {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    kvs::set_error("kvs_paged_decode_static: no usable current device");
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_decode_static_scratch);
+    if (e != cudaSuccess) {
+      kvs::set_error("kvs_paged_decode_static: cudaGetSymbolAddress failed: %s",
+                     cudaGetErrorString(e));
+      return nullptr;
+    }
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+}  // namespace
+
+extern "C" kvs_status kvs_paged_decode_static(const kvs_bf16* q, const kvs_bf16* k_new,
+                                              const kvs_bf16* v_new, kvs_bf16* k_pool,
+                                              kvs_bf16* v_pool, int32_t num_blocks,
+                                              int32_t* block_tables, int32_t max_blocks,
+                                              const int32_t* table_patch, const int32_t* lens,
+                                              int32_t* lens_next, int32_t batch, int32_t h_q,
+                                              int32_t h_kv, int32_t d, float scale,
+                                              kvs_bf16* out, int32_t* status, kvs_stream stream) {
+  KVS_REQUIRE(batch >= 0, "kvs_paged_decode_static: negative batch");
+  if (batch == 0) return KVS_OK;
+  KVS_REQUIRE(h_kv > 0 && h_q > 0 && h_q % h_kv == 0, "kvs_paged_decode_static: bad head counts");
+  const size_t need = kvs_paged_decode_workspace_size(batch, h_q, h_kv, d);
+  if (need > KVS_DECODE_STATIC_SCRATCH_BYTES)
+    return kvs::fail(KVS_ERR_UNSUPPORTED,
+                     "kvs_paged_decode_static: this batch needs %zu bytes of scratch; the "
+                     "built-in array holds %u (use kvs_paged_decode with a workspace)",
+                     need, static_cast<unsigned>(KVS_DECODE_STATIC_SCRATCH_BYTES));
+  void* scratch = static_scratch_address();
+  if (scratch == nullptr) return KVS_ERR_CUDA;
+  return kvs_paged_decode(q, k_new, v_new, k_pool, v_pool, num_blocks, block_tables, max_blocks,
+                          table_patch, lens, lens_next, batch, h_q, h_kv, d, scale, out, scratch,
+                          KVS_DECODE_STATIC_SCRATCH_BYTES, status, stream);
+}

@@ -57,6 +57,8 @@ _SIGS = {
     "kvs_workspace_zero": (_I32, [_VP, _SZ, _VP]),
     "kvs_paged_decode": (_I32, [_VP, _VP, _VP, _VP, _VP, _I32, _VP, _I32, _VP, _VP, _VP, _I32,
                                 _I32, _I32, _I32, _F32, _VP, _VP, _SZ, _VP, _VP]),
+    "kvs_paged_decode_static": (_I32, [_VP, _VP, _VP, _VP, _VP, _I32, _VP, _I32, _VP, _VP, _VP,
+                                       _I32, _I32, _I32, _I32, _F32, _VP, _VP, _VP]),
     "kvs_alloc_create": (_I32, [_I32, _VP, _I32, ctypes.POINTER(_VP)]),
     "kvs_alloc_destroy": (None, [_VP]),
     "kvs_alloc_block": (_I32, [_VP, _P32]),
@@ -201,6 +203,22 @@ def kvs_paged_decode(q, k_new, v_new, k_pool, v_pool, num_blocks, block_tables, 
         _dev(lens, "i32", "lens"), None if lens_next is None else _dev(lens_next, "i32", "lens_next"),
         batch, h_q, h_kv, d, float(scale), _dev(out, "bf16", "out"),
         _dev(workspace, "u8", "workspace"), workspace_bytes,
+        None if status is None else _dev(status, "i32", "status"), _stream(stream)))
+
+
+def kvs_paged_decode_static(q, k_new, v_new, k_pool, v_pool, num_blocks, block_tables,
+                            max_blocks, table_patch, lens, lens_next, batch, h_q, h_kv, d, scale,
+                            out, status=None, stream=None):
+    """kvs_paged_decode for callers that cannot pass a workspace: the library's
+    built-in device scratch holds the split partials (see include/kvs.h)."""
+    _check(library().kvs_paged_decode_static(
+        _dev(q, "bf16", "q"), None if k_new is None else _dev(k_new, "bf16", "k_new"),
+        None if v_new is None else _dev(v_new, "bf16", "v_new"),
+        _dev(k_pool, "bf16", "k_pool"), _dev(v_pool, "bf16", "v_pool"), num_blocks,
+        _dev(block_tables, "i32", "block_tables"), max_blocks,
+        None if table_patch is None else _dev(table_patch, "i32", "table_patch"),
+        _dev(lens, "i32", "lens"), None if lens_next is None else _dev(lens_next, "i32", "lens_next"),
+        batch, h_q, h_kv, d, float(scale), _dev(out, "bf16", "out"),
         None if status is None else _dev(status, "i32", "status"), _stream(stream)))
 
 
