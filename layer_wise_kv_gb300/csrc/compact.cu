@@ -58,21 +58,39 @@ compact_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
       continue;
     }
     const int slot = j % KVS_BLOCK_TOKENS;
-    for (int c = lane; c < per_slot; c += 32) {
-      const int is_v = c >= h_kv * per_head;
-      const int cc = is_v ? c - h_kv * per_head : c;
-      const int h = cc / per_head;
-      const int part = cc - h * per_head;
-      const int p = kept_idx[item.idx_off + static_cast<int64_t>(h) * item.k_eff + j];
-      if (p < 0 || p >= item.n) {
-        flag_status(status, KVS_ERR_INVALID);
-        continue;
+    // the kept token of every head for this slot, one lane per head
+    const int p_lane = lane < h_kv ? kept_idx[item.idx_off + static_cast<int64_t>(lane) * item.k_eff + j] : 0;
+    // all of the slot's loads in flight before its stores (8 x 16 B per lane
+    // covers 2 x h_kv x d x 2 B up to h_kv * d = 1024)
+    constexpr int kUnroll = 8;
+    for (int c0 = 0; c0 < per_slot; c0 += 32 * kUnroll) {
+      uint4 val[kUnroll];
+      int64_t dst[kUnroll];
+      bool is_v[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int c = c0 + u * 32 + lane;
+        const bool in_range = c < per_slot;
+        is_v[u] = in_range && c >= h_kv * per_head;
+        const int cc = !in_range ? 0 : (is_v[u] ? c - h_kv * per_head : c);
+        const int h = cc / per_head;
+        const int part = cc - h * per_head;
+        const int p = __shfl_sync(0xffffffffu, p_lane, h);  // every lane, every step
+        dst[u] = -1;
+        if (in_range) {
+          if (p < 0 || p >= item.n) {
+            flag_status(status, KVS_ERR_INVALID);
+          } else {
+            const int64_t src = ((item.src_tok + p) * h_kv + h) * per_head + part;
+            val[u] = is_v[u] ? __ldg(v + src) : __ldg(k + src);
+            dst[u] = ((static_cast<int64_t>(block) * h_kv + h) * KVS_BLOCK_TOKENS + slot) *
+                         per_head + part;
+          }
+        }
       }
-      const int64_t src = ((item.src_tok + p) * h_kv + h) * per_head + part;
-      const int64_t dst =
-          ((static_cast<int64_t>(block) * h_kv + h) * KVS_BLOCK_TOKENS + slot) * per_head + part;
-      if (is_v) v_pool[dst] = __ldg(v + src);
-      else k_pool[dst] = __ldg(k + src);
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u)
+        if (dst[u] >= 0) (is_v[u] ? v_pool : k_pool)[dst[u]] = val[u];
     }
   }
 }
@@ -130,6 +148,7 @@ kvs_status kvs_compact_blocks(const kvs_bf16* k, const kvs_bf16* v, const kvs_co
               "kvs_compact_blocks: NULL pointer");
   KVS_SUPPORTED(d == 64 || d == 128, "kvs_compact_blocks: d = %d (supported: 64, 128)", d);
   KVS_REQUIRE(h_kv > 0 && num_blocks > 0, "kvs_compact_blocks: h_kv / num_blocks must be > 0");
+  KVS_SUPPORTED(h_kv <= 32, "kvs_compact_blocks: h_kv = %d (supported: up to 32)", h_kv);
   KVS_REQUIRE(kvs::aligned16(k) && kvs::aligned16(v) && kvs::aligned16(k_pool) &&
                   kvs::aligned16(v_pool),
               "kvs_compact_blocks: K/V and pool pointers must be 16-byte aligned");

@@ -18,13 +18,24 @@
 //               PV_A(j), S_A(j+1), PV_B(j), S_B(j+1): the tensor core works on
 //               one tile while the other tile's softmax runs.
 //   warps 0-3   softmax warpgroup of tile A, warps 4-7 of tile B; one thread
-//               per query row: two passes over its S row in TMEM (row maximum,
-//               then exponentials), causal mask on the diagonal tile, online
-//               maximum in the log2 domain with lazy rescaling (O and l are
-//               rescaled only when the row maximum grows by more than 8, a
-//               factor of 256), P as bf16 written back over S in TMEM; finally
-//               O / l, m and l.
+//               per query row holds its whole 128-key S row in registers: causal
+//               mask on the diagonal tile, online maximum in the log2 domain
+//               (the TMEM loads return each 32-key maximum) with lazy rescaling (O and l are rescaled only when the row
+//               maximum grows by more than 8, a factor of 256), P as bf16
+//               written back over S in TMEM; finally O / l, m and l.
 // TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
+//
+// While the tensor core reads both operands of Q K^T from shared memory it
+// takes nearly all of the shared-memory bandwidth, and every shared-memory
+// access of another thread (an mbarrier test, a flag load) then waits on the
+// order of a hundred cycles.  The MMA queue holds only a few instructions, so
+// the issuing warp keeps shared-memory accesses off the boundaries between
+// MMA groups: it tests the K/V "full" barriers where it waits for the softmax
+// anyway (the loads land long before they are needed), it reads no abort flag
+// in the loop, and it commits only what a consumer waits on.  The commit that signals S_t(j)
+// also covers PV_t(j-1), issued before it, so the softmax may rescale O_t as
+// soon as S_t(j) is visible; O_t's own barrier is committed once, after the last
+// PV_t.
 // Every wait on an mbarrier is bounded; on a timeout the kernel records
 // KVS_ERR_DEVICE_TIMEOUT, drains its own copies and MMAs, frees TMEM and ends.
 #include <cuda_runtime.h>
@@ -64,8 +75,8 @@ struct PrefillSmem {
   static constexpr int kQ = kK + kStagesKV * kTile;
   static constexpr int kBar = kQ + 2 * kTile;
   // barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2],
-  // p_full[2], o_done[2], drain
-  static constexpr int kNumBars = 1 + 4 * kStagesKV + 2 + 2 + 2 + 1;
+  // p_half[2], p_full[2], o_done[2], drain
+  static constexpr int kNumBars = 1 + 4 * kStagesKV + 2 + 2 + 2 + 2 + 1;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr size_t kBytes = 1024 + kMisc + 16;
 };
@@ -86,8 +97,9 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
   uint64_t* v_full = k_empty + kStagesKV;
   uint64_t* v_empty = v_full + kStagesKV;
   uint64_t* s_full = v_empty + kStagesKV;  // [tile]
-  uint64_t* p_full = s_full + 2;           // [tile]
-  uint64_t* o_done = p_full + 2;           // [tile]
+  uint64_t* p_half = s_full + 2;           // [tile]: P of keys 0..63 written
+  uint64_t* p_full = p_half + 2;           // [tile]: all of P written
+  uint64_t* o_done = p_full + 2;           // [tile], one phase: after the tile's last PV
   uint64_t* drain = o_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
@@ -119,7 +131,8 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
-      mbar_init(&p_full[t], kBM);
+      mbar_init(&p_half[t], kBM / 32);  // one arrival per softmax warp
+      mbar_init(&p_full[t], kBM / 32);
       mbar_init(&o_done[t], 1);
     }
     mbar_init(drain, 1);
@@ -175,81 +188,95 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, 0);
-      const uint32_t idesc_o = idesc_bf16_f32(kBM, D, 1);
-      const uint32_t qa = smem_u32(smem + L::kQ);
-      bool ok = mbar_wait(q_full, 0);
-      auto issue_s = [&](int t, int j) {
-        const uint32_t kb = smem_u32(smem + L::kK + (j % kStagesKV) * L::kTile);
-        const uint32_t qt = qa + t * L::kTile;
+    // The whole warp runs the issue loop in lockstep and one elected lane
+    // issues each tcgen05 instruction: with uniform control flow the
+    // descriptor arithmetic stays on the uniform datapath, and the issue does
+    // not starve behind the softmax warps that share this SM sub-partition (a
+    // single lane in a divergent branch needs several times the issue slots).
+    const uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, 0);
+    const uint32_t idesc_o = idesc_bf16_f32(kBM, D, 1);
+    // Base descriptors, built once.  The start-address field holds address
+    // >> 4 in its low 14 bits; every operand lies inside shared memory, so
+    // adding (byte offset >> 4) to the descriptor moves the start address
+    // without touching the other fields.
+    const uint64_t dq = smem_desc_sw128(smem_u32(smem + L::kQ), 16, 1024);
+    const uint64_t dk = smem_desc_sw128(smem_u32(smem + L::kK), 16, 1024);
+    // V: MN-major, 64-column atoms kChunk bytes apart (LBO), 8-key groups
+    // 1024 bytes apart (SBO); 16 keys per K-step = 2048 bytes
+    const uint64_t dv = smem_desc_sw128(smem_u32(smem + L::kV), L::kChunk, 1024);
+    bool ok = true;
+    // a bounded wait, uniform over the warp; on success orders the following
+    // MMAs after it
+    auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+      ok = ok && __all_sync(0xffffffffu, mbar_wait(bar, parity));
+      if (ok) tc_fence_after();
+      return ok;
+    };
+    auto commit = [&](uint64_t* bar) {
+      if (elect_one()) mma_commit(bar);
+    };
+    auto issue_s = [&](int t, int j) {
+      const uint64_t qa = dq + static_cast<uint64_t>((t * L::kTile) >> 4);
+      const uint64_t kb = dk + static_cast<uint64_t>(((j % kStagesKV) * L::kTile) >> 4);
+      const uint32_t d_tmem = tmem + t * 128;
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
+      for (int c = 0; c < D / 64; ++c) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t adesc = smem_desc_sw128(qt + c * L::kChunk + kk * 32, 16, 1024);
-            const uint64_t bdesc = smem_desc_sw128(kb + c * L::kChunk + kk * 32, 16, 1024);
-            mma_ss(tmem + t * 128, adesc, bdesc, idesc_s, (c | kk) != 0 ? 1u : 0u);
-          }
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t off = static_cast<uint64_t>(((c * L::kChunk) >> 4) + kk * 2);
+          if (elect_one()) mma_ss(d_tmem, qa + off, kb + off, idesc_s, (c | kk) != 0 ? 1u : 0u);
         }
-        mma_commit(&s_full[t]);
-      };
-      auto issue_pv = [&](int t, int j) {
-        const uint32_t vb = smem_u32(smem + L::kV + (j % kStagesKV) * L::kTile);
+      }
+      commit(&s_full[t]);
+    };
+    // K-steps [k0, k1) of O_t += P_t V_j
+    auto issue_pv = [&](int t, int j, int k0, int k1) {
+      const uint64_t vb = dv + static_cast<uint64_t>(((j % kStagesKV) * L::kTile) >> 4);
+      const uint32_t o_tmem = tmem + 256 + t * 128;
+      const uint32_t p_tmem = tmem + t * 128;
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          // B = V_j: MN-major, 64-column atoms kChunk bytes apart (LBO), 8-key
-          // groups 1024 bytes apart (SBO); 16 keys per step = 2048 bytes
-          const uint64_t bdesc = smem_desc_sw128(vb + kk * 2048, L::kChunk, 1024);
-          mma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, bdesc, idesc_o,
+      for (int kk = k0; kk < k1; ++kk)
+        if (elect_one())
+          mma_ts(o_tmem, p_tmem + kk * 8, vb + static_cast<uint64_t>(kk * (2048 >> 4)), idesc_o,
                  (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(&o_done[t]);
-      };
-      auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-        if (!ok || *abort_flag) return false;
-        if (!mbar_wait(bar, parity)) {
-          ok = false;
-          return false;
-        }
-        tc_fence_after();
-        return true;
-      };
-      if (ok && wait(&k_full[0], 0)) {
-        issue_s(0, 0);
-        issue_s(1, 0);
-        mma_commit(&k_empty[0]);
-      }
-      for (int j = 0; j < nkv_b && ok && !*abort_flag; ++j) {
-        const int sv = j % kStagesKV;
-        const int sk1 = (j + 1) % kStagesKV;
-        const uint32_t ph_v = (j / kStagesKV) & 1;
-        const uint32_t ph_k1 = ((j + 1) / kStagesKV) & 1;
-        if (!wait(&v_full[sv], ph_v)) break;
-        bool k1_ready = false;
-        if (j < nkv_a) {
-          if (!wait(&p_full[0], j & 1)) break;
-          issue_pv(0, j);
-          if (j + 1 < nkv_a) {
-            if (!wait(&k_full[sk1], ph_k1)) break;
-            k1_ready = true;
-            issue_s(0, j + 1);
-          }
-        }
-        if (!wait(&p_full[1], j & 1)) break;
-        issue_pv(1, j);
-        mma_commit(&v_empty[sv]);
-        if (j + 1 < nkv_b) {
-          if (!k1_ready && !wait(&k_full[sk1], ph_k1)) break;
-          issue_s(1, j + 1);
-          mma_commit(&k_empty[sk1]);
-        }
-      }
-      if (!ok) fail_timeout();
-      // drain: all MMAs we issued are complete before TMEM may be freed
-      mma_commit(drain);
-      mbar_wait(drain, 0);
+    };
+    if (wait(q_full, 0) && wait(&k_full[0], 0)) {
+      issue_s(0, 0);
+      issue_s(1, 0);
+      commit(&k_empty[0]);
     }
+    // K_{j+1} and V_j are waited for at the top of iteration j, where the warp
+    // would otherwise wait for the softmax: both loads were issued about an
+    // iteration earlier and have landed, so no wait sits between MMA groups
+    for (int j = 0; j < nkv_b && ok; ++j) {
+      const bool more = j + 1 < nkv_b;
+      const int s1 = (j + 1) % kStagesKV;
+      if (!wait(&v_full[j % kStagesKV], (j / kStagesKV) & 1)) break;
+      if (more && !wait(&k_full[s1], ((j + 1) / kStagesKV) & 1)) break;
+      if (j < nkv_a) {
+        if (!wait(&p_half[0], j & 1)) break;
+        issue_pv(0, j, 0, kBN / 32);
+        if (!wait(&p_full[0], j & 1)) break;
+        issue_pv(0, j, kBN / 32, kBN / 16);
+        if (j + 1 < nkv_a) issue_s(0, j + 1);
+        else commit(&o_done[0]);
+      }
+      if (!wait(&p_half[1], j & 1)) break;
+      issue_pv(1, j, 0, kBN / 32);
+      if (!wait(&p_full[1], j & 1)) break;
+      issue_pv(1, j, kBN / 32, kBN / 16);
+      commit(&v_empty[j % kStagesKV]);
+      if (more) {
+        issue_s(1, j + 1);
+        commit(&k_empty[s1]);
+      } else {
+        commit(&o_done[1]);
+      }
+    }
+    if (!ok && lane == 0) fail_timeout();
+    // drain: all MMAs we issued are complete before TMEM may be freed
+    commit(drain);
+    __all_sync(0xffffffffu, mbar_wait(drain, 0));
   } else {
     // ------------------------------------------------------------ softmax
     const int t = warp >> 2;              // 0: tile A, 1: tile B
@@ -258,111 +285,99 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t s_tm = tmem + lane_base + t * 128;
     const uint32_t o_tm = tmem + lane_base + 256 + t * 128;
+    const float sl2 = p.scale_log2;
     float m_ref = -INFINITY;              // exponent reference (lazy)
     float m_max = -INFINITY;              // true running maximum (log2 units)
     float l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
-      if (*abort_flag) { ok = false; break; }
       if (!__all_sync(0xffffffffu, mbar_wait(&s_full[t], j & 1))) {
-        fail_timeout();
         ok = false;
         break;
       }
       tc_fence_after();
       const bool diag = j == nkv - 1;     // key column c visible iff c <= r
-      // pass 1: the row maximum, 64 columns (two loads in flight) at a time;
-      // eight independent partial maxima keep the dependent chain short
-      float mx8[8];
+      uint32_t sr[kBN];
+      float mx4[kBN / 32];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
+      for (int c = 0; c < kBN / 32; ++c)
+        mx4[c] = tmem_ld32_max(s_tm + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + c * 32));
+      tmem_wait_ld();
+      // the row maximum: off the diagonal it comes with the loads; on the
+      // diagonal tile only keys c <= r count
+      float mt = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+      if (diag) {
+        float mx8[8];
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t sr[64];
-        tmem_ld32(s_tm + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(sr));
-        tmem_ld32(s_tm + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
-        tmem_wait_ld();
-        if (diag) {
+        for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
 #pragma unroll
-          for (int c = 0; c < 64; ++c)
-            mx8[c & 7] = hf * 64 + c > r ? mx8[c & 7] : fmaxf(mx8[c & 7], __uint_as_float(sr[c]));
-        } else {
-#pragma unroll
-          for (int c = 0; c < 64; c += 16)
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              mx8[i] = fmax3(mx8[i], __uint_as_float(sr[c + i]), __uint_as_float(sr[c + 8 + i]));
-        }
+        for (int c = 0; c < kBN; ++c)
+          mx8[c & 7] = c > r ? mx8[c & 7] : fmaxf(mx8[c & 7], __uint_as_float(sr[c]));
+        mt = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]),
+                   fmaxf(fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       }
-      const float mt = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]),
-                             fmaxf(fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      m_max = fmaxf(m_max, mt * p.scale_log2);
+      m_max = fmaxf(m_max, mt * sl2);
       const bool need = m_max > m_ref + kRescaleThreshold;
       const float m_new = need ? m_max : m_ref;
       const float factor = ex2(m_ref - m_new);  // 1 when unchanged, 0 on the first tile
-      // pass 2: P = exp2(s * scale_log2 - m_new) as bf16 over the S columns;
-      // pairs of columns go through the packed fp32x2 pipe
-      const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
+      if (__any_sync(0xffffffffu, need) && j > 0) {
+        // O holds PV of tiles < j, complete: S_t(j), visible above, was
+        // committed after PV_t(j-1).  Rescale it before the first half of P
+        // lets PV_t(j) start.
+        // (16 columns at a time: the S row is still held in registers)
+#pragma unroll 1
+        for (int c = 0; c < D / 16; ++c) {
+          uint32_t rr[16];
+          tmem_ld16(o_tm + c * 16, rr);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * factor);
+          tmem_st16(o_tm + c * 16, rr);
+        }
+      }
+      // P = exp2(s * scale_log2 - m_new) as bf16 over the first half of the S
+      // columns, 64 keys -> 32 packed columns at a time; each half is
+      // announced as soon as it is in TMEM (one arrival per warp), so PV_t(j)
+      // on keys 0..63 overlaps the exponentials of keys 64..127.  The scaling
+      // and the row sum run on fp32 pairs.
+      const uint64_t sc2 = f2_pack(sl2, sl2);
       const uint64_t nm2 = f2_pack(-m_new, -m_new);
       uint64_t acc2[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc2[i] = f2_pack(0.f, 0.f);
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t sr[64];
-        tmem_ld32(s_tm + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(sr));
-        tmem_ld32(s_tm + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
-        tmem_wait_ld();
+      for (int c = 0; c < kBN / 64; ++c) {
         uint32_t pk[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const int c0 = hf * 64 + 2 * e;
+          const int k0 = c * 64 + 2 * e;
           float t0, t1;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])),
-                           sc2, nm2),
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[k0]), __uint_as_float(sr[k0 + 1])), sc2, nm2),
                     t0, t1);
           float p0 = ex2(t0);
           float p1 = ex2(t1);
           if (diag) {
-            p0 = c0 <= r ? p0 : 0.f;
-            p1 = c0 + 1 <= r ? p1 : 0.f;
+            p0 = k0 <= r ? p0 : 0.f;
+            p1 = k0 + 1 <= r ? p1 : 0.f;
           }
           acc2[e & 3] = f2_add(acc2[e & 3], f2_pack(p0, p1));
           pk[e] = pack_bf16x2(p0, p1);
         }
-        tmem_st32(s_tm + hf * 32, pk);
+        tmem_st32(s_tm + c * 32, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(c == 0 ? &p_half[t] : &p_full[t]);
       }
       float rs0, rs1;
       f2_unpack(f2_add(f2_add(acc2[0], acc2[1]), f2_add(acc2[2], acc2[3])), rs0, rs1);
-      const float rs = rs0 + rs1;
-      l_run = l_run * factor + rs;
+      l_run = l_run * factor + (rs0 + rs1);
       m_ref = m_new;
-      if (__any_sync(0xffffffffu, need) && j > 0) {
-        // O holds PV of tiles < j; once PV(j-1) has landed, rescale it (PV(j)
-        // is issued only after p_full, below)
-        if (!__all_sync(0xffffffffu, mbar_wait(&o_done[t], (j - 1) & 1))) {
-          fail_timeout();
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t rr[32];
-          tmem_ld32(o_tm + c * 32, rr);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * factor);
-          tmem_st32(o_tm + c * 32, rr);
-        }
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&p_full[t]);
     }
+    if (!ok) fail_timeout();
     // epilogue: O / l, m, l (tcgen05.ld is warp-collective: decide per warp)
     ok = __all_sync(0xffffffffu, ok && !*abort_flag);
-    const bool o_ready = ok && __all_sync(0xffffffffu, mbar_wait(&o_done[t], (nkv - 1) & 1));
+    const bool o_ready = ok && __all_sync(0xffffffffu, mbar_wait(&o_done[t], 0));
     if (o_ready) {
       tc_fence_after();
       const int qi = q0 + t * kBM + r;

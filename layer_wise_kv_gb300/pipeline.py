@@ -87,6 +87,7 @@ class Engine:
             self.k_pool.view(torch.int16).fill_(-1)
             self.v_pool.view(torch.int16).fill_(-1)
         self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self._plans = {}
 
     # ------------------------------------------------------------------ checks
     def check_status(self):
@@ -95,6 +96,48 @@ class Engine:
             raise kvs.KvsError(code, "a kernel reported a device-side error")
 
     # ------------------------------------------------------------------ prefill
+    def _plan(self, lens, budgets):
+        """Descriptors that depend only on the prompt lengths and budgets, built
+        once and kept on the device (selection and compaction items, offsets)."""
+        s = self.shape
+        L = s.n_layers
+        key = (tuple(lens), tuple(tuple(b) for b in budgets))
+        plan = self._plans.get(key)
+        if plan is not None:
+            return plan
+        dev = self.device
+        B = len(lens)
+        T = int(sum(lens))
+        cu = np.zeros(B + 1, dtype=np.int32)
+        cu[1:] = np.cumsum(lens)
+        keff = [[(n if budgets[b][l] is None else min(int(budgets[b][l]), n))
+                 for l in range(L)] for b, n in enumerate(lens)]
+        budgeted = [[budgets[b][l] is not None and budgets[b][l] < lens[b] for l in range(L)]
+                    for b in range(B)]
+        sel = np.zeros(B * L, dtype=kvs.SELECT_ITEM)
+        comp = np.zeros(B * L, dtype=kvs.COMPACT_ITEM)
+        idx_off = np.zeros((B, L), dtype=np.int64)
+        off = row = toff = 0
+        for b in range(B):
+            for l in range(L):
+                i = b * L + l
+                sel[i] = (l * s.h_kv * T + cu[b], lens[b],
+                          lens[b] if not budgeted[b][l] else int(budgets[b][l]), off)
+                comp[i] = (l * T + cu[b], off, row, lens[b], keff[b][l], toff, 0)
+                idx_off[b, l] = off
+                off += s.h_kv * keff[b][l]
+                row += keff[b][l]
+                toff += blocks_for(keff[b][l])
+        plan = {"T": T, "max_n": max(lens), "keff": keff, "budgeted": budgeted,
+                "any_budget": [any(budgeted[b][l] for b in range(B)) for l in range(L)],
+                "cu_d": torch.from_numpy(cu).to(dev), "sel_d": _u8(sel, dev),
+                "comp_d": _u8(comp, dev), "idx_off": idx_off, "n_kept": off,
+                "total_rows": row, "n_tables": toff}
+        if len(self._plans) > 64:
+            self._plans.clear()
+        self._plans[key] = plan
+        return plan
+
     def prefill_sparsify(self, q_layers: Sequence[torch.Tensor], k_layers: Sequence[torch.Tensor],
                          v_layers: Sequence[torch.Tensor], seq_lens: Sequence[int],
                          budgets: Sequence[Sequence[Optional[int]]], keep_outputs=False,
@@ -111,20 +154,15 @@ class Engine:
         L = s.n_layers
         lens = [int(x) for x in seq_lens]
         B = len(lens)
-        T = int(sum(lens))
-        cu = np.zeros(B + 1, dtype=np.int32)
-        cu[1:] = np.cumsum(lens)
-        cu_d = torch.from_numpy(cu).to(dev, non_blocking=True)
-        max_n = max(lens)
-        keff = [[(n if budgets[b][l] is None else min(int(budgets[b][l]), n))
-                 for l in range(L)] for b, n in enumerate(lens)]
-        budgeted = [[budgets[b][l] is not None and budgets[b][l] < lens[b] for l in range(L)]
-                    for b in range(B)]
-        any_budget = [any(budgeted[b][l] for b in range(B)) for l in range(L)]
+        plan = self._plan(lens, budgets)
+        T, cu_d, max_n = plan["T"], plan["cu_d"], plan["max_n"]
+        keff, budgeted, any_budget = plan["keff"], plan["budgeted"], plan["any_budget"]
 
         if o_buf is None:
             o_buf = torch.empty((T, s.h_q, s.d), dtype=torch.bfloat16, device=dev)
-        scores = torch.zeros((L, s.h_kv, T), dtype=torch.float32, device=dev)
+        # scores of layers without a budget are never read (their selection is
+        # the identity), so the buffer needs no clearing
+        scores = torch.empty((L, s.h_kv, T), dtype=torch.float32, device=dev)
         keep_m, keep_l, keep_o = [], [], []
         for l in range(L):
             if ml_buf is None or keep_outputs:
@@ -148,55 +186,31 @@ class Engine:
                 keep_o.append(o)
 
         # selection over every (sequence, layer) item
-        sel = np.zeros(B * L, dtype=kvs.SELECT_ITEM)
-        idx_off = np.zeros((B, L), dtype=np.int64)
-        off = 0
-        for b in range(B):
-            for l in range(L):
-                i = b * L + l
-                sel[i]["score_off"] = l * s.h_kv * T + cu[b]
-                sel[i]["n"] = lens[b]
-                sel[i]["k"] = lens[b] if not budgeted[b][l] else int(budgets[b][l])
-                sel[i]["idx_off"] = off
-                idx_off[b, l] = off
-                off += s.h_kv * keff[b][l]
-        kept = torch.empty(max(off, 1), dtype=torch.int32, device=dev)
+        kept = torch.empty(max(plan["n_kept"], 1), dtype=torch.int32, device=dev)
         src_scores = scores if select_scores is None else select_scores
-        kvs.kvs_select_topk(src_scores, T, _u8(sel, dev), B * L, s.h_kv, s.recent, kept,
+        kvs.kvs_select_topk(src_scores, T, plan["sel_d"], B * L, s.h_kv, s.recent, kept,
                             self.status, stream)
 
         # host allocator: sequence by sequence, layer by layer
         tables: List[List[List[int]]] = []
-        flat_tables = []
-        table_off = np.zeros((B, L), dtype=np.int64)
+        flat = np.empty(max(plan["n_tables"], 1), dtype=np.int32)
         toff = 0
         for b in range(B):
             per_layer = []
             for l in range(L):
-                ids = self.alloc.alloc_many(blocks_for(keff[b][l])).tolist()
-                per_layer.append(ids)
-                table_off[b, l] = toff
-                flat_tables.extend(ids)
-                toff += len(ids)
+                ids = self.alloc.alloc_many(blocks_for(keff[b][l]))
+                flat[toff:toff + ids.size] = ids
+                toff += ids.size
+                per_layer.append(ids.tolist())
             tables.append(per_layer)
-        tab_d = torch.tensor(flat_tables if flat_tables else [0], dtype=torch.int32).to(dev)
+        tab_d = torch.from_numpy(flat).pin_memory().to(dev, non_blocking=True)
 
-        comp = np.zeros(B * L, dtype=kvs.COMPACT_ITEM)
-        row = 0
-        for b in range(B):
-            for l in range(L):
-                i = b * L + l
-                comp[i]["src_tok"] = l * T + cu[b]     # K/V of all layers viewed as [L*T][h][d]
-                comp[i]["idx_off"] = idx_off[b, l]
-                comp[i]["row_off"] = row
-                comp[i]["n"] = lens[b]
-                comp[i]["k_eff"] = keff[b][l]
-                comp[i]["table_off"] = table_off[b, l]
-                row += keff[b][l]
         k_all = _stacked(k_layers)
         v_all = _stacked(v_layers)
-        kvs.kvs_compact_blocks(k_all, v_all, _u8(comp, dev), B * L, row, s.h_kv, s.d, kept, tab_d,
-                               self.k_pool, self.v_pool, self.num_blocks, self.status, stream)
+        kvs.kvs_compact_blocks(k_all, v_all, plan["comp_d"], B * L, plan["total_rows"], s.h_kv,
+                               s.d, kept, tab_d, self.k_pool, self.v_pool, self.num_blocks,
+                               self.status, stream)
+        idx_off = plan["idx_off"]
         res = PrefillResult(tables=tables, k_eff=keff, kept_idx=kept, idx_off=idx_off,
                             scores=scores)
         if keep_outputs:
