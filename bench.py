@@ -47,9 +47,23 @@ METRIC = "prefill+sparsify tok/s & decode tok/s (1 GB300, 4000/500); % of roofli
 WORKLOAD = "llama3-8b attention shapes, 1 x 4000-token prompt, 500 decode steps, 32 layers"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM bytes per launch from ncu captures (profiles/); None until captured for
-# the current kernel version.
-NCU_TRAFFIC = {"prefill_attn": None, "paged_decode": None}
+# DRAM bytes (read + write) of one captured launch, from the ncu captures
+# summarised under profiles/, with the algorithmic bytes of that same launch:
+# the figure reported is scaled to the launch the bench times (decode length
+# grows over the request).  Set an entry to None once its kernel changes.
+NCU_TRAFFIC = {
+    "prefill_attn": {"bytes": 49244416 + 2151936, "alg_bytes": None},   # same launch shape
+    "paged_decode": {"bytes": 188675072 + 3436032, "alg_bytes": 187432960},
+}
+
+
+def traffic_for(kernel, alg_bytes=None):
+    t = NCU_TRAFFIC.get(kernel)
+    if t is None:
+        return None
+    if t["alg_bytes"] is None or alg_bytes is None:
+        return int(t["bytes"])
+    return int(round(t["bytes"] * alg_bytes / t["alg_bytes"]))
 
 
 def read_peaks():
@@ -308,18 +322,22 @@ def bench_gpu(args):
                    "recent": w.recent, "budgets": "layers 0-2 full, 2048-64*(l-3)",
                    "l2": "inputs 1.57 GB > L2; 512 MB read between decode steps",
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"kernel": "prefill_attn (tcgen05)", "bound": "tensor",
-                     "achieved": round(tflops, 1), "peak": peak_t, "unit": "TFLOP/s",
-                     "frac": round(tflops / peak_t, 4), "traffic": NCU_TRAFFIC["prefill_attn"],
-                     "peak_source": f"{peak_src} bf16 sustained",
-                     "per_launch_ms": round(k1_avg, 4), "flops_per_launch": flops_launch},
-        "roofline_decode": {"kernel": "paged_decode", "bound": "hbm", "achieved": round(gbs, 1),
-                            "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                            "frac": round(gbs / peaks["hbm_gbs"], 4),
-                            "traffic": NCU_TRAFFIC["paged_decode"],
-                            "peak_source": f"{peak_src} copy bandwidth",
-                            "per_launch_ms": round(dec_avg, 4),
-                            "step_ms": round(sum(dec_ms) / len(dec_ms), 4)},
+        # the dominant kernel of a step by device time: paged decode (about
+        # 87 % of a step's device time)
+        "roofline": {"kernel": "paged_decode (+ split merge, one call)", "bound": "hbm",
+                     "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(gbs / peaks["hbm_gbs"], 4),
+                     "traffic": traffic_for("paged_decode", decode_bytes(w, lens)),
+                     "peak_source": f"{peak_src} copy bandwidth",
+                     "per_launch_ms": round(dec_avg, 4),
+                     "bytes_per_launch": decode_bytes(w, lens),
+                     "step_ms": round(sum(dec_ms) / len(dec_ms), 4)},
+        "roofline_prefill": {"kernel": "prefill_attn (tcgen05)", "bound": "tensor",
+                             "achieved": round(tflops, 1), "peak": peak_t, "unit": "TFLOP/s",
+                             "frac": round(tflops / peak_t, 4),
+                             "traffic": traffic_for("prefill_attn"),
+                             "peak_source": f"{peak_src} bf16 sustained",
+                             "per_launch_ms": round(k1_avg, 4), "flops_per_launch": flops_launch},
         "scores_ms_per_launch": round(sum(k2_ms) / max(1, len(k2_ms)), 4),
         "gpu_launches": args.steps * (2 * L - 3 + 2 + 2 * steps),
         "clocks": clk,
