@@ -19,9 +19,10 @@ decode tokens/s beside it, a roofline object for the dominant kernel
 the same metrics end to end through host buffers, the CPU oracle timed on a
 bounded sample, and the SM clocks sampled during the timed region.
 
-L2: the inputs of one request (1.57 GB of Q/K/V) exceed L2; a 512 MB buffer
-is read between decode steps and between bench steps (outside the timed
-events) so every decode step starts from a cold L2.
+L2: the inputs of one request (1.57 GB of Q/K/V) exceed L2; between decode
+steps and between bench steps (outside the timed events) a 512 MB buffer is
+written and another 512 MB read, so every decode step starts from a cold L2
+with no dirty lines left to write back.
 """
 from __future__ import annotations
 
@@ -245,12 +246,15 @@ def bench_gpu(args):
     ml_buf = (torch.empty((w.h_q, n), dtype=torch.float32, device=dev),
               torch.empty((w.h_q, n), dtype=torch.float32, device=dev))
     scrub = torch.ones(128 << 20, dtype=torch.int32, device=dev)   # 512 MB
+    scrub_r = torch.ones(128 << 20, dtype=torch.int32, device=dev)
     dec = DecodeBatch(eng, 1, n + steps)
 
     def flush():
-        # read 512 MB (> L2) so the next step starts cold, without leaving
-        # dirty lines whose write-back would compete with the timed kernels
-        scrub.sum(dtype=torch.int32)
+        # write 512 MB (> L2) so the next step starts cold, then read another
+        # 512 MB so the dirty lines are written back before, not during, the
+        # timed kernels
+        scrub.fill_(1)
+        scrub_r.sum(dtype=torch.int32)
 
     def new_rec(k1=True):
         return {"prefill": [], "decode": [], "k1": {"attn": [], "scores": []} if k1 else None,
@@ -320,7 +324,7 @@ def bench_gpu(args):
         "config": {"workload": WORKLOAD, "prompt": n, "decode_steps": steps, "layers": L,
                    "h_q": w.h_q, "h_kv": w.h_kv, "d": w.d, "alpha": w.alpha,
                    "recent": w.recent, "budgets": "layers 0-2 full, 2048-64*(l-3)",
-                   "l2": "inputs 1.57 GB > L2; 512 MB read between decode steps",
+                   "l2": "inputs 1.57 GB > L2; 512 MB written then 512 MB read between decode steps (L2 flush)",
                    "parallelism": f"replicas x{world}"},
         # the dominant kernel of a step by device time: paged decode (about
         # 87 % of a step's device time)

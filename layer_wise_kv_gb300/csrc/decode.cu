@@ -33,8 +33,9 @@
 //   writes an unnormalised partial (m, l, o) to its workspace slot (warp index
 //   + segment index, unique) and the segment's first piece records where its
 //   pieces lie.  A second, small kernel (one CTA per segment, every partial
-//   load in flight at once) merges them; the decode kernel itself needs no
-//   fence, atomic or wait between warps.
+//   load in flight at once) merges them; it is a programmatic dependent launch,
+//   set up while decode drains.  The decode kernel itself needs no fence,
+//   atomic or wait between warps.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -207,6 +208,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
   int* prefix = reinterpret_cast<int*>(smem + p.idx_off);  // [batch + 1], in blocks
   int* lens_s = prefix + (p.batch + 1);
 
+  // the merge launched after this grid may be set up now; it waits for this
+  // grid's completion (and the visibility of its writes) before reading
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&k_map);
     tma_prefetch_desc(&v_map);
@@ -547,17 +551,25 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
 
 // Merge of the pieces of every split segment: one CTA per (item, KV head).
 // Pieces are combined as softmax partials: with M the largest piece maximum,
-// out = sum_p exp2(m_p - M) o_p / sum_p exp2(m_p - M) l_p.
-constexpr int kMergeThreads = 128;
-constexpr int kMergeWeights = 4096;
+// out = sum_p exp2(m_p - M) o_p / sum_p exp2(m_p - M) l_p.  The CTA's
+// kMergeGroups thread groups take every kMergeGroups-th piece; a thread owns
+// four output values of one head and folds its pieces in one pass with a
+// running maximum (all of its loads independent, eight pieces in flight);
+// the groups' results are then combined the same way through shared memory.
+// Launched as a programmatic dependent of the decode kernel: the grid is set
+// up while decode drains and waits here until decode's writes are visible.
+constexpr int kMergeGroups = 4;
+constexpr int kMergeGroupThreads = 128;
+constexpr int kMergeThreads = kMergeGroups * kMergeGroupThreads;
 
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads)
 decode_merge_kernel(const float* __restrict__ ws_part, const int32_t* __restrict__ ws_seg,
                     const int32_t* __restrict__ lens, int append, int h_q, int h_kv, int G,
                     uint16_t* __restrict__ out) {
-  __shared__ float wsm[kMergeWeights];
-  __shared__ float Ms[kMaxG], Ls[kMaxG];
+  __shared__ float4 s_acc[kMergeGroups][kMergeGroupThreads];
+  __shared__ float2 s_ml[kMergeGroups][kMergeGroupThreads];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int seg = blockIdx.x;
   const int item = seg / h_kv, h = seg - item * h_kv;
   if (lens[item] + append <= 0) return;  // no tokens: no output row
@@ -566,49 +578,62 @@ decode_merge_kernel(const float* __restrict__ ws_part, const int32_t* __restrict
   if (np <= 1) return;                   // written directly by its only piece
   const int rec = G * (D + 2);
   const float* base = ws_part + static_cast<int64_t>(info.x) * rec;
-  const bool cached = np * G <= kMergeWeights;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int r = warp; r < G; r += kMergeThreads / 32) {
-    float mx = -INFINITY;
-    for (int sp = lane; sp < np; sp += 32)
-      mx = fmaxf(mx, __ldcg(base + static_cast<int64_t>(sp) * rec + G * D + r));
-#pragma unroll
-    for (int o2 = 16; o2 > 0; o2 >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
-    float sum = 0.f;
-    for (int sp = lane; sp < np; sp += 32) {
-      const float* pr = base + static_cast<int64_t>(sp) * rec;
-      const float wgt = ex2(__ldcg(pr + G * D + r) - mx);
-      if (cached) wsm[sp * G + r] = wgt;
-      sum += __ldcg(pr + G * D + G + r) * wgt;
-    }
-#pragma unroll
-    for (int o2 = 16; o2 > 0; o2 >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o2);
-    if (lane == 0) {
-      Ms[r] = mx;
-      Ls[r] = sum;
-    }
-  }
-  __syncthreads();
   const int64_t out_row0 = static_cast<int64_t>(item) * h_q + h * G;
-  for (int e4 = threadIdx.x; e4 < G * D / 4; e4 += kMergeThreads) {
-    const int r = (e4 * 4) / D;
+  const int grp = threadIdx.x / kMergeGroupThreads;
+  const int t = threadIdx.x % kMergeGroupThreads;
+  for (int e0 = 0; e0 < G * D / 4; e0 += kMergeGroupThreads) {
+    const int e4 = e0 + t;
+    const bool act = e4 < G * D / 4;
+    const int r = act ? (e4 * 4) / D : 0;
     const int c = e4 * 4 - r * D;
+    float M = -INFINITY, lsum = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (act) {
 #pragma unroll 8
-    for (int sp = 0; sp < np; ++sp) {
-      const float* pr = base + static_cast<int64_t>(sp) * rec;
-      const float wgt = cached ? wsm[sp * G + r] : ex2(__ldcg(pr + G * D + r) - Ms[r]);
-      const float4 v4 = __ldcg(reinterpret_cast<const float4*>(pr + r * D + c));
-      acc.x += wgt * v4.x;
-      acc.y += wgt * v4.y;
-      acc.z += wgt * v4.z;
-      acc.w += wgt * v4.w;
+      for (int sp = grp; sp < np; sp += kMergeGroups) {
+        const float* pr = base + static_cast<int64_t>(sp) * rec;
+        const float m = __ldcg(pr + G * D + r);
+        const float l = __ldcg(pr + G * D + G + r);
+        const float4 v4 = __ldcg(reinterpret_cast<const float4*>(pr + r * D + c));
+        const float mn = fmaxf(M, m);
+        const float sc = ex2(M - mn);  // 0 on the first piece
+        const float wgt = ex2(m - mn);
+        acc.x = acc.x * sc + wgt * v4.x;
+        acc.y = acc.y * sc + wgt * v4.y;
+        acc.z = acc.z * sc + wgt * v4.z;
+        acc.w = acc.w * sc + wgt * v4.w;
+        lsum = lsum * sc + wgt * l;
+        M = mn;
+      }
     }
-    const float il = 1.0f / Ls[r];
-    uint2 w2;
-    w2.x = pack_bf16x2(acc.x * il, acc.y * il);
-    w2.y = pack_bf16x2(acc.z * il, acc.w * il);
-    *reinterpret_cast<uint2*>(out + (out_row0 + r) * D + c) = w2;
+    s_acc[grp][t] = acc;
+    s_ml[grp][t] = make_float2(M, lsum);
+    __syncthreads();
+    if (grp == 0 && act) {
+      float Mt = -INFINITY;
+#pragma unroll
+      for (int g2 = 0; g2 < kMergeGroups; ++g2) Mt = fmaxf(Mt, s_ml[g2][t].x);
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+      float ls = 0.f;
+#pragma unroll
+      for (int g2 = 0; g2 < kMergeGroups; ++g2) {
+        const float2 ml = s_ml[g2][t];
+        if (ml.x == -INFINITY) continue;  // a group without pieces
+        const float wgt = ex2(ml.x - Mt);
+        const float4 v4 = s_acc[g2][t];
+        a.x += wgt * v4.x;
+        a.y += wgt * v4.y;
+        a.z += wgt * v4.z;
+        a.w += wgt * v4.w;
+        ls += wgt * ml.y;
+      }
+      const float il = 1.0f / ls;
+      uint2 w2;
+      w2.x = pack_bf16x2(a.x * il, a.y * il);
+      w2.y = pack_bf16x2(a.z * il, a.w * il);
+      *reinterpret_cast<uint2*>(out + (out_row0 + r) * D + c) = w2;
+    }
+    __syncthreads();
   }
 }
 
@@ -693,9 +718,22 @@ kvs_status launch_decode(DecodeParams& prm, const CUtensorMap& km, const CUtenso
   const int grid = sm_count_dec() < kMaxGrid ? sm_count_dec() : kMaxGrid;
   paged_decode_kernel<D, NT><<<grid, kDecThreads, smem, stream>>>(km, vm, prm);
   KVS_CHECK_LAUNCH("kvs_paged_decode");
-  decode_merge_kernel<D><<<prm.batch * prm.h_kv, kMergeThreads, 0, stream>>>(
-      prm.ws_part, prm.ws_seg, prm.lens, prm.append, prm.h_q, prm.h_kv, prm.group, prm.out);
-  KVS_CHECK_LAUNCH("kvs_paged_decode (merge)");
+  // the merge as a programmatic dependent launch (it waits for decode inside)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(prm.batch * prm.h_kv));
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  KVS_CUDA(cudaLaunchKernelEx(&cfg, decode_merge_kernel<D>, static_cast<const float*>(prm.ws_part),
+                              static_cast<const int32_t*>(prm.ws_seg),
+                              static_cast<const int32_t*>(prm.lens), prm.append, prm.h_q,
+                              prm.h_kv, prm.group, prm.out),
+           "kvs_paged_decode (merge launch)");
   return KVS_OK;
 }
 

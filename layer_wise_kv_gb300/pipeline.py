@@ -281,7 +281,7 @@ class DecodeBatch:
         self.cow_dst = np.zeros(self.n_items, dtype=np.int32)
         self.cow_d = torch.empty(2 * self.n_items, dtype=torch.int32, device=dev)
         self.ws_bytes = kvs.kvs_paged_decode_workspace_size(self.n_items, s.h_q, s.h_kv, s.d)
-        self.ws = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
+        self.ws = torch.zeros(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
         kvs.kvs_workspace_zero(self.ws, self.ws_bytes)
         self.out = torch.empty((self.n_items, s.h_q, s.d), dtype=torch.bfloat16, device=dev)
 

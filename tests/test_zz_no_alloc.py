@@ -38,7 +38,7 @@ def test_static_scratch_matches_workspace_entry_point():
     lens = torch.tensor(lens_l, dtype=torch.int32, device="cuda")
     ws_bytes = kvs.kvs_paged_decode_workspace_size(batch, h_q, h_kv, d)
     assert ws_bytes <= (16 << 20)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     for call in range(2):                           # two calls in a row
         q = torch.randn(batch, h_q, d, device="cuda").bfloat16()
