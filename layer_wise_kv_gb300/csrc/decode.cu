@@ -217,7 +217,15 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
     for (int i = 0; i < kWarps * NS; ++i) mbar_init(reinterpret_cast<uint64_t*>(smem + p.bar_off) + i, 1);
     fence_mbar_init();
   }
-  for (int b = threadIdx.x; b < p.batch; b += kDecThreads) lens_s[b] = p.lens[b];
+  for (int b = threadIdx.x; b < p.batch; b += kDecThreads) {
+    const int len = p.lens[b];
+    lens_s[b] = len;
+    // an item with nothing to attend has no pieces: mark its segments empty in
+    // the split index (every other segment is written by its first piece)
+    if (blockIdx.x == 0 && len + p.append <= 0)
+      for (int hh = 0; hh < p.h_kv; ++hh)
+        *reinterpret_cast<int2*>(p.ws_seg + 2 * (b * p.h_kv + hh)) = make_int2(0, 0);
+  }
   __syncthreads();
   // prefix over items of (blocks x heads); one warp, each lane a contiguous range
   if (warp == 0) {
@@ -565,17 +573,15 @@ constexpr int kMergeThreads = kMergeGroups * kMergeGroupThreads;
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads)
 decode_merge_kernel(const float* __restrict__ ws_part, const int32_t* __restrict__ ws_seg,
-                    const int32_t* __restrict__ lens, int append, int h_q, int h_kv, int G,
-                    uint16_t* __restrict__ out) {
+                    int h_q, int h_kv, int G, uint16_t* __restrict__ out) {
   __shared__ float4 s_acc[kMergeGroups][kMergeGroupThreads];
   __shared__ float2 s_ml[kMergeGroups][kMergeGroupThreads];
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int seg = blockIdx.x;
   const int item = seg / h_kv, h = seg - item * h_kv;
-  if (lens[item] + append <= 0) return;  // no tokens: no output row
   const int2 info = *reinterpret_cast<const int2*>(ws_seg + 2 * seg);
   const int np = info.y;
-  if (np <= 1) return;                   // written directly by its only piece
+  if (np <= 1) return;  // written directly by its only piece, or no tokens at all
   const int rec = G * (D + 2);
   const float* base = ws_part + static_cast<int64_t>(info.x) * rec;
   const int64_t out_row0 = static_cast<int64_t>(item) * h_q + h * G;
@@ -730,9 +736,8 @@ kvs_status launch_decode(DecodeParams& prm, const CUtensorMap& km, const CUtenso
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   KVS_CUDA(cudaLaunchKernelEx(&cfg, decode_merge_kernel<D>, static_cast<const float*>(prm.ws_part),
-                              static_cast<const int32_t*>(prm.ws_seg),
-                              static_cast<const int32_t*>(prm.lens), prm.append, prm.h_q,
-                              prm.h_kv, prm.group, prm.out),
+                              static_cast<const int32_t*>(prm.ws_seg), prm.h_q, prm.h_kv,
+                              prm.group, prm.out),
            "kvs_paged_decode (merge launch)");
   return KVS_OK;
 }
