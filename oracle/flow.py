@@ -123,18 +123,31 @@ def prepare_append(pool, stream: Stream, layer, pool_k=None, pool_v=None):
     return None
 
 
-def append_and_attend(w, stream: Stream, layer, q_bits, k_bits, v_bits, pool_k, pool_v):
-    """Write the step's k/v at slot len, then attend over len + 1 tokens.
-    q_bits [H_q, d], k_bits/v_bits [H_kv, d].  Returns out [H_q, d] float64."""
+def append(stream: Stream, layer, k_bits, v_bits, pool_k, pool_v):
+    """Write the step's k/v [H_kv, d] at slot len of (stream, layer); len + 1."""
     L = stream.lens[layer]
     t = stream.tables[layer]
     b, s = t[L // BLOCK], L % BLOCK
     pool_k[b, :, s] = k_bits
     pool_v[b, :, s] = v_bits
     stream.lens[layer] = L + 1
-    kc = np.stack([gather_rows(pool_k, t, L + 1, h) for h in range(w.h_kv)])
-    vc = np.stack([gather_rows(pool_v, t, L + 1, h) for h in range(w.h_kv)])
+
+
+def attend(w, stream: Stream, layer, q_bits, pool_k, pool_v):
+    """Decode attention of q [H_q, d] over the len tokens of (stream, layer),
+    read back through its block table.  Returns out [H_q, d] float64."""
+    L = stream.lens[layer]
+    t = stream.tables[layer]
+    kc = np.stack([gather_rows(pool_k, t, L, h) for h in range(w.h_kv)])
+    vc = np.stack([gather_rows(pool_v, t, L, h) for h in range(w.h_kv)])
     return decode_attention(_f64(q_bits), _f64(kc), _f64(vc), w.scale)
+
+
+def append_and_attend(w, stream: Stream, layer, q_bits, k_bits, v_bits, pool_k, pool_v):
+    """Write the step's k/v at slot len, then attend over len + 1 tokens.
+    q_bits [H_q, d], k_bits/v_bits [H_kv, d].  Returns out [H_q, d] float64."""
+    append(stream, layer, k_bits, v_bits, pool_k, pool_v)
+    return attend(w, stream, layer, q_bits, pool_k, pool_v)
 
 
 def retire(pool, stream: Stream):

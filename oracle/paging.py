@@ -90,6 +90,7 @@ def compact(k, v, idx, table, pool_k, pool_v, block=BLOCK):
 
 
 def gather_rows(pool, table, length, h, block=BLOCK):
-    """Read slots 0..length-1 of head h back through the table: [length, d]."""
-    return np.stack([pool[table[j // block], h, j % block] for j in range(length)]) \
-        if length > 0 else pool[:0, h, 0]
+    """Read slots 0..length-1 of head h back through the table: [length, d].
+    Slot j is slot j % block of block table[j // block]."""
+    j = np.arange(length)
+    return pool[np.asarray(table, dtype=np.int64)[j // block], h, j % block]
