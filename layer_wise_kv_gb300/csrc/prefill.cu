@@ -8,11 +8,19 @@
 // maximum and l (small outputs, slight cost) so the scoring pass can rebuild
 // softmax probabilities without a second attention pass.
 //
-// Kernel layout (one CTA per (query head, pair of 128-query tiles, sequence);
-// the lower tile A and the upper tile B share every K/V tile):
-//   warp 8      TMA producer: Q_A and Q_B once, then K_j / V_j tiles (128 keys
-//               x d, 128-byte swizzle) into 2-stage rings.
-//   warp 9      MMA issuer (one thread): S_t = Q_t K_j^T into TMEM (M=N=128,
+// Work items are (query head, pair of 128-row query tiles, sequence); the
+// lower tile A and the upper tile B of a pair share every K/V tile.  The CTAs
+// are persistent (one per SM) and walk the items in a snake order over a
+// numbering that runs from the longest pairs down, keeping TMEM, barriers and
+// the K/V ring across items: the next item's Q load and first QK^T overlap the
+// current item's last tiles and epilogue, and only the first item of a CTA
+// pays the start-up.
+// Kernel layout:
+//   warp 8      TMA producer: per item Q_A, K_0, Q_B, V_0, then K_j / V_j tiles
+//               (128 keys x d, 128-byte swizzle) into 2-stage rings; an L2
+//               prefetch of the next item's Q.
+//   warp 9      MMA issuer (the whole warp, one elected lane per instruction):
+//               S_t = Q_t K_j^T into TMEM (M=N=128,
 //               K=d) and O_t += P_t V_j with P_t read from TMEM as the A operand
 //               and V_j as an MN-major shared-memory B operand.  Issue order
 //               PV_A(j), S_A(j+1), PV_B(j), S_B(j+1): the tensor core works on
@@ -61,7 +69,8 @@ struct PrefillParams {
   float* l;
   const int32_t* cu_seqlens;
   int32_t* status;
-  int total, h_q, h_kv, group, n_pairs_max;
+  int total, h_q, h_kv, group, n_pairs_max, batch;
+  int n_items;  // h_q x batch x n_pairs_max work items (some empty)
   float scale_log2;
 };
 
@@ -74,12 +83,45 @@ struct PrefillSmem {
   static constexpr int kK = kV + kStagesKV * kTile;
   static constexpr int kQ = kK + kStagesKV * kTile;
   static constexpr int kBar = kQ + 2 * kTile;
-  // barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2],
-  // p_half[2], p_full[2], o_done[2], drain
-  static constexpr int kNumBars = 1 + 4 * kStagesKV + 2 + 2 + 2 + 2 + 1;
+  // barriers: q_full[2], q_empty[2], k_full[2], k_empty[2], v_full[2],
+  // v_empty[2], s_full[2], p_half[2], p_full[2], o_done[2], drain
+  static constexpr int kNumBars = 4 + 4 * kStagesKV + 2 + 2 + 2 + 2 + 1;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr size_t kBytes = 1024 + kMisc + 16;
 };
+
+// A work item: one query head g of one pair of 128-row query tiles (A: rows
+// q0 .. q0+127, B: q0+128 .. q0+255, q0 = 256 pr) of sequence b.  Items are
+// numbered pair rank from the top of the sequence (y) slowest, then sequence,
+// then head, so the numbering runs from the longest pairs down; an item whose
+// sequence has fewer than y + 1 pairs is empty.
+struct PItem {
+  bool valid;
+  int g, pr, seq0, n;
+  // causal: tile A sees key tiles 0 .. 2pr, tile B 0 .. 2pr+1
+  __device__ __forceinline__ int nkv_a() const { return 2 * pr + 1; }
+  __device__ __forceinline__ int nkv_b() const { return 2 * pr + 2; }
+};
+
+__device__ __forceinline__ PItem item_at(int idx, const PrefillParams& p) {
+  PItem it;
+  it.g = idx % p.h_q;
+  const int rest = idx / p.h_q;
+  const int b = rest % p.batch;
+  const int y = rest / p.batch;
+  it.seq0 = p.cu_seqlens[b];
+  it.n = p.cu_seqlens[b + 1] - it.seq0;
+  const int npairs = (it.n + 2 * kBM - 1) / (2 * kBM);
+  it.pr = npairs - 1 - y;
+  it.valid = it.pr >= 0;
+  return it;
+}
+
+// The k-th item of CTA c out of G persistent CTAs: a snake over the item
+// numbering (c, 2G-1-c, 2G+c, ...), which evens out the descending sizes.
+__device__ __forceinline__ int item_pos(int k, int c, int G) {
+  return k * G + ((k & 1) ? (G - 1 - c) : c);
+}
 
 template <int D>
 __global__ void __launch_bounds__(kPrefillThreads, 1)
@@ -91,30 +133,21 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
-  uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;
+  uint64_t* q_full = bars;                 // [tile]
+  uint64_t* q_empty = bars + 2;            // [tile]: the item's S_t MMAs are done with Q_t
+  uint64_t* k_full = bars + 4;
   uint64_t* k_empty = k_full + kStagesKV;
   uint64_t* v_full = k_empty + kStagesKV;
   uint64_t* v_empty = v_full + kStagesKV;
   uint64_t* s_full = v_empty + kStagesKV;  // [tile]
   uint64_t* p_half = s_full + 2;           // [tile]: P of keys 0..63 written
   uint64_t* p_full = p_half + 2;           // [tile]: all of P written
-  uint64_t* o_done = p_full + 2;           // [tile], one phase: after the tile's last PV
+  uint64_t* o_done = p_full + 2;           // [tile]: one phase per item, after its last PV
   uint64_t* drain = o_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
 
-  const int g = blockIdx.x;   // query head
-  const int b = blockIdx.z;   // sequence
-  const int seq0 = p.cu_seqlens[b];
-  const int n = p.cu_seqlens[b + 1] - seq0;
-  const int npairs = (n + 2 * kBM - 1) / (2 * kBM);
-  const int pr = npairs - 1 - static_cast<int>(blockIdx.y);  // longest pairs first
-  if (pr < 0) return;
-  const int q0 = pr * 2 * kBM;   // first query of tile A (within the sequence)
-  const int nkv_a = 2 * pr + 1;  // causal: key tiles 0 .. 2pr for tile A
-  const int nkv_b = 2 * pr + 2;  //         key tiles 0 .. 2pr+1 for tile B
-  const int hk = g / p.group;    // KV head
+  const int cta = blockIdx.x, n_cta = gridDim.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (warp == 0) {
@@ -122,7 +155,10 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
     tmem_relinquish();
   }
   if (tid == 0) {
-    mbar_init(q_full, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&q_full[t], 1);
+      mbar_init(&q_empty[t], 1);
+    }
     for (int s = 0; s < kStagesKV; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
@@ -151,39 +187,75 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer
+    // Per item: Q_A (once the previous item's last S_A is done with the
+    // buffer), K_0, Q_B (once its last S_B is done), V_0, then K_j / V_j.
+    // K_0 and Q_A come first because the MMA warp starts the item's S_A(0)
+    // inside the previous item's last iteration.
     if (lane == 0) {
-      int issued_k = 0, issued_v = 0;
-      mbar_arrive_expect_tx(q_full, 2 * L::kTile);
-#pragma unroll
-      for (int t = 0; t < 2; ++t)
+      int n_qt[2] = {0, 0}, n_k = 0, n_v = 0;  // Q_t, K and V tiles issued so far
+      bool ok = true;
+      auto load_q = [&](int t, const PItem& it) -> bool {
+        if (n_qt[t] > 0 && !mbar_wait(&q_empty[t], (n_qt[t] - 1) & 1)) return false;
+        mbar_arrive_expect_tx(&q_full[t], L::kTile);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + L::kQ + t * L::kTile + c * L::kChunk, &q_map, q_full, c * 64, g,
-                      seq0 + q0 + t * kBM);
-      for (int j = 0; j < nkv_b && !*abort_flag; ++j) {
-        const int s = j % kStagesKV;
-        const uint32_t ph = (j / kStagesKV) & 1;
-        const int tok = seq0 + j * kBN;
-        if (!mbar_wait(&k_empty[s], ph ^ 1)) { fail_timeout(); break; }
+          tma_load_3d(smem + L::kQ + t * L::kTile + c * L::kChunk, &q_map, &q_full[t], c * 64,
+                      it.g, it.seq0 + it.pr * 2 * kBM + t * kBM);
+        ++n_qt[t];
+        return true;
+      };
+      auto load_k = [&](const PItem& it, int hk, int j) -> bool {
+        const int s = n_k % kStagesKV;
+        if (!mbar_wait(&k_empty[s], ((n_k / kStagesKV) & 1) ^ 1)) return false;
         mbar_arrive_expect_tx(&k_full[s], L::kTile);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
           tma_load_3d(smem + L::kK + s * L::kTile + c * L::kChunk, &k_map, &k_full[s], c * 64, hk,
-                      tok);
-        ++issued_k;
-        if (!mbar_wait(&v_empty[s], ph ^ 1)) { fail_timeout(); break; }
+                      it.seq0 + j * kBN);
+        ++n_k;
+        return true;
+      };
+      auto load_v = [&](const PItem& it, int hk, int j) -> bool {
+        const int s = n_v % kStagesKV;
+        if (!mbar_wait(&v_empty[s], ((n_v / kStagesKV) & 1) ^ 1)) return false;
         mbar_arrive_expect_tx(&v_full[s], L::kTile);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
           tma_load_3d(smem + L::kV + s * L::kTile + c * L::kChunk, &v_map, &v_full[s], c * 64, hk,
-                      tok);
-        ++issued_v;
+                      it.seq0 + j * kBN);
+        ++n_v;
+        return true;
+      };
+      for (int k = 0; ok && !*abort_flag; ++k) {
+        const int pos = item_pos(k, cta, n_cta);
+        if (pos >= p.n_items) break;
+        const PItem it = item_at(pos, p);
+        if (!it.valid) continue;
+        const int hk = it.g / p.group;
+        ok = load_q(0, it) && load_k(it, hk, 0) && load_q(1, it) && load_v(it, hk, 0);
+        if (!ok) break;
+        // the next item's Q is read once, from HBM: start it towards L2 now
+        for (int k2 = k + 1;; ++k2) {
+          const int pos2 = item_pos(k2, cta, n_cta);
+          if (pos2 >= p.n_items) break;
+          const PItem nx = item_at(pos2, p);
+          if (!nx.valid) continue;
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c)
+              tma_prefetch_3d(&q_map, c * 64, nx.g, nx.seq0 + nx.pr * 2 * kBM + t * kBM);
+          break;
+        }
+        for (int j = 1; j < it.nkv_b() && ok; ++j) ok = load_k(it, hk, j) && load_v(it, hk, j);
       }
+      if (!ok) fail_timeout();
       // drain: every load we issued has landed before the CTA may exit
-      mbar_wait(q_full, 0);
-      for (int j = issued_k > kStagesKV ? issued_k - kStagesKV : 0; j < issued_k; ++j)
+      for (int t = 0; t < 2; ++t)
+        if (n_qt[t] > 0) mbar_wait(&q_full[t], (n_qt[t] - 1) & 1);
+      for (int j = n_k > kStagesKV ? n_k - kStagesKV : 0; j < n_k; ++j)
         if (!mbar_wait(&k_full[j % kStagesKV], (j / kStagesKV) & 1)) break;
-      for (int j = issued_v > kStagesKV ? issued_v - kStagesKV : 0; j < issued_v; ++j)
+      for (int j = n_v > kStagesKV ? n_v - kStagesKV : 0; j < n_v; ++j)
         if (!mbar_wait(&v_full[j % kStagesKV], (j / kStagesKV) & 1)) break;
     }
   } else if (warp == 9) {
@@ -215,9 +287,10 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
     auto commit = [&](uint64_t* bar) {
       if (elect_one()) mma_commit(bar);
     };
-    auto issue_s = [&](int t, int j) {
+    // S_t = Q_t K^T with K in ring stage s
+    auto issue_s = [&](int t, int s) {
       const uint64_t qa = dq + static_cast<uint64_t>((t * L::kTile) >> 4);
-      const uint64_t kb = dk + static_cast<uint64_t>(((j % kStagesKV) * L::kTile) >> 4);
+      const uint64_t kb = dk + static_cast<uint64_t>((s * L::kTile) >> 4);
       const uint32_t d_tmem = tmem + t * 128;
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
@@ -229,49 +302,107 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
       }
       commit(&s_full[t]);
     };
-    // K-steps [k0, k1) of O_t += P_t V_j
-    auto issue_pv = [&](int t, int j, int k0, int k1) {
-      const uint64_t vb = dv + static_cast<uint64_t>(((j % kStagesKV) * L::kTile) >> 4);
+    // K-steps [k0, k1) of O_t += P_t V with V in ring stage s; the item's
+    // first key tile (first) overwrites O_t
+    auto issue_pv = [&](int t, int s, bool first, int k0, int k1) {
+      const uint64_t vb = dv + static_cast<uint64_t>((s * L::kTile) >> 4);
       const uint32_t o_tmem = tmem + 256 + t * 128;
       const uint32_t p_tmem = tmem + t * 128;
 #pragma unroll
       for (int kk = k0; kk < k1; ++kk)
         if (elect_one())
           mma_ts(o_tmem, p_tmem + kk * 8, vb + static_cast<uint64_t>(kk * (2048 >> 4)), idesc_o,
-                 (j > 0 || kk > 0) ? 1u : 0u);
+                 (!first || kk > 0) ? 1u : 0u);
     };
-    if (wait(q_full, 0) && wait(&k_full[0], 0)) {
-      issue_s(0, 0);
-      issue_s(1, 0);
-      commit(&k_empty[0]);
-    }
     // K_{j+1} and V_j are waited for at the top of iteration j, where the warp
     // would otherwise wait for the softmax: both loads were issued about an
-    // iteration earlier and have landed, so no wait sits between MMA groups
-    for (int j = 0; j < nkv_b && ok; ++j) {
-      const bool more = j + 1 < nkv_b;
-      const int s1 = (j + 1) % kStagesKV;
-      if (!wait(&v_full[j % kStagesKV], (j / kStagesKV) & 1)) break;
-      if (more && !wait(&k_full[s1], ((j + 1) / kStagesKV) & 1)) break;
-      if (j < nkv_a) {
-        if (!wait(&p_half[0], j & 1)) break;
-        issue_pv(0, j, 0, kBN / 32);
-        if (!wait(&p_full[0], j & 1)) break;
-        issue_pv(0, j, kBN / 32, kBN / 16);
-        if (j + 1 < nkv_a) issue_s(0, j + 1);
-        else commit(&o_done[0]);
+    // iteration earlier and have landed, so no wait sits between MMA groups.
+    // Item boundaries are pipelined: the next item's S_A(0) is issued right
+    // after this item's last PV_A (its Q_A and K_0 are loaded by then) and its
+    // S_B(0) right after the last PV_B, so each softmax warpgroup finds its
+    // next tile ready when it leaves its epilogue.  The softmax's first P of
+    // an item is written after it has read the previous item's O, so the
+    // p_half wait also orders the item's first PV (which overwrites O) after
+    // that read.
+    int k_next = 0;
+    auto next_item = [&]() -> PItem {
+      for (;; ++k_next) {
+        const int pos = item_pos(k_next, cta, n_cta);
+        if (pos >= p.n_items) {
+          PItem none;
+          none.valid = false;
+          return none;
+        }
+        const PItem it = item_at(pos, p);
+        if (it.valid) {
+          ++k_next;
+          return it;
+        }
       }
-      if (!wait(&p_half[1], j & 1)) break;
-      issue_pv(1, j, 0, kBN / 32);
-      if (!wait(&p_full[1], j & 1)) break;
-      issue_pv(1, j, kBN / 32, kBN / 16);
-      commit(&v_empty[j % kStagesKV]);
-      if (more) {
-        issue_s(1, j + 1);
-        commit(&k_empty[s1]);
-      } else {
-        commit(&o_done[1]);
+    };
+    int n_q = 0, ring = 0, n_pa = 0, n_pb = 0;  // items, ring tiles, P tiles of A / B
+    PItem cur = next_item();
+    // the first item's S_A(0), S_B(0)
+    if (cur.valid && wait(&q_full[0], 0) && wait(&k_full[0], 0)) {
+      issue_s(0, 0);
+      if (cur.nkv_a() == 1) commit(&q_empty[0]);
+      if (wait(&q_full[1], 0)) {
+        issue_s(1, 0);
+        commit(&k_empty[0]);
       }
+    }
+    while (cur.valid && ok) {
+      const PItem nxt = next_item();
+      const int ring_n = ring + cur.nkv_b();  // ring position of the next item's K_0 / V_0
+      const uint32_t qph = (n_q + 1) & 1;   // the next item's Q phase
+      for (int j = 0; j < cur.nkv_b(); ++j) {
+        const int r = ring + j;  // ring position of key tile j
+        const bool more = j + 1 < cur.nkv_b();
+        const int s = r % kStagesKV, s1 = (r + 1) % kStagesKV;
+        if (!wait(&v_full[s], (r / kStagesKV) & 1)) break;
+        if (more && !wait(&k_full[s1], ((r + 1) / kStagesKV) & 1)) break;
+        if (j < cur.nkv_a()) {
+          if (!wait(&p_half[0], n_pa & 1)) break;
+          issue_pv(0, s, j == 0, 0, kBN / 32);
+          if (!wait(&p_full[0], n_pa & 1)) break;
+          issue_pv(0, s, j == 0, kBN / 32, kBN / 16);
+          ++n_pa;
+          if (j + 1 < cur.nkv_a()) {
+            issue_s(0, s1);
+            if (j + 2 == cur.nkv_a()) commit(&q_empty[0]);  // the item's last S_A
+          } else {
+            commit(&o_done[0]);
+            if (nxt.valid) {                                // the next item's S_A(0)
+              if (!wait(&q_full[0], qph) ||
+                  !wait(&k_full[ring_n % kStagesKV], (ring_n / kStagesKV) & 1))
+                break;
+              issue_s(0, ring_n % kStagesKV);
+              if (nxt.nkv_a() == 1) commit(&q_empty[0]);
+            }
+          }
+        }
+        if (!wait(&p_half[1], n_pb & 1)) break;
+        issue_pv(1, s, j == 0, 0, kBN / 32);
+        if (!wait(&p_full[1], n_pb & 1)) break;
+        issue_pv(1, s, j == 0, kBN / 32, kBN / 16);
+        ++n_pb;
+        commit(&v_empty[s]);
+        if (more) {
+          issue_s(1, s1);
+          commit(&k_empty[s1]);
+          if (j + 2 == cur.nkv_b()) commit(&q_empty[1]);     // the item's last S_B
+        } else {
+          commit(&o_done[1]);
+          if (nxt.valid) {                                  // the next item's S_B(0)
+            if (!wait(&q_full[1], qph)) break;
+            issue_s(1, ring_n % kStagesKV);
+            commit(&k_empty[ring_n % kStagesKV]);
+          }
+        }
+      }
+      ++n_q;
+      ring = ring_n;
+      cur = nxt;
     }
     if (!ok && lane == 0) fail_timeout();
     // drain: all MMAs we issued are complete before TMEM may be freed
@@ -281,17 +412,40 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
     // ------------------------------------------------------------ softmax
     const int t = warp >> 2;              // 0: tile A, 1: tile B
     const int r = tid & 127;              // row of the tile (TMEM lane)
-    const int nkv = t == 0 ? nkv_a : nkv_b;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t s_tm = tmem + lane_base + t * 128;
     const uint32_t o_tm = tmem + lane_base + 256 + t * 128;
     const float sl2 = p.scale_log2;
+    bool ok = true;
+    int n_s = 0, n_it = 0;                // S tiles and items of this tile slot so far
+    int k_next = 0;
+    // the next non-empty item of this CTA (looked up an item ahead, so its
+    // loads of the sequence bounds stay off the path between items)
+    auto next_item = [&]() -> PItem {
+      for (;; ++k_next) {
+        const int pos = item_pos(k_next, cta, n_cta);
+        if (pos >= p.n_items) {
+          PItem none;
+          none.valid = false;
+          return none;
+        }
+        const PItem x = item_at(pos, p);
+        if (x.valid) {
+          ++k_next;
+          return x;
+        }
+      }
+    };
+    PItem it_next = next_item();
+    while (ok && it_next.valid) {
+    const PItem it = it_next;
+    it_next = next_item();
+    const int nkv = t == 0 ? it.nkv_a() : it.nkv_b();
     float m_ref = -INFINITY;              // exponent reference (lazy)
     float m_max = -INFINITY;              // true running maximum (log2 units)
     float l_run = 0.f;
-    bool ok = true;
-    for (int j = 0; j < nkv; ++j) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[t], j & 1))) {
+    for (int j = 0; j < nkv; ++j, ++n_s) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[t], n_s & 1))) {
         ok = false;
         break;
       }
@@ -374,42 +528,46 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
       l_run = l_run * factor + (rs0 + rs1);
       m_ref = m_new;
     }
-    if (!ok) fail_timeout();
-    // epilogue: O / l, m, l (tcgen05.ld is warp-collective: decide per warp)
-    ok = __all_sync(0xffffffffu, ok && !*abort_flag);
-    const bool o_ready = ok && __all_sync(0xffffffffu, mbar_wait(&o_done[t], 0));
-    if (o_ready) {
-      tc_fence_after();
-      const int qi = q0 + t * kBM + r;
-      const bool row_ok = qi < n;
+    if (!ok) break;
+    // epilogue of the item: O / l, m, l (tcgen05.ld is warp-collective:
+    // decide per warp).  The O reads complete (wait::ld) before this warp
+    // writes the next item's first P, which is what lets that item's first PV
+    // overwrite O.
+    const bool o_ready = __all_sync(0xffffffffu, !*abort_flag && mbar_wait(&o_done[t], n_it & 1));
+    ++n_it;
+    if (!o_ready) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    {
+      const int qi = it.pr * 2 * kBM + t * kBM + r;
+      const bool row_ok = qi < it.n;
       const float inv_l = 1.0f / l_run;
-      uint16_t* orow = p.o + (static_cast<int64_t>(seq0 + qi) * p.h_q + g) * D;
+      uint32_t rr[D];
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t rr[32];
-        tmem_ld32(o_tm + c * 32, rr);
-        tmem_wait_ld();
-        if (row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(rr[8 * v + 0]) * inv_l, __uint_as_float(rr[8 * v + 1]) * inv_l);
-            w.y = pack_bf16x2(__uint_as_float(rr[8 * v + 2]) * inv_l, __uint_as_float(rr[8 * v + 3]) * inv_l);
-            w.z = pack_bf16x2(__uint_as_float(rr[8 * v + 4]) * inv_l, __uint_as_float(rr[8 * v + 5]) * inv_l);
-            w.w = pack_bf16x2(__uint_as_float(rr[8 * v + 6]) * inv_l, __uint_as_float(rr[8 * v + 7]) * inv_l);
-            dst[v] = w;
-          }
-        }
-      }
+      for (int c = 0; c < D / 32; ++c)
+        tmem_ld32(o_tm + c * 32, *reinterpret_cast<uint32_t(*)[32]>(rr + c * 32));
+      tmem_wait_ld();
       if (row_ok) {
-        const int64_t at = static_cast<int64_t>(g) * p.total + seq0 + qi;
+        uint4* dst = reinterpret_cast<uint4*>(
+            p.o + (static_cast<int64_t>(it.seq0 + qi) * p.h_q + it.g) * D);
+#pragma unroll
+        for (int v = 0; v < D / 8; ++v) {
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(rr[8 * v + 0]) * inv_l, __uint_as_float(rr[8 * v + 1]) * inv_l);
+          w.y = pack_bf16x2(__uint_as_float(rr[8 * v + 2]) * inv_l, __uint_as_float(rr[8 * v + 3]) * inv_l);
+          w.z = pack_bf16x2(__uint_as_float(rr[8 * v + 4]) * inv_l, __uint_as_float(rr[8 * v + 5]) * inv_l);
+          w.w = pack_bf16x2(__uint_as_float(rr[8 * v + 6]) * inv_l, __uint_as_float(rr[8 * v + 7]) * inv_l);
+          dst[v] = w;
+        }
+        const int64_t at = static_cast<int64_t>(it.g) * p.total + it.seq0 + qi;
         p.m[at] = m_max * kLn2;
         p.l[at] = l_run * ex2(m_ref - m_max);
       }
-    } else if (ok) {
-      fail_timeout();
     }
+    }  // items
+    if (!ok) fail_timeout();
   }
   tc_fence_before();
   __syncthreads();
@@ -444,7 +602,12 @@ kvs_status launch_prefill(const PrefillMaps& mp, const PrefillParams& prm, int b
              "kvs_prefill_attn_lse: raising the shared-memory limit");
     configured = true;
   }
-  dim3 grid(prm.h_q, prm.n_pairs_max, batch);
+  // persistent: one CTA per SM (fewer if there are fewer items)
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (sms <= 0) sms = 1;
+  const int grid = prm.n_items < sms ? prm.n_items : sms;
   prefill_attn_kernel<D><<<grid, kPrefillThreads, PrefillSmem<D>::kBytes, st>>>(mp.qm, mp.km,
                                                                                mp.vm, prm);
   KVS_CHECK_LAUNCH("kvs_prefill_attn_lse");
@@ -481,8 +644,11 @@ extern "C" kvs_status kvs_prefill_attn_lse(const kvs_bf16* q, const kvs_bf16* k,
   prm.h_kv = h_kv;
   prm.group = h_q / h_kv;
   prm.n_pairs_max = (max_n + 2 * kvs::kBM - 1) / (2 * kvs::kBM);
+  prm.batch = batch;
   prm.scale_log2 = scale * kvs::kLog2eP;
-  KVS_REQUIRE(prm.n_pairs_max <= 65535, "kvs_prefill_attn_lse: max_n too large");
+  KVS_REQUIRE(static_cast<int64_t>(prm.n_pairs_max) * batch * h_q < (1ll << 31),
+              "kvs_prefill_attn_lse: too many work items");
+  prm.n_items = prm.n_pairs_max * batch * h_q;
 
   static thread_local kvs::PrefillMaps cache;
   if (cache.q != q || cache.k != k || cache.v != v || cache.total != total_tokens ||
