@@ -175,6 +175,10 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
     *abort_flag = 0;
     fence_mbar_init();
   }
+  // launched as a programmatic dependent: the set-up above overlaps the
+  // previous kernel's tail; nothing in global memory is touched before it ends
+  griddep_launch_dependents();
+  griddep_wait();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -608,9 +612,20 @@ kvs_status launch_prefill(const PrefillMaps& mp, const PrefillParams& prm, int b
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (sms <= 0) sms = 1;
   const int grid = prm.n_items < sms ? prm.n_items : sms;
-  prefill_attn_kernel<D><<<grid, kPrefillThreads, PrefillSmem<D>::kBytes, st>>>(mp.qm, mp.km,
-                                                                               mp.vm, prm);
-  KVS_CHECK_LAUNCH("kvs_prefill_attn_lse");
+  // a programmatic dependent launch: the kernel waits for the previous grid on
+  // the stream before it reads or writes global memory
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kPrefillThreads);
+  cfg.dynamicSmemBytes = PrefillSmem<D>::kBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  KVS_CUDA(cudaLaunchKernelEx(&cfg, prefill_attn_kernel<D>, mp.qm, mp.km, mp.vm, prm),
+           "kvs_prefill_attn_lse (launch)");
   return KVS_OK;
 }
 

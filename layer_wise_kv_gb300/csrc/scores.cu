@@ -68,6 +68,10 @@ window_scores_kernel(const __grid_constant__ CUtensorMap k_map,
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
+  // launched as a programmatic dependent: wait for the previous grid on the
+  // stream (its m and l) before touching global memory
+  griddep_launch_dependents();
+  griddep_wait();
   const int b = blockIdx.z;
   const int h = blockIdx.y;
   const int seq0 = p.cu_seqlens[b];
@@ -204,9 +208,18 @@ kvs_status launch_scores(const CUtensorMap& km, const CUtensorMap& qm, const Sco
              "kvs_window_scores: raising the shared-memory limit");
     configured = true;
   }
-  dim3 grid((max_n + kKeyTile - 1) / kKeyTile, prm.h_kv, batch);
-  window_scores_kernel<D><<<grid, kScoreThreads, smem, st>>>(km, qm, prm);
-  KVS_CHECK_LAUNCH("kvs_window_scores");
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((max_n + kKeyTile - 1) / kKeyTile, prm.h_kv, batch);
+  cfg.blockDim = dim3(kScoreThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  KVS_CUDA(cudaLaunchKernelEx(&cfg, window_scores_kernel<D>, km, qm, prm),
+           "kvs_window_scores (launch)");
   return KVS_OK;
 }
 

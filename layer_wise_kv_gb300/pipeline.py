@@ -142,13 +142,16 @@ class Engine:
                          v_layers: Sequence[torch.Tensor], seq_lens: Sequence[int],
                          budgets: Sequence[Sequence[Optional[int]]], keep_outputs=False,
                          o_buf=None, ml_buf=None, select_scores: Optional[torch.Tensor] = None,
-                         stream=None, timing=None) -> PrefillResult:
+                         stream=None, timing=None, timing_layers=None) -> PrefillResult:
         """q_layers[l]: [T][h_q][d] bf16, k/v_layers[l]: [T][h_kv][d] (T = sum of
         seq_lens, sequences packed).  budgets[b][l]: k_l for sequence b (None =
         full cache).  select_scores: optional [L][h_kv][T] scores to select on
         instead of the ones computed here.  timing: optional dict of lists
         "attn" / "scores" that receive a (start, end) CUDA event pair around
-        every prefill-attention / window-score launch."""
+        the prefill-attention / window-score launches of the layers in
+        timing_layers (every layer when None).  An event recorded between two
+        launches ends the overlap of the second one's start with the first
+        one's tail, so timing a few layers disturbs the stream less."""
         s = self.shape
         dev = self.device
         L = s.n_layers
@@ -171,12 +174,13 @@ class Engine:
             else:
                 m, lsum = ml_buf
             o = o_buf if not keep_outputs else torch.empty_like(o_buf)
-            ev = _events(timing, "attn", stream)
+            tl = timing if (timing_layers is None or l in timing_layers) else None
+            ev = _events(tl, "attn", stream)
             kvs.kvs_prefill_attn_lse(q_layers[l], k_layers[l], v_layers[l], o, m, lsum, cu_d, B,
                                      max_n, T, s.h_q, s.h_kv, s.d, s.scale, self.status, stream)
             _close(ev, stream)
             if any_budget[l]:
-                ev = _events(timing, "scores", stream)
+                ev = _events(tl, "scores", stream)
                 kvs.kvs_window_scores(q_layers[l], k_layers[l], m, lsum, scores[l], cu_d, B, max_n,
                                       T, s.h_q, s.h_kv, s.d, s.alpha, s.scale, self.status, stream)
                 _close(ev, stream)
