@@ -53,8 +53,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # the figure reported is scaled to the launch the bench times (decode length
 # grows over the request).  Set an entry to None once its kernel changes.
 NCU_TRAFFIC = {
-    "prefill_attn": None,
-    "paged_decode": None,
+    "prefill_attn": {"bytes": 49450496 + 2089216, "alg_bytes": None},   # same launch shape
+    "paged_decode": {"bytes": 188697600 + 3535616, "alg_bytes": 187432960},
 }
 
 
