@@ -65,6 +65,23 @@ NCU_TRAFFIC = {
 TIMED_LAYERS = (5, 15, 25)
 
 
+def max_over_ranks(values, world, dist, device):
+    """Per-rank times (ms) -> the largest over all ranks, elementwise (the
+    job's time is its slowest replica's).  world == 1: unchanged."""
+    if world <= 1:
+        return list(values)
+    import torch
+    tt = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return tt.tolist()
+
+
+def job_rates(t_pre_ms, t_dec_ms, world, n, steps):
+    """Whole-job rates over `world` replicas: prompt tokens/s and decode
+    tokens/s from the slowest replica's times."""
+    return world * n / (t_pre_ms / 1e3), world * steps / (t_dec_ms / 1e3)
+
+
 def traffic_for(kernel, alg_bytes=None):
     t = NCU_TRAFFIC.get(kernel)
     if t is None:
@@ -294,12 +311,8 @@ def bench_gpu(args):
     k2_ms = [a.elapsed_time(b) for a, b in rec["k1"]["scores"]]
     t_pre = sum(pre_ms) / args.steps            # ms per request
     t_dec = sum(dec_ms) / args.steps
-    if world > 1:
-        tt = torch.tensor([t_pre, t_dec], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_pre, t_dec = tt.tolist()
-    prefill_tok_s = world * n / (t_pre / 1e3)
-    decode_tok_s = world * steps / (t_dec / 1e3)
+    t_pre, t_dec = max_over_ranks([t_pre, t_dec], world, dist, dev)
+    prefill_tok_s, decode_tok_s = job_rates(t_pre, t_dec, world, n, steps)
 
     peaks, peak_src = read_peaks()
     k1_avg = sum(k1_ms) / len(k1_ms)
@@ -383,15 +396,13 @@ def bench_e2e(args, eng, dec, w, n, steps, q, k, v, dq, dk, dv, o_buf, ml_buf, f
                     host=host)
     t_pre = sum(a.elapsed_time(b) for a, b in rec["prefill"]) / reps
     t_dec = sum(a.elapsed_time(b) for a, b in rec["decode"]) / reps
-    if world > 1:
-        tt = torch.tensor([t_pre, t_dec], dtype=torch.float64, device=q.device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_pre, t_dec = tt.tolist()
+    t_pre, t_dec = max_over_ranks([t_pre, t_dec], world, dist, q.device)
     kept_bytes = sum(w.k_eff(l, n) for l in range(w.n_layers)) * w.h_kv * 4
     h2d = (q.numel() + k.numel() + v.numel()) * 2 + (dq.numel() + dk.numel() + dv.numel()) * 2
     d2h = kept_bytes + steps * w.n_layers * w.h_q * w.d * 2
-    return {"value": round(world * n / (t_pre / 1e3), 1), "unit": "tok/s",
-            "decode_tok_s": round(world * steps / (t_dec / 1e3), 1),
+    pre_rate, dec_rate = job_rates(t_pre, t_dec, world, n, steps)
+    return {"value": round(pre_rate, 1), "unit": "tok/s",
+            "decode_tok_s": round(dec_rate, 1),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "steps": reps}
 
