@@ -193,10 +193,10 @@ kvs_status kvs_copy_blocks(const int32_t* src, const int32_t* dst, int32_t count
  *   lens_next    [batch] int32, nullable, must not alias lens: receives
  *                lens[i] + (k_new != NULL).
  *   workspace    scratch of kvs_paged_decode_workspace_size(batch, h_q, h_kv,
- *                d) bytes (split partials and their index); needs no
- *                initialisation.  Calls sharing a workspace must not overlap in
- *                time.
- * Two launches on `stream`: the split decode, then a merge of the splits.
+ *                d) bytes (split partials); needs no initialisation.  Calls
+ *                sharing a workspace must not overlap in time.
+ * Two launches on `stream`: the split decode, then a merge of the splits (a
+ * programmatic dependent launch that waits for the decode's partials).
  * An item with zero tokens to attend (lens[i] == 0 and no append) gets no
  * output row.
  * ---------------------------------------------------------------------- */
@@ -228,14 +228,14 @@ kvs_status kvs_paged_decode(const kvs_bf16* q, const kvs_bf16* k_new, const kvs_
  * allocating library routine.
  *   - Sizes whose workspace (kvs_paged_decode_workspace_size) exceeds the
  *     array are rejected with KVS_ERR_UNSUPPORTED before any launch.  With
- *     h_q = 32, h_kv = 8, d = 128 the array serves up to 621 items (one
+ *     h_q = 32, h_kv = 8, d = 128 the array serves up to 624 items (one
  *     32-layer sequence is 32 items and needs about 7 MB).
  *   - The first call on a device looks up the array's device address on that
  *     device (the current one); make that first call before any stream
  *     capture.
  *   - All calls share the one array and it keeps the last call's contents;
- *     nothing in it needs to start at zero (each call writes its split index
- *     and partials before reading them).  Calls that overlap on the GPU (on
+ *     nothing in it needs to start at zero (each call writes its partials
+ *     before reading them).  Calls that overlap on the GPU (on
  *     different streams, or from different threads) race on it.
  * ---------------------------------------------------------------------- */
 #define KVS_DECODE_STATIC_SCRATCH_BYTES (16u << 20)

@@ -31,10 +31,10 @@
 //   count off the issue slots; the bound is HBM.
 // * A segment covered by one piece writes `out` directly; otherwise each piece
 //   writes an unnormalised partial (m, l, o) to its workspace slot (warp index
-//   + segment index, unique) and the segment's first piece records where its
-//   pieces lie.  A second, small kernel (one CTA per segment, every partial
-//   load in flight at once) merges them; it is a programmatic dependent launch,
-//   set up while decode drains.  The decode kernel itself needs no fence,
+//   + segment index, unique).  A second, small kernel (one CTA per segment,
+//   every partial load in flight at once) merges them; it is a programmatic
+//   dependent launch that recomputes the split from the lengths while decode
+//   drains and only then waits for decode's partials.  The decode kernel itself needs no fence,
 //   atomic or wait between warps.
 #include <cuda_runtime.h>
 
@@ -75,7 +75,6 @@ struct DecodeParams {
   int32_t* lens_next;
   uint16_t* out;
   float* ws_part;
-  int32_t* ws_seg;  // [segments][2]: first partial slot, number of pieces
   int32_t* status;
   int batch, max_blocks, num_blocks, h_q, h_kv, group, append, n_stages;
   int q_bytes, q_stride, q_off, bar_off, idx_off;
@@ -217,15 +216,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
     for (int i = 0; i < kWarps * NS; ++i) mbar_init(reinterpret_cast<uint64_t*>(smem + p.bar_off) + i, 1);
     fence_mbar_init();
   }
-  for (int b = threadIdx.x; b < p.batch; b += kDecThreads) {
-    const int len = p.lens[b];
-    lens_s[b] = len;
-    // an item with nothing to attend has no pieces: mark its segments empty in
-    // the split index (every other segment is written by its first piece)
-    if (blockIdx.x == 0 && len + p.append <= 0)
-      for (int hh = 0; hh < p.h_kv; ++hh)
-        *reinterpret_cast<int2*>(p.ws_seg + 2 * (b * p.h_kv + hh)) = make_int2(0, 0);
-  }
+  for (int b = threadIdx.x; b < p.batch; b += kDecThreads) lens_s[b] = p.lens[b];
   __syncthreads();
   // prefix over items of (blocks x heads); one warp, each lane a contiguous range
   if (warp == 0) {
@@ -526,9 +517,6 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
           }
         }
     }
-    // where the segment's pieces lie, for the merge kernel (its first piece)
-    if (lane == 0 && cur.blk0 == 0)
-      *reinterpret_cast<int2*>(p.ws_seg + 2 * cur.seg) = make_int2(cur.first_slot, cur.npieces);
     // table patch and length bookkeeping, once per item (its head-0 segment start)
     if (lane == 0 && cur.blk0 == 0 && cur.h == 0) {
       if (p.append && p.patch != nullptr && p.patch[cur.item] >= 0)
@@ -572,18 +560,43 @@ constexpr int kMergeThreads = kMergeGroups * kMergeGroupThreads;
 
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads)
-decode_merge_kernel(const float* __restrict__ ws_part, const int32_t* __restrict__ ws_seg,
-                    int h_q, int h_kv, int G, uint16_t* __restrict__ out) {
+decode_merge_kernel(const float* __restrict__ ws_part, const int32_t* __restrict__ lens, int batch,
+                    int append, int h_q, int h_kv, int G, int n_warps,
+                    uint16_t* __restrict__ out) {
   __shared__ float4 s_acc[kMergeGroups][kMergeGroupThreads];
   __shared__ float2 s_ml[kMergeGroups][kMergeGroupThreads];
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  __shared__ int s_total, s_before;
   const int seg = blockIdx.x;
   const int item = seg / h_kv, h = seg - item * h_kv;
-  const int2 info = *reinterpret_cast<const int2*>(ws_seg + 2 * seg);
-  const int np = info.y;
-  if (np <= 1) return;  // written directly by its only piece, or no tokens at all
+  // The decode kernel's split, recomputed from the lengths (an input of the
+  // decode, read before waiting for it): T blocks over W = min(T, n_warps)
+  // equal warp ranges; this segment's pieces are the ranges w_lo .. w_hi.
+  {
+    const int per = (batch + kMergeThreads - 1) / kMergeThreads;
+    const int b0 = threadIdx.x * per, b1 = min(batch, b0 + per);
+    int sum = 0, before = 0;
+    for (int b = b0; b < b1; ++b) {
+      const int nbk = (lens[b] + append + KVS_BLOCK_TOKENS - 1) / KVS_BLOCK_TOKENS * h_kv;
+      if (b < item) before += nbk;
+      sum += nbk;
+    }
+    if (threadIdx.x == 0) s_total = s_before = 0;
+    __syncthreads();
+    atomicAdd(&s_total, sum);
+    atomicAdd(&s_before, before);
+    __syncthreads();
+  }
+  const int64_t T = s_total;
+  const int nb = (lens[item] + append + KVS_BLOCK_TOKENS - 1) / KVS_BLOCK_TOKENS;
+  if (nb == 0) return;  // no tokens: no output row
+  const int64_t seg_lo = s_before + static_cast<int64_t>(h) * nb;
+  const int W = static_cast<int>(T < n_warps ? T : n_warps);
+  const int w_lo = owner_of(seg_lo, T, W);
+  const int np = owner_of(seg_lo + nb - 1, T, W) - w_lo + 1;
+  if (np <= 1) return;  // written directly by its only piece
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int rec = G * (D + 2);
-  const float* base = ws_part + static_cast<int64_t>(info.x) * rec;
+  const float* base = ws_part + static_cast<int64_t>(w_lo + seg) * rec;
   const int64_t out_row0 = static_cast<int64_t>(item) * h_q + h * G;
   const int grp = threadIdx.x / kMergeGroupThreads;
   const int t = threadIdx.x % kMergeGroupThreads;
@@ -666,9 +679,6 @@ bool pool_map(MapCache& c, const void* pool, int num_blocks, int h_kv, int d) {
   return true;
 }
 
-int64_t seg_bytes(int batch, int h_kv) {
-  return (static_cast<int64_t>(batch) * h_kv * 8 + 255) / 256 * 256;
-}
 
 int sm_count_dec() {
   static int n = 0;
@@ -736,8 +746,8 @@ kvs_status launch_decode(DecodeParams& prm, const CUtensorMap& km, const CUtenso
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   KVS_CUDA(cudaLaunchKernelEx(&cfg, decode_merge_kernel<D>, static_cast<const float*>(prm.ws_part),
-                              static_cast<const int32_t*>(prm.ws_seg), prm.h_q, prm.h_kv,
-                              prm.group, prm.out),
+                              prm.lens, prm.batch, prm.append, prm.h_q, prm.h_kv, prm.group,
+                              grid * kWarps, prm.out),
            "kvs_paged_decode (merge launch)");
   return KVS_OK;
 }
@@ -753,7 +763,7 @@ size_t kvs_paged_decode_workspace_size(int32_t batch, int32_t h_q, int32_t h_kv,
   // one partial slot per (warp, segment it touches): slot = warp + segment
   const int64_t slots = static_cast<int64_t>(kvs::kMaxGrid) * kvs::kWarps +
                         static_cast<int64_t>(batch) * h_kv;
-  return static_cast<size_t>(kvs::seg_bytes(batch, h_kv) + slots * G * (d + 2) * 4);
+  return static_cast<size_t>(slots * G * (d + 2) * 4);
 }
 
 kvs_status kvs_paged_decode(const kvs_bf16* q, const kvs_bf16* k_new, const kvs_bf16* v_new,
@@ -785,7 +795,6 @@ kvs_status kvs_paged_decode(const kvs_bf16* q, const kvs_bf16* k_new, const kvs_
                   (reinterpret_cast<uintptr_t>(out) & 15) == 0,
               "kvs_paged_decode: q, out and pools must be 16-byte aligned");
   const int64_t G = h_q / h_kv;
-  const int64_t cbytes = kvs::seg_bytes(batch, h_kv);
   const size_t need = kvs_paged_decode_workspace_size(batch, h_q, h_kv, d);
   KVS_REQUIRE(workspace_bytes >= need, "kvs_paged_decode: workspace %zu bytes < %zu needed",
               workspace_bytes, need);
@@ -805,8 +814,7 @@ kvs_status kvs_paged_decode(const kvs_bf16* q, const kvs_bf16* k_new, const kvs_
   prm.lens = lens;
   prm.lens_next = lens_next;
   prm.out = out;
-  prm.ws_seg = static_cast<int32_t*>(workspace);
-  prm.ws_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + cbytes);
+  prm.ws_part = static_cast<float*>(workspace);
   prm.status = status;
   prm.batch = batch;
   prm.max_blocks = max_blocks;
