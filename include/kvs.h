@@ -185,7 +185,7 @@ kvs_status kvs_copy_blocks(const int32_t* src, const int32_t* dst, int32_t count
  * otherwise over lens[i] tokens.  Per query head g (KV head g / G):
  *     out[i][g] = softmax_t(scale * q[i][g] . K_t) V
  *   q, out [batch][h_q][d]; k_new, v_new [batch][h_kv][d] (nullable)
- *   block_tables [batch][max_blocks] int32; lens [batch] int32 (batch <= 4096)
+ *   block_tables [batch][max_blocks] int32; lens [batch] int32 (batch <= 2048)
  *   table_patch  [batch] int32, nullable: entry >= 0 replaces
  *                block_tables[i][lens[i] / 16] before use and is written
  *                back there (the host allocator's new or copied-on-write
@@ -195,6 +195,8 @@ kvs_status kvs_copy_blocks(const int32_t* src, const int32_t* dst, int32_t count
  *   workspace    scratch of kvs_paged_decode_workspace_size(batch, h_q, h_kv,
  *                d) bytes (split partials); needs no initialisation.  Calls
  *                sharing a workspace must not overlap in time.
+ *   q, out, the pools and the workspace must be 16-byte aligned
+ *   (KVS_ERR_INVALID otherwise).
  * Two launches on `stream`: the split decode, then a merge of the splits (a
  * programmatic dependent launch that waits for the decode's partials).
  * An item with zero tokens to attend (lens[i] == 0 and no append) gets no

@@ -124,6 +124,12 @@ __device__ __forceinline__ uint32_t sw_off(int r, int c) {
                                (((c & 7) ^ (r & 7)) << 4));
 }
 
+// floats in one partial record: G rows of D accumulators, then the G maxima and
+// the G sums, padded to whole float4s so that every record starts 16-byte
+// aligned (the merge reads records as float4; G*(D+2) floats alone are not a
+// multiple of four when G is odd)
+__host__ __device__ constexpr int part_floats(int G, int D) { return (G * (D + 2) + 3) & ~3; }
+
 // owner warp of global block b when T blocks are split evenly over W warps
 // (warp w owns [w*T/W, (w+1)*T/W))
 __device__ __forceinline__ int owner_of(int64_t b, int64_t T, int W) {
@@ -497,7 +503,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
           }
         }
     } else {
-      const int rec = G * (D + 2);
+      const int rec = part_floats(G, D);
       float* part = p.ws_part + static_cast<int64_t>(w + cur.seg) * rec;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
@@ -595,7 +601,7 @@ decode_merge_kernel(const float* __restrict__ ws_part, const int32_t* __restrict
   const int np = owner_of(seg_lo + nb - 1, T, W) - w_lo + 1;
   if (np <= 1) return;  // written directly by its only piece
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int rec = G * (D + 2);
+  const int rec = part_floats(G, D);
   const float* base = ws_part + static_cast<int64_t>(w_lo + seg) * rec;
   const int64_t out_row0 = static_cast<int64_t>(item) * h_q + h * G;
   const int grp = threadIdx.x / kMergeGroupThreads;
@@ -763,7 +769,7 @@ size_t kvs_paged_decode_workspace_size(int32_t batch, int32_t h_q, int32_t h_kv,
   // one partial slot per (warp, segment it touches): slot = warp + segment
   const int64_t slots = static_cast<int64_t>(kvs::kMaxGrid) * kvs::kWarps +
                         static_cast<int64_t>(batch) * h_kv;
-  return static_cast<size_t>(slots * G * (d + 2) * 4);
+  return static_cast<size_t>(slots * kvs::part_floats(static_cast<int>(G), d) * 4);
 }
 
 kvs_status kvs_paged_decode(const kvs_bf16* q, const kvs_bf16* k_new, const kvs_bf16* v_new,
@@ -792,8 +798,9 @@ kvs_status kvs_paged_decode(const kvs_bf16* q, const kvs_bf16* k_new, const kvs_
   KVS_REQUIRE((reinterpret_cast<uintptr_t>(k_pool) & 15) == 0 &&
                   (reinterpret_cast<uintptr_t>(v_pool) & 15) == 0 &&
                   (reinterpret_cast<uintptr_t>(q) & 15) == 0 &&
-                  (reinterpret_cast<uintptr_t>(out) & 15) == 0,
-              "kvs_paged_decode: q, out and pools must be 16-byte aligned");
+                  (reinterpret_cast<uintptr_t>(out) & 15) == 0 &&
+                  (reinterpret_cast<uintptr_t>(workspace) & 15) == 0,
+              "kvs_paged_decode: q, out, pools and workspace must be 16-byte aligned");
   const int64_t G = h_q / h_kv;
   const size_t need = kvs_paged_decode_workspace_size(batch, h_q, h_kv, d);
   KVS_REQUIRE(workspace_bytes >= need, "kvs_paged_decode: workspace %zu bytes < %zu needed",

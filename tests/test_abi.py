@@ -60,6 +60,9 @@ def test_invalid_arguments_rejected_before_launch(kvs):
     rc = lib.kvs_paged_decode(1, None, None, 1, 1, 4, 1, 4, None, 1, None, 1, 8, 8, 96,
                               0.1, 1, 1, 1 << 20, None, None)
     assert rc == kvs.KVS_ERR_UNSUPPORTED and "d = 96" in kvs.last_error()
+    rc = lib.kvs_paged_decode(256, None, None, 256, 256, 4, 256, 4, None, 256, None, 1, 32, 8,
+                              128, 0.1, 256, 264, 1 << 20, None, None)  # workspace at 8 mod 16
+    assert rc == kvs.KVS_ERR_INVALID and "workspace" in kvs.last_error()
     assert lib.kvs_window_scores(1, 1, 1, 1, 1, 1, 1, 64, 64, 32, 8, 128, 128, 0.1, None,
                                  None) == kvs.KVS_ERR_UNSUPPORTED  # alpha * G > 256
     assert lib.kvs_prefill_attn_lse(1, 1, 1, 1, 1, 1, 1, 1, 16, 16, 6, 4, 128, 0.1, None,

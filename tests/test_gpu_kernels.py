@@ -225,7 +225,8 @@ def test_window_scores_vs_oracle(lens, h_q, h_kv, d, alpha):
 # ---------------------------------------------------------------------------
 # paged decode with appends, several splits, copy-on-write blocks
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("h_q,h_kv,d", [(32, 8, 128), (4, 2, 64), (16, 1, 128)])
+@pytest.mark.parametrize("h_q,h_kv,d", [(32, 8, 128), (4, 2, 64), (16, 1, 128), (6, 2, 128),
+                                        (4, 4, 64)])
 def test_paged_decode_vs_oracle(h_q, h_kv, d):
     kvs = kvs_lib()
     rng = np.random.default_rng(h_q * d)
@@ -267,8 +268,8 @@ def test_paged_decode_vs_oracle(h_q, h_kv, d):
         vn = _randn_bits(rng, (n_items, h_kv, d))
         cur = step % 2
         if step == 5:
-            # merge counters tagged with a call number no call will have: the
-            # kernel must treat them as zero (leftovers of some other call)
+            # leftovers of some other call in the partial slots: every slot a
+            # call reads must be one it wrote
             ws.fill_(0xAB)
         kvs.kvs_paged_decode(dev_bf16(q), dev_bf16(kn), dev_bf16(vn), k_pool, v_pool, N,
                              tables_d, max_blocks, torch.from_numpy(patch).cuda(), lens_d[cur],
@@ -297,3 +298,4 @@ def test_paged_decode_vs_oracle(h_q, h_kv, d):
     np.testing.assert_array_equal(host_bits(k_pool), pk)
     np.testing.assert_array_equal(host_bits(v_pool), pv)
     a.close()
+
