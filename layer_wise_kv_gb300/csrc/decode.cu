@@ -555,17 +555,18 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
 // Pieces are combined as softmax partials: with M the largest piece maximum,
 // out = sum_p exp2(m_p - M) o_p / sum_p exp2(m_p - M) l_p.  The CTA's
 // kMergeGroups thread groups take every kMergeGroups-th piece; a thread owns
-// four output values of one head and folds its pieces in one pass with a
-// running maximum (all of its loads independent, eight pieces in flight);
+// four output values of one head and folds its pieces in batches of up to
+// kMergeBatch, all loads of a batch in flight together, with a running maximum;
 // the groups' results are then combined the same way through shared memory.
 // Launched as a programmatic dependent of the decode kernel: the grid is set
 // up while decode drains and waits here until decode's writes are visible.
 constexpr int kMergeGroups = 4;
 constexpr int kMergeGroupThreads = 128;
 constexpr int kMergeThreads = kMergeGroups * kMergeGroupThreads;
+constexpr int kMergeBatch = 6;
 
 template <int D>
-__global__ void __launch_bounds__(kMergeThreads)
+__global__ void __launch_bounds__(kMergeThreads, 2)
 decode_merge_kernel(const float* __restrict__ ws_part, const int32_t* __restrict__ lens, int batch,
                     int append, int h_q, int h_kv, int G, int n_warps,
                     uint16_t* __restrict__ out) {
@@ -614,20 +615,45 @@ decode_merge_kernel(const float* __restrict__ ws_part, const int32_t* __restrict
     float M = -INFINITY, lsum = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (act) {
-#pragma unroll 8
-      for (int sp = grp; sp < np; sp += kMergeGroups) {
-        const float* pr = base + static_cast<int64_t>(sp) * rec;
-        const float m = __ldcg(pr + G * D + r);
-        const float l = __ldcg(pr + G * D + G + r);
-        const float4 v4 = __ldcg(reinterpret_cast<const float4*>(pr + r * D + c));
-        const float mn = fmaxf(M, m);
-        const float sc = ex2(M - mn);  // 0 on the first piece
-        const float wgt = ex2(m - mn);
-        acc.x = acc.x * sc + wgt * v4.x;
-        acc.y = acc.y * sc + wgt * v4.y;
-        acc.z = acc.z * sc + wgt * v4.z;
-        acc.w = acc.w * sc + wgt * v4.w;
-        lsum = lsum * sc + wgt * l;
+      // pieces in batches of kMergeBatch per thread: every load of a batch is
+      // issued before any is used (a guarded body, not a loop remainder, so
+      // short folds do not serialise their L2 round trips)
+      for (int sp0 = grp; sp0 < np; sp0 += kMergeGroups * kMergeBatch) {
+        float mm[kMergeBatch], ll[kMergeBatch];
+        float4 vv[kMergeBatch];
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) {
+          const int sp = sp0 + u * kMergeGroups;
+          mm[u] = -INFINITY;
+          ll[u] = 0.f;
+          vv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (sp < np) {
+            const float* pr = base + static_cast<int64_t>(sp) * rec;
+            mm[u] = __ldcg(pr + G * D + r);
+            ll[u] = __ldcg(pr + G * D + G + r);
+            vv[u] = __ldcg(reinterpret_cast<const float4*>(pr + r * D + c));
+          }
+        }
+        float mn = M;
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) mn = fmaxf(mn, mm[u]);
+        const float sc = ex2(M - mn);  // 0 on the first batch (M = -inf, mn finite)
+        acc.x *= sc;
+        acc.y *= sc;
+        acc.z *= sc;
+        acc.w *= sc;
+        lsum *= sc;
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) {
+          if (sp0 + u * kMergeGroups < np) {
+            const float wgt = ex2(mm[u] - mn);
+            acc.x += wgt * vv[u].x;
+            acc.y += wgt * vv[u].y;
+            acc.z += wgt * vv[u].z;
+            acc.w += wgt * vv[u].w;
+            lsum += wgt * ll[u];
+          }
+        }
         M = mn;
       }
     }
