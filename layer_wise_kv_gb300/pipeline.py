@@ -142,7 +142,9 @@ class Engine:
                          v_layers: Sequence[torch.Tensor], seq_lens: Sequence[int],
                          budgets: Sequence[Sequence[Optional[int]]], keep_outputs=False,
                          o_buf=None, ml_buf=None, select_scores: Optional[torch.Tensor] = None,
-                         stream=None, timing=None, timing_layers=None) -> PrefillResult:
+                         stream=None, timing=None, timing_layers=None,
+                         ready: Optional[Sequence[Sequence[torch.cuda.Event]]] = None
+                         ) -> PrefillResult:
         """q_layers[l]: [T][h_q][d] bf16, k/v_layers[l]: [T][h_kv][d] (T = sum of
         seq_lens, sequences packed).  budgets[b][l]: k_l for sequence b (None =
         full cache).  select_scores: optional [L][h_kv][T] scores to select on
@@ -151,7 +153,10 @@ class Engine:
         the prefill-attention / window-score launches of the layers in
         timing_layers (every layer when None).  An event recorded between two
         launches ends the overlap of the second one's start with the first
-        one's tail, so timing a few layers disturbs the stream less."""
+        one's tail, so timing a few layers disturbs the stream less.
+        ready: optional per-layer lists of CUDA events (see upload_layers);
+        layer l's launches wait for every event in ready[l], so the layers'
+        inputs may still be on their way to the device when this is called."""
         s = self.shape
         dev = self.device
         L = s.n_layers
@@ -174,6 +179,9 @@ class Engine:
             else:
                 m, lsum = ml_buf
             o = o_buf if not keep_outputs else torch.empty_like(o_buf)
+            if ready is not None:
+                for e in ready[l]:
+                    (torch.cuda.current_stream() if stream is None else stream).wait_event(e)
             tl = timing if (timing_layers is None or l in timing_layers) else None
             ev = _events(tl, "attn", stream)
             kvs.kvs_prefill_attn_lse(q_layers[l], k_layers[l], v_layers[l], o, m, lsum, cu_d, B,
@@ -220,6 +228,32 @@ class Engine:
         if keep_outputs:
             res.m, res.l, res.o = keep_m, keep_l, keep_o
         return res
+
+
+def upload_layers(host: Sequence[Sequence[torch.Tensor]], dev: Sequence[Sequence[torch.Tensor]],
+                  streams: Sequence[torch.cuda.Stream]) -> List[List[torch.cuda.Event]]:
+    """Layer-wise upload of a prompt's inputs: host[i][l] (pinned host memory)
+    is copied into dev[i][l] for every tensor kind i (e.g. Q, K, V), layer by
+    layer, kind i on streams[i % len(streams)].  Returns, per layer, the events
+    of its copies; prefill_sparsify(ready=...) starts layer l once they have
+    completed, so layer l computes while layers l+1, ... are still being
+    copied.  Each copy stream first waits for the work already queued on the
+    current stream."""
+    cur = torch.cuda.current_stream()
+    for st in streams:
+        st.wait_stream(cur)
+    events = []
+    for l in range(len(dev[0])):
+        per_layer = []
+        for i, (h, d) in enumerate(zip(host, dev)):
+            st = streams[i % len(streams)]
+            with torch.cuda.stream(st):
+                d[l].copy_(h[l], non_blocking=True)
+                e = torch.cuda.Event()
+                e.record(st)
+            per_layer.append(e)
+        events.append(per_layer)
+    return events
 
 
 def _events(timing, key, stream):
