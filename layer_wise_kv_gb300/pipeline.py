@@ -274,13 +274,18 @@ def _close(ev, stream):
 
 def _stacked(layers):
     """View per-layer [T][h][d] tensors as one [L*T][h][d] tensor when they are
-    slices of one contiguous buffer; otherwise concatenate."""
+    consecutive slices of one contiguous buffer (one storage: separate
+    allocations that merely sit next to each other do not count); otherwise
+    concatenate."""
     first = layers[0]
     T = first.shape[0]
     n = len(layers)
     base = first.data_ptr()
     step = first.numel() * first.element_size()
-    if all(t.data_ptr() == base + i * step for i, t in enumerate(layers)) and first.is_contiguous():
+    storage = first.untyped_storage().data_ptr()
+    if (first.is_contiguous()
+            and all(t.untyped_storage().data_ptr() == storage and t.is_contiguous()
+                    and t.data_ptr() == base + i * step for i, t in enumerate(layers))):
         return torch.as_strided(first, (n * T, *first.shape[1:]),
                                 (first.stride(0), first.stride(1), first.stride(2)))
     return torch.cat(list(layers), dim=0)

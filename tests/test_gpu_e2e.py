@@ -337,3 +337,35 @@ def test_llama3_8b_full_size_sampled():
     torch.cuda.synchronize()
     eng.check_status()
     print(f"kept-set swaps within the 1e-3 band: {swaps}")
+
+
+def test_layerwise_upload_matches_resident_inputs():
+    """prefill_sparsify(ready=upload_layers(...)): the prompt's Q/K/V start in
+    pinned host memory and reach the device layer by layer on a copy stream
+    while earlier layers compute.  Every kept index, block table entry and
+    compacted pool byte equals the run on inputs already on the device."""
+    kvs_lib()
+    from layer_wise_kv_gb300.pipeline import Engine, upload_layers
+    w = tiny()
+    n = w.prompt_lens[0]
+    L = w.n_layers
+    budgets = [[w.budget(l, n) for l in range(L)]]
+    ql, kl, vl, _ = _layers_to_device(w, [0], [n])
+    eng_a = Engine(_shape(w), 64, poison=True)
+    res_a = eng_a.prefill_sparsify(ql, kl, vl, [n], budgets)
+    hq = [x.cpu().pin_memory() for x in ql]
+    hk = [x.cpu().pin_memory() for x in kl]
+    hv = [x.cpu().pin_memory() for x in vl]
+    dq = [torch.full_like(x, float("nan")) for x in ql]
+    dk = [torch.full_like(x, float("nan")) for x in kl]
+    dv = [torch.full_like(x, float("nan")) for x in vl]
+    eng_b = Engine(_shape(w), 64, poison=True)
+    ready = upload_layers((hq, hk, hv), (dq, dk, dv), [torch.cuda.Stream()])
+    res_b = eng_b.prefill_sparsify(dq, dk, dv, [n], budgets, ready=ready)
+    torch.cuda.synchronize()
+    eng_a.check_status()
+    eng_b.check_status()
+    assert res_a.tables == res_b.tables
+    assert torch.equal(res_a.kept_idx, res_b.kept_idx)
+    np.testing.assert_array_equal(host_bits(eng_a.k_pool), host_bits(eng_b.k_pool))
+    np.testing.assert_array_equal(host_bits(eng_a.v_pool), host_bits(eng_b.v_pool))
