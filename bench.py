@@ -268,8 +268,8 @@ def bench_gpu(args):
     blocks = sum(blocks_for(w.k_eff(l, n) + steps) + 1 for l in range(L))
     eng = Engine(shape, blocks + 64, device=dev)
     o_buf = torch.empty((n, w.h_q, w.d), dtype=torch.bfloat16, device=dev)
-    ml_buf = (torch.empty((w.h_q, n), dtype=torch.float32, device=dev),
-              torch.empty((w.h_q, n), dtype=torch.float32, device=dev))
+    ml_buf = (torch.empty((L, w.h_q, n), dtype=torch.float32, device=dev),
+              torch.empty((L, w.h_q, n), dtype=torch.float32, device=dev))
     scrub = torch.ones(128 << 20, dtype=torch.int32, device=dev)   # 512 MB
     scrub_r = torch.ones(128 << 20, dtype=torch.int32, device=dev)
     dec = DecodeBatch(eng, 1, n + steps)
@@ -363,7 +363,10 @@ def bench_gpu(args):
                              "traffic": traffic_for("prefill_attn"),
                              "peak_source": f"{peak_src} bf16 sustained",
                              "per_launch_ms": round(k1_avg, 4), "flops_per_launch": flops_launch},
+        # one window-score launch per request covers the budgeted layers
         "scores_ms_per_launch": round(sum(k2_ms) / max(1, len(k2_ms)), 4),
+        "scores_layers_per_launch": sum(1 for l in range(L) if w.budget(l, n) is not None
+                                        and w.budget(l, n) < n),
         "gpu_launches": args.steps * (2 * L - 3 + 2 + 2 * steps),
         "clocks": clk,
         "wall_s": round(t_wall, 2),

@@ -108,6 +108,24 @@ kvs_status kvs_window_scores(const kvs_bf16* q, const kvs_bf16* k, const float* 
                              int32_t d, int32_t alpha, float scale, int32_t* status,
                              kvs_stream stream);
 
+/* The same scores for n_layers consecutive layers in one launch.  Layer j's
+ * tensors follow layer j-1's in the same buffers: q [n_layers][T][h_q][d],
+ * k [n_layers][T][h_kv][d], m, l [n_layers][h_q][T], scores
+ * [n_layers][h_kv][T] (one cu_seqlens for all layers).  A layer's scores
+ * read only that layer's q, k, m and l, so they may be computed any time
+ * after its prefill and before its selection: one launch over every
+ * budgeted layer after the prefill loop replaces a launch per layer between
+ * the prefills.  Results are bit-identical to kvs_window_scores per layer.
+ * batch x n_layers <= 65535 and n_layers x T < 2^31; n_layers = 0 is a no-op.
+ * (The batching over layers is this library's, not a step of the method.)
+ */
+kvs_status kvs_window_scores_layers(const kvs_bf16* q, const kvs_bf16* k, const float* m,
+                                    const float* l, float* scores, const int32_t* cu_seqlens,
+                                    int32_t batch, int32_t max_n, int32_t total_tokens,
+                                    int32_t h_q, int32_t h_kv, int32_t d, int32_t alpha,
+                                    float scale, int32_t n_layers, int32_t* status,
+                                    kvs_stream stream);
+
 /* ------------------------------------------------------------------------
  * 3. Top-k_l selection.
  * Source: Novita article, section "System model" (keep the higher-scoring and

@@ -9,7 +9,8 @@
 // kept in registers; only the window's query block is visited (the
 // article's example: 5000 x 256 instead of 5000 x 5000 pairs).
 //
-// One CTA per (sequence, KV head, tile of 128 keys).  TMA brings the key tile
+// One CTA per (layer, sequence, KV head, tile of 128 keys); a launch covers
+// one or several consecutive layers of stacked buffers.  TMA brings the key tile
 // (128 x d) and the window block of the head's G query heads (alpha x G rows
 // x d, ordered [query][head]) into 128-byte-swizzled shared memory; one
 // thread issues tcgen05.mma with M = 128 keys, N = alpha*G (rounded up to 16)
@@ -36,7 +37,7 @@ struct ScoreParams {
   float* scores;
   const int32_t* cu_seqlens;
   int32_t* status;
-  int total, h_q, h_kv, group, alpha, n_cols, n_pad;
+  int total, h_q, h_kv, group, alpha, n_cols, n_pad, batch;
   float scale_log2;
 };
 
@@ -72,8 +73,16 @@ window_scores_kernel(const __grid_constant__ CUtensorMap k_map,
   // stream (its m and l) before touching global memory
   griddep_launch_dependents();
   griddep_wait();
-  const int b = blockIdx.z;
+  // blockIdx.z = layer * batch + sequence; a layer's Q and K rows follow the
+  // previous layer's in the tensor maps (row = layer * total + token), its
+  // m, l and scores sit one [heads][total] plane further on
+  const int li = blockIdx.z / p.batch;
+  const int b = blockIdx.z - li * p.batch;
   const int h = blockIdx.y;
+  const int row0 = li * p.total;
+  const float* m_l = p.m + static_cast<int64_t>(li) * p.h_q * p.total;
+  const float* l_l = p.l + static_cast<int64_t>(li) * p.h_q * p.total;
+  float* scores_l = p.scores + static_cast<int64_t>(li) * p.h_kv * p.total;
   const int seq0 = p.cu_seqlens[b];
   const int n = p.cu_seqlens[b + 1] - seq0;
   const int key0 = blockIdx.x * kKeyTile;
@@ -102,8 +111,8 @@ window_scores_kernel(const __grid_constant__ CUtensorMap k_map,
     mbar_arrive_expect_tx(&bars[0], L::kKBytes + (D / 64) * p.n_cols * 128);
 #pragma unroll
     for (int c = 0; c < D / 64; ++c) {
-      tma_load_3d(k_s + c * (kKeyTile * 128), &k_map, &bars[0], c * 64, h, seq0 + key0);
-      tma_load_3d(q_s + c * q_chunk, &q_map, &bars[0], c * 64, h * p.group, win_start);
+      tma_load_3d(k_s + c * (kKeyTile * 128), &k_map, &bars[0], c * 64, h, row0 + seq0 + key0);
+      tma_load_3d(q_s + c * q_chunk, &q_map, &bars[0], c * 64, h * p.group, row0 + win_start);
     }
   }
   // per window column: m * log2(e), 1 / l and the query position (-1 for a
@@ -116,8 +125,8 @@ window_scores_kernel(const __grid_constant__ CUtensorMap k_map,
       const int g = h * p.group + (c - t * p.group);
       if (t >= p.alpha - w) {
         const int64_t at = static_cast<int64_t>(g) * p.total + win_start + t;
-        mc = p.m[at] * kLog2eS;
-        il = 1.0f / p.l[at];
+        mc = m_l[at] * kLog2eS;
+        il = 1.0f / l_l[at];
         qc = n - p.alpha + t;
       }
     }
@@ -172,7 +181,7 @@ window_scores_kernel(const __grid_constant__ CUtensorMap k_map,
       }
     }
   }
-  if (key < n) p.scores[static_cast<int64_t>(h) * p.total + seq0 + key] = acc;
+  if (key < n) scores_l[static_cast<int64_t>(h) * p.total + seq0 + key] = acc;
 
   tc_fence_before();
   __syncthreads();
@@ -199,7 +208,7 @@ bool map_thd(CUtensorMap* m, const void* base, int total, int heads, int d, int 
 
 template <int D>
 kvs_status launch_scores(const CUtensorMap& km, const CUtensorMap& qm, const ScoreParams& prm,
-                         int max_n, int batch, cudaStream_t st) {
+                         int max_n, int batch, int n_layers, cudaStream_t st) {
   const size_t smem = ScoreSmem<D>::bytes(prm.n_pad);
   static bool configured = false;
   if (!configured) {
@@ -209,7 +218,7 @@ kvs_status launch_scores(const CUtensorMap& km, const CUtensorMap& qm, const Sco
     configured = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((max_n + kKeyTile - 1) / kKeyTile, prm.h_kv, batch);
+  cfg.gridDim = dim3((max_n + kKeyTile - 1) / kKeyTile, prm.h_kv, batch * n_layers);
   cfg.blockDim = dim3(kScoreThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
@@ -226,22 +235,30 @@ kvs_status launch_scores(const CUtensorMap& km, const CUtensorMap& qm, const Sco
 }  // namespace
 }  // namespace kvs
 
-extern "C" kvs_status kvs_window_scores(const kvs_bf16* q, const kvs_bf16* k, const float* m,
-                                        const float* l, float* scores, const int32_t* cu_seqlens,
-                                        int32_t batch, int32_t max_n, int32_t total_tokens,
-                                        int32_t h_q, int32_t h_kv, int32_t d, int32_t alpha,
-                                        float scale, int32_t* status, kvs_stream stream) {
-  KVS_REQUIRE(batch >= 0, "kvs_window_scores: negative batch");
-  if (batch == 0 || total_tokens == 0) return KVS_OK;
-  KVS_REQUIRE(q && k && m && l && scores && cu_seqlens, "kvs_window_scores: NULL pointer");
-  KVS_SUPPORTED(d == 64 || d == 128, "kvs_window_scores: d = %d (supported: 64, 128)", d);
-  KVS_REQUIRE(h_kv > 0 && h_q > 0 && h_q % h_kv == 0, "kvs_window_scores: bad head counts");
-  KVS_REQUIRE(alpha >= 1 && max_n >= 1 && total_tokens >= 1, "kvs_window_scores: bad sizes");
+namespace kvs {
+namespace {
+
+kvs_status window_scores(const char* fn, const kvs_bf16* q, const kvs_bf16* k, const float* m,
+                         const float* l, float* scores, const int32_t* cu_seqlens, int32_t batch,
+                         int32_t max_n, int32_t total_tokens, int32_t h_q, int32_t h_kv, int32_t d,
+                         int32_t alpha, float scale, int32_t n_layers, int32_t* status,
+                         kvs_stream stream) {
+  KVS_REQUIRE(batch >= 0 && n_layers >= 0, "%s: negative batch or layer count", fn);
+  if (batch == 0 || total_tokens == 0 || n_layers == 0) return KVS_OK;
+  KVS_REQUIRE(q && k && m && l && scores && cu_seqlens, "%s: NULL pointer", fn);
+  KVS_SUPPORTED(d == 64 || d == 128, "%s: d = %d (supported: 64, 128)", fn, d);
+  KVS_REQUIRE(h_kv > 0 && h_q > 0 && h_q % h_kv == 0, "%s: bad head counts", fn);
+  KVS_REQUIRE(alpha >= 1 && max_n >= 1 && total_tokens >= 1, "%s: bad sizes", fn);
+  KVS_SUPPORTED(static_cast<int64_t>(batch) * n_layers <= 65535,
+                "%s: batch x layers = %lld > 65535", fn,
+                static_cast<long long>(batch) * n_layers);
+  KVS_REQUIRE(static_cast<int64_t>(total_tokens) * n_layers < (1ll << 31),
+              "%s: layers x tokens exceed 32-bit TMA row coordinates", fn);
   const int G = h_q / h_kv;
-  KVS_SUPPORTED(alpha * G <= 256, "kvs_window_scores: alpha * G = %d > 256", alpha * G);
+  KVS_SUPPORTED(alpha * G <= 256, "%s: alpha * G = %d > 256", fn, alpha * G);
   KVS_REQUIRE((reinterpret_cast<uintptr_t>(q) & 15) == 0 && (reinterpret_cast<uintptr_t>(k) & 15) == 0,
-              "kvs_window_scores: q and k must be 16-byte aligned");
-  kvs::ScoreParams prm;
+              "%s: q and k must be 16-byte aligned", fn);
+  ScoreParams prm;
   prm.m = m;
   prm.l = l;
   prm.scores = scores;
@@ -254,19 +271,22 @@ extern "C" kvs_status kvs_window_scores(const kvs_bf16* q, const kvs_bf16* k, co
   prm.alpha = alpha;
   prm.n_cols = alpha * G;
   prm.n_pad = (alpha * G + 15) / 16 * 16;
-  prm.scale_log2 = scale * kvs::kLog2eS;
+  prm.batch = batch;
+  prm.scale_log2 = scale * kLog2eS;
 
-  static thread_local kvs::QKMaps cache;
-  if (cache.q != q || cache.k != k || cache.total != total_tokens || cache.h_q != h_q ||
+  // the maps cover every layer of the call: rows = layers x tokens
+  const int rows = total_tokens * n_layers;
+  static thread_local QKMaps cache;
+  if (cache.q != q || cache.k != k || cache.total != rows || cache.h_q != h_q ||
       cache.h_kv != h_kv || cache.d != d || cache.box_rows != alpha || cache.box_heads != G) {
-    if (!kvs::map_thd(&cache.km, k, total_tokens, h_kv, d, 1, kvs::kKeyTile) ||
-        !kvs::map_thd(&cache.qm, q, total_tokens, h_q, d, G, alpha)) {
+    if (!map_thd(&cache.km, k, rows, h_kv, d, 1, kKeyTile) ||
+        !map_thd(&cache.qm, q, rows, h_q, d, G, alpha)) {
       cache.q = nullptr;
       return KVS_ERR_CUDA;
     }
     cache.q = q;
     cache.k = k;
-    cache.total = total_tokens;
+    cache.total = rows;
     cache.h_q = h_q;
     cache.h_kv = h_kv;
     cache.d = d;
@@ -274,6 +294,30 @@ extern "C" kvs_status kvs_window_scores(const kvs_bf16* q, const kvs_bf16* k, co
     cache.box_heads = G;
   }
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (d == 128) return kvs::launch_scores<128>(cache.km, cache.qm, prm, max_n, batch, st);
-  return kvs::launch_scores<64>(cache.km, cache.qm, prm, max_n, batch, st);
+  if (d == 128) return launch_scores<128>(cache.km, cache.qm, prm, max_n, batch, n_layers, st);
+  return launch_scores<64>(cache.km, cache.qm, prm, max_n, batch, n_layers, st);
+}
+
+}  // namespace
+}  // namespace kvs
+
+extern "C" kvs_status kvs_window_scores(const kvs_bf16* q, const kvs_bf16* k, const float* m,
+                                        const float* l, float* scores, const int32_t* cu_seqlens,
+                                        int32_t batch, int32_t max_n, int32_t total_tokens,
+                                        int32_t h_q, int32_t h_kv, int32_t d, int32_t alpha,
+                                        float scale, int32_t* status, kvs_stream stream) {
+  return kvs::window_scores("kvs_window_scores", q, k, m, l, scores, cu_seqlens, batch, max_n,
+                            total_tokens, h_q, h_kv, d, alpha, scale, 1, status, stream);
+}
+
+extern "C" kvs_status kvs_window_scores_layers(const kvs_bf16* q, const kvs_bf16* k,
+                                               const float* m, const float* l, float* scores,
+                                               const int32_t* cu_seqlens, int32_t batch,
+                                               int32_t max_n, int32_t total_tokens, int32_t h_q,
+                                               int32_t h_kv, int32_t d, int32_t alpha, float scale,
+                                               int32_t n_layers, int32_t* status,
+                                               kvs_stream stream) {
+  return kvs::window_scores("kvs_window_scores_layers", q, k, m, l, scores, cu_seqlens, batch,
+                            max_n, total_tokens, h_q, h_kv, d, alpha, scale, n_layers, status,
+                            stream);
 }

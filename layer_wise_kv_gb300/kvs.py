@@ -49,6 +49,8 @@ _SIGS = {
                                     _I32, _I32, _F32, _VP, _VP]),
     "kvs_window_scores": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _I32, _I32, _I32, _I32, _I32,
                                  _I32, _I32, _F32, _VP, _VP]),
+    "kvs_window_scores_layers": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _I32, _I32, _I32, _I32,
+                                        _I32, _I32, _I32, _F32, _I32, _VP, _VP]),
     "kvs_select_topk": (_I32, [_VP, _I64, _VP, _I32, _I32, _I32, _VP, _VP, _VP]),
     "kvs_compact_blocks": (_I32, [_VP, _VP, _VP, _I32, _I64, _I32, _I32, _VP, _VP, _VP, _VP,
                                   _I32, _VP, _VP]),
@@ -144,6 +146,17 @@ def kvs_prefill_attn_lse(q, k, v, o, m, l, cu_seqlens, batch, max_n, total_token
         _dev(q, "bf16", "q"), _dev(k, "bf16", "k"), _dev(v, "bf16", "v"), _dev(o, "bf16", "o"),
         _dev(m, "f32", "m"), _dev(l, "f32", "l"), _dev(cu_seqlens, "i32", "cu_seqlens"),
         batch, max_n, total_tokens, h_q, h_kv, d, float(scale),
+        None if status is None else _dev(status, "i32", "status"), _stream(stream)))
+
+
+def kvs_window_scores_layers(q, k, m, l, scores, cu_seqlens, batch, max_n, total_tokens, h_q,
+                             h_kv, d, alpha, scale, n_layers, status=None, stream=None):
+    """q, k, m, l, scores: the first of n_layers consecutive layers of stacked
+    buffers (each next layer one tensor further on)."""
+    _check(library().kvs_window_scores_layers(
+        _dev(q, "bf16", "q"), _dev(k, "bf16", "k"), _dev(m, "f32", "m"), _dev(l, "f32", "l"),
+        _dev(scores, "f32", "scores"), _dev(cu_seqlens, "i32", "cu_seqlens"), batch, max_n,
+        total_tokens, h_q, h_kv, d, alpha, float(scale), n_layers,
         None if status is None else _dev(status, "i32", "status"), _stream(stream)))
 
 

@@ -2,9 +2,12 @@
 of prompts over all layers, then decode steps over the paged cache.
 
 Step orders (the same ones the CPU oracle uses):
-* prefill: for each layer, prefill attention (+ m, l) and, for layers with a
-  budget below the prompt length, the window scores; then one selection launch
-  over every (sequence, layer) item; then, sequence by sequence and layer by
+* prefill: for each layer, prefill attention (+ m, l); then the window scores
+  of the layers with a budget below the prompt length (one launch per run of
+  consecutive such layers: a layer's scores read only its own q, k, m, l;
+  while the layers' inputs are still being copied in, each layer's scores
+  follow its prefill instead); then one selection launch over every
+  (sequence, layer) item; then, sequence by sequence and layer by
   layer, ceil(k_eff / 16) blocks from the allocator; then one compaction
   launch over all items.
 * decode step: the host allocator prepares every (stream, layer) item in order
@@ -148,12 +151,16 @@ class Engine:
         """q_layers[l]: [T][h_q][d] bf16, k/v_layers[l]: [T][h_kv][d] (T = sum of
         seq_lens, sequences packed).  budgets[b][l]: k_l for sequence b (None =
         full cache).  select_scores: optional [L][h_kv][T] scores to select on
-        instead of the ones computed here.  timing: optional dict of lists
-        "attn" / "scores" that receive a (start, end) CUDA event pair around
-        the prefill-attention / window-score launches of the layers in
-        timing_layers (every layer when None).  An event recorded between two
-        launches ends the overlap of the second one's start with the first
-        one's tail, so timing a few layers disturbs the stream less.
+        instead of the ones computed here.  ml_buf: optional pair of
+        [L][h_q][T] fp32 buffers for every layer's m and l.  timing: optional
+        dict of lists "attn" / "scores" that receive a (start, end) CUDA event
+        pair around the prefill-attention launches of the layers in
+        timing_layers (every layer when None) / around each window-score
+        launch (one per run of consecutive budgeted layers; per layer when
+        `ready` is given).  An event
+        recorded between two launches ends the overlap of the second one's
+        start with the first one's tail, so timing a few layers disturbs the
+        stream less.
         ready: optional per-layer lists of CUDA events (see upload_layers);
         layer l's launches wait for every event in ready[l], so the layers'
         inputs may still be on their way to the device when this is called."""
@@ -171,13 +178,18 @@ class Engine:
         # scores of layers without a budget are never read (their selection is
         # the identity), so the buffer needs no clearing
         scores = torch.empty((L, s.h_kv, T), dtype=torch.float32, device=dev)
-        keep_m, keep_l, keep_o = [], [], []
+        # every layer's m and l stay until the window scores read them after
+        # the prefill loop
+        if ml_buf is None or keep_outputs:
+            m_all = torch.empty((L, s.h_q, T), dtype=torch.float32, device=dev)
+            l_all = torch.empty_like(m_all)
+        else:
+            m_all, l_all = ml_buf
+            if tuple(m_all.shape) != (L, s.h_q, T) or tuple(l_all.shape) != (L, s.h_q, T):
+                raise ValueError(f"ml_buf must be two [{L}][{s.h_q}][{T}] fp32 tensors")
+        keep_o = []
         for l in range(L):
-            if ml_buf is None or keep_outputs:
-                m = torch.empty((s.h_q, T), dtype=torch.float32, device=dev)
-                lsum = torch.empty_like(m)
-            else:
-                m, lsum = ml_buf
+            m, lsum = m_all[l], l_all[l]
             o = o_buf if not keep_outputs else torch.empty_like(o_buf)
             if ready is not None:
                 for e in ready[l]:
@@ -187,15 +199,42 @@ class Engine:
             kvs.kvs_prefill_attn_lse(q_layers[l], k_layers[l], v_layers[l], o, m, lsum, cu_d, B,
                                      max_n, T, s.h_q, s.h_kv, s.d, s.scale, self.status, stream)
             _close(ev, stream)
-            if any_budget[l]:
-                ev = _events(tl, "scores", stream)
+            if keep_outputs:
+                keep_o.append(o)
+            if ready is not None and any_budget[l]:
+                # inputs still arriving: the GPU waits for the next layer's
+                # copies anyway, so this layer's scores go in that gap
+                ev = _events(timing, "scores", stream)
                 kvs.kvs_window_scores(q_layers[l], k_layers[l], m, lsum, scores[l], cu_d, B, max_n,
                                       T, s.h_q, s.h_kv, s.d, s.alpha, s.scale, self.status, stream)
                 _close(ev, stream)
-            if keep_outputs:
-                keep_m.append(m)
-                keep_l.append(lsum)
-                keep_o.append(o)
+
+        # inputs resident: the window scores of every budgeted layer after the
+        # prefill loop.  A layer's scores need only its own q, k, m and l, so
+        # each run of consecutive budgeted layers is one launch (when their q
+        # and k are slices of one buffer) instead of a latency-bound launch
+        # between every two prefills
+        l0 = 0 if ready is None else L
+        while l0 < L:
+            if not any_budget[l0]:
+                l0 += 1
+                continue
+            l1 = l0
+            while l1 < L and any_budget[l1]:
+                l1 += 1
+            qs, ks = _stacked_view(q_layers[l0:l1]), _stacked_view(k_layers[l0:l1])
+            ev = _events(timing, "scores", stream)
+            if qs is not None and ks is not None:
+                kvs.kvs_window_scores_layers(qs, ks, m_all[l0:l1], l_all[l0:l1], scores[l0:l1],
+                                             cu_d, B, max_n, T, s.h_q, s.h_kv, s.d, s.alpha,
+                                             s.scale, l1 - l0, self.status, stream)
+            else:
+                for l in range(l0, l1):
+                    kvs.kvs_window_scores(q_layers[l], k_layers[l], m_all[l], l_all[l], scores[l],
+                                          cu_d, B, max_n, T, s.h_q, s.h_kv, s.d, s.alpha, s.scale,
+                                          self.status, stream)
+            _close(ev, stream)
+            l0 = l1
 
         # selection over every (sequence, layer) item
         kept = torch.empty(max(plan["n_kept"], 1), dtype=torch.int32, device=dev)
@@ -226,7 +265,7 @@ class Engine:
         res = PrefillResult(tables=tables, k_eff=keff, kept_idx=kept, idx_off=idx_off,
                             scores=scores)
         if keep_outputs:
-            res.m, res.l, res.o = keep_m, keep_l, keep_o
+            res.m, res.l, res.o = list(m_all), list(l_all), keep_o
         return res
 
 
@@ -270,6 +309,22 @@ def _events(timing, key, stream):
 def _close(ev, stream):
     if ev is not None:
         ev.record(torch.cuda.current_stream() if stream is None else stream)
+
+
+def _stacked_view(layers):
+    """[n][T][h][d] view of per-layer tensors that are consecutive slices of
+    one contiguous buffer, else None."""
+    first = layers[0]
+    n = len(layers)
+    base = first.data_ptr()
+    step = first.numel() * first.element_size()
+    storage = first.untyped_storage().data_ptr()
+    if (first.is_contiguous()
+            and all(t.untyped_storage().data_ptr() == storage and t.is_contiguous()
+                    and t.shape == first.shape and t.data_ptr() == base + i * step
+                    for i, t in enumerate(layers))):
+        return torch.as_strided(first, (n, *first.shape), (first.numel(), *first.stride()))
+    return None
 
 
 def _stacked(layers):

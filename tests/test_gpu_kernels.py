@@ -222,6 +222,36 @@ def test_window_scores_vs_oracle(lens, h_q, h_kv, d, alpha):
         np.testing.assert_allclose(got[:, s0:s0 + n].sum(axis=1), w * (h_q // h_kv), rtol=1e-4)
 
 
+def test_window_scores_layers_match_per_layer_launches():
+    """kvs_window_scores_layers over layers stacked in one buffer gives, bit
+    for bit, what kvs_window_scores gives layer by layer (whose values the
+    test above checks against the oracle): ragged sequences, one shorter than
+    the window."""
+    kvs = kvs_lib()
+    rng = np.random.default_rng(77)
+    lens, h_q, h_kv, d, alpha, n_layers = [300, 129, 20], 8, 2, 128, 32, 3
+    T = sum(lens)
+    cu = torch.from_numpy(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)).cuda()
+    q = dev_bf16(_randn_bits(rng, (n_layers, T, h_q, d), 1.5))
+    k = dev_bf16(_randn_bits(rng, (n_layers, T, h_kv, d)))
+    # any finite m and positive l exercise the same arithmetic
+    m = torch.from_numpy(rng.uniform(8.0, 12.0, (n_layers, h_q, T)).astype(np.float32)).cuda()
+    l = torch.from_numpy(rng.uniform(0.5, 4.0, (n_layers, h_q, T)).astype(np.float32)).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    scale = 1 / np.sqrt(d)
+    one = torch.full((n_layers, h_kv, T), -1.0, dtype=torch.float32, device="cuda")
+    for li in range(n_layers):
+        kvs.kvs_window_scores(q[li], k[li], m[li], l[li], one[li], cu, len(lens), max(lens), T,
+                              h_q, h_kv, d, alpha, scale, status)
+    many = torch.full_like(one, -2.0)
+    kvs.kvs_window_scores_layers(q, k, m, l, many, cu, len(lens), max(lens), T, h_q, h_kv, d,
+                                 alpha, scale, n_layers, status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    assert torch.equal(one, many)
+    assert (one >= 0).all()
+
+
 # ---------------------------------------------------------------------------
 # paged decode with appends, several splits, copy-on-write blocks
 # ---------------------------------------------------------------------------
