@@ -53,8 +53,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # the figure reported is scaled to the launch the bench times (decode length
 # grows over the request).  Set an entry to None once its kernel changes.
 NCU_TRAFFIC = {
-    "prefill_attn": {"bytes": 49450496 + 2089216, "alg_bytes": None},   # same launch shape
-    "paged_decode": {"bytes": 188697600 + 3535616, "alg_bytes": 187432960},
+    # cleared until recaptured: both kernels changed since their captures
+    "prefill_attn": None,
+    "paged_decode": None,
 }
 
 
@@ -267,7 +268,7 @@ def bench_gpu(args):
     shape = Shape(w.n_layers, w.h_q, w.h_kv, w.d, w.alpha, w.recent)
     blocks = sum(blocks_for(w.k_eff(l, n) + steps) + 1 for l in range(L))
     eng = Engine(shape, blocks + 64, device=dev)
-    o_buf = torch.empty((n, w.h_q, w.d), dtype=torch.bfloat16, device=dev)
+    o_buf = torch.empty((L, n, w.h_q, w.d), dtype=torch.bfloat16, device=dev)
     ml_buf = (torch.empty((L, w.h_q, n), dtype=torch.float32, device=dev),
               torch.empty((L, w.h_q, n), dtype=torch.float32, device=dev))
     scrub = torch.ones(128 << 20, dtype=torch.int32, device=dev)   # 512 MB
@@ -317,7 +318,9 @@ def bench_gpu(args):
 
     peaks, peak_src = read_peaks()
     k1_avg = sum(k1_ms) / len(k1_ms)
-    flops_launch = prefill_flops(w, n)
+    # layers per timed prefill launch (all 32 when the layers go in one launch)
+    k1_layers = rec["k1"].get("attn_layers") or [1] * len(k1_ms)
+    flops_launch = prefill_flops(w, n) * (sum(k1_layers) / len(k1_layers))
     tflops = flops_launch / (k1_avg / 1e3) / 1e12
     peak_t = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
     dk_ms = [a.elapsed_time(b) for a, b in rec["dk"]]

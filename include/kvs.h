@@ -89,6 +89,25 @@ kvs_status kvs_prefill_attn_lse(const kvs_bf16* q, const kvs_bf16* k, const kvs_
                                 int32_t total_tokens, int32_t h_q, int32_t h_kv, int32_t d,
                                 float scale, int32_t* status, kvs_stream stream);
 
+/* The same attention for n_layers layers in one launch.  Layer j's tensors
+ * follow layer j-1's in the same buffers: q [n_layers][T][h_q][d], k, v
+ * [n_layers][T][h_kv][d], o [n_layers][T][h_q][d], m, l [n_layers][h_q][T]
+ * (one cu_seqlens for all layers).  Given every layer's Q, K and V at once,
+ * the layers are independent: the persistent CTAs take the work items of all
+ * layers, longest first, so the launch, start-up and uneven end of a launch
+ * are paid once instead of per layer.  Results are bit-identical to
+ * kvs_prefill_attn_lse per layer.  n_layers x T < 2^31; n_layers = 0 is a
+ * no-op.  (The batching over layers is this library's, not a step of the
+ * method: a model whose layer l+1 inputs come from layer l's output calls
+ * kvs_prefill_attn_lse layer by layer.)
+ */
+kvs_status kvs_prefill_attn_lse_layers(const kvs_bf16* q, const kvs_bf16* k, const kvs_bf16* v,
+                                       kvs_bf16* o, float* m, float* l,
+                                       const int32_t* cu_seqlens, int32_t batch, int32_t max_n,
+                                       int32_t total_tokens, int32_t h_q, int32_t h_kv,
+                                       int32_t d, float scale, int32_t n_layers,
+                                       int32_t* status, kvs_stream stream);
+
 /* ------------------------------------------------------------------------
  * 2. Window scores.
  * Source: Novita article, section "Key techniques 2" (PyramidKV-style score

@@ -69,8 +69,8 @@ struct PrefillParams {
   float* l;
   const int32_t* cu_seqlens;
   int32_t* status;
-  int total, h_q, h_kv, group, n_pairs_max, batch;
-  int n_items;  // h_q x batch x n_pairs_max work items (some empty)
+  int total, h_q, h_kv, group, n_pairs_max, batch, n_layers;
+  int n_items;  // h_q x batch x n_layers x n_pairs_max work items (some empty)
   float scale_log2;
 };
 
@@ -91,13 +91,16 @@ struct PrefillSmem {
 };
 
 // A work item: one query head g of one pair of 128-row query tiles (A: rows
-// q0 .. q0+127, B: q0+128 .. q0+255, q0 = 256 pr) of sequence b.  Items are
-// numbered pair rank from the top of the sequence (y) slowest, then sequence,
-// then head, so the numbering runs from the longest pairs down; an item whose
-// sequence has fewer than y + 1 pairs is empty.
+// q0 .. q0+127, B: q0+128 .. q0+255, q0 = 256 pr) of sequence b of one layer.
+// Items are numbered pair rank from the top of the sequence (y) slowest, then
+// layer, then sequence, then head, so the numbering runs from the longest
+// pairs of every layer down; an item whose sequence has fewer than y + 1
+// pairs is empty.  Layers are stacked: layer j's rows follow layer j-1's in
+// the Q/K/V maps and in O (row = j * total + token), its m and l sit one
+// [h_q][total] plane further on.
 struct PItem {
   bool valid;
-  int g, pr, seq0, n;
+  int g, pr, seq0, n;  // seq0: the sequence's first row in the stacked rows
   // causal: tile A sees key tiles 0 .. 2pr, tile B 0 .. 2pr+1
   __device__ __forceinline__ int nkv_a() const { return 2 * pr + 1; }
   __device__ __forceinline__ int nkv_b() const { return 2 * pr + 2; }
@@ -108,9 +111,12 @@ __device__ __forceinline__ PItem item_at(int idx, const PrefillParams& p) {
   it.g = idx % p.h_q;
   const int rest = idx / p.h_q;
   const int b = rest % p.batch;
-  const int y = rest / p.batch;
-  it.seq0 = p.cu_seqlens[b];
-  it.n = p.cu_seqlens[b + 1] - it.seq0;
+  const int rest2 = rest / p.batch;
+  const int layer = rest2 % p.n_layers;
+  const int y = rest2 / p.n_layers;
+  const int tok0 = p.cu_seqlens[b];
+  it.n = p.cu_seqlens[b + 1] - tok0;
+  it.seq0 = layer * p.total + tok0;
   const int npairs = (it.n + 2 * kBM - 1) / (2 * kBM);
   it.pr = npairs - 1 - y;
   it.valid = it.pr >= 0;
@@ -565,7 +571,10 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap q_map,
           w.w = pack_bf16x2(__uint_as_float(rr[8 * v + 6]) * inv_l, __uint_as_float(rr[8 * v + 7]) * inv_l);
           dst[v] = w;
         }
-        const int64_t at = static_cast<int64_t>(it.g) * p.total + it.seq0 + qi;
+        // m, l [layer][h_q][total]; seq0 = layer * total + first token
+        const int layer = it.seq0 / p.total;
+        const int64_t at = (static_cast<int64_t>(layer) * p.h_q + it.g) * p.total +
+                           (it.seq0 - layer * p.total) + qi;
         p.m[at] = m_max * kLn2;
         p.l[at] = l_run * ex2(m_ref - m_max);
       }
@@ -632,23 +641,25 @@ kvs_status launch_prefill(const PrefillMaps& mp, const PrefillParams& prm, int b
 }  // namespace
 }  // namespace kvs
 
-extern "C" kvs_status kvs_prefill_attn_lse(const kvs_bf16* q, const kvs_bf16* k,
-                                           const kvs_bf16* v, kvs_bf16* o, float* m, float* l,
-                                           const int32_t* cu_seqlens, int32_t batch,
-                                           int32_t max_n, int32_t total_tokens, int32_t h_q,
-                                           int32_t h_kv, int32_t d, float scale,
-                                           int32_t* status, kvs_stream stream) {
-  KVS_REQUIRE(batch >= 0, "kvs_prefill_attn_lse: negative batch");
-  if (batch == 0 || total_tokens == 0) return KVS_OK;
-  KVS_REQUIRE(q && k && v && o && m && l && cu_seqlens, "kvs_prefill_attn_lse: NULL pointer");
-  KVS_SUPPORTED(d == 64 || d == 128, "kvs_prefill_attn_lse: d = %d (supported: 64, 128)", d);
-  KVS_REQUIRE(h_kv > 0 && h_q > 0 && h_q % h_kv == 0, "kvs_prefill_attn_lse: bad head counts");
-  KVS_REQUIRE(max_n >= 1 && total_tokens >= 1 && batch <= 65535,
-              "kvs_prefill_attn_lse: bad sizes");
+namespace kvs {
+namespace {
+
+kvs_status prefill_attn(const char* fn, const kvs_bf16* q, const kvs_bf16* k, const kvs_bf16* v,
+                        kvs_bf16* o, float* m, float* l, const int32_t* cu_seqlens, int32_t batch,
+                        int32_t max_n, int32_t total_tokens, int32_t h_q, int32_t h_kv, int32_t d,
+                        float scale, int32_t n_layers, int32_t* status, kvs_stream stream) {
+  KVS_REQUIRE(batch >= 0 && n_layers >= 0, "%s: negative batch or layer count", fn);
+  if (batch == 0 || total_tokens == 0 || n_layers == 0) return KVS_OK;
+  KVS_REQUIRE(q && k && v && o && m && l && cu_seqlens, "%s: NULL pointer", fn);
+  KVS_SUPPORTED(d == 64 || d == 128, "%s: d = %d (supported: 64, 128)", fn, d);
+  KVS_REQUIRE(h_kv > 0 && h_q > 0 && h_q % h_kv == 0, "%s: bad head counts", fn);
+  KVS_REQUIRE(max_n >= 1 && total_tokens >= 1 && batch <= 65535, "%s: bad sizes", fn);
+  KVS_REQUIRE(static_cast<int64_t>(total_tokens) * n_layers < (1ll << 31),
+              "%s: layers x tokens exceed 32-bit TMA row coordinates", fn);
   KVS_REQUIRE(((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
                 reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o)) & 15) == 0,
-              "kvs_prefill_attn_lse: q, k, v, o must be 16-byte aligned");
-  kvs::PrefillParams prm;
+              "%s: q, k, v, o must be 16-byte aligned", fn);
+  PrefillParams prm;
   prm.o = o;
   prm.m = m;
   prm.l = l;
@@ -658,31 +669,57 @@ extern "C" kvs_status kvs_prefill_attn_lse(const kvs_bf16* q, const kvs_bf16* k,
   prm.h_q = h_q;
   prm.h_kv = h_kv;
   prm.group = h_q / h_kv;
-  prm.n_pairs_max = (max_n + 2 * kvs::kBM - 1) / (2 * kvs::kBM);
+  prm.n_pairs_max = (max_n + 2 * kBM - 1) / (2 * kBM);
   prm.batch = batch;
-  prm.scale_log2 = scale * kvs::kLog2eP;
-  KVS_REQUIRE(static_cast<int64_t>(prm.n_pairs_max) * batch * h_q < (1ll << 31),
-              "kvs_prefill_attn_lse: too many work items");
-  prm.n_items = prm.n_pairs_max * batch * h_q;
+  prm.n_layers = n_layers;
+  prm.scale_log2 = scale * kLog2eP;
+  KVS_REQUIRE(static_cast<int64_t>(prm.n_pairs_max) * batch * h_q * n_layers < (1ll << 31),
+              "%s: too many work items", fn);
+  prm.n_items = prm.n_pairs_max * batch * h_q * n_layers;
 
-  static thread_local kvs::PrefillMaps cache;
-  if (cache.q != q || cache.k != k || cache.v != v || cache.total != total_tokens ||
+  // the maps cover every layer of the call: rows = layers x tokens
+  const int rows = total_tokens * n_layers;
+  static thread_local PrefillMaps cache;
+  if (cache.q != q || cache.k != k || cache.v != v || cache.total != rows ||
       cache.h_q != h_q || cache.h_kv != h_kv || cache.d != d) {
-    if (!kvs::map_rows(&cache.qm, q, total_tokens, h_q, d) ||
-        !kvs::map_rows(&cache.km, k, total_tokens, h_kv, d) ||
-        !kvs::map_rows(&cache.vm, v, total_tokens, h_kv, d)) {
+    if (!map_rows(&cache.qm, q, rows, h_q, d) || !map_rows(&cache.km, k, rows, h_kv, d) ||
+        !map_rows(&cache.vm, v, rows, h_kv, d)) {
       cache.q = nullptr;
       return KVS_ERR_CUDA;
     }
     cache.q = q;
     cache.k = k;
     cache.v = v;
-    cache.total = total_tokens;
+    cache.total = rows;
     cache.h_q = h_q;
     cache.h_kv = h_kv;
     cache.d = d;
   }
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (d == 128) return kvs::launch_prefill<128>(cache, prm, batch, st);
-  return kvs::launch_prefill<64>(cache, prm, batch, st);
+  if (d == 128) return launch_prefill<128>(cache, prm, batch, st);
+  return launch_prefill<64>(cache, prm, batch, st);
+}
+
+}  // namespace
+}  // namespace kvs
+
+extern "C" kvs_status kvs_prefill_attn_lse(const kvs_bf16* q, const kvs_bf16* k,
+                                           const kvs_bf16* v, kvs_bf16* o, float* m, float* l,
+                                           const int32_t* cu_seqlens, int32_t batch,
+                                           int32_t max_n, int32_t total_tokens, int32_t h_q,
+                                           int32_t h_kv, int32_t d, float scale,
+                                           int32_t* status, kvs_stream stream) {
+  return kvs::prefill_attn("kvs_prefill_attn_lse", q, k, v, o, m, l, cu_seqlens, batch, max_n,
+                           total_tokens, h_q, h_kv, d, scale, 1, status, stream);
+}
+
+extern "C" kvs_status kvs_prefill_attn_lse_layers(const kvs_bf16* q, const kvs_bf16* k,
+                                                  const kvs_bf16* v, kvs_bf16* o, float* m,
+                                                  float* l, const int32_t* cu_seqlens,
+                                                  int32_t batch, int32_t max_n,
+                                                  int32_t total_tokens, int32_t h_q, int32_t h_kv,
+                                                  int32_t d, float scale, int32_t n_layers,
+                                                  int32_t* status, kvs_stream stream) {
+  return kvs::prefill_attn("kvs_prefill_attn_lse_layers", q, k, v, o, m, l, cu_seqlens, batch,
+                           max_n, total_tokens, h_q, h_kv, d, scale, n_layers, status, stream);
 }

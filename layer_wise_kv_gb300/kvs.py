@@ -47,6 +47,8 @@ _SIGS = {
     "kvs_version": (_I32, []),
     "kvs_prefill_attn_lse": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I32, _I32, _I32, _I32,
                                     _I32, _I32, _F32, _VP, _VP]),
+    "kvs_prefill_attn_lse_layers": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I32, _I32, _I32,
+                                           _I32, _I32, _I32, _F32, _I32, _VP, _VP]),
     "kvs_window_scores": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _I32, _I32, _I32, _I32, _I32,
                                  _I32, _I32, _F32, _VP, _VP]),
     "kvs_window_scores_layers": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _I32, _I32, _I32, _I32,
@@ -140,6 +142,20 @@ def _dev(t, dtype_name, what):
 # ---------------------------------------------------------------------------
 # the five hot-path calls
 # ---------------------------------------------------------------------------
+def kvs_prefill_attn_lse_layers(q, k, v, o, m, l, cu_seqlens, batch, max_n, total_tokens, h_q,
+                                h_kv, d, scale, n_layers, status=None, stream=None):
+    """q, k, v, o, m, l: n_layers layers stacked in one buffer each (leading
+    dimension n_layers)."""
+    for t, what in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (m, "m"), (l, "l")):
+        if t.shape[0] != n_layers:
+            raise ValueError(f"{what} must have n_layers = {n_layers} as its leading dimension")
+    _check(library().kvs_prefill_attn_lse_layers(
+        _dev(q, "bf16", "q"), _dev(k, "bf16", "k"), _dev(v, "bf16", "v"), _dev(o, "bf16", "o"),
+        _dev(m, "f32", "m"), _dev(l, "f32", "l"), _dev(cu_seqlens, "i32", "cu_seqlens"),
+        batch, max_n, total_tokens, h_q, h_kv, d, float(scale), n_layers,
+        None if status is None else _dev(status, "i32", "status"), _stream(stream)))
+
+
 def kvs_prefill_attn_lse(q, k, v, o, m, l, cu_seqlens, batch, max_n, total_tokens, h_q, h_kv,
                          d, scale, status=None, stream=None):
     _check(library().kvs_prefill_attn_lse(
@@ -151,8 +167,11 @@ def kvs_prefill_attn_lse(q, k, v, o, m, l, cu_seqlens, batch, max_n, total_token
 
 def kvs_window_scores_layers(q, k, m, l, scores, cu_seqlens, batch, max_n, total_tokens, h_q,
                              h_kv, d, alpha, scale, n_layers, status=None, stream=None):
-    """q, k, m, l, scores: the first of n_layers consecutive layers of stacked
-    buffers (each next layer one tensor further on)."""
+    """q, k, m, l, scores: n_layers layers stacked in one buffer each (leading
+    dimension n_layers)."""
+    for t, what in ((q, "q"), (k, "k"), (m, "m"), (l, "l"), (scores, "scores")):
+        if t.shape[0] != n_layers:
+            raise ValueError(f"{what} must have n_layers = {n_layers} as its leading dimension")
     _check(library().kvs_window_scores_layers(
         _dev(q, "bf16", "q"), _dev(k, "bf16", "k"), _dev(m, "f32", "m"), _dev(l, "f32", "l"),
         _dev(scores, "f32", "scores"), _dev(cu_seqlens, "i32", "cu_seqlens"), batch, max_n,

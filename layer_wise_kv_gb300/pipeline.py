@@ -2,7 +2,8 @@
 of prompts over all layers, then decode steps over the paged cache.
 
 Step orders (the same ones the CPU oracle uses):
-* prefill: for each layer, prefill attention (+ m, l); then the window scores
+* prefill: for each layer, prefill attention (+ m, l) -- one launch over all
+  layers when every layer's inputs are resident in one buffer; then the window scores
   of the layers with a budget below the prompt length (one launch per run of
   consecutive such layers: a layer's scores read only its own q, k, m, l;
   while the layers' inputs are still being copied in, each layer's scores
@@ -151,11 +152,16 @@ class Engine:
         """q_layers[l]: [T][h_q][d] bf16, k/v_layers[l]: [T][h_kv][d] (T = sum of
         seq_lens, sequences packed).  budgets[b][l]: k_l for sequence b (None =
         full cache).  select_scores: optional [L][h_kv][T] scores to select on
-        instead of the ones computed here.  ml_buf: optional pair of
-        [L][h_q][T] fp32 buffers for every layer's m and l.  timing: optional
+        instead of the ones computed here.  o_buf: optional [L][T][h_q][d]
+        buffer for every layer's attention output, or one [T][h_q][d] buffer
+        that each layer overwrites (which rules out the single launch over
+        all layers).  ml_buf: optional pair of [L][h_q][T] fp32 buffers for
+        every layer's m and l.  timing: optional
         dict of lists "attn" / "scores" that receive a (start, end) CUDA event
         pair around the prefill-attention launches of the layers in
-        timing_layers (every layer when None) / around each window-score
+        timing_layers (every layer when None; the one launch over all layers
+        when inputs are resident and stacked, "attn_layers" receiving the
+        layers each timed launch covers) / around each window-score
         launch (one per run of consecutive budgeted layers; per layer when
         `ready` is given).  An event
         recorded between two launches ends the overlap of the second one's
@@ -173,8 +179,15 @@ class Engine:
         T, cu_d, max_n = plan["T"], plan["cu_d"], plan["max_n"]
         keff, budgeted, any_budget = plan["keff"], plan["budgeted"], plan["any_budget"]
 
-        if o_buf is None:
-            o_buf = torch.empty((T, s.h_q, s.d), dtype=torch.bfloat16, device=dev)
+        # O of every layer ([L][T][h_q][d]) unless the caller passes one
+        # [T][h_q][d] buffer that every layer overwrites
+        o_all = None
+        if keep_outputs or o_buf is None:
+            o_all = torch.empty((L, T, s.h_q, s.d), dtype=torch.bfloat16, device=dev)
+        elif o_buf.dim() == 4:
+            if tuple(o_buf.shape) != (L, T, s.h_q, s.d):
+                raise ValueError(f"o_buf must be [{L}][{T}][{s.h_q}][{s.d}] or [{T}][{s.h_q}][{s.d}]")
+            o_all = o_buf
         # scores of layers without a budget are never read (their selection is
         # the identity), so the buffer needs no clearing
         scores = torch.empty((L, s.h_kv, T), dtype=torch.float32, device=dev)
@@ -187,10 +200,22 @@ class Engine:
             m_all, l_all = ml_buf
             if tuple(m_all.shape) != (L, s.h_q, T) or tuple(l_all.shape) != (L, s.h_q, T):
                 raise ValueError(f"ml_buf must be two [{L}][{s.h_q}][{T}] fp32 tensors")
-        keep_o = []
-        for l in range(L):
+        # inputs resident and every layer's Q, K, V (and O) slices of one
+        # buffer each: one persistent launch over all layers' work items, so
+        # the launch, start-up and uneven tail are paid once, not per layer
+        qa, ka, va = _stacked_view(q_layers), _stacked_view(k_layers), _stacked_view(v_layers)
+        one_launch = (ready is None and o_all is not None and qa is not None and ka is not None
+                      and va is not None)
+        if one_launch:
+            ev = _events(timing, "attn", stream)
+            kvs.kvs_prefill_attn_lse_layers(qa, ka, va, o_all, m_all, l_all, cu_d, B, max_n, T,
+                                            s.h_q, s.h_kv, s.d, s.scale, L, self.status, stream)
+            _close(ev, stream)
+            if timing is not None:
+                timing.setdefault("attn_layers", []).append(L)
+        for l in range(L if not one_launch else 0):
             m, lsum = m_all[l], l_all[l]
-            o = o_buf if not keep_outputs else torch.empty_like(o_buf)
+            o = o_all[l] if o_all is not None else o_buf
             if ready is not None:
                 for e in ready[l]:
                     (torch.cuda.current_stream() if stream is None else stream).wait_event(e)
@@ -199,8 +224,8 @@ class Engine:
             kvs.kvs_prefill_attn_lse(q_layers[l], k_layers[l], v_layers[l], o, m, lsum, cu_d, B,
                                      max_n, T, s.h_q, s.h_kv, s.d, s.scale, self.status, stream)
             _close(ev, stream)
-            if keep_outputs:
-                keep_o.append(o)
+            if tl is not None:
+                timing.setdefault("attn_layers", []).append(1)
             if ready is not None and any_budget[l]:
                 # inputs still arriving: the GPU waits for the next layer's
                 # copies anyway, so this layer's scores go in that gap
@@ -265,7 +290,7 @@ class Engine:
         res = PrefillResult(tables=tables, k_eff=keff, kept_idx=kept, idx_off=idx_off,
                             scores=scores)
         if keep_outputs:
-            res.m, res.l, res.o = list(m_all), list(l_all), keep_o
+            res.m, res.l, res.o = list(m_all), list(l_all), list(o_all)
         return res
 
 

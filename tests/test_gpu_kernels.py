@@ -174,6 +174,43 @@ def test_prefill_vs_oracle(lens, h_q, h_kv, d):
         check_rel(gl[:, s0:s0 + n], rl, REL_ML, what="l")
 
 
+@pytest.mark.parametrize("lens,h_q,h_kv,d", [([1, 127, 128, 129, 300], 8, 2, 128),
+                                              ([256], 4, 2, 64)])
+def test_prefill_layers_match_per_layer_launches(lens, h_q, h_kv, d):
+    """kvs_prefill_attn_lse_layers over layers stacked in one buffer gives, bit
+    for bit, the O, m and l that kvs_prefill_attn_lse gives layer by layer
+    (whose values the test above checks against the oracle); its work items
+    of all layers share one persistent grid."""
+    kvs = kvs_lib()
+    rng = np.random.default_rng(5 * sum(lens) + d)
+    n_layers, T = 3, sum(lens)
+    cu = torch.from_numpy(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)).cuda()
+    q = dev_bf16(_randn_bits(rng, (n_layers, T, h_q, d), 1.5))
+    k = dev_bf16(_randn_bits(rng, (n_layers, T, h_kv, d)))
+    v = dev_bf16(_randn_bits(rng, (n_layers, T, h_kv, d)))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    scale = 1 / np.sqrt(d)
+    outs = []
+    for one_launch in (False, True):
+        o = torch.full((n_layers, T, h_q, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+        m = torch.full((n_layers, h_q, T), float("nan"), dtype=torch.float32, device="cuda")
+        l = torch.full_like(m, float("nan"))
+        if one_launch:
+            kvs.kvs_prefill_attn_lse_layers(q, k, v, o, m, l, cu, len(lens), max(lens), T, h_q,
+                                            h_kv, d, scale, n_layers, status)
+        else:
+            for li in range(n_layers):
+                kvs.kvs_prefill_attn_lse(q[li], k[li], v[li], o[li], m[li], l[li], cu, len(lens),
+                                         max(lens), T, h_q, h_kv, d, scale, status)
+        outs.append((o, m, l))
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    for a, b in zip(outs[0], outs[1]):
+        assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a.view(torch.int32),
+                           b.view(torch.int16) if b.dtype == torch.bfloat16 else b.view(torch.int32))
+    assert not torch.isnan(outs[1][0]).any() and not torch.isnan(outs[1][1]).any()
+
+
 # ---------------------------------------------------------------------------
 # window scores, given the oracle's m and l
 # ---------------------------------------------------------------------------
