@@ -27,6 +27,7 @@ with no dirty lines left to write back.
 from __future__ import annotations
 
 import argparse
+import gc
 import json
 import os
 import statistics
@@ -296,6 +297,11 @@ def bench_gpu(args):
         dist.barrier()
     clocks = ClockSampler(local)
     clocks.start()
+    # no Python garbage collection inside the timed region: a collection
+    # pauses the host thread that enqueues the work (tens of ms after the
+    # warm-up's allocations) and the GPU idles meanwhile
+    gc.collect()
+    gc.disable()
     rec = new_rec()
     t_wall = time.perf_counter()
     for _ in range(args.steps):
@@ -303,6 +309,7 @@ def bench_gpu(args):
         run_request(eng, dec, w, n, steps, q, k, v, dq, dk, dv, o_buf, ml_buf, flush, rec)
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
+    gc.enable()
     clk = clocks.stop()
     if world > 1:
         dist.barrier()
@@ -411,12 +418,24 @@ def bench_e2e(args, eng, dec, w, n, steps, q, k, v, dq, dk, dv, o_buf, ml_buf, f
             "streams": [torch.cuda.Stream()],
             "out": torch.empty((steps, w.n_layers, w.h_q, w.d), dtype=torch.bfloat16).pin_memory(),
             "kept": torch.empty(n * w.n_layers * w.h_kv, dtype=torch.int32).pin_memory()}
+    # untimed warm-up through the host buffers: the first copies out of newly
+    # pinned memory run about 10x slower than later ones (the pages are mapped
+    # for the device on first use)
+    for _ in range(max(1, min(args.warmup, 2))):
+        flush()
+        run_request(eng, dec, w, n, steps, q, k, v, pq, pk, pv, o_buf, ml_buf, flush,
+                    {"prefill": [], "decode": [], "k1": None}, host=host)
+    torch.cuda.synchronize()
     rec = {"prefill": [], "decode": [], "k1": None}
     reps = max(1, min(args.steps, 3))
+    gc.collect()
+    gc.disable()
     for _ in range(reps):
         flush()
         run_request(eng, dec, w, n, steps, q, k, v, pq, pk, pv, o_buf, ml_buf, flush, rec,
                     host=host)
+    torch.cuda.synchronize()
+    gc.enable()
     t_pre = sum(a.elapsed_time(b) for a, b in rec["prefill"]) / reps
     t_dec = sum(a.elapsed_time(b) for a, b in rec["decode"]) / reps
     t_pre, t_dec = max_over_ranks([t_pre, t_dec], world, dist, q.device)

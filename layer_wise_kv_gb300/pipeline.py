@@ -298,23 +298,28 @@ def upload_layers(host: Sequence[Sequence[torch.Tensor]], dev: Sequence[Sequence
                   streams: Sequence[torch.cuda.Stream]) -> List[List[torch.cuda.Event]]:
     """Layer-wise upload of a prompt's inputs: host[i][l] (pinned host memory)
     is copied into dev[i][l] for every tensor kind i (e.g. Q, K, V), layer by
-    layer, kind i on streams[i % len(streams)].  Returns, per layer, the events
-    of its copies; prefill_sparsify(ready=...) starts layer l once they have
-    completed, so layer l computes while layers l+1, ... are still being
-    copied.  Each copy stream first waits for the work already queued on the
-    current stream."""
+    layer, kind i on streams[i % len(streams)].  Returns, per layer, one event
+    per copy stream that carried part of it; prefill_sparsify(ready=...)
+    starts layer l once they have completed, so layer l computes while layers
+    l+1, ... are still being copied.  Each copy stream first waits for the
+    work already queued on the current stream."""
     cur = torch.cuda.current_stream()
     for st in streams:
         st.wait_stream(cur)
     events = []
     for l in range(len(dev[0])):
-        per_layer = []
+        used = []
         for i, (h, d) in enumerate(zip(host, dev)):
             st = streams[i % len(streams)]
             with torch.cuda.stream(st):
                 d[l].copy_(h[l], non_blocking=True)
-                e = torch.cuda.Event()
-                e.record(st)
+            if st not in used:
+                used.append(st)
+        # one event per copy stream that carried a part of this layer
+        per_layer = []
+        for st in used:
+            e = torch.cuda.Event()
+            e.record(st)
             per_layer.append(e)
         events.append(per_layer)
     return events
