@@ -92,10 +92,12 @@ struct PrefillSmem {
 
 // A work item: one query head g of one pair of 128-row query tiles (A: rows
 // q0 .. q0+127, B: q0+128 .. q0+255, q0 = 256 pr) of sequence b of one layer.
-// Items are numbered pair rank from the top of the sequence (y) slowest, then
-// layer, then sequence, then head, so the numbering runs from the longest
-// pairs of every layer down; an item whose sequence has fewer than y + 1
-// pairs is empty.  Layers are stacked: layer j's rows follow layer j-1's in
+// Items are numbered layer slowest, then pair rank from the top of the
+// sequence (y), then sequence, then head: within a layer the numbering runs
+// from the longest pairs down (an item whose sequence has fewer than y + 1
+// pairs is empty), and the layers follow one another, so a layer's K and V
+// stay in L2 while its items run and only the last layer's short items make
+// the launch's tail.  Layers are stacked: layer j's rows follow layer j-1's in
 // the Q/K/V maps and in O (row = j * total + token), its m and l sit one
 // [h_q][total] plane further on.
 struct PItem {
@@ -112,8 +114,8 @@ __device__ __forceinline__ PItem item_at(int idx, const PrefillParams& p) {
   const int rest = idx / p.h_q;
   const int b = rest % p.batch;
   const int rest2 = rest / p.batch;
-  const int layer = rest2 % p.n_layers;
-  const int y = rest2 / p.n_layers;
+  const int y = rest2 % p.n_pairs_max;
+  const int layer = rest2 / p.n_pairs_max;
   const int tok0 = p.cu_seqlens[b];
   it.n = p.cu_seqlens[b + 1] - tok0;
   it.seq0 = layer * p.total + tok0;
