@@ -54,9 +54,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # the figure reported is scaled to the launch the bench times (decode length
 # grows over the request).  Set an entry to None once its kernel changes.
 NCU_TRAFFIC = {
-    # cleared until recaptured: both kernels changed since their captures
-    "prefill_attn": None,
-    "paged_decode": None,
+    # the one prefill launch over all 32 layers: the bench's own launch shape
+    "prefill_attn": {"bytes": 1694695936 + 1057856512, "alg_bytes": None},
+    "paged_decode": {"bytes": 188684544 + 3636736, "alg_bytes": 187432960},
 }
 
 
