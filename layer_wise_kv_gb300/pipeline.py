@@ -412,6 +412,51 @@ class DecodeBatch:
         self.ws = torch.zeros(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
         kvs.kvs_workspace_zero(self.ws, self.ws_bytes)
         self.out = torch.empty((self.n_items, s.h_q, s.d), dtype=torch.bfloat16, device=dev)
+        self._graphs = None
+
+    # ------------------------------------------------------------ CUDA graphs
+    def capture_graphs(self):
+        """Capture the decode step as CUDA graphs, so that a step costs the host
+        one graph launch instead of the library's launches (the method's
+        serving loop runs in CUDA-graph mode).  Four graphs: the two
+        directions of the length ping-pong, each with and without the upload
+        of the allocator's table patch.  Afterwards step() replays the
+        matching graph, and launches eagerly only on a step where a block
+        needs copy-on-write (its count of copies varies).  The graphs read
+        the step's inputs from the fixed buffers self.q_in, self.k_in,
+        self.v_in (step() copies other tensors into them) and the patch from
+        two pinned buffers, one per direction."""
+        s, dev = self.eng.shape, self.eng.device
+        n = self.n_items
+        self.q_in = torch.zeros((n, s.h_q, s.d), dtype=torch.bfloat16, device=dev)
+        self.k_in = torch.zeros((n, s.h_kv, s.d), dtype=torch.bfloat16, device=dev)
+        self.v_in = torch.zeros_like(self.k_in)
+        self._patch_g = [torch.full((n,), -1, dtype=torch.int32).pin_memory() for _ in range(2)]
+        self._patch_g_np = [t.numpy() for t in self._patch_g]
+        self._gev = [None, None]
+        eng = self.eng
+        # one-time library set-up (kernel attributes, tensor maps) outside the
+        # capture: a call that appends nothing and writes only out and the
+        # workspace leaves the caches as they are
+        kvs.kvs_paged_decode(self.q_in, None, None, eng.k_pool, eng.v_pool, eng.num_blocks,
+                             self.tables_d, self.max_blocks, None, self.lens_d[self.cur], None, n,
+                             s.h_q, s.h_kv, s.d, s.scale, self.out, self.ws, self.ws_bytes,
+                             eng.status)
+        torch.cuda.synchronize()
+        graphs = {}
+        for cur in (0, 1):
+            for with_patch in (False, True):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    if with_patch:
+                        self.patch_d.copy_(self._patch_g[cur], non_blocking=True)
+                    kvs.kvs_paged_decode(self.q_in, self.k_in, self.v_in, eng.k_pool, eng.v_pool,
+                                         eng.num_blocks, self.tables_d, self.max_blocks,
+                                         self.patch_d if with_patch else None, self.lens_d[cur],
+                                         self.lens_d[1 - cur], n, s.h_q, s.h_kv, s.d, s.scale,
+                                         self.out, self.ws, self.ws_bytes, eng.status)
+                graphs[(cur, with_patch)] = g
+        self._graphs = graphs
 
     def set_stream(self, slot: int, tables: List[List[int]], lens: List[int]):
         """Install a stream's per-layer tables (host copy + device rows)."""
@@ -451,12 +496,40 @@ class DecodeBatch:
         n = self.n_items
         slot = self._slot
         patch_t, cow_t = self.patch_h[slot], self.cow_h[slot]
+        patch_np = self._patch_np[slot]
+        if self._graphs is not None:
+            # the patch goes to this direction's fixed pinned buffer, last read
+            # by the replay two steps ago
+            if self._gev[self.cur] is not None:
+                self._gev[self.cur].synchronize()
+            patch_t, patch_np = self._patch_g[self.cur], self._patch_g_np[self.cur]
         if self._ev[slot] is not None:
             self._ev[slot].synchronize()
-        n_cow, n_patch = eng.alloc.decode_prepare(self.tables_h, self.lens_h, self._patch_np[slot],
+        n_cow, n_patch = eng.alloc.decode_prepare(self.tables_h, self.lens_h, patch_np,
                                                   self.cow_src, self.cow_dst,
                                                   with_patch_count=True)
         cur_stream = torch.cuda.current_stream() if stream is None else stream
+        nxt = 1 - self.cur
+        if self._graphs is not None and n_cow == 0:
+            with torch.cuda.stream(cur_stream):
+                for src, dst in ((q, self.q_in), (k_new, self.k_in), (v_new, self.v_in)):
+                    if src is not dst:
+                        dst.copy_(src, non_blocking=True)
+                if timing is not None:
+                    a = torch.cuda.Event(enable_timing=True)
+                    b = torch.cuda.Event(enable_timing=True)
+                    a.record(cur_stream)
+                self._graphs[(self.cur, bool(n_patch))].replay()
+                if timing is not None:
+                    b.record(cur_stream)
+                    timing.append((a, b))
+                if n_patch:
+                    ev = torch.cuda.Event()
+                    ev.record(cur_stream)
+                    self._gev[self.cur] = ev
+            self.cur = nxt
+            self.lens_h += 1
+            return self.out
         patch_arg = None
         if n_patch or n_cow:
             self._slot = (slot + 1) % self._ring
@@ -474,7 +547,8 @@ class DecodeBatch:
                 ev = torch.cuda.Event()
                 ev.record(cur_stream)
                 self._ev[slot] = ev
-        nxt = 1 - self.cur
+                if self._graphs is not None:
+                    self._gev[self.cur] = ev
         if timing is not None:
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)

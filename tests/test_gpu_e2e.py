@@ -369,3 +369,51 @@ def test_layerwise_upload_matches_resident_inputs():
     assert torch.equal(res_a.kept_idx, res_b.kept_idx)
     np.testing.assert_array_equal(host_bits(eng_a.k_pool), host_bits(eng_b.k_pool))
     np.testing.assert_array_equal(host_bits(eng_a.v_pool), host_bits(eng_b.v_pool))
+
+
+def test_decode_graphs_match_eager():
+    """DecodeBatch.capture_graphs(): steps replayed from CUDA graphs give, bit
+    for bit, the outputs, block tables, lengths, refcounts and pool bytes of
+    eager steps.  Three samples share a prompt's blocks, so the first step
+    copies blocks on write (launched eagerly), and later steps cross block
+    boundaries (graphs that upload a table patch) and stay inside blocks
+    (graphs without one)."""
+    kvs_lib()
+    from layer_wise_kv_gb300.pipeline import DecodeBatch, Engine
+    w = tiny()
+    n, L, N, S, steps = 100, w.n_layers, 64, 3, 24
+    ql, kl, vl, _ = _layers_to_device(w, [3], [n])
+    budgets = [[w.budget(l, n) for l in range(L)]]
+    dq = {(s, l): decode_qkv(w, 3, l, steps, sample=s) for s in range(S) for l in range(L)}
+    runs = []
+    for graphs in (False, True):
+        eng = Engine(_shape(w), N, poison=True)
+        res = eng.prefill_sparsify(ql, kl, vl, [n], budgets)
+        dec = DecodeBatch(eng, S, n + 40)
+        dec.set_stream(0, res.tables[0], res.k_eff[0])
+        for s in range(1, S):
+            for t in res.tables[0]:
+                for b in t:
+                    eng.alloc.incref(b)
+            dec.set_stream(s, res.tables[0], res.k_eff[0])
+        if graphs:
+            dec.capture_graphs()
+        outs = []
+        for t in range(steps):
+            q = dev_bf16(np.stack([dq[(s, l)][0][t] for s in range(S) for l in range(L)]))
+            k = dev_bf16(np.stack([dq[(s, l)][1][t] for s in range(S) for l in range(L)]))
+            v = dev_bf16(np.stack([dq[(s, l)][2][t] for s in range(S) for l in range(L)]))
+            outs.append(dec.step(q, k, v).clone())
+        torch.cuda.synchronize()
+        eng.check_status()
+        runs.append((eng, dec, outs))
+    (ea, da, oa), (eb, db, ob) = runs
+    for t in range(steps):
+        assert torch.equal(oa[t].view(torch.int16), ob[t].view(torch.int16)), t
+    for s in range(S):
+        assert da.stream_tables(s) == db.stream_tables(s)
+    assert torch.equal(da.tables_d, db.tables_d)
+    assert torch.equal(da.lens_d[da.cur], db.lens_d[db.cur])
+    assert [ea.alloc.refcount(b) for b in range(N)] == [eb.alloc.refcount(b) for b in range(N)]
+    np.testing.assert_array_equal(host_bits(ea.k_pool), host_bits(eb.k_pool))
+    np.testing.assert_array_equal(host_bits(ea.v_pool), host_bits(eb.v_pool))
