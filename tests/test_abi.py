@@ -68,6 +68,18 @@ def test_invalid_arguments_rejected_before_launch(kvs):
     assert lib.kvs_prefill_attn_lse(1, 1, 1, 1, 1, 1, 1, 1, 16, 16, 6, 4, 128, 0.1, None,
                                     None) == kvs.KVS_ERR_INVALID  # 6 % 4 != 0
     assert kvs.kvs_paged_decode_workspace_size(0, 32, 8, 128) == 0
+    # the multi-layer entries: zero layers is a no-op, a negative count an error,
+    # both before any launch
+    assert lib.kvs_prefill_attn_lse_layers(256, 256, 256, 256, 256, 256, 256, 1, 16, 16, 8, 2,
+                                           128, 0.1, 0, None, None) == kvs.KVS_OK
+    assert lib.kvs_prefill_attn_lse_layers(256, 256, 256, 256, 256, 256, 256, 1, 16, 16, 8, 2,
+                                           128, 0.1, -1, None, None) == kvs.KVS_ERR_INVALID
+    assert lib.kvs_window_scores_layers(256, 256, 256, 256, 256, 256, 1, 16, 16, 8, 2, 128, 16,
+                                        0.1, 0, None, None) == kvs.KVS_OK
+    assert lib.kvs_window_scores_layers(256, 256, 256, 256, 256, 256, 1, 16, 16, 8, 2, 128, 16,
+                                        0.1, -2, None, None) == kvs.KVS_ERR_INVALID
+    assert lib.kvs_window_scores_layers(256, 256, 256, 256, 256, 256, 1, 16, 16, 8, 2, 128, 16,
+                                        0.1, 70000, None, None) == kvs.KVS_ERR_UNSUPPORTED
 
 
 def test_worked_example_allocator(kvs, golden_dir):

@@ -142,6 +142,7 @@ PREFILL_CASES = [  # (lens, h_q, h_kv, d)
     ([256], 4, 2, 64),                     # the tiny workload's shape
     ([1, 127, 128, 129, 300], 8, 2, 128),  # ragged varlen batch
     ([700], 8, 8, 128),                    # no grouping, several diagonal rows
+    ([0, 130, 0, 1], 4, 2, 128),           # empty sequences inside the batch
 ]
 
 
@@ -166,6 +167,8 @@ def test_prefill_vs_oracle(lens, h_q, h_kv, d):
     assert status.item() == 0
     go, gm, gl = bf16_f64(o), m.cpu().numpy(), l.cpu().numpy()
     for b, n in enumerate(lens):
+        if n == 0:
+            continue                       # an empty sequence owns no rows
         s0 = cu[b]
         ro, rm, rl = oracle.prefill_rows(bf16_to_f64(qb[s0:s0 + n]), bf16_to_f64(kb[s0:s0 + n]),
                                          bf16_to_f64(vb[s0:s0 + n]), scale)
@@ -218,6 +221,7 @@ SCORE_CASES = [  # (lens, h_q, h_kv, d, alpha)
     ([256], 4, 2, 64, 16),
     ([300, 129, 20], 8, 2, 128, 32),       # the last sequence is shorter than alpha
     ([1000], 32, 8, 128, 32),
+    ([0, 40, 0, 7], 8, 2, 64, 16),         # empty sequences; one shorter than alpha
 ]
 
 
@@ -234,6 +238,9 @@ def test_window_scores_vs_oracle(lens, h_q, h_kv, d, alpha):
     l_in = np.ones((h_q, T), np.float32)
     refs = []
     for b, n in enumerate(lens):
+        if n == 0:
+            refs.append(None)              # an empty sequence has no keys
+            continue
         s0 = cu[b]
         w = min(alpha, n)
         win = np.arange(n - w, n)
@@ -253,6 +260,8 @@ def test_window_scores_vs_oracle(lens, h_q, h_kv, d, alpha):
     assert status.item() == 0
     got = scores.cpu().numpy().astype(np.float64)
     for b, n in enumerate(lens):
+        if n == 0:
+            continue
         s0 = cu[b]
         check_rel(got[:, s0:s0 + n], refs[b], REL_S, ABS_S, what=f"S seq {b}")
         w = min(alpha, n)
