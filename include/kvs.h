@@ -338,6 +338,40 @@ kvs_status kvs_decode_prepare(kvs_allocator* a, int32_t* tables, int32_t max_blo
                               int32_t* cow_src, int32_t* cow_dst, int32_t* n_cow,
                               int32_t* n_patch, int32_t* n_done);
 
+/* ------------------------------------------------------------------------
+ * One whole decode step in one native call: the host preparation above, the
+ * uploads it needs and the paged decode (the per-step sequence of the
+ * Ultralytics glossary "PagedAttention", section "How paging works", and of
+ * the Novita article's serving loop; bundling it is this library's calling
+ * convention, so that a serving loop spends microseconds of host time per
+ * step).  In order, on `stream`:
+ *   1. kvs_decode_prepare over the host mirrors tables_h [n_items][max_blocks]
+ *      and lens_h [n_items] (lengths before this step's append);
+ *   2. if blocks must be copied on write: the (old, new) pairs, staged in
+ *      cow_h [2 n_items] host, are uploaded to cow_d [2 n_items] device and
+ *      kvs_copy_blocks runs;
+ *   3. if any table entry changed: patch_h [n_items] host is uploaded to
+ *      patch_d [n_items] device and passed as table_patch;
+ *   4. kvs_paged_decode with k_new / v_new appended (both required), lens ->
+ *      lens_next on the device;
+ *   5. lens_h[i] += 1 on the host.
+ * patch_h and cow_h are read by copies queued on `stream`: use pinned memory
+ * for an asynchronous upload, and do not write them again before those
+ * copies have run (a ring of staging buffers guarded by events).  n_cow,
+ * n_patch (nullable) receive this step's counts.  A preparation error
+ * (KVS_ERR_OOM_BLOCKS, bad sizes) launches nothing; a launch error after the
+ * preparation leaves the host mirrors prepared for the step.
+ * ---------------------------------------------------------------------- */
+kvs_status kvs_decode_step(kvs_allocator* a, int32_t* tables_h, int32_t* lens_h,
+                           int32_t* patch_h, int32_t* cow_h, int32_t* patch_d, int32_t* cow_d,
+                           const kvs_bf16* q, const kvs_bf16* k_new, const kvs_bf16* v_new,
+                           kvs_bf16* k_pool, kvs_bf16* v_pool, int32_t num_blocks,
+                           int32_t* block_tables, int32_t max_blocks, const int32_t* lens,
+                           int32_t* lens_next, int32_t n_items, int32_t h_q, int32_t h_kv,
+                           int32_t d, float scale, kvs_bf16* out, void* workspace,
+                           size_t workspace_bytes, int32_t* status, int32_t* n_cow,
+                           int32_t* n_patch, kvs_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -54,6 +54,9 @@ _SIGS = {
     "kvs_window_scores_layers": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _I32, _I32, _I32, _I32,
                                         _I32, _I32, _I32, _F32, _I32, _VP, _VP]),
     "kvs_select_topk": (_I32, [_VP, _I64, _VP, _I32, _I32, _I32, _VP, _VP, _VP]),
+    "kvs_decode_step": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I32,
+                               _VP, _I32, _VP, _VP, _I32, _I32, _I32, _I32, _F32, _VP, _VP, _SZ,
+                               _VP, _VP, _VP, _VP]),
     "kvs_compact_blocks": (_I32, [_VP, _VP, _VP, _I32, _I64, _I32, _I32, _VP, _VP, _VP, _VP,
                                   _I32, _VP, _VP]),
     "kvs_copy_blocks": (_I32, [_VP, _VP, _I32, _VP, _VP, _I32, _I32, _I32, _VP, _VP]),
@@ -257,6 +260,33 @@ def kvs_paged_decode_static(q, k_new, v_new, k_pool, v_pool, num_blocks, block_t
 # ---------------------------------------------------------------------------
 # block allocator (host)
 # ---------------------------------------------------------------------------
+def kvs_decode_step(alloc, tables_h, lens_h, patch_h, cow_h, patch_d, cow_d, q, k_new, v_new,
+                    k_pool, v_pool, num_blocks, block_tables, max_blocks, lens, lens_next,
+                    n_items, h_q, h_kv, d, scale, out, workspace, workspace_bytes, status=None,
+                    stream=None):
+    """One decode step in one native call (host preparation, uploads, paged
+    decode).  tables_h [n_items][max_blocks], lens_h [n_items]: host int32
+    numpy mirrors (updated in place); patch_h [n_items], cow_h [2 n_items]:
+    pinned host int32 staging tensors; the rest as for kvs_paged_decode.
+    Returns (n_cow, n_patch)."""
+    assert tables_h.dtype == np.int32 and tables_h.flags.c_contiguous
+    assert lens_h.dtype == np.int32 and lens_h.flags.c_contiguous
+    for t, what in ((patch_h, "patch_h"), (cow_h, "cow_h")):
+        if t.is_cuda or t.dtype != __import__("torch").int32 or not t.is_contiguous():
+            raise TypeError(f"{what} must be a contiguous host int32 tensor")
+    n_cow, n_patch = ctypes.c_int32(), ctypes.c_int32()
+    _check(library().kvs_decode_step(
+        alloc._h, tables_h.ctypes.data, lens_h.ctypes.data, patch_h.data_ptr(), cow_h.data_ptr(),
+        _dev(patch_d, "i32", "patch_d"), _dev(cow_d, "i32", "cow_d"), _dev(q, "bf16", "q"),
+        _dev(k_new, "bf16", "k_new"), _dev(v_new, "bf16", "v_new"), _dev(k_pool, "bf16", "k_pool"),
+        _dev(v_pool, "bf16", "v_pool"), num_blocks, _dev(block_tables, "i32", "block_tables"),
+        max_blocks, _dev(lens, "i32", "lens"), _dev(lens_next, "i32", "lens_next"), n_items, h_q,
+        h_kv, d, float(scale), _dev(out, "bf16", "out"), _dev(workspace, "u8", "workspace"),
+        workspace_bytes, None if status is None else _dev(status, "i32", "status"),
+        ctypes.byref(n_cow), ctypes.byref(n_patch), _stream(stream)))
+    return n_cow.value, n_patch.value
+
+
 class BlockAllocator:
     """kvs_alloc_*: FIFO free list, reference counts, copy-on-write."""
 

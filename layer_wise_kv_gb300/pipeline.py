@@ -22,6 +22,7 @@ sequences").
 """
 from __future__ import annotations
 
+import ctypes
 from dataclasses import dataclass, field
 from typing import List, Optional, Sequence
 
@@ -325,6 +326,17 @@ def upload_layers(host: Sequence[Sequence[torch.Tensor]], dev: Sequence[Sequence
     return events
 
 
+def _raw_stream(stream, device_index):
+    """cudaStream_t of `stream`, else of the current stream (the cheapest
+    lookup torch offers, with the public one as the fallback)."""
+    if stream is not None:
+        return stream.cuda_stream
+    get = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if get is not None:
+        return get(device_index)
+    return torch.cuda.current_stream().cuda_stream
+
+
 def _events(timing, key, stream):
     if timing is None:
         return None
@@ -384,6 +396,7 @@ class DecodeBatch:
         self.eng = eng
         self.n_streams = n_streams
         self.n_items = n_streams * s.n_layers
+        self.shape_ = s
         self.max_len = max_len
         self.max_blocks = blocks_for(max_len)
         dev = eng.device
@@ -413,6 +426,51 @@ class DecodeBatch:
         kvs.kvs_workspace_zero(self.ws, self.ws_bytes)
         self.out = torch.empty((self.n_items, s.h_q, s.d), dtype=torch.bfloat16, device=dev)
         self._graphs = None
+        # the native step's fixed arguments, looked up once (raw addresses of
+        # buffers this object owns for its whole life)
+        self._nat = (eng.alloc._h, self.tables_h.ctypes.data, self.lens_h.ctypes.data,
+                     [t.data_ptr() for t in self.patch_h], [t.data_ptr() for t in self.cow_h],
+                     self.patch_d.data_ptr(), self.cow_d.data_ptr(), eng.k_pool.data_ptr(),
+                     eng.v_pool.data_ptr(), self.tables_d.data_ptr(),
+                     [t.data_ptr() for t in self.lens_d], self.out.data_ptr(),
+                     self.ws.data_ptr(), eng.status.data_ptr())
+        self._counts = (ctypes.c_int32(), ctypes.c_int32())
+        self._count_refs = tuple(ctypes.byref(c) for c in self._counts)
+        self._lib = kvs.library()
+        self._dev_index = self.eng.device.index if self.eng.device.index is not None \
+            else torch.cuda.current_device()
+
+    def _native_step(self, q, k_new, v_new, stream):
+        s = self.shape_
+        for t, shape in ((q, (self.n_items, s.h_q, s.d)), (k_new, (self.n_items, s.h_kv, s.d)),
+                         (v_new, (self.n_items, s.h_kv, s.d))):
+            if (not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous()
+                    or tuple(t.shape) != shape):
+                raise ValueError(f"decode inputs must be contiguous CUDA bf16 {shape} tensors")
+        slot = self._slot
+        if self._ev[slot] is not None:
+            # the copies that last read this slot's staging have run; once
+            # seen, the slot needs no further wait
+            self._ev[slot].synchronize()
+            self._ev[slot] = None
+        (alloc, tables_h, lens_h, patch_h, cow_h, patch_d, cow_d, k_pool, v_pool, tables_d,
+         lens_d, out, ws, status) = self._nat
+        raw_stream = _raw_stream(stream, self._dev_index)
+        n_cow, n_patch = self._counts
+        kvs._check(self._lib.kvs_decode_step(
+            alloc, tables_h, lens_h, patch_h[slot], cow_h[slot], patch_d, cow_d, q.data_ptr(),
+            k_new.data_ptr(), v_new.data_ptr(), k_pool, v_pool, self.eng.num_blocks, tables_d,
+            self.max_blocks, lens_d[self.cur], lens_d[1 - self.cur], self.n_items, s.h_q, s.h_kv,
+            s.d, s.scale, out, ws, self.ws_bytes, status, self._count_refs[0],
+            self._count_refs[1], raw_stream))
+        if n_patch.value or n_cow.value:
+            # this slot's staging buffers are read by copies queued above
+            ev = torch.cuda.Event()
+            ev.record(torch.cuda.current_stream() if stream is None else stream)
+            self._ev[slot] = ev
+            self._slot = (slot + 1) % self._ring
+        self.cur = 1 - self.cur
+        return self.out
 
     # ------------------------------------------------------------ CUDA graphs
     def capture_graphs(self):
@@ -491,7 +549,10 @@ class DecodeBatch:
         """One decode step for every item: q [n_items][h_q][d], k_new/v_new
         [n_items][h_kv][d] bf16 on the device.  Returns the output tensor.
         timing: optional list receiving a (start, end) event pair around the
-        decode kernel."""
+        decode kernel.  Without graphs or timing, the step is one native call
+        (kvs_decode_step: host preparation, uploads and decode)."""
+        if self._graphs is None and timing is None:
+            return self._native_step(q, k_new, v_new, stream)
         eng, s = self.eng, self.eng.shape
         n = self.n_items
         slot = self._slot

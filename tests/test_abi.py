@@ -80,6 +80,16 @@ def test_invalid_arguments_rejected_before_launch(kvs):
                                         0.1, -2, None, None) == kvs.KVS_ERR_INVALID
     assert lib.kvs_window_scores_layers(256, 256, 256, 256, 256, 256, 1, 16, 16, 8, 2, 128, 16,
                                         0.1, 70000, None, None) == kvs.KVS_ERR_UNSUPPORTED
+    # the native decode step: nothing to do for zero items; NULL staging and a
+    # step without an append are rejected before the allocator is touched
+    args = [None] * 29
+    for i in (12, 14, 17, 18, 19, 20, 24):           # the integer arguments
+        args[i] = 0
+    args[21] = 0.0                                  # scale
+    args[17] = 0                                    # n_items
+    assert lib.kvs_decode_step(*args) == kvs.KVS_OK
+    args[17] = 4
+    assert lib.kvs_decode_step(*args) == kvs.KVS_ERR_INVALID
 
 
 def test_worked_example_allocator(kvs, golden_dir):
