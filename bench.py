@@ -381,8 +381,9 @@ def bench_gpu(args):
         "clocks": clk,
         "wall_s": round(t_wall, 2),
     }
-    out["decode_wall"] = bench_decode_wall(args, eng, dec, w, n, steps, q, k, v, dq, dk, dv,
-                                           o_buf, ml_buf, world, dist)
+    if args.decode_wall:
+        out["decode_wall"] = bench_decode_wall(args, eng, dec, w, n, steps, q, k, v, dq, dk, dv,
+                                               o_buf, ml_buf, world, dist)
     if args.e2e:
         out["e2e"] = bench_e2e(args, eng, dec, w, n, steps, q, k, v, dq, dk, dv, o_buf, ml_buf,
                                flush, world, dist)
@@ -569,6 +570,8 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=500)
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--no-decode-wall", dest="decode_wall", action="store_false",
+                    help="skip the back-to-back decode pass timed by the host clock")
     ap.add_argument("--cpu-rows", type=int, default=400,
                     help="prefill rows the CPU oracle evaluates (sample size)")
     args = ap.parse_args()
