@@ -24,6 +24,7 @@ paging    : list-based block pool (FIFO free list, ref counts, copy-on-write),
             compaction into 16-token blocks and table gathers.
 flow      : the step orders that tie these together (prefill+sparsify of a
             sequence, one decode step, retirement).
+eviction  : decode-time scores and fixed-budget replacement in budgeted layers.
 
 Every function is pinned by a ``-m "not gpu"`` test against something other
 than itself (closed forms, library routines, brute force, the worked paging
@@ -34,3 +35,4 @@ from .scoring import window_scores  # noqa: F401
 from .selection import select_kept  # noqa: F401
 from .paging import BlockPool, OutOfBlocks, compact, gather_rows, blocks_for  # noqa: F401
 from . import flow  # noqa: F401
+from . import eviction  # noqa: F401

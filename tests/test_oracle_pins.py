@@ -316,3 +316,90 @@ def test_bf16_rounding_matches_torch():
     ours = bf16_bits(x)
     ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     np.testing.assert_array_equal(ours, ref)
+
+
+# ---------------------------------------------------------------------------
+# decode-time scoring and replacement (oracle/eviction.py)
+# ---------------------------------------------------------------------------
+def _heads(rng, h_kv, k_l, d, n_prompt):
+    """k_l kept prompt tokens per head at distinct positions < n_prompt."""
+    from oracle.eviction import HeadCache
+    out = []
+    for _ in range(h_kv):
+        pos = np.sort(rng.choice(n_prompt, k_l, replace=False)).astype(np.int64)
+        pos[-4:] = np.arange(n_prompt - 4, n_prompt)        # the recent prompt tokens
+        out.append(HeadCache(rng.standard_normal((k_l, d)), rng.standard_normal((k_l, d)),
+                             rng.uniform(0, 3, k_l), pos))
+    return out
+
+
+def test_eviction_step_attention_is_sdpa_over_the_cache():
+    """The step's output is torch's fp64 SDPA of the query over the cache as it
+    stands after the replacement (the new row in its slot, every other row
+    unchanged), and its per-slot probabilities are softmax columns summed over
+    the query group."""
+    from oracle import eviction
+    rng = np.random.default_rng(3)
+    h_q, h_kv, d, k_l = 8, 2, 16, 12
+    heads = _heads(rng, h_kv, k_l, d, 40)
+    before = [(hc.k.copy(), hc.v.copy()) for hc in heads]
+    q = rng.standard_normal((h_q, d))
+    kn, vn = rng.standard_normal((h_kv, d)), rng.standard_normal((h_kv, d))
+    out, probs, used = eviction.step(heads, q, kn, vn, 40, 4, 0.25)
+    for h, hc in enumerate(heads):
+        kb, vb = before[h]
+        changed = [i for i in range(k_l) if not np.array_equal(kb[i], hc.k[i])]
+        assert changed == [used[h]] and np.array_equal(hc.k[used[h]], kn[h])
+        assert np.array_equal(np.delete(hc.v, used[h], 0), np.delete(vb, used[h], 0))
+    kc = np.stack([hc.k for hc in heads], 1)    # [k_l, H_kv, d]
+    vc = np.stack([hc.v for hc in heads], 1)
+    tq = torch.from_numpy(q[:, None, :])        # [H_q, 1, d]
+    tk = torch.from_numpy(kc).permute(1, 0, 2).repeat_interleave(h_q // h_kv, 0)
+    tv = torch.from_numpy(vc).permute(1, 0, 2).repeat_interleave(h_q // h_kv, 0)
+    ref = F.scaled_dot_product_attention(tq, tk, tv, scale=0.25)[:, 0].numpy()
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+    sm = torch.softmax(torch.einsum("gd,gtd->gt", torch.from_numpy(q), tk) * 0.25, -1).numpy()
+    np.testing.assert_allclose(probs, sm.reshape(h_kv, h_q // h_kv, k_l).sum(1), rtol=1e-12)
+    np.testing.assert_allclose(probs.sum(1), h_q // h_kv, rtol=1e-12)   # softmax rows sum to 1
+
+
+def test_eviction_replaces_lowest_outside_recent_window_brute_force():
+    """Over a run of steps, every replaced token is (by exhaustive comparison)
+    the lowest-scoring one among tokens older than the recent window, ties to
+    the lower position; no token inside the window is ever replaced; scores
+    grow by exactly the step's probabilities."""
+    from oracle import eviction
+    rng = np.random.default_rng(4)
+    h_q, h_kv, d, k_l, recent = 4, 2, 8, 10, 4
+    heads = _heads(rng, h_kv, k_l, d, 30)
+    for h in range(h_kv):                                   # constructed ties
+        heads[h].score[:3] = 0.5
+    for t in range(25):
+        new_pos = 30 + t
+        snap = [(hc.score.copy(), hc.pos.copy()) for hc in heads]
+        q = rng.standard_normal((h_q, d)) * (0.0 if t % 5 == 0 else 1.0)   # some uniform steps
+        kn, vn = rng.standard_normal((h_kv, d)), rng.standard_normal((h_kv, d))
+        _, probs, used = eviction.step(heads, q, kn, vn, new_pos, recent, 0.3)
+        for h, hc in enumerate(heads):
+            sc, ps = snap[h]
+            elig = [i for i in range(k_l) if ps[i] <= new_pos - recent]
+            assert all(ps[i] > new_pos - recent for i in range(k_l) if i not in elig)
+            best = sorted(elig, key=lambda i: (sc[i], ps[i]))[0]
+            assert used[h] == best
+            assert ps[used[h]] <= new_pos - recent            # never a recent token
+            expect = sc.copy()
+            expect[used[h]] = 0.0
+            np.testing.assert_allclose(hc.score, expect + probs[h], rtol=1e-12, atol=1e-15)
+            assert hc.pos[used[h]] == new_pos
+        if t % 5 == 0:                                       # q = 0: uniform attention
+            np.testing.assert_allclose(probs, np.full((h_kv, k_l), (h_q // h_kv) / k_l))
+
+
+def test_eviction_valid_choice_tolerance():
+    from oracle.eviction import is_valid_choice
+    score = np.array([1.0, 0.5, 0.5000001, 2.0])
+    pos = np.array([0, 1, 2, 9])
+    assert is_valid_choice(score, pos, 10, 2, 1, 1e-5)
+    assert is_valid_choice(score, pos, 10, 2, 2, 1e-5)      # within the error of the lowest
+    assert not is_valid_choice(score, pos, 10, 2, 0, 1e-5)
+    assert not is_valid_choice(score, pos, 10, 2, 3, 1e-5)  # pos 9 > 10 - 2: recent
