@@ -372,6 +372,50 @@ kvs_status kvs_decode_step(kvs_allocator* a, int32_t* tables_h, int32_t* lens_h,
                            size_t workspace_bytes, int32_t* status, int32_t* n_cow,
                            int32_t* n_patch, kvs_stream stream);
 
+/* ------------------------------------------------------------------------
+ * 7. Decode-time scoring and fixed-budget replacement (budgeted layers).
+ * Source: Novita article, section "Key techniques 1" (after the first three
+ * layers a sliding-window strategy replaces the lowest-scoring KVs
+ * automatically) and section "Key techniques 2" (the decode-side
+ * PagedAttention works toward the same score S as the prefill).  Readings
+ * (the pages give no formula): a budgeted item keeps exactly lens[i] = k_l
+ * slots per KV head; a step's new token takes, per KV head, the slot of the
+ * token with the lowest accumulated score among those at positions
+ * <= new_pos[i] - recent (ties to the lower position); each step adds to
+ * every cached token the attention probability the step's query heads give
+ * it, summed over the KV head's query group.  A step is
+ *   kvs_evict_place -> kvs_paged_decode (k_new = NULL, over lens[i] slots)
+ *   -> kvs_decode_scores
+ * on one stream.  State, device, per item i and KV head h, slot j < lens[i]:
+ *   score [n_items][h_kv][max_slots] fp32: the accumulated score;
+ *   pos   [n_items][h_kv][max_slots] int32: the token's position;
+ *   new_pos [n_items] int32: the position of the step's new token.
+ * Slot j lives at row j % 16 of block block_tables[i][j / 16] (as written by
+ * kvs_compact_blocks).  Out-of-range table entries, lens[i] > max_slots, or
+ * a head whose cached tokens are all recent store KVS_ERR_INVALID in status.
+ * ---------------------------------------------------------------------- */
+
+/* Choose each (item, KV head)'s slot for the step's token and write
+ * k_new / v_new [n_items][h_kv][d] bf16 there; the slot's score becomes 0 and
+ * its position new_pos[i].  One CTA per (item, KV head). */
+kvs_status kvs_evict_place(const kvs_bf16* k_new, const kvs_bf16* v_new, kvs_bf16* k_pool,
+                           kvs_bf16* v_pool, int32_t num_blocks, const int32_t* block_tables,
+                           int32_t max_blocks, const int32_t* lens, const int32_t* new_pos,
+                           float* score, int32_t* pos, int32_t max_slots, int32_t n_items,
+                           int32_t h_kv, int32_t d, int32_t recent, int32_t* status,
+                           kvs_stream stream);
+
+/* Add the step's attention probabilities to the scores: for each (item, KV
+ * head), softmax over the lens[i] slots of scale * q_g . k_j for each query
+ * head g of the group (q [n_items][h_q][d] bf16, K read from the pool), summed
+ * over the group.  Then new_pos[i] += 1.  fp32 arithmetic; G <= 16 and
+ * G * max_slots * 4 bytes <= 200 KB. */
+kvs_status kvs_decode_scores(const kvs_bf16* q, const kvs_bf16* k_pool, int32_t num_blocks,
+                             const int32_t* block_tables, int32_t max_blocks, const int32_t* lens,
+                             float* score, int32_t* new_pos, int32_t max_slots, int32_t n_items,
+                             int32_t h_q, int32_t h_kv, int32_t d, float scale, int32_t* status,
+                             kvs_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -54,6 +54,10 @@ _SIGS = {
     "kvs_window_scores_layers": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _I32, _I32, _I32, _I32,
                                         _I32, _I32, _I32, _F32, _I32, _VP, _VP]),
     "kvs_select_topk": (_I32, [_VP, _I64, _VP, _I32, _I32, _I32, _VP, _VP, _VP]),
+    "kvs_evict_place": (_I32, [_VP, _VP, _VP, _VP, _I32, _VP, _I32, _VP, _VP, _VP, _VP, _I32,
+                               _I32, _I32, _I32, _I32, _VP, _VP]),
+    "kvs_decode_scores": (_I32, [_VP, _VP, _I32, _VP, _I32, _VP, _VP, _VP, _I32, _I32, _I32,
+                                 _I32, _I32, _F32, _VP, _VP]),
     "kvs_decode_step": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I32,
                                _VP, _I32, _VP, _VP, _I32, _I32, _I32, _I32, _F32, _VP, _VP, _SZ,
                                _VP, _VP, _VP, _VP]),
@@ -285,6 +289,27 @@ def kvs_decode_step(alloc, tables_h, lens_h, patch_h, cow_h, patch_d, cow_d, q, 
         workspace_bytes, None if status is None else _dev(status, "i32", "status"),
         ctypes.byref(n_cow), ctypes.byref(n_patch), _stream(stream)))
     return n_cow.value, n_patch.value
+
+
+def kvs_evict_place(k_new, v_new, k_pool, v_pool, num_blocks, block_tables, max_blocks, lens,
+                    new_pos, score, pos, max_slots, n_items, h_kv, d, recent, status=None,
+                    stream=None):
+    _check(library().kvs_evict_place(
+        _dev(k_new, "bf16", "k_new"), _dev(v_new, "bf16", "v_new"), _dev(k_pool, "bf16", "k_pool"),
+        _dev(v_pool, "bf16", "v_pool"), num_blocks, _dev(block_tables, "i32", "block_tables"),
+        max_blocks, _dev(lens, "i32", "lens"), _dev(new_pos, "i32", "new_pos"),
+        _dev(score, "f32", "score"), _dev(pos, "i32", "pos"), max_slots, n_items, h_kv, d, recent,
+        None if status is None else _dev(status, "i32", "status"), _stream(stream)))
+
+
+def kvs_decode_scores(q, k_pool, num_blocks, block_tables, max_blocks, lens, score, new_pos,
+                      max_slots, n_items, h_q, h_kv, d, scale, status=None, stream=None):
+    _check(library().kvs_decode_scores(
+        _dev(q, "bf16", "q"), _dev(k_pool, "bf16", "k_pool"), num_blocks,
+        _dev(block_tables, "i32", "block_tables"), max_blocks, _dev(lens, "i32", "lens"),
+        _dev(score, "f32", "score"), _dev(new_pos, "i32", "new_pos"), max_slots, n_items, h_q,
+        h_kv, d, float(scale), None if status is None else _dev(status, "i32", "status"),
+        _stream(stream)))
 
 
 class BlockAllocator:

@@ -624,3 +624,74 @@ class DecodeBatch:
         self.cur = nxt
         self.lens_h += 1
         return self.out
+
+
+class EvictingDecode:
+    """Decode of budgeted (stream, layer) items with a fixed budget: the cache
+    of each keeps exactly its k_l slots per KV head; each step's new token
+    takes the slot of the lowest-scoring token outside the recent window, the
+    step attends over the k_l slots, and its attention probabilities are added
+    to the scores (kvs_evict_place, kvs_paged_decode, kvs_decode_scores).
+
+    Sources: Novita AI, "How KV Sparsity achieves 1.5x acceleration for vLLM",
+    section "Key techniques 1" (later layers replace their lowest-scoring KVs
+    with a sliding-window strategy) and section "Key techniques 2" (the
+    decode-side PagedAttention works toward the same score).  The score of a
+    prompt token starts at its prefill window score; a decode token's at 0.
+    Layers without a budget keep growing through DecodeBatch."""
+
+    def __init__(self, eng: Engine, res: PrefillResult, seq: int, seq_start: int, prompt_len: int,
+                 layers: Sequence[int]):
+        s = eng.shape
+        dev = eng.device
+        self.eng, self.layers = eng, list(layers)
+        n = len(self.layers)
+        self.n_items = n
+        keff = [int(res.k_eff[seq][l]) for l in self.layers]
+        if any(k >= prompt_len for k in keff):
+            raise ValueError("every layer of an EvictingDecode needs a budget below the prompt")
+        if any(k < s.recent for k in keff):
+            raise ValueError("a budget below the recent window leaves nothing to replace")
+        self.max_slots = max(keff)
+        self.max_blocks = blocks_for(self.max_slots)
+        tables = np.full((n, self.max_blocks), -1, dtype=np.int32)
+        for i, l in enumerate(self.layers):
+            t = res.tables[seq][l]
+            tables[i, :len(t)] = t
+        self.tables_h = tables
+        self.tables_d = torch.from_numpy(tables).to(dev)
+        self.lens_d = torch.tensor(keff, dtype=torch.int32, device=dev)
+        self.new_pos = torch.full((n,), prompt_len, dtype=torch.int32, device=dev)
+        self.score = torch.zeros((n, s.h_kv, self.max_slots), dtype=torch.float32, device=dev)
+        self.pos = torch.full((n, s.h_kv, self.max_slots), -1, dtype=torch.int32, device=dev)
+        for i, l in enumerate(self.layers):
+            off, ke = int(res.idx_off[seq, l]), keff[i]
+            idx = res.kept_idx[off:off + s.h_kv * ke].view(s.h_kv, ke).long()
+            self.pos[i, :, :ke] = idx.int()
+            self.score[i, :, :ke] = res.scores[l].gather(1, seq_start + idx)
+        self.out = torch.empty((n, s.h_q, s.d), dtype=torch.bfloat16, device=dev)
+        self.ws_bytes = kvs.kvs_paged_decode_workspace_size(n, s.h_q, s.h_kv, s.d)
+        self.ws = torch.zeros(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
+
+    def step(self, q, k_new, v_new, stream=None):
+        """q [n_items][h_q][d], k_new / v_new [n_items][h_kv][d] bf16 (items in
+        the order of `layers`).  Returns the attention output."""
+        eng, s = self.eng, self.eng.shape
+        n = self.n_items
+        kvs.kvs_evict_place(k_new, v_new, eng.k_pool, eng.v_pool, eng.num_blocks, self.tables_d,
+                            self.max_blocks, self.lens_d, self.new_pos, self.score, self.pos,
+                            self.max_slots, n, s.h_kv, s.d, s.recent, eng.status, stream)
+        kvs.kvs_paged_decode(q, None, None, eng.k_pool, eng.v_pool, eng.num_blocks, self.tables_d,
+                             self.max_blocks, None, self.lens_d, None, n, s.h_q, s.h_kv, s.d,
+                             s.scale, self.out, self.ws, self.ws_bytes, eng.status, stream)
+        kvs.kvs_decode_scores(q, eng.k_pool, eng.num_blocks, self.tables_d, self.max_blocks,
+                              self.lens_d, self.score, self.new_pos, self.max_slots, n, s.h_q,
+                              s.h_kv, s.d, s.scale, eng.status, stream)
+        return self.out
+
+    def release(self):
+        """Give the items' blocks back to the allocator."""
+        for i in range(self.n_items):
+            for b in self.tables_h[i]:
+                if b >= 0:
+                    self.eng.alloc.decref(int(b))

@@ -80,6 +80,20 @@ def test_invalid_arguments_rejected_before_launch(kvs):
                                         0.1, -2, None, None) == kvs.KVS_ERR_INVALID
     assert lib.kvs_window_scores_layers(256, 256, 256, 256, 256, 256, 1, 16, 16, 8, 2, 128, 16,
                                         0.1, 70000, None, None) == kvs.KVS_ERR_UNSUPPORTED
+    # decode-time replacement: zero items are a no-op; bad arguments fail before
+    # any launch
+    assert lib.kvs_evict_place(256, 256, 256, 256, 4, 256, 1, 256, 256, 256, 256, 16, 0, 8, 128,
+                               32, None, None) == kvs.KVS_OK
+    assert lib.kvs_evict_place(256, 256, 256, 256, 4, 256, 1, 256, 256, 256, 256, 16, 2, 8, 96,
+                               32, None, None) == kvs.KVS_ERR_UNSUPPORTED
+    assert lib.kvs_evict_place(None, 256, 256, 256, 4, 256, 1, 256, 256, 256, 256, 16, 2, 8, 128,
+                               32, None, None) == kvs.KVS_ERR_INVALID
+    assert lib.kvs_decode_scores(256, 256, 4, 256, 1, 256, 256, 256, 16, 0, 32, 8, 128, 0.1,
+                                 None, None) == kvs.KVS_OK
+    assert lib.kvs_decode_scores(256, 256, 4, 256, 1, 256, 256, 256, 100000, 2, 32, 8, 128, 0.1,
+                                 None, None) == kvs.KVS_ERR_UNSUPPORTED   # logits exceed smem
+    assert lib.kvs_decode_scores(256, 256, 4, 256, 1, 256, 256, 256, 16, 2, 32, 6, 128, 0.1,
+                                 None, None) == kvs.KVS_ERR_INVALID      # 32 % 6 != 0
     # the native decode step: nothing to do for zero items; NULL staging and a
     # step without an append are rejected before the allocator is touched
     args = [None] * 29

@@ -417,3 +417,109 @@ def test_decode_graphs_match_eager():
     assert [ea.alloc.refcount(b) for b in range(N)] == [eb.alloc.refcount(b) for b in range(N)]
     np.testing.assert_array_equal(host_bits(ea.k_pool), host_bits(eb.k_pool))
     np.testing.assert_array_equal(host_bits(ea.v_pool), host_bits(eb.v_pool))
+
+
+def test_evicting_decode_vs_oracle():
+    """Decode-time replacement in the tiny workload's budgeted layer (k = 64,
+    recent window 16): every step, each KV head's replaced slot must be a
+    valid choice for the oracle's fp64 scores (the lowest outside the recent
+    window, up to fp32 rounding; the oracle then follows it), the attention
+    output must match the oracle's, and the accumulated scores and positions
+    must track the oracle's through 48 steps -- long enough for decode tokens
+    to age out of the window and be replaced in turn."""
+    kvs_lib()
+    from oracle import eviction
+    from layer_wise_kv_gb300.pipeline import EvictingDecode, Engine
+    w = tiny()
+    n, L, layer, steps = w.prompt_lens[0], w.n_layers, 1, 48
+    eng = Engine(_shape(w), 64, poison=True)
+    ql, kl, vl, host = _layers_to_device(w, [0], [n])
+    res = eng.prefill_sparsify(ql, kl, vl, [n], [[w.budget(l, n) for l in range(L)]])
+    torch.cuda.synchronize()
+    qb, kb, vb = host[(0, layer)]
+    rec = flow.sparsify_layer(w, layer, qb, kb, vb)
+    ke = rec.k_eff
+    gidx = _gpu_idx(res, 0, layer, w.h_kv, ke)
+    heads = [eviction.HeadCache(bf16_to_f64(kb[gidx[h], h]), bf16_to_f64(vb[gidx[h], h]),
+                                rec.scores[h][gidx[h]].astype(np.float64),
+                                gidx[h].astype(np.int64)) for h in range(w.h_kv)]
+    ev = EvictingDecode(eng, res, 0, 0, n, [layer])
+    dq, dk, dv = decode_qkv(w, 0, layer, steps)
+    scale = 1 / np.sqrt(w.d)
+    replaced_decode_token = False
+    for t in range(steps):
+        new_pos = n + t
+        out = ev.step(dev_bf16(dq[t][None]), dev_bf16(dk[t][None]), dev_bf16(dv[t][None]))
+        torch.cuda.synchronize()
+        pos_g = ev.pos[0, :, :ke].cpu().numpy()
+        slots = []
+        for h, hc in enumerate(heads):
+            where = np.nonzero(pos_g[h] == new_pos)[0]
+            assert where.size == 1, (t, h)
+            s = int(where[0])
+            assert eviction.is_valid_choice(hc.score, hc.pos, new_pos, w.recent, s, 1e-3, 1e-6), \
+                (t, h, s, hc.score[s], hc.score.min())
+            replaced_decode_token |= hc.pos[s] >= n
+            slots.append(s)
+        ref, _, _ = eviction.step(heads, bf16_to_f64(dq[t]), bf16_to_f64(dk[t]), bf16_to_f64(dv[t]),
+                                  new_pos, w.recent, scale, slots=slots)
+        assert np.abs(bf16_f64(out)[0] - ref).max() <= ABS_O, t
+        sc_g = ev.score[0, :, :ke].cpu().numpy().astype(np.float64)
+        for h, hc in enumerate(heads):
+            np.testing.assert_array_equal(pos_g[h], hc.pos)
+            np.testing.assert_allclose(sc_g[h], hc.score, rtol=1e-3, atol=1e-5)
+    eng.check_status()
+    assert replaced_decode_token            # the window moved past some decode tokens
+    assert int(ev.new_pos[0]) == n + steps
+
+
+def test_evicting_decode_llama_shapes():
+    """The same at Llama-3-8B shapes (32/8 heads, d = 128, recent window 32,
+    one 4000-token prompt) for layers 3 and 31 (budgets 2048 and 256), two
+    items in one launch each step."""
+    kvs_lib()
+    from oracle import eviction
+    from layer_wise_kv_gb300.pipeline import EvictingDecode, Engine, Shape
+    w = llama3_8b()
+    n, steps, real = w.prompt_lens[0], 12, [3, 31]
+    shape = Shape(len(real), w.h_q, w.h_kv, w.d, w.alpha, w.recent)
+    eng = Engine(shape, 512, poison=True)
+    ql, kl, vl, host = _layers_to_device(w, [0], [n], layers=real)
+    res = eng.prefill_sparsify(ql, kl, vl, [n], [[w.budget(l, n) for l in real]])
+    torch.cuda.synchronize()
+    heads, kes = [], []
+    for li, l in enumerate(real):
+        qb, kb, vb = host[(0, l)]
+        rec = flow.sparsify_layer(w, l, qb, kb, vb)
+        gidx = _gpu_idx(res, 0, li, w.h_kv, rec.k_eff)
+        kes.append(rec.k_eff)
+        heads.append([eviction.HeadCache(bf16_to_f64(kb[gidx[h], h]), bf16_to_f64(vb[gidx[h], h]),
+                                         rec.scores[h][gidx[h]].astype(np.float64),
+                                         gidx[h].astype(np.int64)) for h in range(w.h_kv)])
+    ev = EvictingDecode(eng, res, 0, 0, n, [0, 1])
+    dqkv = [decode_qkv(w, 0, l, steps) for l in real]
+    scale = 1 / np.sqrt(w.d)
+    for t in range(steps):
+        new_pos = n + t
+        q = dev_bf16(np.stack([dqkv[i][0][t] for i in range(2)]))
+        k = dev_bf16(np.stack([dqkv[i][1][t] for i in range(2)]))
+        v = dev_bf16(np.stack([dqkv[i][2][t] for i in range(2)]))
+        out = bf16_f64(ev.step(q, k, v))
+        torch.cuda.synchronize()
+        for i in range(2):
+            pos_g = ev.pos[i, :, :kes[i]].cpu().numpy()
+            slots = []
+            for h, hc in enumerate(heads[i]):
+                s = int(np.nonzero(pos_g[h] == new_pos)[0][0])
+                assert eviction.is_valid_choice(hc.score, hc.pos, new_pos, w.recent, s, 1e-3,
+                                                1e-6), (t, i, h)
+                slots.append(s)
+            ref, _, _ = eviction.step(heads[i], bf16_to_f64(dqkv[i][0][t]),
+                                      bf16_to_f64(dqkv[i][1][t]), bf16_to_f64(dqkv[i][2][t]),
+                                      new_pos, w.recent, scale, slots=slots)
+            assert np.abs(out[i] - ref).max() <= ABS_O, (t, i)
+            sc_g = ev.score[i, :, :kes[i]].cpu().numpy().astype(np.float64)
+            for h, hc in enumerate(heads[i]):
+                np.testing.assert_array_equal(pos_g[h], hc.pos)
+                np.testing.assert_allclose(sc_g[h], hc.score, rtol=1e-3, atol=1e-5)
+    eng.check_status()
