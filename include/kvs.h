@@ -409,7 +409,7 @@ kvs_status kvs_evict_place(const kvs_bf16* k_new, const kvs_bf16* v_new, kvs_bf1
  * head), softmax over the lens[i] slots of scale * q_g . k_j for each query
  * head g of the group (q [n_items][h_q][d] bf16, K read from the pool), summed
  * over the group.  Then new_pos[i] += 1.  fp32 arithmetic; G <= 16 and
- * G * max_slots * 4 bytes <= 200 KB. */
+ * (G * max_slots + G * d) * 4 bytes <= 200 KB. */
 kvs_status kvs_decode_scores(const kvs_bf16* q, const kvs_bf16* k_pool, int32_t num_blocks,
                              const int32_t* block_tables, int32_t max_blocks, const int32_t* lens,
                              float* score, int32_t* new_pos, int32_t max_slots, int32_t n_items,

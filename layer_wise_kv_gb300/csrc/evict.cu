@@ -30,7 +30,6 @@ namespace kvs {
 namespace {
 
 constexpr int kEvictThreads = 256;
-constexpr int kScoreWarps = 8;
 constexpr float kLog2eE = 1.4426950408889634f;
 
 // row of slot j (block table[j / 16], row j % 16) of KV head h, or -1 when the
@@ -136,70 +135,103 @@ evict_place_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_
 
 // One CTA per (item, KV head): logits of the G query heads against every
 // slot, then per head the maximum and the sum of exponentials, then each
-// slot's probability summed over the group, added to its score.  The CTA of
+// slot's probability summed over the group, added to its score.  A thread
+// owns whole slots: it issues every 16-byte load of a K row before it needs
+// the first, and reads the group's query rows (fp32, shared memory) as
+// broadcasts.  The item's block table is staged in shared memory.  The CTA of
 // KV head 0 advances the item's next position once it is done.
+constexpr int kScoreThreads = 256;
+constexpr int kMaxTableSmem = 2048;  // table entries staged in shared memory
+
 template <int D>
-__global__ void __launch_bounds__(kScoreWarps * 32)
-decode_scores_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k_pool,
+__global__ void __launch_bounds__(kScoreThreads, 2)
+decode_scores_kernel(const uint16_t* __restrict__ q, const uint4* __restrict__ k_pool,
                      int num_blocks, const int32_t* __restrict__ tables, int max_blocks,
                      const int32_t* __restrict__ lens, float* __restrict__ score,
                      int32_t* __restrict__ new_pos, int max_slots, int h_q, int h_kv, int G,
                      float scale_log2, int32_t* status) {
-  extern __shared__ float s_logit[];  // [G][max_slots]
-  __shared__ float s_red[kScoreWarps][16];
+  extern __shared__ __align__(16) float s_dyn[];  // logits [G][max_slots], then q [G][D]
+  __shared__ int s_table[kMaxTableSmem];
+  __shared__ float s_red[kScoreThreads / 32][16];
   __shared__ float s_m[16], s_il[16];
+  constexpr int C = D / 8;  // 16-byte chunks per row
+  float* s_logit = s_dyn;
+  // q after the logits, padded to a multiple of four floats (16-byte reads)
+  float* s_q = s_dyn + ((static_cast<size_t>(G) * max_slots + 3) & ~static_cast<size_t>(3));
   const int item = blockIdx.x, h = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n = lens[item];
   if (n > 0 && n <= max_slots) {
-    // this lane's D/32 elements of each query row of the group, as floats
-    constexpr int E = D / 32;
-    float qf[16][E];
-#pragma unroll
-    for (int g = 0; g < 16; ++g)
-#pragma unroll
-      for (int e = 0; e < E; ++e) {
-        qf[g][e] = 0.f;
-        if (g < G)
-          qf[g][e] = bf16_lo(static_cast<uint32_t>(
-              q[(static_cast<int64_t>(item) * h_q + h * G + g) * D + lane * E + e]));
-      }
     const int32_t* table = tables + static_cast<int64_t>(item) * max_blocks;
+    const int nb = (n + KVS_BLOCK_TOKENS - 1) / KVS_BLOCK_TOKENS;
+    const bool staged = nb <= kMaxTableSmem && nb <= max_blocks;
+    if (staged)
+      for (int b = threadIdx.x; b < nb; b += kScoreThreads) s_table[b] = table[b];
+    for (int i = threadIdx.x; i < G * D; i += kScoreThreads)
+      s_q[i] = bf16_lo(static_cast<uint32_t>(
+          q[(static_cast<int64_t>(item) * h_q + h * G) * D + i]));
+    __syncthreads();
     float mx[16];
 #pragma unroll
     for (int g = 0; g < 16; ++g) mx[g] = -INFINITY;
-    for (int j = warp; j < n; j += kScoreWarps) {
-      const int64_t row = slot_row(table, max_blocks, num_blocks, h_kv, h, j);
-      float kf[E];
-      if (row < 0) {
-        if (lane == 0) flag_status(status, KVS_ERR_INVALID);
+    for (int j = threadIdx.x; j < n; j += kScoreThreads) {
+      const int lb = j / KVS_BLOCK_TOKENS;
+      const int pb = staged ? s_table[lb] : (lb < max_blocks ? table[lb] : -1);
+      const bool ok = pb >= 0 && pb < num_blocks;
+      if (!ok) flag_status(status, KVS_ERR_INVALID);
+      const uint4* src = k_pool + ((static_cast<int64_t>(ok ? pb : 0) * h_kv + h) * KVS_BLOCK_TOKENS +
+                                   (j % KVS_BLOCK_TOKENS)) * C;
+      // the row in halves of H chunks: every load of a half in flight at once
+      constexpr int H = C < 8 ? C : 8;
+      float acc[16][2];
 #pragma unroll
-        for (int e = 0; e < E; ++e) kf[e] = 0.f;
-      } else {
+      for (int g = 0; g < 16; ++g) acc[g][0] = acc[g][1] = 0.f;
 #pragma unroll
-        for (int e = 0; e < E; ++e) kf[e] = bf16_lo(static_cast<uint32_t>(k_pool[row * D + lane * E + e]));
+      for (int c0 = 0; c0 < C; c0 += H) {
+        uint4 kr[H];
+#pragma unroll
+        for (int c = 0; c < H; ++c) kr[c] = ok ? __ldg(src + c0 + c) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int g = 0; g < 16; ++g) {
+          if (g >= G) break;
+          // the query elements of a chunk as two 16-byte shared-memory reads
+          const float4* qg = reinterpret_cast<const float4*>(s_q + g * D + c0 * 8);
+#pragma unroll
+          for (int c = 0; c < H; ++c) {
+            const float4 qa = qg[2 * c], qb = qg[2 * c + 1];
+            acc[g][0] = fmaf(qa.x, bf16_lo(kr[c].x), acc[g][0]);
+            acc[g][1] = fmaf(qa.y, bf16_hi(kr[c].x), acc[g][1]);
+            acc[g][0] = fmaf(qa.z, bf16_lo(kr[c].y), acc[g][0]);
+            acc[g][1] = fmaf(qa.w, bf16_hi(kr[c].y), acc[g][1]);
+            acc[g][0] = fmaf(qb.x, bf16_lo(kr[c].z), acc[g][0]);
+            acc[g][1] = fmaf(qb.y, bf16_hi(kr[c].z), acc[g][1]);
+            acc[g][0] = fmaf(qb.z, bf16_lo(kr[c].w), acc[g][0]);
+            acc[g][1] = fmaf(qb.w, bf16_hi(kr[c].w), acc[g][1]);
+          }
+        }
       }
 #pragma unroll
       for (int g = 0; g < 16; ++g) {
         if (g >= G) break;
-        float acc = 0.f;
-#pragma unroll
-        for (int e = 0; e < E; ++e) acc = fmaf(qf[g][e], kf[e], acc);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        const float lg = acc * scale_log2;
-        if (lane == 0) s_logit[g * max_slots + j] = lg;
+        const float a0 = acc[g][0], a1 = acc[g][1];
+        const float lg = (a0 + a1) * scale_log2;
+        s_logit[g * max_slots + j] = lg;
         mx[g] = fmaxf(mx[g], lg);
       }
     }
     // per head: maximum over the slots
 #pragma unroll
-    for (int g = 0; g < 16; ++g)
-      if (g < G && lane == 0) s_red[warp][g] = mx[g];
+    for (int g = 0; g < 16; ++g) {
+      if (g >= G) break;
+      float v = mx[g];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+      if (lane == 0) s_red[warp][g] = v;
+    }
     __syncthreads();
     if (threadIdx.x < G) {
       float m = -INFINITY;
-      for (int w = 0; w < kScoreWarps; ++w) m = fmaxf(m, s_red[w][threadIdx.x]);
+      for (int w = 0; w < kScoreThreads / 32; ++w) m = fmaxf(m, s_red[w][threadIdx.x]);
       s_m[threadIdx.x] = m;
     }
     __syncthreads();
@@ -207,7 +239,7 @@ decode_scores_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict_
     float sm[16];
 #pragma unroll
     for (int g = 0; g < 16; ++g) sm[g] = 0.f;
-    for (int j = threadIdx.x; j < n; j += kScoreWarps * 32)
+    for (int j = threadIdx.x; j < n; j += kScoreThreads)
 #pragma unroll
       for (int g = 0; g < 16; ++g)
         if (g < G) sm[g] += ex2(s_logit[g * max_slots + j] - s_m[g]);
@@ -222,13 +254,13 @@ decode_scores_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict_
     __syncthreads();
     if (threadIdx.x < G) {
       float l = 0.f;
-      for (int w = 0; w < kScoreWarps; ++w) l += s_red[w][threadIdx.x];
+      for (int w = 0; w < kScoreThreads / 32; ++w) l += s_red[w][threadIdx.x];
       s_il[threadIdx.x] = 1.0f / l;
     }
     __syncthreads();
     // each slot's probability, summed over the group, added to its score
     float* sc = score + (static_cast<int64_t>(item) * h_kv + h) * max_slots;
-    for (int j = threadIdx.x; j < n; j += kScoreWarps * 32) {
+    for (int j = threadIdx.x; j < n; j += kScoreThreads) {
       float p = 0.f;
 #pragma unroll
       for (int g = 0; g < 16; ++g)
@@ -288,25 +320,31 @@ extern "C" kvs_status kvs_decode_scores(const kvs_bf16* q, const kvs_bf16* k_poo
               "kvs_decode_scores: bad sizes");
   const int G = h_q / h_kv;
   KVS_SUPPORTED(G <= 16, "kvs_decode_scores: group size %d > 16", G);
-  const size_t smem = static_cast<size_t>(G) * max_slots * sizeof(float);
+  const size_t smem =
+      (((static_cast<size_t>(G) * max_slots + 3) & ~static_cast<size_t>(3)) +
+       static_cast<size_t>(G) * d) * sizeof(float);
   KVS_SUPPORTED(smem <= 200 * 1024, "kvs_decode_scores: %d slots x %d heads exceed shared memory",
                 max_slots, G);
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   const float sl2 = scale * kvs::kLog2eE;
   const dim3 grid(n_items, h_kv);
-  if (d == 128) {
+  static bool configured = false;  // the shared-memory limit, once per process
+  if (!configured) {
     KVS_CUDA(cudaFuncSetAttribute(kvs::decode_scores_kernel<128>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024),
              "kvs_decode_scores: shared-memory limit");
-    kvs::decode_scores_kernel<128><<<grid, kvs::kScoreWarps * 32, smem, st>>>(
-        reinterpret_cast<const uint16_t*>(q), reinterpret_cast<const uint16_t*>(k_pool), num_blocks,
-        block_tables, max_blocks, lens, score, new_pos, max_slots, h_q, h_kv, G, sl2, status);
-  } else {
     KVS_CUDA(cudaFuncSetAttribute(kvs::decode_scores_kernel<64>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024),
              "kvs_decode_scores: shared-memory limit");
-    kvs::decode_scores_kernel<64><<<grid, kvs::kScoreWarps * 32, smem, st>>>(
-        reinterpret_cast<const uint16_t*>(q), reinterpret_cast<const uint16_t*>(k_pool), num_blocks,
+    configured = true;
+  }
+  if (d == 128) {
+    kvs::decode_scores_kernel<128><<<grid, kvs::kScoreThreads, smem, st>>>(
+        reinterpret_cast<const uint16_t*>(q), reinterpret_cast<const uint4*>(k_pool), num_blocks,
+        block_tables, max_blocks, lens, score, new_pos, max_slots, h_q, h_kv, G, sl2, status);
+  } else {
+    kvs::decode_scores_kernel<64><<<grid, kvs::kScoreThreads, smem, st>>>(
+        reinterpret_cast<const uint16_t*>(q), reinterpret_cast<const uint4*>(k_pool), num_blocks,
         block_tables, max_blocks, lens, score, new_pos, max_slots, h_q, h_kv, G, sl2, status);
   }
   KVS_CHECK_LAUNCH("kvs_decode_scores");
