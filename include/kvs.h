@@ -408,13 +408,19 @@ kvs_status kvs_evict_place(const kvs_bf16* k_new, const kvs_bf16* v_new, kvs_bf1
 /* Add the step's attention probabilities to the scores: for each (item, KV
  * head), softmax over the lens[i] slots of scale * q_g . k_j for each query
  * head g of the group (q [n_items][h_q][d] bf16, K read from the pool), summed
- * over the group.  Then new_pos[i] += 1.  fp32 arithmetic; G <= 16 and
- * (G * max_slots + G * d) * 4 bytes <= 200 KB. */
+ * over the group.  Then new_pos[i] += 1.  fp32 arithmetic; G <= 16.  Two
+ * launches: the logits of every slot (a thread per slot, 256-slot chunks),
+ * then per (item, KV head) the softmax and the score update.  workspace:
+ * device scratch of kvs_decode_scores_workspace_size bytes (the logits and
+ * each chunk's maxima; needs no initialisation). */
+size_t kvs_decode_scores_workspace_size(int32_t n_items, int32_t h_q, int32_t h_kv,
+                                        int32_t max_slots);
+
 kvs_status kvs_decode_scores(const kvs_bf16* q, const kvs_bf16* k_pool, int32_t num_blocks,
                              const int32_t* block_tables, int32_t max_blocks, const int32_t* lens,
                              float* score, int32_t* new_pos, int32_t max_slots, int32_t n_items,
-                             int32_t h_q, int32_t h_kv, int32_t d, float scale, int32_t* status,
-                             kvs_stream stream);
+                             int32_t h_q, int32_t h_kv, int32_t d, float scale, void* workspace,
+                             size_t workspace_bytes, int32_t* status, kvs_stream stream);
 
 #ifdef __cplusplus
 }

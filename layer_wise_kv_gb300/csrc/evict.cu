@@ -133,116 +133,135 @@ evict_place_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_
   }
 }
 
-// One CTA per (item, KV head): logits of the G query heads against every
-// slot, then per head the maximum and the sum of exponentials, then each
-// slot's probability summed over the group, added to its score.  A thread
-// owns whole slots: it issues every 16-byte load of a K row before it needs
-// the first, and reads the group's query rows (fp32, shared memory) as
-// broadcasts.  The item's block table is staged in shared memory.  The CTA of
-// KV head 0 advances the item's next position once it is done.
-constexpr int kScoreThreads = 256;
-constexpr int kMaxTableSmem = 2048;  // table entries staged in shared memory
+// The scores in two launches.  decode_logits_kernel: one CTA per (256-slot
+// chunk, item, KV head), a thread per slot; the thread issues every 16-byte
+// load of its K row (in halves) before it needs one, takes the group's query
+// rows (fp32, shared memory) as 16-byte broadcasts, and writes the G logits
+// (log2 units) of its slot; the CTA writes each head's maximum over its
+// chunk.  decode_scores_update_kernel: one CTA per (item, KV head): each
+// head's maximum over the chunks, its sum of exponentials, then every slot's
+// probability summed over the group, added to the slot's score; the CTA of KV
+// head 0 advances the item's next position.
+constexpr int kScoreThreads = 256;  // also the slots of one chunk
+
+// workspace: logits [n_items][h_kv][G][ld], then chunk maxima
+// [n_items][h_kv][n_chunks][G]; ld = max_slots rounded up to four floats
+__host__ __device__ inline int64_t logit_ld(int max_slots) { return (max_slots + 3) & ~3; }
 
 template <int D>
 __global__ void __launch_bounds__(kScoreThreads, 2)
-decode_scores_kernel(const uint16_t* __restrict__ q, const uint4* __restrict__ k_pool,
+decode_logits_kernel(const uint16_t* __restrict__ q, const uint4* __restrict__ k_pool,
                      int num_blocks, const int32_t* __restrict__ tables, int max_blocks,
-                     const int32_t* __restrict__ lens, float* __restrict__ score,
-                     int32_t* __restrict__ new_pos, int max_slots, int h_q, int h_kv, int G,
-                     float scale_log2, int32_t* status) {
-  extern __shared__ __align__(16) float s_dyn[];  // logits [G][max_slots], then q [G][D]
-  __shared__ int s_table[kMaxTableSmem];
+                     const int32_t* __restrict__ lens, float* __restrict__ logits,
+                     float* __restrict__ chunk_max, int max_slots, int n_chunks, int h_q, int h_kv,
+                     int G, float scale_log2, int32_t* status) {
+  __shared__ __align__(16) float s_q[16 * D];
+  __shared__ float s_red[kScoreThreads / 32][16];
+  constexpr int C = D / 8;  // 16-byte chunks per row
+  const int chunk = blockIdx.x, item = blockIdx.y, h = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = lens[item];
+  const int j0 = chunk * kScoreThreads;
+  if (n <= 0 || n > max_slots) {
+    if (chunk == 0 && h == 0 && threadIdx.x == 0 && n > max_slots)
+      flag_status(status, KVS_ERR_INVALID);
+    return;
+  }
+  if (j0 >= n) return;
+  for (int i = threadIdx.x; i < G * D; i += kScoreThreads)
+    s_q[i] = bf16_lo(static_cast<uint32_t>(q[(static_cast<int64_t>(item) * h_q + h * G) * D + i]));
+  __syncthreads();
+  const int j = j0 + threadIdx.x;
+  float lg[16];
+#pragma unroll
+  for (int g = 0; g < 16; ++g) lg[g] = -INFINITY;
+  if (j < n) {
+    const int lb = j / KVS_BLOCK_TOKENS;
+    const int pb = lb < max_blocks ? tables[static_cast<int64_t>(item) * max_blocks + lb] : -1;
+    const bool ok = pb >= 0 && pb < num_blocks;
+    if (!ok) flag_status(status, KVS_ERR_INVALID);
+    const uint4* src = k_pool + ((static_cast<int64_t>(ok ? pb : 0) * h_kv + h) * KVS_BLOCK_TOKENS +
+                                 (j % KVS_BLOCK_TOKENS)) * C;
+    constexpr int H = C < 8 ? C : 8;
+    float acc[16][2];
+#pragma unroll
+    for (int g = 0; g < 16; ++g) acc[g][0] = acc[g][1] = 0.f;
+#pragma unroll
+    for (int c0 = 0; c0 < C; c0 += H) {
+      uint4 kr[H];
+#pragma unroll
+      for (int c = 0; c < H; ++c) kr[c] = ok ? __ldg(src + c0 + c) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int g = 0; g < 16; ++g) {
+        if (g >= G) break;
+        const float4* qg = reinterpret_cast<const float4*>(s_q + g * D + c0 * 8);
+#pragma unroll
+        for (int c = 0; c < H; ++c) {
+          const float4 qa = qg[2 * c], qb = qg[2 * c + 1];
+          acc[g][0] = fmaf(qa.x, bf16_lo(kr[c].x), acc[g][0]);
+          acc[g][1] = fmaf(qa.y, bf16_hi(kr[c].x), acc[g][1]);
+          acc[g][0] = fmaf(qa.z, bf16_lo(kr[c].y), acc[g][0]);
+          acc[g][1] = fmaf(qa.w, bf16_hi(kr[c].y), acc[g][1]);
+          acc[g][0] = fmaf(qb.x, bf16_lo(kr[c].z), acc[g][0]);
+          acc[g][1] = fmaf(qb.y, bf16_hi(kr[c].z), acc[g][1]);
+          acc[g][0] = fmaf(qb.z, bf16_lo(kr[c].w), acc[g][0]);
+          acc[g][1] = fmaf(qb.w, bf16_hi(kr[c].w), acc[g][1]);
+        }
+      }
+    }
+    float* out = logits + (static_cast<int64_t>(item) * h_kv + h) * G * logit_ld(max_slots);
+#pragma unroll
+    for (int g = 0; g < 16; ++g) {
+      if (g >= G) break;
+      lg[g] = (acc[g][0] + acc[g][1]) * scale_log2;
+      out[g * logit_ld(max_slots) + j] = lg[g];
+    }
+  }
+#pragma unroll
+  for (int g = 0; g < 16; ++g) {
+    if (g >= G) break;
+    float v = lg[g];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (lane == 0) s_red[warp][g] = v;
+  }
+  __syncthreads();
+  if (threadIdx.x < G) {
+    float m = -INFINITY;
+    for (int w = 0; w < kScoreThreads / 32; ++w) m = fmaxf(m, s_red[w][threadIdx.x]);
+    chunk_max[((static_cast<int64_t>(item) * h_kv + h) * n_chunks + chunk) * G + threadIdx.x] = m;
+  }
+}
+
+__global__ void __launch_bounds__(kScoreThreads)
+decode_scores_update_kernel(const float* __restrict__ logits, const float* __restrict__ chunk_max,
+                            const int32_t* __restrict__ lens, float* __restrict__ score,
+                            int32_t* __restrict__ new_pos, int max_slots, int n_chunks, int h_kv,
+                            int G) {
   __shared__ float s_red[kScoreThreads / 32][16];
   __shared__ float s_m[16], s_il[16];
-  constexpr int C = D / 8;  // 16-byte chunks per row
-  float* s_logit = s_dyn;
-  // q after the logits, padded to a multiple of four floats (16-byte reads)
-  float* s_q = s_dyn + ((static_cast<size_t>(G) * max_slots + 3) & ~static_cast<size_t>(3));
   const int item = blockIdx.x, h = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n = lens[item];
   if (n > 0 && n <= max_slots) {
-    const int32_t* table = tables + static_cast<int64_t>(item) * max_blocks;
-    const int nb = (n + KVS_BLOCK_TOKENS - 1) / KVS_BLOCK_TOKENS;
-    const bool staged = nb <= kMaxTableSmem && nb <= max_blocks;
-    if (staged)
-      for (int b = threadIdx.x; b < nb; b += kScoreThreads) s_table[b] = table[b];
-    for (int i = threadIdx.x; i < G * D; i += kScoreThreads)
-      s_q[i] = bf16_lo(static_cast<uint32_t>(
-          q[(static_cast<int64_t>(item) * h_q + h * G) * D + i]));
-    __syncthreads();
-    float mx[16];
-#pragma unroll
-    for (int g = 0; g < 16; ++g) mx[g] = -INFINITY;
-    for (int j = threadIdx.x; j < n; j += kScoreThreads) {
-      const int lb = j / KVS_BLOCK_TOKENS;
-      const int pb = staged ? s_table[lb] : (lb < max_blocks ? table[lb] : -1);
-      const bool ok = pb >= 0 && pb < num_blocks;
-      if (!ok) flag_status(status, KVS_ERR_INVALID);
-      const uint4* src = k_pool + ((static_cast<int64_t>(ok ? pb : 0) * h_kv + h) * KVS_BLOCK_TOKENS +
-                                   (j % KVS_BLOCK_TOKENS)) * C;
-      // the row in halves of H chunks: every load of a half in flight at once
-      constexpr int H = C < 8 ? C : 8;
-      float acc[16][2];
-#pragma unroll
-      for (int g = 0; g < 16; ++g) acc[g][0] = acc[g][1] = 0.f;
-#pragma unroll
-      for (int c0 = 0; c0 < C; c0 += H) {
-        uint4 kr[H];
-#pragma unroll
-        for (int c = 0; c < H; ++c) kr[c] = ok ? __ldg(src + c0 + c) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-        for (int g = 0; g < 16; ++g) {
-          if (g >= G) break;
-          // the query elements of a chunk as two 16-byte shared-memory reads
-          const float4* qg = reinterpret_cast<const float4*>(s_q + g * D + c0 * 8);
-#pragma unroll
-          for (int c = 0; c < H; ++c) {
-            const float4 qa = qg[2 * c], qb = qg[2 * c + 1];
-            acc[g][0] = fmaf(qa.x, bf16_lo(kr[c].x), acc[g][0]);
-            acc[g][1] = fmaf(qa.y, bf16_hi(kr[c].x), acc[g][1]);
-            acc[g][0] = fmaf(qa.z, bf16_lo(kr[c].y), acc[g][0]);
-            acc[g][1] = fmaf(qa.w, bf16_hi(kr[c].y), acc[g][1]);
-            acc[g][0] = fmaf(qb.x, bf16_lo(kr[c].z), acc[g][0]);
-            acc[g][1] = fmaf(qb.y, bf16_hi(kr[c].z), acc[g][1]);
-            acc[g][0] = fmaf(qb.z, bf16_lo(kr[c].w), acc[g][0]);
-            acc[g][1] = fmaf(qb.w, bf16_hi(kr[c].w), acc[g][1]);
-          }
-        }
-      }
-#pragma unroll
-      for (int g = 0; g < 16; ++g) {
-        if (g >= G) break;
-        const float a0 = acc[g][0], a1 = acc[g][1];
-        const float lg = (a0 + a1) * scale_log2;
-        s_logit[g * max_slots + j] = lg;
-        mx[g] = fmaxf(mx[g], lg);
-      }
-    }
-    // per head: maximum over the slots
-#pragma unroll
-    for (int g = 0; g < 16; ++g) {
-      if (g >= G) break;
-      float v = mx[g];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-      if (lane == 0) s_red[warp][g] = v;
-    }
-    __syncthreads();
+    const int64_t ld = logit_ld(max_slots);
+    const float* lgt = logits + (static_cast<int64_t>(item) * h_kv + h) * G * ld;
+    const int nc = (n + kScoreThreads - 1) / kScoreThreads;
     if (threadIdx.x < G) {
       float m = -INFINITY;
-      for (int w = 0; w < kScoreThreads / 32; ++w) m = fmaxf(m, s_red[w][threadIdx.x]);
+      for (int c = 0; c < nc; ++c)
+        m = fmaxf(m, chunk_max[((static_cast<int64_t>(item) * h_kv + h) * n_chunks + c) * G +
+                               threadIdx.x]);
       s_m[threadIdx.x] = m;
     }
     __syncthreads();
-    // per head: sum of exp2(logit - max)
     float sm[16];
 #pragma unroll
     for (int g = 0; g < 16; ++g) sm[g] = 0.f;
     for (int j = threadIdx.x; j < n; j += kScoreThreads)
 #pragma unroll
       for (int g = 0; g < 16; ++g)
-        if (g < G) sm[g] += ex2(s_logit[g * max_slots + j] - s_m[g]);
+        if (g < G) sm[g] += ex2(lgt[g * ld + j] - s_m[g]);
 #pragma unroll
     for (int g = 0; g < 16; ++g) {
       if (g >= G) break;
@@ -258,17 +277,14 @@ decode_scores_kernel(const uint16_t* __restrict__ q, const uint4* __restrict__ k
       s_il[threadIdx.x] = 1.0f / l;
     }
     __syncthreads();
-    // each slot's probability, summed over the group, added to its score
     float* sc = score + (static_cast<int64_t>(item) * h_kv + h) * max_slots;
     for (int j = threadIdx.x; j < n; j += kScoreThreads) {
       float p = 0.f;
 #pragma unroll
       for (int g = 0; g < 16; ++g)
-        if (g < G) p += ex2(s_logit[g * max_slots + j] - s_m[g]) * s_il[g];
+        if (g < G) p += ex2(lgt[g * ld + j] - s_m[g]) * s_il[g];
       sc[j] += p;
     }
-  } else if (n > max_slots && threadIdx.x == 0) {
-    flag_status(status, KVS_ERR_INVALID);
   }
   if (h == 0 && threadIdx.x == 0) new_pos[item] += 1;
 }
@@ -304,15 +320,25 @@ extern "C" kvs_status kvs_evict_place(const kvs_bf16* k_new, const kvs_bf16* v_n
   return KVS_OK;
 }
 
+extern "C" size_t kvs_decode_scores_workspace_size(int32_t n_items, int32_t h_q, int32_t h_kv,
+                                                   int32_t max_slots) {
+  if (n_items <= 0 || h_q <= 0 || h_kv <= 0 || max_slots <= 0 || h_q % h_kv != 0) return 0;
+  const int64_t G = h_q / h_kv;
+  const int64_t n_chunks = (max_slots + kvs::kScoreThreads - 1) / kvs::kScoreThreads;
+  return static_cast<size_t>(static_cast<int64_t>(n_items) * h_kv * G *
+                             (kvs::logit_ld(max_slots) + n_chunks) * sizeof(float));
+}
+
 extern "C" kvs_status kvs_decode_scores(const kvs_bf16* q, const kvs_bf16* k_pool,
                                         int32_t num_blocks, const int32_t* block_tables,
                                         int32_t max_blocks, const int32_t* lens, float* score,
                                         int32_t* new_pos, int32_t max_slots, int32_t n_items,
                                         int32_t h_q, int32_t h_kv, int32_t d, float scale,
-                                        int32_t* status, kvs_stream stream) {
+                                        void* workspace, size_t workspace_bytes, int32_t* status,
+                                        kvs_stream stream) {
   KVS_REQUIRE(n_items >= 0, "kvs_decode_scores: negative item count");
   if (n_items == 0) return KVS_OK;
-  KVS_REQUIRE(q && k_pool && block_tables && lens && score && new_pos,
+  KVS_REQUIRE(q && k_pool && block_tables && lens && score && new_pos && workspace,
               "kvs_decode_scores: NULL pointer");
   KVS_SUPPORTED(d == 64 || d == 128, "kvs_decode_scores: d = %d (supported: 64, 128)", d);
   KVS_REQUIRE(h_kv > 0 && h_q > 0 && h_q % h_kv == 0 && num_blocks > 0 && max_blocks > 0 &&
@@ -320,33 +346,31 @@ extern "C" kvs_status kvs_decode_scores(const kvs_bf16* q, const kvs_bf16* k_poo
               "kvs_decode_scores: bad sizes");
   const int G = h_q / h_kv;
   KVS_SUPPORTED(G <= 16, "kvs_decode_scores: group size %d > 16", G);
-  const size_t smem =
-      (((static_cast<size_t>(G) * max_slots + 3) & ~static_cast<size_t>(3)) +
-       static_cast<size_t>(G) * d) * sizeof(float);
-  KVS_SUPPORTED(smem <= 200 * 1024, "kvs_decode_scores: %d slots x %d heads exceed shared memory",
-                max_slots, G);
+  const size_t need = kvs_decode_scores_workspace_size(n_items, h_q, h_kv, max_slots);
+  KVS_REQUIRE(workspace_bytes >= need, "kvs_decode_scores: workspace %zu bytes < %zu needed",
+              workspace_bytes, need);
+  KVS_REQUIRE((reinterpret_cast<uintptr_t>(k_pool) & 15) == 0,
+              "kvs_decode_scores: the K pool must be 16-byte aligned");
+  const int n_chunks = (max_slots + kvs::kScoreThreads - 1) / kvs::kScoreThreads;
+  KVS_SUPPORTED(n_chunks <= 65535, "kvs_decode_scores: %d slots per item is too many", max_slots);
+  float* logits = static_cast<float*>(workspace);
+  float* chunk_max = logits + static_cast<int64_t>(n_items) * h_kv * G * kvs::logit_ld(max_slots);
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   const float sl2 = scale * kvs::kLog2eE;
-  const dim3 grid(n_items, h_kv);
-  static bool configured = false;  // the shared-memory limit, once per process
-  if (!configured) {
-    KVS_CUDA(cudaFuncSetAttribute(kvs::decode_scores_kernel<128>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024),
-             "kvs_decode_scores: shared-memory limit");
-    KVS_CUDA(cudaFuncSetAttribute(kvs::decode_scores_kernel<64>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024),
-             "kvs_decode_scores: shared-memory limit");
-    configured = true;
-  }
-  if (d == 128) {
-    kvs::decode_scores_kernel<128><<<grid, kvs::kScoreThreads, smem, st>>>(
+  const dim3 grid_l(n_chunks, n_items, h_kv);
+  if (d == 128)
+    kvs::decode_logits_kernel<128><<<grid_l, kvs::kScoreThreads, 0, st>>>(
         reinterpret_cast<const uint16_t*>(q), reinterpret_cast<const uint4*>(k_pool), num_blocks,
-        block_tables, max_blocks, lens, score, new_pos, max_slots, h_q, h_kv, G, sl2, status);
-  } else {
-    kvs::decode_scores_kernel<64><<<grid, kvs::kScoreThreads, smem, st>>>(
+        block_tables, max_blocks, lens, logits, chunk_max, max_slots, n_chunks, h_q, h_kv, G, sl2,
+        status);
+  else
+    kvs::decode_logits_kernel<64><<<grid_l, kvs::kScoreThreads, 0, st>>>(
         reinterpret_cast<const uint16_t*>(q), reinterpret_cast<const uint4*>(k_pool), num_blocks,
-        block_tables, max_blocks, lens, score, new_pos, max_slots, h_q, h_kv, G, sl2, status);
-  }
-  KVS_CHECK_LAUNCH("kvs_decode_scores");
+        block_tables, max_blocks, lens, logits, chunk_max, max_slots, n_chunks, h_q, h_kv, G, sl2,
+        status);
+  KVS_CHECK_LAUNCH("kvs_decode_scores (logits)");
+  kvs::decode_scores_update_kernel<<<dim3(n_items, h_kv), kvs::kScoreThreads, 0, st>>>(
+      logits, chunk_max, lens, score, new_pos, max_slots, n_chunks, h_kv, G);
+  KVS_CHECK_LAUNCH("kvs_decode_scores (update)");
   return KVS_OK;
 }

@@ -56,8 +56,9 @@ _SIGS = {
     "kvs_select_topk": (_I32, [_VP, _I64, _VP, _I32, _I32, _I32, _VP, _VP, _VP]),
     "kvs_evict_place": (_I32, [_VP, _VP, _VP, _VP, _I32, _VP, _I32, _VP, _VP, _VP, _VP, _I32,
                                _I32, _I32, _I32, _I32, _VP, _VP]),
+    "kvs_decode_scores_workspace_size": (_SZ, [_I32, _I32, _I32, _I32]),
     "kvs_decode_scores": (_I32, [_VP, _VP, _I32, _VP, _I32, _VP, _VP, _VP, _I32, _I32, _I32,
-                                 _I32, _I32, _F32, _VP, _VP]),
+                                 _I32, _I32, _F32, _VP, _SZ, _VP, _VP]),
     "kvs_decode_step": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I32,
                                _VP, _I32, _VP, _VP, _I32, _I32, _I32, _I32, _F32, _VP, _VP, _SZ,
                                _VP, _VP, _VP, _VP]),
@@ -302,14 +303,19 @@ def kvs_evict_place(k_new, v_new, k_pool, v_pool, num_blocks, block_tables, max_
         None if status is None else _dev(status, "i32", "status"), _stream(stream)))
 
 
+def kvs_decode_scores_workspace_size(n_items, h_q, h_kv, max_slots) -> int:
+    return int(library().kvs_decode_scores_workspace_size(n_items, h_q, h_kv, max_slots))
+
+
 def kvs_decode_scores(q, k_pool, num_blocks, block_tables, max_blocks, lens, score, new_pos,
-                      max_slots, n_items, h_q, h_kv, d, scale, status=None, stream=None):
+                      max_slots, n_items, h_q, h_kv, d, scale, workspace, workspace_bytes,
+                      status=None, stream=None):
     _check(library().kvs_decode_scores(
         _dev(q, "bf16", "q"), _dev(k_pool, "bf16", "k_pool"), num_blocks,
         _dev(block_tables, "i32", "block_tables"), max_blocks, _dev(lens, "i32", "lens"),
         _dev(score, "f32", "score"), _dev(new_pos, "i32", "new_pos"), max_slots, n_items, h_q,
-        h_kv, d, float(scale), None if status is None else _dev(status, "i32", "status"),
-        _stream(stream)))
+        h_kv, d, float(scale), _dev(workspace, "u8", "workspace"), workspace_bytes,
+        None if status is None else _dev(status, "i32", "status"), _stream(stream)))
 
 
 class BlockAllocator:

@@ -672,6 +672,8 @@ class EvictingDecode:
         self.out = torch.empty((n, s.h_q, s.d), dtype=torch.bfloat16, device=dev)
         self.ws_bytes = kvs.kvs_paged_decode_workspace_size(n, s.h_q, s.h_kv, s.d)
         self.ws = torch.zeros(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
+        self.sws_bytes = kvs.kvs_decode_scores_workspace_size(n, s.h_q, s.h_kv, self.max_slots)
+        self.sws = torch.empty(max(self.sws_bytes, 256), dtype=torch.uint8, device=dev)
 
     def step(self, q, k_new, v_new, stream=None):
         """q [n_items][h_q][d], k_new / v_new [n_items][h_kv][d] bf16 (items in
@@ -686,7 +688,7 @@ class EvictingDecode:
                              s.scale, self.out, self.ws, self.ws_bytes, eng.status, stream)
         kvs.kvs_decode_scores(q, eng.k_pool, eng.num_blocks, self.tables_d, self.max_blocks,
                               self.lens_d, self.score, self.new_pos, self.max_slots, n, s.h_q,
-                              s.h_kv, s.d, s.scale, eng.status, stream)
+                              s.h_kv, s.d, s.scale, self.sws, self.sws_bytes, eng.status, stream)
         return self.out
 
     def release(self):

@@ -89,11 +89,12 @@ def test_invalid_arguments_rejected_before_launch(kvs):
     assert lib.kvs_evict_place(None, 256, 256, 256, 4, 256, 1, 256, 256, 256, 256, 16, 2, 8, 128,
                                32, None, None) == kvs.KVS_ERR_INVALID
     assert lib.kvs_decode_scores(256, 256, 4, 256, 1, 256, 256, 256, 16, 0, 32, 8, 128, 0.1,
-                                 None, None) == kvs.KVS_OK
-    assert lib.kvs_decode_scores(256, 256, 4, 256, 1, 256, 256, 256, 100000, 2, 32, 8, 128, 0.1,
-                                 None, None) == kvs.KVS_ERR_UNSUPPORTED   # logits exceed smem
+                                 256, 1 << 20, None, None) == kvs.KVS_OK
+    assert lib.kvs_decode_scores(256, 256, 4, 256, 1, 256, 256, 256, 2048, 2, 32, 8, 128, 0.1,
+                                 256, 1024, None, None) == kvs.KVS_ERR_INVALID   # workspace short
     assert lib.kvs_decode_scores(256, 256, 4, 256, 1, 256, 256, 256, 16, 2, 32, 6, 128, 0.1,
-                                 None, None) == kvs.KVS_ERR_INVALID      # 32 % 6 != 0
+                                 256, 1 << 20, None, None) == kvs.KVS_ERR_INVALID  # 32 % 6 != 0
+    assert kvs.kvs_decode_scores_workspace_size(2, 32, 8, 2048) == 2 * 8 * 4 * (2048 + 8) * 4
     # the native decode step: nothing to do for zero items; NULL staging and a
     # step without an append are rejected before the allocator is touched
     args = [None] * 29
