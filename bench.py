@@ -384,6 +384,9 @@ def bench_gpu(args):
     if args.decode_wall:
         out["decode_wall"] = bench_decode_wall(args, eng, dec, w, n, steps, q, k, v, dq, dk, dv,
                                                o_buf, ml_buf, world, dist)
+    if args.decode_evicting:
+        out["decode_evicting"] = bench_decode_evicting(args, eng, w, n, steps, q, k, v, dq, dk,
+                                                       dv, o_buf, ml_buf, flush, world, dist)
     if args.e2e:
         out["e2e"] = bench_e2e(args, eng, dec, w, n, steps, q, k, v, dq, dk, dv, o_buf, ml_buf,
                                flush, world, dist)
@@ -432,6 +435,61 @@ def bench_decode_wall(args, eng, dec, w, n, steps, q, k, v, dq, dk, dv, o_buf, m
             "ms_per_token": round(dt / steps, 4),
             "what": "500 back-to-back native decode steps (host allocator + uploads + decode + "
                     "merge), host wall clock, no L2 flush (220 MB per step > L2)"}
+
+
+def bench_decode_evicting(args, eng, w, n, steps, q, k, v, dq, dk, dv, o_buf, ml_buf, flush,
+                          world, dist):
+    """Decode with decode-time replacement in the budgeted layers (3-31 keep
+    exactly k_l slots: each step's token replaces the lowest-scoring one
+    outside the recent window), the full-cache layers 0-2 growing as usual:
+    the request's 500 steps with the same L2 flush and per-step events as the
+    headline decode.  Bytes per step: the K/V rows every step reads (full
+    layers at the mean length, budgeted layers at k_l) plus the budgeted
+    layers' K rows read again for the scores."""
+    import torch
+    from layer_wise_kv_gb300.pipeline import DecodeBatch, EvictingDecode
+    L = w.n_layers
+    budgets = [[w.budget(l, n) for l in range(L)]]
+    full = [l for l in range(L) if w.budget(l, n) is None or w.budget(l, n) >= n]
+    bud = [l for l in range(L) if l not in full]
+    res = eng.prefill_sparsify(list(q), list(k), list(v), [n], budgets, o_buf=o_buf, ml_buf=ml_buf)
+    dec_f = DecodeBatch(eng, 1, n + steps, n_layers=len(full))
+    dec_f.set_stream(0, [res.tables[0][l] for l in full], [res.k_eff[0][l] for l in full])
+    ev = EvictingDecode(eng, res, 0, 0, n, bud)
+    fq, fk, fv = (x[:, full].contiguous() for x in (dq, dk, dv))
+    bq, bk, bv = (x[:, bud].contiguous() for x in (dq, dk, dv))
+    torch.cuda.synchronize()
+    pairs = []
+    gc.collect()
+    gc.disable()
+    for t in range(steps):
+        flush()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        dec_f.step(fq[t], fk[t], fv[t])
+        ev.step(bq[t], bk[t], bv[t])
+        b.record()
+        pairs.append((a, b))
+    torch.cuda.synchronize()
+    gc.enable()
+    eng.check_status()
+    dec_f.retire(0)
+    ev.release()
+    t_ms = sum(a.elapsed_time(b) for a, b in pairs)
+    (t_ms,) = max_over_ranks([t_ms], world, dist, q.device)
+    row = w.h_kv * w.d * 2
+    kv_full = sum((w.k_eff(l, n) + steps // 2 + 1) * row * 2 for l in full)
+    kv_bud = sum(w.k_eff(l, n) * row * 2 for l in bud)
+    bytes_step = kv_full + kv_bud + sum(w.k_eff(l, n) * row for l in bud)
+    per = t_ms / steps
+    peaks, _ = read_peaks()
+    return {"value": round(world * steps / (t_ms / 1e3), 1), "unit": "tok/s",
+            "ms_per_token": round(per, 4), "bytes_per_step": int(bytes_step),
+            "achieved_gbs": round(bytes_step / (per / 1e3) / 1e9, 1),
+            "frac_of_hbm": round(bytes_step / (per / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+            "what": "layers 3-31 replace their lowest-scoring token each step (k_l slots kept), "
+                    "layers 0-2 grow; events per step, L2 flushed before each"}
 
 
 def bench_e2e(args, eng, dec, w, n, steps, q, k, v, dq, dk, dv, o_buf, ml_buf, flush, world,
@@ -572,6 +630,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-decode-wall", dest="decode_wall", action="store_false",
                     help="skip the back-to-back decode pass timed by the host clock")
+    ap.add_argument("--no-decode-evicting", dest="decode_evicting", action="store_false",
+                    help="skip the decode pass with decode-time replacement")
     ap.add_argument("--cpu-rows", type=int, default=400,
                     help="prefill rows the CPU oracle evaluates (sample size)")
     args = ap.parse_args()

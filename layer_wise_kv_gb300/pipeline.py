@@ -391,11 +391,14 @@ def _stacked(layers):
 class DecodeBatch:
     """Decode items (one per (stream, layer)) over an Engine's pools."""
 
-    def __init__(self, eng: Engine, n_streams: int, max_len: int):
+    def __init__(self, eng: Engine, n_streams: int, max_len: int, n_layers: Optional[int] = None):
+        """n_layers: layers per stream (default: the engine's), e.g. only the
+        full-cache layers when the budgeted ones run in an EvictingDecode."""
         s = eng.shape
         self.eng = eng
         self.n_streams = n_streams
-        self.n_items = n_streams * s.n_layers
+        self.n_layers = s.n_layers if n_layers is None else int(n_layers)
+        self.n_items = n_streams * self.n_layers
         self.shape_ = s
         self.max_len = max_len
         self.max_blocks = blocks_for(max_len)
@@ -518,7 +521,7 @@ class DecodeBatch:
 
     def set_stream(self, slot: int, tables: List[List[int]], lens: List[int]):
         """Install a stream's per-layer tables (host copy + device rows)."""
-        L = self.eng.shape.n_layers
+        L = self.n_layers
         for l in range(L):
             i = slot * L + l
             self.tables_h[i, :] = -1
@@ -529,7 +532,7 @@ class DecodeBatch:
         self.lens_d[self.cur][rows] = torch.from_numpy(self.lens_h[rows]).to(self.eng.device)
 
     def stream_tables(self, slot: int) -> List[List[int]]:
-        L = self.eng.shape.n_layers
+        L = self.n_layers
         out = []
         for l in range(L):
             i = slot * L + l
@@ -541,7 +544,7 @@ class DecodeBatch:
         for t in self.stream_tables(slot):
             for b in t:
                 self.eng.alloc.decref(b)
-        L = self.eng.shape.n_layers
+        L = self.n_layers
         self.tables_h[slot * L:(slot + 1) * L] = -1
         self.lens_h[slot * L:(slot + 1) * L] = 0
 
