@@ -445,7 +445,7 @@ def bench_decode_evicting(args, eng, w, n, steps, q, k, v, dq, dk, dv, o_buf, ml
     the request's 500 steps with the same L2 flush and per-step events as the
     headline decode.  Bytes per step: the K/V rows every step reads (full
     layers at the mean length, budgeted layers at k_l) plus the budgeted
-    layers' K rows read again for the scores."""
+    layers' logits written by the decode launch and read by the score update."""
     import torch
     from layer_wise_kv_gb300.pipeline import DecodeBatch, EvictingDecode
     L = w.n_layers
@@ -481,7 +481,10 @@ def bench_decode_evicting(args, eng, w, n, steps, q, k, v, dq, dk, dv, o_buf, ml
     row = w.h_kv * w.d * 2
     kv_full = sum((w.k_eff(l, n) + steps // 2 + 1) * row * 2 for l in full)
     kv_bud = sum(w.k_eff(l, n) * row * 2 for l in bud)
-    bytes_step = kv_full + kv_bud + sum(w.k_eff(l, n) * row for l in bud)
+    # the decode launch writes the budgeted slots' logits (fp32, per query
+    # head) and the score update reads them back
+    logit_bytes = sum(w.k_eff(l, n) * w.h_q * 4 * 2 for l in bud)
+    bytes_step = kv_full + kv_bud + logit_bytes
     per = t_ms / steps
     peaks, _ = read_peaks()
     return {"value": round(world * steps / (t_ms / 1e3), 1), "unit": "tok/s",

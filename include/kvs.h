@@ -386,7 +386,8 @@ kvs_status kvs_decode_step(kvs_allocator* a, int32_t* tables_h, int32_t* lens_h,
  * it, summed over the KV head's query group.  A step is
  *   kvs_evict_place -> kvs_paged_decode (k_new = NULL, over lens[i] slots)
  *   -> kvs_decode_scores
- * on one stream.  State, device, per item i and KV head h, slot j < lens[i]:
+ * on one stream (or, with the logits written by the decode itself,
+ * kvs_evict_place -> kvs_paged_decode_logits -> kvs_decode_scores_from_logits).  State, device, per item i and KV head h, slot j < lens[i]:
  *   score [n_items][h_kv][max_slots] fp32: the accumulated score;
  *   pos   [n_items][h_kv][max_slots] int32: the token's position;
  *   new_pos [n_items] int32: the position of the step's new token.
@@ -415,6 +416,28 @@ kvs_status kvs_evict_place(const kvs_bf16* k_new, const kvs_bf16* v_new, kvs_bf1
  * each chunk's maxima; needs no initialisation). */
 size_t kvs_decode_scores_workspace_size(int32_t n_items, int32_t h_q, int32_t h_kv,
                                         int32_t max_slots);
+
+/* kvs_paged_decode that also writes every attended slot's logit, log2-scaled
+ * (scale * log2(e) * q_g . k_j), to logits [batch][h_kv][G][logit_ld] fp32 at
+ * [i][h][g][j]; slots j >= logit_ld are not written.  With it a step's score
+ * update reads the logits instead of K again:
+ *   kvs_evict_place -> kvs_paged_decode_logits -> kvs_decode_scores_from_logits */
+kvs_status kvs_paged_decode_logits(const kvs_bf16* q, const kvs_bf16* k_new,
+                                   const kvs_bf16* v_new, kvs_bf16* k_pool, kvs_bf16* v_pool,
+                                   int32_t num_blocks, int32_t* block_tables, int32_t max_blocks,
+                                   const int32_t* table_patch, const int32_t* lens,
+                                   int32_t* lens_next, int32_t batch, int32_t h_q, int32_t h_kv,
+                                   int32_t d, float scale, kvs_bf16* out, void* workspace,
+                                   size_t workspace_bytes, float* logits, int32_t logit_ld,
+                                   int32_t* status, kvs_stream stream);
+
+/* The score update of kvs_decode_scores from those logits: per (item, KV head)
+ * the softmax over the lens[i] slots per query head, summed over the group,
+ * added to score; then new_pos[i] += 1.  One launch; lens[i] <= logit_ld. */
+kvs_status kvs_decode_scores_from_logits(const float* logits, int32_t logit_ld,
+                                         const int32_t* lens, float* score, int32_t* new_pos,
+                                         int32_t max_slots, int32_t n_items, int32_t h_q,
+                                         int32_t h_kv, int32_t* status, kvs_stream stream);
 
 kvs_status kvs_decode_scores(const kvs_bf16* q, const kvs_bf16* k_pool, int32_t num_blocks,
                              const int32_t* block_tables, int32_t max_blocks, const int32_t* lens,

@@ -75,6 +75,8 @@ struct DecodeParams {
   int32_t* lens_next;
   uint16_t* out;
   float* ws_part;
+  float* logits;   // optional: [batch][h_kv][G][logit_ld] fp32, log2-scaled logits
+  int logit_ld;
   int32_t* status;
   int batch, max_blocks, num_blocks, h_q, h_kv, group, append, n_stages;
   int q_bytes, q_stride, q_off, bar_off, idx_off;
@@ -195,7 +197,7 @@ __device__ __forceinline__ int fetch_chunk(const Piece& x, int base, int lane,
   return pb;
 }
 
-template <int D, int NT>
+template <int D, int NT, bool kLogits>
 __global__ void __launch_bounds__(kDecThreads, 1)
 paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
                     const __grid_constant__ CUtensorMap v_map, const DecodeParams p) {
@@ -427,6 +429,17 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
         for (int e = 0; e < 2; ++e) {
           s0[e] = v0 ? (sa[nt][e] + sb[nt][e]) * p.scale_log2 : -INFINITY;
           s1[e] = v1 ? (sa[nt][2 + e] + sb[nt][2 + e]) * p.scale_log2 : -INFINITY;
+          if constexpr (kLogits) {
+            // every slot's logit for the score update (head hd, slots tok0 + lane/4, +8)
+            const int hd = nt * 8 + (lane & 3) * 2 + e;
+            if (hd < G) {
+              float* lg = p.logits +
+                          ((static_cast<int64_t>(cur.item) * p.h_kv + cur.h) * G + hd) * p.logit_ld;
+              const int t0 = tok0 + (lane >> 2);
+              if (v0 && t0 < p.logit_ld) lg[t0] = s0[e];
+              if (v1 && t0 + 8 < p.logit_ld) lg[t0 + 8] = s1[e];
+            }
+          }
           mx[e] = fmaxf(s0[e], s1[e]);
           mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 4));
           mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 8));
@@ -758,13 +771,19 @@ kvs_status launch_decode(DecodeParams& prm, const CUtensorMap& km, const CUtenso
   if (smem == 0) return fail(KVS_ERR_UNSUPPORTED, "kvs_paged_decode: shared-memory plan does not fit");
   static bool configured = false;
   if (!configured) {
-    KVS_CUDA(cudaFuncSetAttribute(paged_decode_kernel<D, NT>,
+    KVS_CUDA(cudaFuncSetAttribute(paged_decode_kernel<D, NT, false>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit),
+             "kvs_paged_decode: raising the shared-memory limit");
+    KVS_CUDA(cudaFuncSetAttribute(paged_decode_kernel<D, NT, true>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit),
              "kvs_paged_decode: raising the shared-memory limit");
     configured = true;
   }
   const int grid = sm_count_dec() < kMaxGrid ? sm_count_dec() : kMaxGrid;
-  paged_decode_kernel<D, NT><<<grid, kDecThreads, smem, stream>>>(km, vm, prm);
+  if (prm.logits != nullptr)
+    paged_decode_kernel<D, NT, true><<<grid, kDecThreads, smem, stream>>>(km, vm, prm);
+  else
+    paged_decode_kernel<D, NT, false><<<grid, kDecThreads, smem, stream>>>(km, vm, prm);
   KVS_CHECK_LAUNCH("kvs_paged_decode");
   // the merge as a programmatic dependent launch (it waits for decode inside)
   cudaLaunchConfig_t cfg = {};
@@ -798,12 +817,17 @@ size_t kvs_paged_decode_workspace_size(int32_t batch, int32_t h_q, int32_t h_kv,
   return static_cast<size_t>(slots * kvs::part_floats(static_cast<int>(G), d) * 4);
 }
 
-kvs_status kvs_paged_decode(const kvs_bf16* q, const kvs_bf16* k_new, const kvs_bf16* v_new,
-                            kvs_bf16* k_pool, kvs_bf16* v_pool, int32_t num_blocks,
-                            int32_t* block_tables, int32_t max_blocks, const int32_t* table_patch,
-                            const int32_t* lens, int32_t* lens_next, int32_t batch, int32_t h_q,
-                            int32_t h_kv, int32_t d, float scale, kvs_bf16* out, void* workspace,
-                            size_t workspace_bytes, int32_t* status, kvs_stream stream) {
+}  // extern "C"
+
+namespace {
+
+kvs_status paged_decode_impl(const kvs_bf16* q, const kvs_bf16* k_new, const kvs_bf16* v_new,
+                             kvs_bf16* k_pool, kvs_bf16* v_pool, int32_t num_blocks,
+                             int32_t* block_tables, int32_t max_blocks, const int32_t* table_patch,
+                             const int32_t* lens, int32_t* lens_next, int32_t batch, int32_t h_q,
+                             int32_t h_kv, int32_t d, float scale, kvs_bf16* out, void* workspace,
+                             size_t workspace_bytes, int32_t* status, kvs_stream stream,
+                             float* logits, int32_t logit_ld) {
   KVS_REQUIRE(batch >= 0, "kvs_paged_decode: negative batch");
   if (batch == 0) return KVS_OK;
   KVS_REQUIRE(q && k_pool && v_pool && block_tables && lens && out && workspace,
@@ -848,6 +872,8 @@ kvs_status kvs_paged_decode(const kvs_bf16* q, const kvs_bf16* k_new, const kvs_
   prm.lens_next = lens_next;
   prm.out = out;
   prm.ws_part = static_cast<float*>(workspace);
+  prm.logits = logits;
+  prm.logit_ld = logit_ld;
   prm.status = status;
   prm.batch = batch;
   prm.max_blocks = max_blocks;
@@ -864,6 +890,35 @@ kvs_status kvs_paged_decode(const kvs_bf16* q, const kvs_bf16* k_new, const kvs_
   }
   if (d == 128) return kvs::launch_decode<128, 2>(prm, kc.map, vc.map, st);
   return kvs::launch_decode<64, 2>(prm, kc.map, vc.map, st);
+}
+
+}  // namespace
+
+extern "C" {
+
+kvs_status kvs_paged_decode(const kvs_bf16* q, const kvs_bf16* k_new, const kvs_bf16* v_new,
+                            kvs_bf16* k_pool, kvs_bf16* v_pool, int32_t num_blocks,
+                            int32_t* block_tables, int32_t max_blocks, const int32_t* table_patch,
+                            const int32_t* lens, int32_t* lens_next, int32_t batch, int32_t h_q,
+                            int32_t h_kv, int32_t d, float scale, kvs_bf16* out, void* workspace,
+                            size_t workspace_bytes, int32_t* status, kvs_stream stream) {
+  return paged_decode_impl(q, k_new, v_new, k_pool, v_pool, num_blocks, block_tables, max_blocks,
+                           table_patch, lens, lens_next, batch, h_q, h_kv, d, scale, out,
+                           workspace, workspace_bytes, status, stream, nullptr, 0);
+}
+
+kvs_status kvs_paged_decode_logits(const kvs_bf16* q, const kvs_bf16* k_new,
+                                   const kvs_bf16* v_new, kvs_bf16* k_pool, kvs_bf16* v_pool,
+                                   int32_t num_blocks, int32_t* block_tables, int32_t max_blocks,
+                                   const int32_t* table_patch, const int32_t* lens,
+                                   int32_t* lens_next, int32_t batch, int32_t h_q, int32_t h_kv,
+                                   int32_t d, float scale, kvs_bf16* out, void* workspace,
+                                   size_t workspace_bytes, float* logits, int32_t logit_ld,
+                                   int32_t* status, kvs_stream stream) {
+  KVS_REQUIRE(logits != nullptr && logit_ld > 0, "kvs_paged_decode_logits: no logits buffer");
+  return paged_decode_impl(q, k_new, v_new, k_pool, v_pool, num_blocks, block_tables, max_blocks,
+                           table_patch, lens, lens_next, batch, h_q, h_kv, d, scale, out,
+                           workspace, workspace_bytes, status, stream, logits, logit_ld);
 }
 
 }  // extern "C"

@@ -644,8 +644,12 @@ class EvictingDecode:
     Layers without a budget keep growing through DecodeBatch."""
 
     def __init__(self, eng: Engine, res: PrefillResult, seq: int, seq_start: int, prompt_len: int,
-                 layers: Sequence[int]):
+                 layers: Sequence[int], fused: bool = True):
+        """fused: the decode launch writes the slots' logits and the score
+        update reads them (kvs_paged_decode_logits); otherwise the update
+        recomputes them from K (kvs_decode_scores)."""
         s = eng.shape
+        self.fused = fused
         dev = eng.device
         self.eng, self.layers = eng, list(layers)
         n = len(self.layers)
@@ -677,6 +681,9 @@ class EvictingDecode:
         self.ws = torch.zeros(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
         self.sws_bytes = kvs.kvs_decode_scores_workspace_size(n, s.h_q, s.h_kv, self.max_slots)
         self.sws = torch.empty(max(self.sws_bytes, 256), dtype=torch.uint8, device=dev)
+        self.logit_ld = (self.max_slots + 3) // 4 * 4
+        self.logits = torch.empty((n, s.h_kv, s.h_q // s.h_kv, self.logit_ld), dtype=torch.float32,
+                                  device=dev)
 
     def step(self, q, k_new, v_new, stream=None):
         """q [n_items][h_q][d], k_new / v_new [n_items][h_kv][d] bf16 (items in
@@ -686,6 +693,16 @@ class EvictingDecode:
         kvs.kvs_evict_place(k_new, v_new, eng.k_pool, eng.v_pool, eng.num_blocks, self.tables_d,
                             self.max_blocks, self.lens_d, self.new_pos, self.score, self.pos,
                             self.max_slots, n, s.h_kv, s.d, s.recent, eng.status, stream)
+        if self.fused:
+            kvs.kvs_paged_decode_logits(q, None, None, eng.k_pool, eng.v_pool, eng.num_blocks,
+                                        self.tables_d, self.max_blocks, None, self.lens_d, None, n,
+                                        s.h_q, s.h_kv, s.d, s.scale, self.out, self.ws,
+                                        self.ws_bytes, self.logits, self.logit_ld, eng.status,
+                                        stream)
+            kvs.kvs_decode_scores_from_logits(self.logits, self.logit_ld, self.lens_d, self.score,
+                                              self.new_pos, self.max_slots, n, s.h_q, s.h_kv,
+                                              eng.status, stream)
+            return self.out
         kvs.kvs_paged_decode(q, None, None, eng.k_pool, eng.v_pool, eng.num_blocks, self.tables_d,
                              self.max_blocks, None, self.lens_d, None, n, s.h_q, s.h_kv, s.d,
                              s.scale, self.out, self.ws, self.ws_bytes, eng.status, stream)

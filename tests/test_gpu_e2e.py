@@ -419,7 +419,8 @@ def test_decode_graphs_match_eager():
     np.testing.assert_array_equal(host_bits(ea.v_pool), host_bits(eb.v_pool))
 
 
-def test_evicting_decode_vs_oracle():
+@pytest.mark.parametrize("fused", [True, False])
+def test_evicting_decode_vs_oracle(fused):
     """Decode-time replacement in the tiny workload's budgeted layer (k = 64,
     recent window 16): every step, each KV head's replaced slot must be a
     valid choice for the oracle's fp64 scores (the lowest outside the recent
@@ -443,7 +444,7 @@ def test_evicting_decode_vs_oracle():
     heads = [eviction.HeadCache(bf16_to_f64(kb[gidx[h], h]), bf16_to_f64(vb[gidx[h], h]),
                                 rec.scores[h][gidx[h]].astype(np.float64),
                                 gidx[h].astype(np.int64)) for h in range(w.h_kv)]
-    ev = EvictingDecode(eng, res, 0, 0, n, [layer])
+    ev = EvictingDecode(eng, res, 0, 0, n, [layer], fused=fused)
     dq, dk, dv = decode_qkv(w, 0, layer, steps)
     scale = 1 / np.sqrt(w.d)
     replaced_decode_token = False
@@ -473,7 +474,8 @@ def test_evicting_decode_vs_oracle():
     assert int(ev.new_pos[0]) == n + steps
 
 
-def test_evicting_decode_llama_shapes():
+@pytest.mark.parametrize("fused", [True, False])
+def test_evicting_decode_llama_shapes(fused):
     """The same at Llama-3-8B shapes (32/8 heads, d = 128, recent window 32,
     one 4000-token prompt) for layers 3 and 31 (budgets 2048 and 256), two
     items in one launch each step."""
@@ -496,7 +498,7 @@ def test_evicting_decode_llama_shapes():
         heads.append([eviction.HeadCache(bf16_to_f64(kb[gidx[h], h]), bf16_to_f64(vb[gidx[h], h]),
                                          rec.scores[h][gidx[h]].astype(np.float64),
                                          gidx[h].astype(np.int64)) for h in range(w.h_kv)])
-    ev = EvictingDecode(eng, res, 0, 0, n, [0, 1])
+    ev = EvictingDecode(eng, res, 0, 0, n, [0, 1], fused=fused)
     dqkv = [decode_qkv(w, 0, l, steps) for l in real]
     scale = 1 / np.sqrt(w.d)
     for t in range(steps):
