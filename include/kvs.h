@@ -419,8 +419,11 @@ size_t kvs_decode_scores_workspace_size(int32_t n_items, int32_t h_q, int32_t h_
 
 /* kvs_paged_decode that also writes every attended slot's logit, log2-scaled
  * (scale * log2(e) * q_g . k_j), to logits [batch][h_kv][G][logit_ld] fp32 at
- * [i][h][g][j]; slots j >= logit_ld are not written.  With it a step's score
- * update reads the logits instead of K again:
+ * [i][h][g][j] (slots j >= logit_ld are not written), and each query head's
+ * log2 softmax denominator, log2(sum_j exp2(logit_j)), to lse [batch][h_q]
+ * fp32 (items with no tokens leave theirs unwritten).  Both buffers are
+ * caller-owned device memory and must be non-NULL.  With them a step's score
+ * update reads the logits instead of K again and needs no reduction:
  *   kvs_evict_place -> kvs_paged_decode_logits -> kvs_decode_scores_from_logits */
 kvs_status kvs_paged_decode_logits(const kvs_bf16* q, const kvs_bf16* k_new,
                                    const kvs_bf16* v_new, kvs_bf16* k_pool, kvs_bf16* v_pool,
@@ -429,12 +432,14 @@ kvs_status kvs_paged_decode_logits(const kvs_bf16* q, const kvs_bf16* k_new,
                                    int32_t* lens_next, int32_t batch, int32_t h_q, int32_t h_kv,
                                    int32_t d, float scale, kvs_bf16* out, void* workspace,
                                    size_t workspace_bytes, float* logits, int32_t logit_ld,
-                                   int32_t* status, kvs_stream stream);
+                                   float* lse, int32_t* status, kvs_stream stream);
 
-/* The score update of kvs_decode_scores from those logits: per (item, KV head)
- * the softmax over the lens[i] slots per query head, summed over the group,
- * added to score; then new_pos[i] += 1.  One launch; lens[i] <= logit_ld. */
-kvs_status kvs_decode_scores_from_logits(const float* logits, int32_t logit_ld,
+/* The score update of kvs_decode_scores from those logits and denominators:
+ * slot j of (item i, KV head h) gains sum_g exp2(logits[i][h][g][j] -
+ * lse[i][h*G + g]) (the step's softmax over the lens[i] slots, summed over the
+ * group); then new_pos[i] += 1.  One launch, a thread per slot; lens[i] <=
+ * logit_ld and lens[i] <= max_slots, else KVS_ERR_INVALID in status. */
+kvs_status kvs_decode_scores_from_logits(const float* logits, int32_t logit_ld, const float* lse,
                                          const int32_t* lens, float* score, int32_t* new_pos,
                                          int32_t max_slots, int32_t n_items, int32_t h_q,
                                          int32_t h_kv, int32_t* status, kvs_stream stream);

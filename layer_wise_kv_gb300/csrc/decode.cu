@@ -77,6 +77,7 @@ struct DecodeParams {
   float* ws_part;
   float* logits;   // optional: [batch][h_kv][G][logit_ld] fp32, log2-scaled logits
   int logit_ld;
+  float* lse;      // with logits: [batch][h_q] fp32, log2 of each head's softmax denominator
   int32_t* status;
   int batch, max_blocks, num_blocks, h_q, h_kv, group, append, n_stages;
   int q_bytes, q_stride, q_off, bar_off, idx_off;
@@ -505,6 +506,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
           const int hd = nt * 8 + (lane & 3) * 2 + e;
           if (hd < G) {
             const float il = 1.0f / l_h[nt][e];
+            if constexpr (kLogits)
+              if (lane < 4) p.lse[out_row0 + hd] = m_h[nt][e] + log2f(l_h[nt][e]);
             uint16_t* orow = p.out + (out_row0 + hd) * D;
 #pragma unroll
             for (int mt = 0; mt < D / 16; ++mt) {
@@ -571,6 +574,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
 // four output values of one head and folds its pieces in batches of up to
 // kMergeBatch, all loads of a batch in flight together, with a running maximum;
 // the groups' results are then combined the same way through shared memory.
+// With lse given, each head's log2(sum_p exp2(m_p - M) l_p) + M is written too.
 // Launched as a programmatic dependent of the decode kernel: the grid is set
 // up while decode drains and waits here until decode's writes are visible.
 constexpr int kMergeGroups = 4;
@@ -582,7 +586,7 @@ template <int D>
 __global__ void __launch_bounds__(kMergeThreads, 2)
 decode_merge_kernel(const float* __restrict__ ws_part, const int32_t* __restrict__ lens, int batch,
                     int append, int h_q, int h_kv, int G, int n_warps,
-                    uint16_t* __restrict__ out) {
+                    uint16_t* __restrict__ out, float* __restrict__ lse) {
   __shared__ float4 s_acc[kMergeGroups][kMergeGroupThreads];
   __shared__ float2 s_ml[kMergeGroups][kMergeGroupThreads];
   __shared__ int s_total, s_before;
@@ -692,6 +696,7 @@ decode_merge_kernel(const float* __restrict__ ws_part, const int32_t* __restrict
         ls += wgt * ml.y;
       }
       const float il = 1.0f / ls;
+      if (lse != nullptr && c == 0) lse[out_row0 + r] = Mt + log2f(ls);
       uint2 w2;
       w2.x = pack_bf16x2(a.x * il, a.y * il);
       w2.y = pack_bf16x2(a.z * il, a.w * il);
@@ -798,7 +803,7 @@ kvs_status launch_decode(DecodeParams& prm, const CUtensorMap& km, const CUtenso
   cfg.numAttrs = 1;
   KVS_CUDA(cudaLaunchKernelEx(&cfg, decode_merge_kernel<D>, static_cast<const float*>(prm.ws_part),
                               prm.lens, prm.batch, prm.append, prm.h_q, prm.h_kv, prm.group,
-                              grid * kWarps, prm.out),
+                              grid * kWarps, prm.out, prm.logits != nullptr ? prm.lse : nullptr),
            "kvs_paged_decode (merge launch)");
   return KVS_OK;
 }
@@ -827,7 +832,7 @@ kvs_status paged_decode_impl(const kvs_bf16* q, const kvs_bf16* k_new, const kvs
                              const int32_t* lens, int32_t* lens_next, int32_t batch, int32_t h_q,
                              int32_t h_kv, int32_t d, float scale, kvs_bf16* out, void* workspace,
                              size_t workspace_bytes, int32_t* status, kvs_stream stream,
-                             float* logits, int32_t logit_ld) {
+                             float* logits, int32_t logit_ld, float* lse) {
   KVS_REQUIRE(batch >= 0, "kvs_paged_decode: negative batch");
   if (batch == 0) return KVS_OK;
   KVS_REQUIRE(q && k_pool && v_pool && block_tables && lens && out && workspace,
@@ -874,6 +879,7 @@ kvs_status paged_decode_impl(const kvs_bf16* q, const kvs_bf16* k_new, const kvs
   prm.ws_part = static_cast<float*>(workspace);
   prm.logits = logits;
   prm.logit_ld = logit_ld;
+  prm.lse = lse;
   prm.status = status;
   prm.batch = batch;
   prm.max_blocks = max_blocks;
@@ -904,7 +910,7 @@ kvs_status kvs_paged_decode(const kvs_bf16* q, const kvs_bf16* k_new, const kvs_
                             size_t workspace_bytes, int32_t* status, kvs_stream stream) {
   return paged_decode_impl(q, k_new, v_new, k_pool, v_pool, num_blocks, block_tables, max_blocks,
                            table_patch, lens, lens_next, batch, h_q, h_kv, d, scale, out,
-                           workspace, workspace_bytes, status, stream, nullptr, 0);
+                           workspace, workspace_bytes, status, stream, nullptr, 0, nullptr);
 }
 
 kvs_status kvs_paged_decode_logits(const kvs_bf16* q, const kvs_bf16* k_new,
@@ -914,11 +920,12 @@ kvs_status kvs_paged_decode_logits(const kvs_bf16* q, const kvs_bf16* k_new,
                                    int32_t* lens_next, int32_t batch, int32_t h_q, int32_t h_kv,
                                    int32_t d, float scale, kvs_bf16* out, void* workspace,
                                    size_t workspace_bytes, float* logits, int32_t logit_ld,
-                                   int32_t* status, kvs_stream stream) {
-  KVS_REQUIRE(logits != nullptr && logit_ld > 0, "kvs_paged_decode_logits: no logits buffer");
+                                   float* lse, int32_t* status, kvs_stream stream) {
+  KVS_REQUIRE(logits != nullptr && logit_ld > 0 && lse != nullptr,
+              "kvs_paged_decode_logits: no logits or lse buffer");
   return paged_decode_impl(q, k_new, v_new, k_pool, v_pool, num_blocks, block_tables, max_blocks,
                            table_patch, lens, lens_next, batch, h_q, h_kv, d, scale, out,
-                           workspace, workspace_bytes, status, stream, logits, logit_ld);
+                           workspace, workspace_bytes, status, stream, logits, logit_ld, lse);
 }
 
 }  // extern "C"

@@ -289,73 +289,33 @@ decode_scores_update_kernel(const float* __restrict__ logits, const float* __res
   if (h == 0 && threadIdx.x == 0) new_pos[item] += 1;
 }
 
-// The score update from logits the decode kernel wrote (kvs_paged_decode_logits):
-// one CTA per (item, KV head); one pass keeps each head's running maximum and
-// sum of exponentials per thread, the CTA combines them, a second pass adds
-// each slot's probability summed over the group to its score.  The CTA of KV
-// head 0 advances the item's next position.
-__device__ __forceinline__ void ms_combine(float& m, float& s, float m2, float s2) {
-  const float mn = fmaxf(m, m2);
-  if (mn == -INFINITY) return;  // both empty
-  s = (m == -INFINITY ? 0.f : s * ex2(m - mn)) + (m2 == -INFINITY ? 0.f : s2 * ex2(m2 - mn));
-  m = mn;
-}
-
+// The score update from what the decode kernel wrote (kvs_paged_decode_logits):
+// each slot's log2-scaled logit per query head and each head's log2 softmax
+// denominator, so a slot's probability is exp2(logit - lse) with no reduction
+// left to do.  A thread per slot, kScoreThreads-slot chunks; grid (chunks,
+// h_kv, items).  The first CTA of KV head 0 advances the item's next position.
 __global__ void __launch_bounds__(kScoreThreads)
-scores_from_logits_kernel(const float* __restrict__ logits, int ld, const int32_t* __restrict__ lens,
-                          float* __restrict__ score, int32_t* __restrict__ new_pos, int max_slots,
-                          int h_kv, int G, int32_t* status) {
-  __shared__ float s_rm[kScoreThreads / 32][16], s_rs[kScoreThreads / 32][16];
-  __shared__ float s_m[16], s_il[16];
-  const int item = blockIdx.x, h = blockIdx.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+scores_from_logits_kernel(const float* __restrict__ logits, int ld, const float* __restrict__ lse,
+                          const int32_t* __restrict__ lens, float* __restrict__ score,
+                          int32_t* __restrict__ new_pos, int max_slots, int h_kv, int G,
+                          int32_t* status) {
+  const int item = blockIdx.z, h = blockIdx.y;
+  const int j = blockIdx.x * kScoreThreads + threadIdx.x;
   const int n = lens[item];
-  if (n > 0 && n <= max_slots && n <= ld) {
-    const float* lgt = logits + (static_cast<int64_t>(item) * h_kv + h) * G * ld;
-    float m[16], sm[16];
+  const bool lead = blockIdx.x == 0 && h == 0 && threadIdx.x == 0;
+  if (n > max_slots || n > ld) {
+    if (lead) flag_status(status, KVS_ERR_INVALID);
+  } else if (j < n) {
+    const int64_t ih = static_cast<int64_t>(item) * h_kv + h;
+    const float* lg = logits + ih * G * ld + j;
+    const float* ls = lse + ih * G;
+    float p = 0.f;
 #pragma unroll
-    for (int g = 0; g < 16; ++g) {
-      m[g] = -INFINITY;
-      sm[g] = 0.f;
-    }
-    for (int j = threadIdx.x; j < n; j += kScoreThreads)
-#pragma unroll
-      for (int g = 0; g < 16; ++g)
-        if (g < G) ms_combine(m[g], sm[g], lgt[g * ld + j], 1.f);
-#pragma unroll
-    for (int g = 0; g < 16; ++g) {
-      if (g >= G) break;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float m2 = __shfl_xor_sync(0xffffffffu, m[g], o);
-        const float s2 = __shfl_xor_sync(0xffffffffu, sm[g], o);
-        ms_combine(m[g], sm[g], m2, s2);
-      }
-      if (lane == 0) {
-        s_rm[warp][g] = m[g];
-        s_rs[warp][g] = sm[g];
-      }
-    }
-    __syncthreads();
-    if (threadIdx.x < G) {
-      float mm = -INFINITY, ss = 0.f;
-      for (int w = 0; w < kScoreThreads / 32; ++w) ms_combine(mm, ss, s_rm[w][threadIdx.x], s_rs[w][threadIdx.x]);
-      s_m[threadIdx.x] = mm;
-      s_il[threadIdx.x] = 1.0f / ss;
-    }
-    __syncthreads();
-    float* sc = score + (static_cast<int64_t>(item) * h_kv + h) * max_slots;
-    for (int j = threadIdx.x; j < n; j += kScoreThreads) {
-      float p = 0.f;
-#pragma unroll
-      for (int g = 0; g < 16; ++g)
-        if (g < G) p += ex2(lgt[g * ld + j] - s_m[g]) * s_il[g];
-      sc[j] += p;
-    }
-  } else if ((n > max_slots || n > ld) && threadIdx.x == 0) {
-    flag_status(status, KVS_ERR_INVALID);
+    for (int g = 0; g < 16; ++g)
+      if (g < G) p += ex2(lg[static_cast<int64_t>(g) * ld] - ls[g]);
+    score[ih * max_slots + j] += p;
   }
-  if (h == 0 && threadIdx.x == 0) new_pos[item] += 1;
+  if (lead) new_pos[item] += 1;
 }
 
 }  // namespace
@@ -445,21 +405,25 @@ extern "C" kvs_status kvs_decode_scores(const kvs_bf16* q, const kvs_bf16* k_poo
 }
 
 extern "C" kvs_status kvs_decode_scores_from_logits(const float* logits, int32_t logit_ld,
-                                                    const int32_t* lens, float* score,
+                                                    const float* lse, const int32_t* lens,
+                                                    float* score,
                                                     int32_t* new_pos, int32_t max_slots,
                                                     int32_t n_items, int32_t h_q, int32_t h_kv,
                                                     int32_t* status, kvs_stream stream) {
   KVS_REQUIRE(n_items >= 0, "kvs_decode_scores_from_logits: negative item count");
   if (n_items == 0) return KVS_OK;
-  KVS_REQUIRE(logits && lens && score && new_pos, "kvs_decode_scores_from_logits: NULL pointer");
+  KVS_REQUIRE(logits && lse && lens && score && new_pos,
+              "kvs_decode_scores_from_logits: NULL pointer");
   KVS_REQUIRE(h_kv > 0 && h_q > 0 && h_q % h_kv == 0 && max_slots > 0 && logit_ld > 0 &&
                   n_items <= 65535 && h_kv <= 65535,
               "kvs_decode_scores_from_logits: bad sizes");
   KVS_SUPPORTED(h_q / h_kv <= 16, "kvs_decode_scores_from_logits: group size %d > 16",
                 h_q / h_kv);
-  kvs::scores_from_logits_kernel<<<dim3(n_items, h_kv), kvs::kScoreThreads, 0,
+  const unsigned chunks = static_cast<unsigned>((max_slots + kvs::kScoreThreads - 1) /
+                                                kvs::kScoreThreads);
+  kvs::scores_from_logits_kernel<<<dim3(chunks, h_kv, n_items), kvs::kScoreThreads, 0,
                                    static_cast<cudaStream_t>(stream)>>>(
-      logits, logit_ld, lens, score, new_pos, max_slots, h_kv, h_q / h_kv, status);
+      logits, logit_ld, lse, lens, score, new_pos, max_slots, h_kv, h_q / h_kv, status);
   KVS_CHECK_LAUNCH("kvs_decode_scores_from_logits");
   return KVS_OK;
 }

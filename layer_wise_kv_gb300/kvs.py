@@ -59,9 +59,9 @@ _SIGS = {
     "kvs_decode_scores_workspace_size": (_SZ, [_I32, _I32, _I32, _I32]),
     "kvs_paged_decode_logits": (_I32, [_VP, _VP, _VP, _VP, _VP, _I32, _VP, _I32, _VP, _VP, _VP,
                                        _I32, _I32, _I32, _I32, _F32, _VP, _VP, _SZ, _VP, _I32,
-                                       _VP, _VP]),
-    "kvs_decode_scores_from_logits": (_I32, [_VP, _I32, _VP, _VP, _VP, _I32, _I32, _I32, _I32,
-                                             _VP, _VP]),
+                                       _VP, _VP, _VP]),
+    "kvs_decode_scores_from_logits": (_I32, [_VP, _I32, _VP, _VP, _VP, _VP, _I32, _I32, _I32,
+                                             _I32, _VP, _VP]),
     "kvs_decode_scores": (_I32, [_VP, _VP, _I32, _VP, _I32, _VP, _VP, _VP, _I32, _I32, _I32,
                                  _I32, _I32, _F32, _VP, _SZ, _VP, _VP]),
     "kvs_decode_step": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I32,
@@ -310,10 +310,12 @@ def kvs_evict_place(k_new, v_new, k_pool, v_pool, num_blocks, block_tables, max_
 
 def kvs_paged_decode_logits(q, k_new, v_new, k_pool, v_pool, num_blocks, block_tables,
                             max_blocks, table_patch, lens, lens_next, batch, h_q, h_kv, d, scale,
-                            out, workspace, workspace_bytes, logits, logit_ld, status=None,
+                            out, workspace, workspace_bytes, logits, logit_ld, lse, status=None,
                             stream=None):
     if logits.numel() < batch * h_kv * (h_q // h_kv) * logit_ld:
         raise ValueError("logits must hold batch x h_kv x G x logit_ld floats")
+    if lse.numel() < batch * h_q:
+        raise ValueError("lse must hold batch x h_q floats")
     _check(library().kvs_paged_decode_logits(
         _dev(q, "bf16", "q"), None if k_new is None else _dev(k_new, "bf16", "k_new"),
         None if v_new is None else _dev(v_new, "bf16", "v_new"), _dev(k_pool, "bf16", "k_pool"),
@@ -322,13 +324,14 @@ def kvs_paged_decode_logits(q, k_new, v_new, k_pool, v_pool, num_blocks, block_t
         _dev(lens, "i32", "lens"), None if lens_next is None else _dev(lens_next, "i32", "lens_next"),
         batch, h_q, h_kv, d, float(scale), _dev(out, "bf16", "out"),
         _dev(workspace, "u8", "workspace"), workspace_bytes, _dev(logits, "f32", "logits"),
-        logit_ld, None if status is None else _dev(status, "i32", "status"), _stream(stream)))
+        logit_ld, _dev(lse, "f32", "lse"), None if status is None else _dev(status, "i32", "status"),
+        _stream(stream)))
 
 
-def kvs_decode_scores_from_logits(logits, logit_ld, lens, score, new_pos, max_slots, n_items, h_q,
-                                  h_kv, status=None, stream=None):
+def kvs_decode_scores_from_logits(logits, logit_ld, lse, lens, score, new_pos, max_slots, n_items,
+                                  h_q, h_kv, status=None, stream=None):
     _check(library().kvs_decode_scores_from_logits(
-        _dev(logits, "f32", "logits"), logit_ld, _dev(lens, "i32", "lens"),
+        _dev(logits, "f32", "logits"), logit_ld, _dev(lse, "f32", "lse"), _dev(lens, "i32", "lens"),
         _dev(score, "f32", "score"), _dev(new_pos, "i32", "new_pos"), max_slots, n_items, h_q,
         h_kv, None if status is None else _dev(status, "i32", "status"), _stream(stream)))
 

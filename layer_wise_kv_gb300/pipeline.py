@@ -645,9 +645,10 @@ class EvictingDecode:
 
     def __init__(self, eng: Engine, res: PrefillResult, seq: int, seq_start: int, prompt_len: int,
                  layers: Sequence[int], fused: bool = True):
-        """fused: the decode launch writes the slots' logits and the score
-        update reads them (kvs_paged_decode_logits); otherwise the update
-        recomputes them from K (kvs_decode_scores)."""
+        """fused: the decode launch writes the slots' logits and each query
+        head's softmax denominator, and the score update reads them
+        (kvs_paged_decode_logits); otherwise the update recomputes the logits
+        from K (kvs_decode_scores)."""
         s = eng.shape
         self.fused = fused
         dev = eng.device
@@ -684,6 +685,7 @@ class EvictingDecode:
         self.logit_ld = (self.max_slots + 3) // 4 * 4
         self.logits = torch.empty((n, s.h_kv, s.h_q // s.h_kv, self.logit_ld), dtype=torch.float32,
                                   device=dev)
+        self.lse = torch.empty((n, s.h_q), dtype=torch.float32, device=dev)
 
     def step(self, q, k_new, v_new, stream=None):
         """q [n_items][h_q][d], k_new / v_new [n_items][h_kv][d] bf16 (items in
@@ -697,11 +699,11 @@ class EvictingDecode:
             kvs.kvs_paged_decode_logits(q, None, None, eng.k_pool, eng.v_pool, eng.num_blocks,
                                         self.tables_d, self.max_blocks, None, self.lens_d, None, n,
                                         s.h_q, s.h_kv, s.d, s.scale, self.out, self.ws,
-                                        self.ws_bytes, self.logits, self.logit_ld, eng.status,
-                                        stream)
-            kvs.kvs_decode_scores_from_logits(self.logits, self.logit_ld, self.lens_d, self.score,
-                                              self.new_pos, self.max_slots, n, s.h_q, s.h_kv,
-                                              eng.status, stream)
+                                        self.ws_bytes, self.logits, self.logit_ld, self.lse,
+                                        eng.status, stream)
+            kvs.kvs_decode_scores_from_logits(self.logits, self.logit_ld, self.lse, self.lens_d,
+                                              self.score, self.new_pos, self.max_slots, n, s.h_q,
+                                              s.h_kv, eng.status, stream)
             return self.out
         kvs.kvs_paged_decode(q, None, None, eng.k_pool, eng.v_pool, eng.num_blocks, self.tables_d,
                              self.max_blocks, None, self.lens_d, None, n, s.h_q, s.h_kv, s.d,

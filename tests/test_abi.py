@@ -95,6 +95,20 @@ def test_invalid_arguments_rejected_before_launch(kvs):
     assert lib.kvs_decode_scores(256, 256, 4, 256, 1, 256, 256, 256, 16, 2, 32, 6, 128, 0.1,
                                  256, 1 << 20, None, None) == kvs.KVS_ERR_INVALID  # 32 % 6 != 0
     assert kvs.kvs_decode_scores_workspace_size(2, 32, 8, 2048) == 2 * 8 * 4 * (2048 + 8) * 4
+    # decode that writes its logits and denominators: both buffers are required
+    dl = [256, None, None, 256, 256, 4, 256, 1, None, 256, None, 0, 32, 8, 128, 0.1, 256, 256,
+          1 << 20, 256, 16, 256, None, None]
+    assert lib.kvs_paged_decode_logits(*dl) == kvs.KVS_OK
+    dl[21] = None
+    assert lib.kvs_paged_decode_logits(*dl) == kvs.KVS_ERR_INVALID
+    assert lib.kvs_decode_scores_from_logits(256, 16, 256, 256, 256, 256, 16, 0, 32, 8, None,
+                                             None) == kvs.KVS_OK
+    assert lib.kvs_decode_scores_from_logits(256, 16, None, 256, 256, 256, 16, 2, 32, 8, None,
+                                             None) == kvs.KVS_ERR_INVALID
+    assert lib.kvs_decode_scores_from_logits(256, 16, 256, 256, 256, 256, 16, 2, 32, 6, None,
+                                             None) == kvs.KVS_ERR_INVALID    # 32 % 6 != 0
+    assert lib.kvs_decode_scores_from_logits(256, 16, 256, 256, 256, 256, 16, 2, 64, 2, None,
+                                             None) == kvs.KVS_ERR_UNSUPPORTED  # group 32 > 16
     # the native decode step: nothing to do for zero items; NULL staging and a
     # step without an append are rejected before the allocator is touched
     args = [None] * 29

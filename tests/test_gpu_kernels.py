@@ -375,3 +375,91 @@ def test_paged_decode_vs_oracle(h_q, h_kv, d):
     np.testing.assert_array_equal(host_bits(v_pool), pv)
     a.close()
 
+
+
+# ---------------------------------------------------------------------------
+# decode that also writes its logits and softmax denominators, and the score
+# update that reads them (decode-time replacement)
+# ---------------------------------------------------------------------------
+def _oracle_probs(q, kc, d, scale):
+    """Per query head, the softmax probabilities over the cache, from the
+    oracle's decode attention with one-hot value rows: with v_j = e_(j - c*d)
+    for the slots j of column chunk c (zero elsewhere), the output row is
+    that chunk's probabilities."""
+    h_kv, n, _ = kc.shape
+    out = np.zeros((q.shape[0], n))
+    for c0 in range(0, n, d):
+        w = min(d, n - c0)
+        vc = np.zeros((h_kv, n, d))
+        vc[:, np.arange(c0, c0 + w), np.arange(w)] = 1.0
+        out[:, c0:c0 + w] = oracle.decode_attention(q, kc, vc, scale)[:, :w]
+    return out
+
+
+@pytest.mark.parametrize("h_q,h_kv,d", [(32, 8, 128), (6, 2, 128), (4, 4, 64)])
+def test_paged_decode_logits_and_score_update_vs_oracle(h_q, h_kv, d):
+    """kvs_paged_decode_logits: the same output as kvs_paged_decode, bit for
+    bit, and per slot exp2(logit - lse) equal to the oracle's softmax
+    probability, for items short enough to be one decode piece (their
+    denominators written by the decode kernel) and long enough to be split
+    (written by the merge).  kvs_decode_scores_from_logits then adds the
+    group's probabilities to each slot's score; an empty item is left alone."""
+    kvs = kvs_lib()
+    rng = np.random.default_rng(7 * h_q + d)
+    lens = [1, 0, 15, 16, 17, 200, 700, 2048, 3001]
+    n_items, G = len(lens), h_q // h_kv
+    max_blocks = oracle.blocks_for(max(lens))
+    N = n_items * max_blocks + 4
+    perm = rng.permutation(N).astype(np.int32)
+    pk = np.full((N, h_kv, 16, d), 0xFFFF, np.uint16)
+    pv = pk.copy()
+    tables = np.full((n_items, max_blocks), -1, np.int32)
+    at = 0
+    for i, n in enumerate(lens):
+        nb = oracle.blocks_for(n)
+        tables[i, :nb] = perm[at:at + nb]
+        at += nb
+        for j in range(n):
+            pk[tables[i, j // 16], :, j % 16] = _randn_bits(rng, (h_kv, d))
+            pv[tables[i, j // 16], :, j % 16] = _randn_bits(rng, (h_kv, d))
+    k_pool, v_pool = dev_bf16(pk), dev_bf16(pv)
+    tables_d = torch.from_numpy(tables).cuda()
+    lens_d = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    q = _randn_bits(rng, (n_items, h_q, d), 2.0)
+    scale = 1 / np.sqrt(d)
+    ws_bytes = kvs.kvs_paged_decode_workspace_size(n_items, h_q, h_kv, d)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    outs = [torch.zeros((n_items, h_q, d), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    kvs.kvs_paged_decode(dev_bf16(q), None, None, k_pool, v_pool, N, tables_d, max_blocks, None,
+                         lens_d, None, n_items, h_q, h_kv, d, scale, outs[0], ws, ws_bytes, status)
+    max_slots = max(lens)
+    ld = (max_slots + 3) // 4 * 4
+    logits = torch.full((n_items, h_kv, G, ld), float("nan"), dtype=torch.float32, device="cuda")
+    lse = torch.full((n_items, h_q), float("nan"), dtype=torch.float32, device="cuda")
+    kvs.kvs_paged_decode_logits(dev_bf16(q), None, None, k_pool, v_pool, N, tables_d, max_blocks,
+                                None, lens_d, None, n_items, h_q, h_kv, d, scale, outs[1], ws,
+                                ws_bytes, logits, ld, lse, status)
+    score0 = rng.uniform(0.0, 3.0, (n_items, h_kv, max_slots)).astype(np.float32)
+    score = torch.from_numpy(score0).cuda()
+    new_pos = torch.arange(n_items, dtype=torch.int32, device="cuda")
+    kvs.kvs_decode_scores_from_logits(logits, ld, lse, lens_d, score, new_pos, max_slots, n_items,
+                                      h_q, h_kv, status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    assert torch.equal(outs[0], outs[1])
+    lg = logits.cpu().numpy().astype(np.float64)
+    ls = lse.cpu().numpy().astype(np.float64)
+    sc = score.cpu().numpy().astype(np.float64)
+    np.testing.assert_array_equal(new_pos.cpu().numpy(), np.arange(n_items) + 1)
+    for i, n in enumerate(lens):
+        if n == 0:
+            np.testing.assert_array_equal(sc[i], score0[i])
+            continue
+        kc = np.stack([oracle.gather_rows(pk, tables[i], n, h) for h in range(h_kv)])
+        ref = _oracle_probs(bf16_to_f64(q[i]), bf16_to_f64(kc), d, scale)
+        got = np.exp2(lg[i, :, :, :n].reshape(h_q, n) - ls[i][:, None])
+        check_rel(got, ref, REL_S, ABS_S, what=f"probabilities item {i} (n={n})")
+        want = score0[i].astype(np.float64)
+        want[:, :n] += ref.reshape(h_kv, G, n).sum(axis=1)
+        check_rel(sc[i], want, REL_S, ABS_S, what=f"scores item {i}")
