@@ -8,7 +8,8 @@ two sources the method is described in:
   (sections "System model", "Key techniques 1: layer-wise sparsity and tensor
   parallelism", "Key techniques 2: attention modification"), and
 * Ultralytics glossary, "PagedAttention" (sections "How paging works",
-  including its worked example, and "Block sharing between sequences").
+  including its worked example, "Block sharing between sequences" and
+  "Related techniques").
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline / reference
 legs of ``bench.py`` import it.  It shares no code with the CUDA library and
@@ -25,6 +26,7 @@ paging    : list-based block pool (FIFO free list, ref counts, copy-on-write),
 flow      : the step orders that tie these together (prefill+sparsify of a
             sequence, one decode step, retirement).
 eviction  : decode-time scores and fixed-budget replacement in budgeted layers.
+fp8       : the 8-bit (e4m3, per-row scale) storage of cached keys and values.
 
 Every function is pinned by a ``-m "not gpu"`` test against something other
 than itself (closed forms, library routines, brute force, the worked paging
@@ -36,3 +38,4 @@ from .selection import select_kept  # noqa: F401
 from .paging import BlockPool, OutOfBlocks, compact, gather_rows, blocks_for  # noqa: F401
 from . import flow  # noqa: F401
 from . import eviction  # noqa: F401
+from . import fp8  # noqa: F401

@@ -403,3 +403,53 @@ def test_eviction_valid_choice_tolerance():
     assert is_valid_choice(score, pos, 10, 2, 2, 1e-5)      # within the error of the lowest
     assert not is_valid_choice(score, pos, 10, 2, 0, 1e-5)
     assert not is_valid_choice(score, pos, 10, 2, 3, 1e-5)  # pos 9 > 10 - 2: recent
+
+
+# ---------------------------------------------------------------------------
+# FP8 (e4m3) storage of cached rows: pinned to torch's float8_e4m3fn casts and
+# to the format's round-trip bound
+# ---------------------------------------------------------------------------
+def test_fp8_decode_matches_torch_for_every_code():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = oracle.fp8.e4m3_decode(codes)
+    nan = np.isnan(ref)
+    assert nan.sum() == 2 and np.array_equal(nan, np.isnan(got))
+    np.testing.assert_array_equal(got[~nan], ref[~nan])
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9
+
+
+def test_fp8_encode_matches_torch_round_to_nearest_even():
+    rng = np.random.default_rng(11)
+    vals = oracle.fp8.e4m3_decode(np.arange(0x7F))
+    mids = (vals[:-1] + vals[1:]) / 2            # every tie between neighbours
+    rand = np.exp(rng.uniform(np.log(2.0 ** -12), np.log(448.0), 4000))
+    x = np.concatenate([vals, mids, rand, np.nextafter(mids, 0), np.nextafter(mids, 1e9)])
+    x = np.concatenate([x, -x]).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(oracle.fp8.e4m3_encode(x), ref)
+
+
+def test_fp8_encode_saturates_and_keeps_signed_zero():
+    enc = oracle.fp8.e4m3_encode_one
+    assert enc(448.0) == 0x7E and enc(460.0) == 0x7E and enc(1e9) == 0x7E
+    assert enc(-500.0) == 0xFE
+    assert enc(0.0) == 0x00 and enc(-0.0) == 0x80
+    assert enc(2.0 ** -10) == 0x00        # a tie between 0 and the smallest subnormal: even
+
+
+def test_fp8_row_quantisation_bounds():
+    rng = np.random.default_rng(12)
+    for scale in (1e-3, 0.5, 30.0):
+        x = (rng.standard_normal((64, 128)) * scale).astype(np.float32)
+        codes, s = oracle.fp8.quantize_rows(x)
+        for i in range(x.shape[0]):
+            v = oracle.fp8.dequantize_row(codes[i], s[i])
+            # half a step of the format: 2^-4 relative (normals), 2^-10 s (subnormals)
+            bound = np.maximum(np.abs(x[i]) * 2.0 ** -4, s[i] * 2.0 ** -10) * (1 + 1e-6)
+            assert (np.abs(v - x[i]) <= bound).all()
+            j = np.argmax(np.abs(x[i]))
+            assert codes[i, j] & 0x7F == 0x7E            # the largest magnitude maps to 448
+            assert s[i] == np.float32(np.float32(np.abs(x[i]).max()) / np.float32(448))
+    codes, s = oracle.fp8.quantize_row(np.zeros(16, np.float32))
+    assert (codes == 0).all() and s == 1.0
