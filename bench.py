@@ -387,6 +387,9 @@ def bench_gpu(args):
     if args.decode_evicting:
         out["decode_evicting"] = bench_decode_evicting(args, eng, w, n, steps, q, k, v, dq, dk,
                                                        dv, o_buf, ml_buf, flush, world, dist)
+    if args.decode_fp8:
+        out["decode_fp8"] = bench_decode_fp8(args, shape, blocks + 64, w, n, steps, q, k, v, dq,
+                                             dk, dv, o_buf, ml_buf, flush, world, dist)
     if args.e2e:
         out["e2e"] = bench_e2e(args, eng, dec, w, n, steps, q, k, v, dq, dk, dv, o_buf, ml_buf,
                                flush, world, dist)
@@ -493,6 +496,63 @@ def bench_decode_evicting(args, eng, w, n, steps, q, k, v, dq, dk, dv, o_buf, ml
             "frac_of_hbm": round(bytes_step / (per / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
             "what": "layers 3-31 replace their lowest-scoring token each step (k_l slots kept), "
                     "layers 0-2 grow; events per step, L2 flushed before each"}
+
+
+def bench_decode_fp8(args, shape, num_blocks, w, n, steps, q, k, v, dq, dk, dv, o_buf, ml_buf,
+                     flush, world, dist):
+    """The headline request's decode over FP8 pools (e4m3 codes, per-row fp32
+    scales): the prefill compacts into them, then 500 steps, each the
+    allocator's preparation, the table-patch upload and one FP8 decode
+    launch over the 32 layers, with the same L2 flush and per-step events as
+    the headline decode; kernel events around each decode launch give the
+    roofline.  Bytes per decode launch: every cached row's d codes and 4-byte
+    scale, K and V, plus q, out and the new rows."""
+    import torch
+    from layer_wise_kv_gb300.pipeline import DecodeBatch, Engine
+    L = w.n_layers
+    budgets = [[w.budget(l, n) for l in range(L)]]
+    eng8 = Engine(shape, num_blocks, device=q.device, kv_dtype="fp8")
+    dec8 = DecodeBatch(eng8, 1, n + steps)
+    res = eng8.prefill_sparsify(list(q), list(k), list(v), [n], budgets, o_buf=o_buf,
+                                ml_buf=ml_buf)
+    dec8.set_stream(0, res.tables[0], res.k_eff[0])
+    torch.cuda.synchronize()
+    pairs, kern = [], []
+    gc.collect()
+    gc.disable()
+    for t in range(steps):
+        flush()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        dec8.step(dq[t], dk[t], dv[t], timing=kern)
+        b.record()
+        pairs.append((a, b))
+    torch.cuda.synchronize()
+    gc.enable()
+    eng8.check_status()
+    dec8.retire(0)
+    t_ms = sum(a.elapsed_time(b) for a, b in pairs)
+    k_ms = sum(a.elapsed_time(b) for a, b in kern)
+    t_ms, k_ms = max_over_ranks([t_ms, k_ms], world, dist, q.device)
+    row = w.h_kv * (w.d + 4)
+    lens = [w.k_eff(l, n) for l in range(L)]
+    per_launch = []
+    for t in range(steps):
+        kv = sum((Lq + t + 1) * row * 2 for Lq in lens)
+        per_launch.append(kv + L * (w.h_q * w.d * 2 * 2 + w.h_kv * w.d * 2 * 2))
+    alg = sum(per_launch) / steps
+    per_k = k_ms / steps
+    peaks, _ = read_peaks()
+    ach = alg / (per_k / 1e3) / 1e9
+    del dec8, eng8
+    return {"value": round(world * steps / (t_ms / 1e3), 1), "unit": "tok/s",
+            "ms_per_token": round(t_ms / steps, 4), "kernel_ms": round(per_k, 4),
+            "bytes_per_launch": int(alg), "achieved_gbs": round(ach, 1),
+            "frac_of_hbm": round(ach / peaks["hbm_gbs"], 4),
+            "what": "decode over e4m3 pools with per-row scales (codes + scales read), "
+                    "eager steps with allocator preparation, events per step, L2 flushed "
+                    "before each"}
 
 
 def bench_e2e(args, eng, dec, w, n, steps, q, k, v, dq, dk, dv, o_buf, ml_buf, flush, world,
@@ -635,6 +695,8 @@ def main():
                     help="skip the back-to-back decode pass timed by the host clock")
     ap.add_argument("--no-decode-evicting", dest="decode_evicting", action="store_false",
                     help="skip the decode pass with decode-time replacement")
+    ap.add_argument("--no-decode-fp8", dest="decode_fp8", action="store_false",
+                    help="skip the decode pass over FP8 pools")
     ap.add_argument("--cpu-rows", type=int, default=400,
                     help="prefill rows the CPU oracle evaluates (sample size)")
     args = ap.parse_args()

@@ -203,6 +203,32 @@ kvs_status kvs_compact_blocks(const kvs_bf16* k, const kvs_bf16* v, const kvs_co
                               kvs_bf16* k_pool, kvs_bf16* v_pool, int32_t num_blocks,
                               int32_t* status, kvs_stream stream);
 
+/* kvs_compact_blocks into an FP8 pool (d = 128 only).  Source: Ultralytics
+ * glossary "PagedAttention", section "Related techniques" (FP8 cache
+ * quantisation: keys and values at 8-bit precision, about half the memory of
+ * 16-bit formats); format and scaling are this library's reading:
+ *   - each cached row (slot r of block b, KV head h; d values) is stored as
+ *     e4m3 codes with one fp32 scale s = amax / 448 (s = 1 for an all-zero
+ *     row): code = e4m3 nearest to x / s, ties to even, saturating at 448;
+ *     amax / 448 and x / s are IEEE fp32 divisions; the stored value is
+ *     e4m3(code) * s;
+ *   - k_pool [num_blocks][h_kv][16][128] uint8: row r of (b, h) at byte
+ *     ((b * h_kv + h) * 16 + r) * 128, its 16-byte chunk c at chunk position
+ *     c ^ (4 * (r & 1)) within the row;
+ *   - v_pool [num_blocks][h_kv][128][16] uint8: transposed, element dd of
+ *     slot r at byte ((b * h_kv + h) * 128 + dd) * 16 + r;
+ *   - k_scale, v_scale [num_blocks][h_kv][16] fp32.
+ * Slots past k_eff in an item's last block get zero codes and zero scales.
+ * Other arguments as kvs_compact_blocks; n_items <= 4096; pool and scale
+ * pointers 16-byte aligned. */
+kvs_status kvs_compact_blocks_fp8(const kvs_bf16* k, const kvs_bf16* v,
+                                  const kvs_compact_item* items, int32_t n_items,
+                                  int64_t total_rows, int32_t h_kv, int32_t d,
+                                  const int32_t* kept_idx, const int32_t* block_tables,
+                                  uint8_t* k_pool, uint8_t* v_pool, float* k_scale,
+                                  float* v_scale, int32_t num_blocks, int32_t* status,
+                                  kvs_stream stream);
+
 /* Copy whole blocks src[i] -> dst[i] in both pools (the copy of
  * copy-on-write; Ultralytics glossary "PagedAttention", section "Block
  * sharing between sequences").  src, dst: device int32 [count]. */
@@ -416,6 +442,21 @@ kvs_status kvs_evict_place(const kvs_bf16* k_new, const kvs_bf16* v_new, kvs_bf1
  * each chunk's maxima; needs no initialisation). */
 size_t kvs_decode_scores_workspace_size(int32_t n_items, int32_t h_q, int32_t h_kv,
                                         int32_t max_slots);
+
+/* kvs_paged_decode over FP8 pools (layout and quantisation as
+ * kvs_compact_blocks_fp8; d = 128 only).  The appended k_new / v_new rows
+ * are quantised the same way into slot lens[i] (codes and scales).  The
+ * result is the attention over the stored values e4m3(code) * s with q and
+ * the probabilities rounded to fp16 (fp32 accumulation): q values must lie
+ * in fp16's range.  Workspace, status and every other argument as
+ * kvs_paged_decode. */
+kvs_status kvs_paged_decode_fp8(const kvs_bf16* q, const kvs_bf16* k_new, const kvs_bf16* v_new,
+                                uint8_t* k_pool, uint8_t* v_pool, float* k_scale, float* v_scale,
+                                int32_t num_blocks, int32_t* block_tables, int32_t max_blocks,
+                                const int32_t* table_patch, const int32_t* lens,
+                                int32_t* lens_next, int32_t batch, int32_t h_q, int32_t h_kv,
+                                int32_t d, float scale, kvs_bf16* out, void* workspace,
+                                size_t workspace_bytes, int32_t* status, kvs_stream stream);
 
 /* kvs_paged_decode that also writes every attended slot's logit, log2-scaled
  * (scale * log2(e) * q_g . k_j), to logits [batch][h_kv][G][logit_ld] fp32 at

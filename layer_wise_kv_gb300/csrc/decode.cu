@@ -40,6 +40,7 @@
 
 #include <mutex>
 
+#include "fp8.cuh"
 #include "host_common.h"
 #include "ptx.cuh"
 #include "tma_host.h"
@@ -78,17 +79,25 @@ struct DecodeParams {
   float* logits;   // optional: [batch][h_kv][G][logit_ld] fp32, log2-scaled logits
   int logit_ld;
   float* lse;      // with logits: [batch][h_q] fp32, log2 of each head's softmax denominator
+  float* k_scale;  // FP8 pools: per-row scales [num_blocks][h_kv][16]
+  float* v_scale;
   int32_t* status;
   int batch, max_blocks, num_blocks, h_q, h_kv, group, append, n_stages;
   int q_bytes, q_stride, q_off, bar_off, idx_off;
   float scale_log2;
 };
 
-template <int D>
+// A stage: one head's K block then its V block (bf16: 16 x d each, as D/64
+// TMA boxes; FP8: 16 x d codes and the transposed V codes, then the 16 K and
+// 16 V row scales).
+template <int D, bool kF8 = false>
 struct DecodeLayout {
   static constexpr int kBoxBytes = KVS_BLOCK_TOKENS * 128;       // 16 rows x 64 bf16
-  static constexpr int kBlockBytes = KVS_BLOCK_TOKENS * D * 2;   // one head's K (or V) block
-  static constexpr int kStageBytes = 2 * kBlockBytes;
+  static constexpr int kBlockBytes = KVS_BLOCK_TOKENS * D * (kF8 ? 1 : 2);
+  static constexpr int kScaleOff = 2 * kBlockBytes;
+  static constexpr int kStageBytes = 2 * kBlockBytes + (kF8 ? 2 * KVS_BLOCK_TOKENS * 4 : 0);
+  static_assert(kStageBytes % 16 == 0 && kScaleOff % 16 == 0 && kBoxBytes % 1024 == 0,
+                "stages, scale rows and TMA boxes keep their alignment");
 };
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
@@ -109,6 +118,15 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
                                          uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma16816_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                             uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
@@ -198,11 +216,21 @@ __device__ __forceinline__ int fetch_chunk(const Piece& x, int base, int lane,
   return pb;
 }
 
-template <int D, int NT, bool kLogits>
+// kF8: the pools hold FP8 codes and row scales (layout in fp8.cuh; d = 128).
+// Each block's K and V codes and scales arrive by linear bulk copies; K and V
+// fragments are 4-byte shared-memory loads turned into f16 pairs (exact), the
+// products run on the f16 form of the same MMA, the K scales multiply the
+// logits and the V scales the value fragments (f16).  So that K and V need
+// no byte transposes, the MMA's token order inside a block is permuted: row
+// rho of S^T (and k-slot rho of P^T V) is token tau(rho) = 4 (rho/2 % 4) +
+// rho % 2 + 2 (rho / 8), and q's d order follows the order of the K bytes a
+// thread holds.
+template <int D, int NT, bool kLogits, bool kF8 = false>
 __global__ void __launch_bounds__(kDecThreads, 1)
 paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
                     const __grid_constant__ CUtensorMap v_map, const DecodeParams p) {
-  using L = DecodeLayout<D>;
+  static_assert(!kF8 || (D == 128 && !kLogits), "FP8 pools: d = 128, no logits output");
+  using L = DecodeLayout<D, kF8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -220,8 +248,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
   // grid's completion (and the visibility of its writes) before reading
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {
-    tma_prefetch_desc(&k_map);
-    tma_prefetch_desc(&v_map);
+    if constexpr (!kF8) {
+      tma_prefetch_desc(&k_map);
+      tma_prefetch_desc(&v_map);
+    }
     for (int i = 0; i < kWarps * NS; ++i) mbar_init(reinterpret_cast<uint64_t*>(smem + p.bar_off) + i, 1);
     fence_mbar_init();
   }
@@ -280,10 +310,21 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
       uint8_t* st = my_stages + s * L::kStageBytes;
       mbar_arrive_expect_tx(&my_full[s], L::kStageBytes + (j == 0 ? p.q_bytes : 0));
       const int row = (pb * p.h_kv + x.h) * KVS_BLOCK_TOKENS;
+      if constexpr (kF8) {
+        const int64_t off = static_cast<int64_t>(row) * D;
+        bulk_load(st, reinterpret_cast<const uint8_t*>(p.k_pool) + off, L::kBlockBytes,
+                  &my_full[s]);
+        bulk_load(st + L::kBlockBytes, reinterpret_cast<const uint8_t*>(p.v_pool) + off,
+                  L::kBlockBytes, &my_full[s]);
+        bulk_load(st + L::kScaleOff, p.k_scale + row, KVS_BLOCK_TOKENS * 4, &my_full[s]);
+        bulk_load(st + L::kScaleOff + KVS_BLOCK_TOKENS * 4, p.v_scale + row,
+                  KVS_BLOCK_TOKENS * 4, &my_full[s]);
+      } else {
 #pragma unroll
-      for (int b = 0; b < D / 64; ++b) {
-        tma_load_2d(st + b * L::kBoxBytes, &k_map, &my_full[s], b * 64, row);
-        tma_load_2d(st + L::kBlockBytes + b * L::kBoxBytes, &v_map, &my_full[s], b * 64, row);
+        for (int b = 0; b < D / 64; ++b) {
+          tma_load_2d(st + b * L::kBoxBytes, &k_map, &my_full[s], b * 64, row);
+          tma_load_2d(st + L::kBlockBytes + b * L::kBoxBytes, &v_map, &my_full[s], b * 64, row);
+        }
       }
       if (j == 0)
         bulk_load(my_q + qpar * p.q_stride,
@@ -345,9 +386,20 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             const int hd = nt * 8 + (lane >> 2);
-            const int off = hd * D * 2 + (ks * 16 + (lane & 3) * 2) * 2;
-            qb[ks][nt][0] = hd < G ? *reinterpret_cast<const uint32_t*>(qs + off) : 0u;
-            qb[ks][nt][1] = hd < G ? *reinterpret_cast<const uint32_t*>(qs + off + 16) : 0u;
+            if constexpr (kF8) {
+              // k-slots 2t, 2t+1 / 2t+8, 2t+9 of step ks are d = base + 0, 1 / 2, 3
+              const int t = lane & 3;
+              const int base = ks < 4 ? 16 * t + 4 * ks : 64 + 16 * t + 4 * (ks - 4);
+              const int off = (hd * D + base) * 2;
+              qb[ks][nt][0] =
+                  hd < G ? bf16x2_to_f16x2(*reinterpret_cast<const uint32_t*>(qs + off)) : 0u;
+              qb[ks][nt][1] =
+                  hd < G ? bf16x2_to_f16x2(*reinterpret_cast<const uint32_t*>(qs + off + 4)) : 0u;
+            } else {
+              const int off = hd * D * 2 + (ks * 16 + (lane & 3) * 2) * 2;
+              qb[ks][nt][0] = hd < G ? *reinterpret_cast<const uint32_t*>(qs + off) : 0u;
+              qb[ks][nt][1] = hd < G ? *reinterpret_cast<const uint32_t*>(qs + off + 16) : 0u;
+            }
           }
       }
       const uint32_t kst = stages_u32 + s * L::kStageBytes;
@@ -362,8 +414,47 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
         const int pb = (p.patch != nullptr && p.patch[cur.item] >= 0)
                            ? p.patch[cur.item]
                            : p.tables[static_cast<int64_t>(cur.item) * p.max_blocks + lb];
+        if constexpr (kF8) {
+          // quantise the new rows (lane l holds d = 4l .. 4l+3) into the stage and the pool
+          const int64_t nrow = (static_cast<int64_t>(cur.item) * p.h_kv + cur.h) * D + 4 * lane;
+          const uint2 kw = __ldg(reinterpret_cast<const uint2*>(p.k_new + nrow));
+          const uint2 vw = __ldg(reinterpret_cast<const uint2*>(p.v_new + nrow));
+          const float k0 = bf16_lo(kw.x), k1 = bf16_hi(kw.x), k2 = bf16_lo(kw.y), k3 = bf16_hi(kw.y);
+          const float v0 = bf16_lo(vw.x), v1 = bf16_hi(vw.x), v2 = bf16_lo(vw.y), v3 = bf16_hi(vw.y);
+          const float sk = f8_row_scale(
+              warp_max(fmaxf(fmaxf(fabsf(k0), fabsf(k1)), fmaxf(fabsf(k2), fabsf(k3)))));
+          const float sv = f8_row_scale(
+              warp_max(fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)))));
+          const uint32_t kc = f8_quant4(k0, k1, k2, k3, sk);
+          const uint32_t vc = f8_quant4(v0, v1, v2, v3, sv);
+          uint8_t* st = my_stages + s * L::kStageBytes;
+          const int ko = f8_k_off(slot, 4 * lane);
+          *reinterpret_cast<uint32_t*>(st + ko) = kc;
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            st[L::kBlockBytes + (4 * lane + i) * KVS_BLOCK_TOKENS + slot] =
+                static_cast<uint8_t>(vc >> (8 * i));
+          if (lane == 0) {
+            reinterpret_cast<float*>(st + L::kScaleOff)[slot] = sk;
+            reinterpret_cast<float*>(st + L::kScaleOff)[KVS_BLOCK_TOKENS + slot] = sv;
+          }
+          if (pb >= 0 && pb < p.num_blocks) {
+            const int64_t row = (static_cast<int64_t>(pb) * p.h_kv + cur.h) * KVS_BLOCK_TOKENS;
+            uint8_t* kp = reinterpret_cast<uint8_t*>(p.k_pool) + row * D;
+            uint8_t* vp = reinterpret_cast<uint8_t*>(p.v_pool) + row * D;
+            *reinterpret_cast<uint32_t*>(kp + ko) = kc;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              vp[(4 * lane + i) * KVS_BLOCK_TOKENS + slot] = static_cast<uint8_t>(vc >> (8 * i));
+            if (lane == 0) {
+              p.k_scale[row + slot] = sk;
+              p.v_scale[row + slot] = sv;
+            }
+          }
+          fence_proxy_async_smem();  // before a later bulk refill of this stage
+        }
         const int per = D / 8;  // 16-byte chunks per row
-        if (lane < 2 * per) {
+        if (!kF8 && lane < 2 * per) {
           const bool is_v = lane >= per;
           const int c = is_v ? lane - per : lane;
           const uint4* src = reinterpret_cast<const uint4*>(
@@ -387,9 +478,29 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
         const int valid = cur.len - tok0;
         const int per = D / 8;
         uint8_t* vs = my_stages + s * L::kStageBytes + L::kBlockBytes;
-        for (int idx = lane; idx < (KVS_BLOCK_TOKENS - valid) * per; idx += 32) {
-          const int r = valid + idx / per;
-          *reinterpret_cast<uint4*>(vs + sw_off(r, idx % per)) = make_uint4(0u, 0u, 0u, 0u);
+        if constexpr (kF8) {
+          // transposed V: keep the first `valid` bytes of each of the d rows
+          uint32_t m[4];
+#pragma unroll
+          for (int w4 = 0; w4 < 4; ++w4) {
+            const int nb = min(4, max(0, valid - 4 * w4));
+            m[w4] = nb >= 4 ? 0xFFFFFFFFu : ((1u << (8 * nb)) - 1u);
+          }
+#pragma unroll
+          for (int i = 0; i < D / 32; ++i) {
+            uint4* r = reinterpret_cast<uint4*>(vs + ((D / 32) * lane + i) * KVS_BLOCK_TOKENS);
+            uint4 x = *r;
+            x.x &= m[0];
+            x.y &= m[1];
+            x.z &= m[2];
+            x.w &= m[3];
+            *r = x;
+          }
+        } else {
+          for (int idx = lane; idx < (KVS_BLOCK_TOKENS - valid) * per; idx += 32) {
+            const int r = valid + idx / per;
+            *reinterpret_cast<uint4*>(vs + sw_off(r, idx % per)) = make_uint4(0u, 0u, 0u, 0u);
+          }
         }
         fence_proxy_async_smem();  // before a later TMA refill of this stage
         __syncwarp();
@@ -402,7 +513,31 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) sa[nt][e] = sb[nt][e] = 0.f;
-      {
+      // the block tokens of this thread's S^T rows (g = lane / 4 and g + 8)
+      const int tr0 = kF8 ? (((lane >> 3) << 2) | ((lane >> 2) & 1)) : (lane >> 2);
+      const int tr1 = kF8 ? tr0 + 2 : tr0 + 8;
+      if constexpr (kF8) {
+        // K rows tr0, tr1: this thread's 16-byte chunks t and t + 4 of each
+        const int t = lane & 3, sw = (tr0 & 1) << 2;
+        const uint8_t* kt = my_stages + s * L::kStageBytes;
+        const uint4 c00 = *reinterpret_cast<const uint4*>(kt + tr0 * D + ((t ^ sw) << 4));
+        const uint4 c01 = *reinterpret_cast<const uint4*>(kt + tr0 * D + (((t + 4) ^ sw) << 4));
+        const uint4 c10 = *reinterpret_cast<const uint4*>(kt + tr1 * D + ((t ^ sw) << 4));
+        const uint4 c11 = *reinterpret_cast<const uint4*>(kt + tr1 * D + (((t + 4) ^ sw) << 4));
+        const uint32_t w0[8] = {c00.x, c00.y, c00.z, c00.w, c01.x, c01.y, c01.z, c01.w};
+        const uint32_t w1[8] = {c10.x, c10.y, c10.z, c10.w, c11.x, c11.y, c11.z, c11.w};
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          uint32_t a[4];
+          e4m3x4_to_f16x2(w0[ks], a[0], a[2]);
+          e4m3x4_to_f16x2(w1[ks], a[1], a[3]);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            if (ks & 1) mma16816_f16(sb[nt], a, qb[ks][nt][0], qb[ks][nt][1]);
+            else mma16816_f16(sa[nt], a, qb[ks][nt][0], qb[ks][nt][1]);
+          }
+        }
+      } else {
         const int mi = lane >> 3, rr = lane & 7;
         const int tok = (mi & 1) * 8 + rr;
 #pragma unroll
@@ -418,8 +553,15 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
       }
       // online softmax per head (log2 domain): a head's 16 scores sit in the 8
       // lanes with the same lane % 4 (rows lane/4 and lane/4 + 8)
-      const bool v0 = tok0 + (lane >> 2) < cur.len;
-      const bool v1 = tok0 + (lane >> 2) + 8 < cur.len;
+      const bool v0 = tok0 + tr0 < cur.len;
+      const bool v1 = tok0 + tr1 < cur.len;
+      float sc0 = p.scale_log2, sc1 = p.scale_log2;
+      if constexpr (kF8) {
+        const float* sks = reinterpret_cast<const float*>(my_stages + s * L::kStageBytes +
+                                                          L::kScaleOff);
+        sc0 *= sks[tr0];
+        sc1 *= sks[tr1];
+      }
       uint32_t pb0[NT], pb1[NT];
       bool rescale = false;
       float al[NT][2];
@@ -428,17 +570,17 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
         float s0[2], s1[2], mx[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          s0[e] = v0 ? (sa[nt][e] + sb[nt][e]) * p.scale_log2 : -INFINITY;
-          s1[e] = v1 ? (sa[nt][2 + e] + sb[nt][2 + e]) * p.scale_log2 : -INFINITY;
+          s0[e] = v0 ? (sa[nt][e] + sb[nt][e]) * sc0 : -INFINITY;
+          s1[e] = v1 ? (sa[nt][2 + e] + sb[nt][2 + e]) * sc1 : -INFINITY;
           if constexpr (kLogits) {
             // every slot's logit for the score update (head hd, slots tok0 + lane/4, +8)
             const int hd = nt * 8 + (lane & 3) * 2 + e;
             if (hd < G) {
               float* lg = p.logits +
                           ((static_cast<int64_t>(cur.item) * p.h_kv + cur.h) * G + hd) * p.logit_ld;
-              const int t0 = tok0 + (lane >> 2);
+              const int t0 = tok0 + tr0, t1 = tok0 + tr1;
               if (v0 && t0 < p.logit_ld) lg[t0] = s0[e];
-              if (v1 && t0 + 8 < p.logit_ld) lg[t0 + 8] = s1[e];
+              if (v1 && t1 < p.logit_ld) lg[t1] = s1[e];
             }
           }
           mx[e] = fmaxf(s0[e], s1[e]);
@@ -454,8 +596,13 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
           l_h[nt][e] = l_h[nt][e] * al[nt][e] + (s0[e] + s1[e]);
         }
         // P^T (tokens x heads) -> B fragments (k = tokens, n = heads)
-        pb0[nt] = movmatrix_t(pack_bf16x2(s0[0], s0[1]));
-        pb1[nt] = movmatrix_t(pack_bf16x2(s1[0], s1[1]));
+        if constexpr (kF8) {
+          pb0[nt] = movmatrix_t(pack_f16x2(s0[0], s0[1]));
+          pb1[nt] = movmatrix_t(pack_f16x2(s1[0], s1[1]));
+        } else {
+          pb0[nt] = movmatrix_t(pack_bf16x2(s0[0], s0[1]));
+          pb1[nt] = movmatrix_t(pack_bf16x2(s1[0], s1[1]));
+        }
       }
       if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
@@ -469,7 +616,33 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
           }
       }
       // O^T += V^T P^T: A = V^T (m = d, k = tokens) by ldmatrix.trans
-      {
+      if constexpr (kF8) {
+        // transposed V codes: row d, bytes 4t .. 4t+3 = tokens of k-slots 2t, 2t+1, 2t+8, 2t+9
+        const int gq = lane >> 2, t = lane & 3;
+        const uint8_t* vt = my_stages + s * L::kStageBytes + L::kBlockBytes;
+        const float* svs = reinterpret_cast<const float*>(my_stages + s * L::kStageBytes +
+                                                          L::kScaleOff) + KVS_BLOCK_TOKENS;
+        float sv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sv[i] = tok0 + 4 * t + i < cur.len ? svs[4 * t + i] : 0.f;
+        const uint32_t sc_lo = pack_f16x2(sv[0], sv[1]), sc_hi = pack_f16x2(sv[2], sv[3]);
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+          const uint32_t x0 =
+              *reinterpret_cast<const uint32_t*>(vt + (mt * 16 + gq) * KVS_BLOCK_TOKENS + 4 * t);
+          const uint32_t x1 = *reinterpret_cast<const uint32_t*>(
+              vt + (mt * 16 + gq + 8) * KVS_BLOCK_TOKENS + 4 * t);
+          uint32_t a[4];
+          e4m3x4_to_f16x2(x0, a[0], a[2]);
+          e4m3x4_to_f16x2(x1, a[1], a[3]);
+          a[0] = hmul2(a[0], sc_lo);
+          a[1] = hmul2(a[1], sc_lo);
+          a[2] = hmul2(a[2], sc_hi);
+          a[3] = hmul2(a[3], sc_hi);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma16816_f16(o[mt][nt], a, pb0[nt], pb1[nt]);
+        }
+      } else {
         const int mi = lane >> 3, rr = lane & 7;
         const int tok = (mi >> 1) * 8 + rr;
 #pragma unroll
@@ -744,9 +917,9 @@ int sm_count_dec() {
 constexpr int kSmemLimit = 232448;
 
 // Shared-memory plan for a launch; returns the bytes, 0 if it cannot fit.
-template <int D>
+template <int D, bool kF8>
 size_t plan_smem(DecodeParams& prm) {
-  using L = DecodeLayout<D>;
+  using L = DecodeLayout<D, kF8>;
   prm.q_bytes = prm.group * D * 2;
   prm.q_stride = (prm.q_bytes + 127) / 128 * 128;
   for (int ns = kMaxStages; ns >= 1; --ns) {
@@ -769,23 +942,31 @@ size_t plan_smem(DecodeParams& prm) {
   return 0;
 }
 
-template <int D, int NT>
+template <int D, int NT, bool kF8 = false>
 kvs_status launch_decode(DecodeParams& prm, const CUtensorMap& km, const CUtensorMap& vm,
                          cudaStream_t stream) {
-  const size_t smem = plan_smem<D>(prm);
+  const size_t smem = plan_smem<D, kF8>(prm);
   if (smem == 0) return fail(KVS_ERR_UNSUPPORTED, "kvs_paged_decode: shared-memory plan does not fit");
   static bool configured = false;
   if (!configured) {
-    KVS_CUDA(cudaFuncSetAttribute(paged_decode_kernel<D, NT, false>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit),
-             "kvs_paged_decode: raising the shared-memory limit");
-    KVS_CUDA(cudaFuncSetAttribute(paged_decode_kernel<D, NT, true>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit),
-             "kvs_paged_decode: raising the shared-memory limit");
+    if constexpr (kF8) {
+      KVS_CUDA(cudaFuncSetAttribute(paged_decode_kernel<D, NT, false, true>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit),
+               "kvs_paged_decode: raising the shared-memory limit");
+    } else {
+      KVS_CUDA(cudaFuncSetAttribute(paged_decode_kernel<D, NT, false>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit),
+               "kvs_paged_decode: raising the shared-memory limit");
+      KVS_CUDA(cudaFuncSetAttribute(paged_decode_kernel<D, NT, true>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit),
+               "kvs_paged_decode: raising the shared-memory limit");
+    }
     configured = true;
   }
   const int grid = sm_count_dec() < kMaxGrid ? sm_count_dec() : kMaxGrid;
-  if (prm.logits != nullptr)
+  if constexpr (kF8)
+    paged_decode_kernel<D, NT, false, true><<<grid, kDecThreads, smem, stream>>>(km, vm, prm);
+  else if (prm.logits != nullptr)
     paged_decode_kernel<D, NT, true><<<grid, kDecThreads, smem, stream>>>(km, vm, prm);
   else
     paged_decode_kernel<D, NT, false><<<grid, kDecThreads, smem, stream>>>(km, vm, prm);
@@ -832,7 +1013,9 @@ kvs_status paged_decode_impl(const kvs_bf16* q, const kvs_bf16* k_new, const kvs
                              const int32_t* lens, int32_t* lens_next, int32_t batch, int32_t h_q,
                              int32_t h_kv, int32_t d, float scale, kvs_bf16* out, void* workspace,
                              size_t workspace_bytes, int32_t* status, kvs_stream stream,
-                             float* logits, int32_t logit_ld, float* lse) {
+                             float* logits, int32_t logit_ld, float* lse,
+                             float* k_scale = nullptr, float* v_scale = nullptr,
+                             bool fp8 = false) {
   KVS_REQUIRE(batch >= 0, "kvs_paged_decode: negative batch");
   if (batch == 0) return KVS_OK;
   KVS_REQUIRE(q && k_pool && v_pool && block_tables && lens && out && workspace,
@@ -861,9 +1044,15 @@ kvs_status paged_decode_impl(const kvs_bf16* q, const kvs_bf16* k_new, const kvs
   KVS_REQUIRE(workspace_bytes >= need, "kvs_paged_decode: workspace %zu bytes < %zu needed",
               workspace_bytes, need);
   static thread_local kvs::MapCache kc, vc;
-  if (!kvs::pool_map(kc, k_pool, num_blocks, h_kv, d) ||
-      !kvs::pool_map(vc, v_pool, num_blocks, h_kv, d))
+  if (fp8) {
+    KVS_SUPPORTED(d == 128, "kvs_paged_decode_fp8: d = %d (supported: 128)", d);
+    KVS_REQUIRE(k_scale && v_scale && (reinterpret_cast<uintptr_t>(k_scale) & 15) == 0 &&
+                    (reinterpret_cast<uintptr_t>(v_scale) & 15) == 0,
+                "kvs_paged_decode_fp8: scales must be non-NULL and 16-byte aligned");
+  } else if (!kvs::pool_map(kc, k_pool, num_blocks, h_kv, d) ||
+             !kvs::pool_map(vc, v_pool, num_blocks, h_kv, d)) {
     return KVS_ERR_CUDA;
+  }
 
   kvs::DecodeParams prm;
   prm.q = q;
@@ -880,6 +1069,8 @@ kvs_status paged_decode_impl(const kvs_bf16* q, const kvs_bf16* k_new, const kvs
   prm.logits = logits;
   prm.logit_ld = logit_ld;
   prm.lse = lse;
+  prm.k_scale = k_scale;
+  prm.v_scale = v_scale;
   prm.status = status;
   prm.batch = batch;
   prm.max_blocks = max_blocks;
@@ -890,6 +1081,11 @@ kvs_status paged_decode_impl(const kvs_bf16* q, const kvs_bf16* k_new, const kvs
   prm.append = k_new != nullptr ? 1 : 0;
   prm.scale_log2 = scale * kvs::kLog2e;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (fp8) {
+    static const CUtensorMap unused = {};  // FP8 blocks arrive by linear bulk copies
+    if (G <= 8) return kvs::launch_decode<128, 1, true>(prm, unused, unused, st);
+    return kvs::launch_decode<128, 2, true>(prm, unused, unused, st);
+  }
   if (G <= 8) {
     if (d == 128) return kvs::launch_decode<128, 1>(prm, kc.map, vc.map, st);
     return kvs::launch_decode<64, 1>(prm, kc.map, vc.map, st);
@@ -911,6 +1107,20 @@ kvs_status kvs_paged_decode(const kvs_bf16* q, const kvs_bf16* k_new, const kvs_
   return paged_decode_impl(q, k_new, v_new, k_pool, v_pool, num_blocks, block_tables, max_blocks,
                            table_patch, lens, lens_next, batch, h_q, h_kv, d, scale, out,
                            workspace, workspace_bytes, status, stream, nullptr, 0, nullptr);
+}
+
+kvs_status kvs_paged_decode_fp8(const kvs_bf16* q, const kvs_bf16* k_new, const kvs_bf16* v_new,
+                                uint8_t* k_pool, uint8_t* v_pool, float* k_scale, float* v_scale,
+                                int32_t num_blocks, int32_t* block_tables, int32_t max_blocks,
+                                const int32_t* table_patch, const int32_t* lens,
+                                int32_t* lens_next, int32_t batch, int32_t h_q, int32_t h_kv,
+                                int32_t d, float scale, kvs_bf16* out, void* workspace,
+                                size_t workspace_bytes, int32_t* status, kvs_stream stream) {
+  return paged_decode_impl(q, k_new, v_new, reinterpret_cast<kvs_bf16*>(k_pool),
+                           reinterpret_cast<kvs_bf16*>(v_pool), num_blocks, block_tables,
+                           max_blocks, table_patch, lens, lens_next, batch, h_q, h_kv, d, scale,
+                           out, workspace, workspace_bytes, status, stream, nullptr, 0, nullptr,
+                           k_scale, v_scale, true);
 }
 
 kvs_status kvs_paged_decode_logits(const kvs_bf16* q, const kvs_bf16* k_new,

@@ -69,6 +69,10 @@ _SIGS = {
                                _VP, _VP, _VP, _VP]),
     "kvs_compact_blocks": (_I32, [_VP, _VP, _VP, _I32, _I64, _I32, _I32, _VP, _VP, _VP, _VP,
                                   _I32, _VP, _VP]),
+    "kvs_compact_blocks_fp8": (_I32, [_VP, _VP, _VP, _I32, _I64, _I32, _I32, _VP, _VP, _VP, _VP,
+                                      _VP, _VP, _I32, _VP, _VP]),
+    "kvs_paged_decode_fp8": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I32, _VP, _I32, _VP, _VP,
+                                    _VP, _I32, _I32, _I32, _I32, _F32, _VP, _VP, _SZ, _VP, _VP]),
     "kvs_copy_blocks": (_I32, [_VP, _VP, _I32, _VP, _VP, _I32, _I32, _I32, _VP, _VP]),
     "kvs_paged_decode_workspace_size": (_SZ, [_I32, _I32, _I32, _I32]),
     "kvs_workspace_zero": (_I32, [_VP, _SZ, _VP]),
@@ -216,6 +220,35 @@ def kvs_compact_blocks(k, v, items, n_items, total_rows, h_kv, d, kept_idx, bloc
         int(total_rows), h_kv, d, _dev(kept_idx, "i32", "kept_idx"),
         _dev(block_tables, "i32", "block_tables"), _dev(k_pool, "bf16", "k_pool"),
         _dev(v_pool, "bf16", "v_pool"), num_blocks,
+        None if status is None else _dev(status, "i32", "status"), _stream(stream)))
+
+
+def kvs_compact_blocks_fp8(k, v, items, n_items, total_rows, h_kv, d, kept_idx, block_tables,
+                           k_pool, v_pool, k_scale, v_scale, num_blocks, status=None,
+                           stream=None):
+    """kvs_compact_blocks into FP8 pools: k_pool, v_pool uint8 [num_blocks][h_kv][16 * d] (V
+    transposed per block and head), k_scale, v_scale float32 [num_blocks][h_kv][16]."""
+    _check(library().kvs_compact_blocks_fp8(
+        _dev(k, "bf16", "k"), _dev(v, "bf16", "v"), _dev(items, "u8", "items"), n_items,
+        int(total_rows), h_kv, d, _dev(kept_idx, "i32", "kept_idx"),
+        _dev(block_tables, "i32", "block_tables"), _dev(k_pool, "u8", "k_pool"),
+        _dev(v_pool, "u8", "v_pool"), _dev(k_scale, "f32", "k_scale"),
+        _dev(v_scale, "f32", "v_scale"), num_blocks,
+        None if status is None else _dev(status, "i32", "status"), _stream(stream)))
+
+
+def kvs_paged_decode_fp8(q, k_new, v_new, k_pool, v_pool, k_scale, v_scale, num_blocks,
+                         block_tables, max_blocks, table_patch, lens, lens_next, batch, h_q, h_kv,
+                         d, scale, out, workspace, workspace_bytes, status=None, stream=None):
+    _check(library().kvs_paged_decode_fp8(
+        _dev(q, "bf16", "q"), None if k_new is None else _dev(k_new, "bf16", "k_new"),
+        None if v_new is None else _dev(v_new, "bf16", "v_new"), _dev(k_pool, "u8", "k_pool"),
+        _dev(v_pool, "u8", "v_pool"), _dev(k_scale, "f32", "k_scale"),
+        _dev(v_scale, "f32", "v_scale"), num_blocks, _dev(block_tables, "i32", "block_tables"),
+        max_blocks, None if table_patch is None else _dev(table_patch, "i32", "table_patch"),
+        _dev(lens, "i32", "lens"), None if lens_next is None else _dev(lens_next, "i32", "lens_next"),
+        batch, h_q, h_kv, d, float(scale), _dev(out, "bf16", "out"),
+        _dev(workspace, "u8", "workspace"), workspace_bytes,
         None if status is None else _dev(status, "i32", "status"), _stream(stream)))
 
 

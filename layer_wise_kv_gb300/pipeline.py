@@ -77,20 +77,36 @@ class Engine:
     """Device pools, the host block allocator and scratch for one workload."""
 
     def __init__(self, shape: Shape, num_blocks: int, device="cuda", initial_free=None,
-                 poison=False):
-        """poison: fill the pools with bf16 NaN patterns (0xFFFF) so that any
-        read of an unwritten slot shows up in the outputs (tests)."""
+                 poison=False, kv_dtype: str = "bf16"):
+        """poison: fill the pools with NaN patterns (bf16 0xFFFF, e4m3 0xFF)
+        so that any read of an unwritten slot shows up in the outputs (tests).
+        kv_dtype "fp8": the pools hold e4m3 codes with per-row fp32 scales
+        (k_scale, v_scale; layout of kvs_compact_blocks_fp8, d = 128); the
+        prefill compacts into them and DecodeBatch decodes from them."""
         self.shape = shape
         self.device = torch.device(device)
         self.num_blocks = num_blocks
         self.alloc = kvs.BlockAllocator(num_blocks, initial_free)
         s = shape
-        self.k_pool = torch.empty((num_blocks, s.h_kv, BLOCK, s.d), dtype=torch.bfloat16,
-                                  device=self.device)
+        if kv_dtype not in ("bf16", "fp8"):
+            raise ValueError("kv_dtype is 'bf16' or 'fp8'")
+        self.kv_fp8 = kv_dtype == "fp8"
+        self.k_scale = self.v_scale = None
+        if self.kv_fp8:
+            if s.d != 128:
+                raise ValueError("FP8 pools need d = 128")
+            self.k_pool = torch.empty((num_blocks, s.h_kv, BLOCK * s.d), dtype=torch.uint8,
+                                      device=self.device)
+            self.k_scale = torch.zeros((num_blocks, s.h_kv, BLOCK), dtype=torch.float32,
+                                       device=self.device)
+            self.v_scale = torch.zeros_like(self.k_scale)
+        else:
+            self.k_pool = torch.empty((num_blocks, s.h_kv, BLOCK, s.d), dtype=torch.bfloat16,
+                                      device=self.device)
         self.v_pool = torch.empty_like(self.k_pool)
         if poison:
-            self.k_pool.view(torch.int16).fill_(-1)
-            self.v_pool.view(torch.int16).fill_(-1)
+            self.k_pool.view(torch.uint8).fill_(0xFF)
+            self.v_pool.view(torch.uint8).fill_(0xFF)
         self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
         self._plans = {}
 
@@ -284,9 +300,15 @@ class Engine:
 
         k_all = _stacked(k_layers)
         v_all = _stacked(v_layers)
-        kvs.kvs_compact_blocks(k_all, v_all, plan["comp_d"], B * L, plan["total_rows"], s.h_kv,
-                               s.d, kept, tab_d, self.k_pool, self.v_pool, self.num_blocks,
-                               self.status, stream)
+        if self.kv_fp8:
+            kvs.kvs_compact_blocks_fp8(k_all, v_all, plan["comp_d"], B * L, plan["total_rows"],
+                                       s.h_kv, s.d, kept, tab_d, self.k_pool, self.v_pool,
+                                       self.k_scale, self.v_scale, self.num_blocks, self.status,
+                                       stream)
+        else:
+            kvs.kvs_compact_blocks(k_all, v_all, plan["comp_d"], B * L, plan["total_rows"],
+                                   s.h_kv, s.d, kept, tab_d, self.k_pool, self.v_pool,
+                                   self.num_blocks, self.status, stream)
         idx_off = plan["idx_off"]
         res = PrefillResult(tables=tables, k_eff=keff, kept_idx=kept, idx_off=idx_off,
                             scores=scores)
@@ -487,6 +509,8 @@ class DecodeBatch:
         the step's inputs from the fixed buffers self.q_in, self.k_in,
         self.v_in (step() copies other tensors into them) and the patch from
         two pinned buffers, one per direction."""
+        if self.eng.kv_fp8:
+            raise NotImplementedError("graph capture of the FP8 decode step")
         s, dev = self.eng.shape, self.eng.device
         n = self.n_items
         self.q_in = torch.zeros((n, s.h_q, s.d), dtype=torch.bfloat16, device=dev)
@@ -554,7 +578,7 @@ class DecodeBatch:
         timing: optional list receiving a (start, end) event pair around the
         decode kernel.  Without graphs or timing, the step is one native call
         (kvs_decode_step: host preparation, uploads and decode)."""
-        if self._graphs is None and timing is None:
+        if self._graphs is None and timing is None and not self.eng.kv_fp8:
             return self._native_step(q, k_new, v_new, stream)
         eng, s = self.eng, self.eng.shape
         n = self.n_items
@@ -600,6 +624,8 @@ class DecodeBatch:
             with torch.cuda.stream(cur_stream):
                 self.patch_d.copy_(patch_t, non_blocking=True)
                 patch_arg = self.patch_d
+                if n_cow and eng.kv_fp8:
+                    raise NotImplementedError("copy-on-write of shared FP8 blocks")
                 if n_cow:
                     cow = self._cow_np[slot]
                     cow[:n_cow] = self.cow_src[:n_cow]
@@ -617,10 +643,18 @@ class DecodeBatch:
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(cur_stream)
-        kvs.kvs_paged_decode(q, k_new, v_new, eng.k_pool, eng.v_pool, eng.num_blocks,
-                             self.tables_d, self.max_blocks, patch_arg, self.lens_d[self.cur],
-                             self.lens_d[nxt], n, s.h_q, s.h_kv, s.d, s.scale,
-                             self.out, self.ws, self.ws_bytes, eng.status, cur_stream)
+        if eng.kv_fp8:
+            kvs.kvs_paged_decode_fp8(q, k_new, v_new, eng.k_pool, eng.v_pool, eng.k_scale,
+                                     eng.v_scale, eng.num_blocks, self.tables_d, self.max_blocks,
+                                     patch_arg, self.lens_d[self.cur], self.lens_d[nxt], n,
+                                     s.h_q, s.h_kv, s.d, s.scale, self.out, self.ws,
+                                     self.ws_bytes, eng.status, cur_stream)
+        else:
+            kvs.kvs_paged_decode(q, k_new, v_new, eng.k_pool, eng.v_pool, eng.num_blocks,
+                                 self.tables_d, self.max_blocks, patch_arg,
+                                 self.lens_d[self.cur], self.lens_d[nxt], n, s.h_q, s.h_kv, s.d,
+                                 s.scale, self.out, self.ws, self.ws_bytes, eng.status,
+                                 cur_stream)
         if timing is not None:
             b.record(cur_stream)
             timing.append((a, b))
@@ -650,6 +684,8 @@ class EvictingDecode:
         (kvs_paged_decode_logits); otherwise the update recomputes the logits
         from K (kvs_decode_scores)."""
         s = eng.shape
+        if eng.kv_fp8:
+            raise NotImplementedError("decode-time replacement over FP8 pools")
         self.fused = fused
         dev = eng.device
         self.eng, self.layers = eng, list(layers)

@@ -95,6 +95,21 @@ def test_invalid_arguments_rejected_before_launch(kvs):
     assert lib.kvs_decode_scores(256, 256, 4, 256, 1, 256, 256, 256, 16, 2, 32, 6, 128, 0.1,
                                  256, 1 << 20, None, None) == kvs.KVS_ERR_INVALID  # 32 % 6 != 0
     assert kvs.kvs_decode_scores_workspace_size(2, 32, 8, 2048) == 2 * 8 * 4 * (2048 + 8) * 4
+    # FP8 pools: d = 128 only, scales required, zero work is a no-op
+    assert lib.kvs_compact_blocks_fp8(256, 256, 256, 0, 0, 8, 128, 256, 256, 256, 256, 256, 256,
+                                      4, None, None) == kvs.KVS_OK
+    assert lib.kvs_compact_blocks_fp8(256, 256, 256, 2, 64, 8, 64, 256, 256, 256, 256, 256, 256,
+                                      4, None, None) == kvs.KVS_ERR_UNSUPPORTED
+    assert lib.kvs_compact_blocks_fp8(256, 256, 256, 2, 64, 8, 128, 256, 256, 256, 256, None, 256,
+                                      4, None, None) == kvs.KVS_ERR_INVALID
+    df = [256, None, None, 256, 256, 256, 256, 4, 256, 1, None, 256, None, 2, 32, 8, 128, 0.1, 256,
+          256, 1 << 26, None, None]
+    df[16] = 64
+    assert lib.kvs_paged_decode_fp8(*df) == kvs.KVS_ERR_UNSUPPORTED
+    df[16], df[5] = 128, None
+    assert lib.kvs_paged_decode_fp8(*df) == kvs.KVS_ERR_INVALID
+    df[5], df[13] = 256, 0
+    assert lib.kvs_paged_decode_fp8(*df) == kvs.KVS_OK
     # decode that writes its logits and denominators: both buffers are required
     dl = [256, None, None, 256, 256, 4, 256, 1, None, 256, None, 0, 32, 8, 128, 0.1, 256, 256,
           1 << 20, 256, 16, 256, None, None]

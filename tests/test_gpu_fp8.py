@@ -1,0 +1,219 @@
+"""FP8 (e4m3, per-row scale) KV pools: compaction and paged decode through the
+C ABI against the oracle (oracle/fp8.py for the codes, the oracle's decode
+attention over the values the codes stand for)."""
+import numpy as np
+import pytest
+
+import oracle
+from synth import bf16_bits, bf16_to_f64
+from gpu_helpers import ABS_O, bf16_f64, dev_bf16, kvs_lib, torch
+
+pytestmark = pytest.mark.gpu
+
+D = 128
+
+
+def _randn_bits(rng, shape, scale=1.0):
+    return bf16_bits((rng.standard_normal(shape) * scale).astype(np.float32))
+
+
+# the library's FP8 pool layout (per block and KV head), written out from its
+# description: K rows token-major with the 16-byte chunks of odd rows swapped
+# (chunk c at position c ^ 4), V transposed (row = element, byte = slot)
+_K_CHUNKS_ODD = np.array([4, 5, 6, 7, 0, 1, 2, 3])
+
+
+def k_physical(kc):
+    """[..., 16, 128] codes in logical order -> the stored byte order."""
+    ph = kc.copy()
+    odd = kc[..., 1::2, :].reshape(kc.shape[:-2] + (8, 8, 16))
+    ph[..., 1::2, :] = odd[..., _K_CHUNKS_ODD, :].reshape(odd.shape[:-2] + (128,))
+    return ph
+
+
+def v_physical(vc):
+    """[..., 16, 128] codes -> [..., 128, 16]."""
+    return np.ascontiguousarray(np.swapaxes(vc, -1, -2))
+
+
+def test_pool_layout_helpers_match_the_documented_offsets():
+    rng = np.random.default_rng(0)
+    kc = rng.integers(0, 256, (16, D), dtype=np.uint8)
+    ph = k_physical(kc).reshape(-1)
+    for r in range(16):
+        for e in range(D):
+            off = r * 128 + (((e >> 4) ^ ((r & 1) << 2)) << 4) + (e & 15)
+            assert ph[off] == kc[r, e]
+    pv = v_physical(kc).reshape(-1)
+    for r in range(16):
+        for e in range(D):
+            assert pv[e * 16 + r] == kc[r, e]
+
+
+def _cuda(t):
+    return torch.from_numpy(np.ascontiguousarray(t)).cuda()
+
+
+@pytest.mark.parametrize("h_kv", [8, 2])
+def test_compact_fp8_bit_exact(h_kv):
+    """Codes and scales bit for bit against the oracle's quantiser (fp32
+    divisions, round to nearest even): ragged items, partial last blocks
+    (zero codes and scales past k_eff), blocks outside every table untouched."""
+    kvs = kvs_lib()
+    from layer_wise_kv_gb300.pipeline import _u8 as pack_items
+    rng = np.random.default_rng(21 + h_kv)
+    lens = [100, 37, 300, 1, 64]
+    keff = [64, 37, 201, 1, 48]
+    T = sum(lens)
+    # rows of very different magnitudes, one all-zero row
+    kb = bf16_bits((rng.standard_normal((T, h_kv, D)) *
+                    np.exp(rng.uniform(-6, 4, (T, h_kv, 1)))).astype(np.float32))
+    vb = _randn_bits(rng, (T, h_kv, D), 3.0)
+    kb[5, 0] = 0
+    N = 64
+    pool = oracle.BlockPool(N, free=rng.permutation(N))
+    items = np.zeros(len(lens), dtype=kvs.COMPACT_ITEM)
+    ref_kc = np.full((N, h_kv, 16, D), 0xAB, np.uint8)
+    ref_vc = ref_kc.copy()
+    ref_ks = np.full((N, h_kv, 16), -7.0, np.float32)
+    ref_vs = ref_ks.copy()
+    idx_all, tab_all = [], []
+    tok = row = ioff = toff = 0
+    for i, (n, ke) in enumerate(zip(lens, keff)):
+        idx = np.stack([np.sort(rng.choice(n, ke, replace=False)) for _ in range(h_kv)])
+        if i == 0:
+            idx[0, 3] = 5 - tok                          # the all-zero row is kept
+        table = [pool.alloc() for _ in range(oracle.blocks_for(ke))]
+        for b in table:
+            ref_kc[b] = 0
+            ref_vc[b] = 0
+            ref_ks[b] = 0
+            ref_vs[b] = 0
+        for h in range(h_kv):
+            rows_k = bf16_to_f64(kb[tok + idx[h], h]).astype(np.float32)
+            rows_v = bf16_to_f64(vb[tok + idx[h], h]).astype(np.float32)
+            ck, sk = oracle.fp8.quantize_rows_fast(rows_k)
+            cv, sv = oracle.fp8.quantize_rows_fast(rows_v)
+            for j in range(ke):
+                b, r = table[j // 16], j % 16
+                ref_kc[b, h, r], ref_ks[b, h, r] = ck[j], sk[j]
+                ref_vc[b, h, r], ref_vs[b, h, r] = cv[j], sv[j]
+        items[i] = (tok, ioff, row, n, ke, toff, 0)
+        idx_all.append(idx.reshape(-1))
+        tab_all.extend(table)
+        tok += n
+        row += ke
+        ioff += idx.size
+        toff += len(table)
+    k_pool = _cuda(np.full((N, h_kv, 16 * D), 0xAB, np.uint8))
+    v_pool = k_pool.clone()
+    k_scale = torch.full((N, h_kv, 16), -7.0, dtype=torch.float32, device="cuda")
+    v_scale = k_scale.clone()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvs.kvs_compact_blocks_fp8(dev_bf16(kb), dev_bf16(vb), pack_items(items, "cuda"), len(lens),
+                               row, h_kv, D,
+                               torch.from_numpy(np.concatenate(idx_all).astype(np.int32)).cuda(),
+                               torch.tensor(tab_all, dtype=torch.int32).cuda(), k_pool, v_pool,
+                               k_scale, v_scale, N, status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    used = np.zeros(N, bool)
+    used[tab_all] = True
+    got_k = k_pool.cpu().numpy().reshape(N, h_kv, 16, D)
+    got_v = v_pool.cpu().numpy().reshape(N, h_kv, D, 16)
+    np.testing.assert_array_equal(got_k[used], k_physical(ref_kc[used]))
+    np.testing.assert_array_equal(got_v[used], v_physical(ref_vc[used]))
+    np.testing.assert_array_equal(got_k[~used], ref_kc[~used])
+    np.testing.assert_array_equal(k_scale.cpu().numpy(), ref_ks)
+    np.testing.assert_array_equal(v_scale.cpu().numpy(), ref_vs)
+
+
+@pytest.mark.parametrize("h_q,h_kv", [(32, 8), (6, 2), (16, 1)])
+def test_paged_decode_fp8_vs_oracle(h_q, h_kv):
+    """Several decode steps with appends over FP8 pools: every step's output
+    against the oracle's decode attention over the stored values (codes times
+    scales), the appended rows' codes and scales bit for bit against the
+    oracle's quantiser, lengths and table patches as in the bf16 decode.
+    Lengths 0, 1, 15, 16, 17, 255 .. 1100: empty, partial and full blocks,
+    items split across warps and items that are one piece."""
+    kvs = kvs_lib()
+    rng = np.random.default_rng(h_q * 7 + h_kv)
+    start_lens = [0, 1, 15, 16, 17, 255, 256, 257, 700, 1100]
+    steps = 6
+    n_items = len(start_lens)
+    max_blocks = oracle.blocks_for(max(start_lens) + steps)
+    N = n_items * max_blocks + 8
+    a = kvs.BlockAllocator(N, rng.permutation(N))
+    # logical codes (NaN patterns everywhere no row was written) and scales
+    kc = np.full((N, h_kv, 16, D), 0x7F, np.uint8)
+    vc = kc.copy()
+    ks = np.full((N, h_kv, 16), np.nan, np.float32)
+    vs = ks.copy()
+    tables = np.full((n_items, max_blocks), -1, np.int32)
+    for i, L0 in enumerate(start_lens):
+        ids = a.alloc_many(oracle.blocks_for(L0))
+        tables[i, :len(ids)] = ids
+        for h in range(h_kv):
+            rk = bf16_to_f64(_randn_bits(rng, (L0, D), 2.0)).astype(np.float32)
+            rv = bf16_to_f64(_randn_bits(rng, (L0, D))).astype(np.float32)
+            ck, sk = oracle.fp8.quantize_rows_fast(rk)
+            cv, sv = oracle.fp8.quantize_rows_fast(rv)
+            for j in range(L0):
+                b, r = ids[j // 16], j % 16
+                kc[b, h, r], ks[b, h, r], vc[b, h, r], vs[b, h, r] = ck[j], sk[j], cv[j], sv[j]
+    k_pool = _cuda(k_physical(kc).reshape(N, h_kv, 16 * D))
+    v_pool = _cuda(v_physical(vc).reshape(N, h_kv, 16 * D))
+    k_scale, v_scale = _cuda(ks), _cuda(vs)
+    tables_d = torch.from_numpy(tables).cuda()
+    lens_h = np.array(start_lens, np.int32)
+    lens_d = [torch.from_numpy(lens_h.copy()).cuda(),
+              torch.zeros(n_items, dtype=torch.int32, device="cuda")]
+    ws_bytes = kvs.kvs_paged_decode_workspace_size(n_items, h_q, h_kv, D)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
+    out = torch.empty((n_items, h_q, D), dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    patch = np.zeros(n_items, np.int32)
+    cs, cd = np.zeros(n_items, np.int32), np.zeros(n_items, np.int32)
+    for step in range(steps):
+        a.decode_prepare(tables, lens_h, patch, cs, cd)
+        q = _randn_bits(rng, (n_items, h_q, D))
+        kn = _randn_bits(rng, (n_items, h_kv, D), 2.0)
+        vn = _randn_bits(rng, (n_items, h_kv, D))
+        cur = step % 2
+        kvs.kvs_paged_decode_fp8(dev_bf16(q), dev_bf16(kn), dev_bf16(vn), k_pool, v_pool,
+                                 k_scale, v_scale, N, tables_d, max_blocks,
+                                 torch.from_numpy(patch).cuda(), lens_d[cur], lens_d[1 - cur],
+                                 n_items, h_q, h_kv, D, 1 / np.sqrt(D), out, ws, ws_bytes, status)
+        torch.cuda.synchronize()
+        assert status.item() == 0
+        for i in range(n_items):
+            L0 = lens_h[i]
+            b, r = tables[i, L0 // 16], L0 % 16
+            ck, sk = oracle.fp8.quantize_rows_fast(bf16_to_f64(kn[i]).astype(np.float32))
+            cv, sv = oracle.fp8.quantize_rows_fast(bf16_to_f64(vn[i]).astype(np.float32))
+            kc[b, :, r], ks[b, :, r], vc[b, :, r], vs[b, :, r] = ck, sk, cv, sv
+        lens_h += 1
+        np.testing.assert_array_equal(tables_d.cpu().numpy(), tables)
+        np.testing.assert_array_equal(lens_d[1 - cur].cpu().numpy(), lens_h)
+        kval = oracle.fp8.dequantize_rows(kc, ks)
+        vval = oracle.fp8.dequantize_rows(vc, vs)
+        got = bf16_f64(out)
+        for i in range(n_items):
+            L1 = lens_h[i]
+            kk = np.stack([oracle.gather_rows(kval, tables[i], L1, h) for h in range(h_kv)])
+            vv = np.stack([oracle.gather_rows(vval, tables[i], L1, h) for h in range(h_kv)])
+            ref = oracle.decode_attention(bf16_to_f64(q[i]), kk, vv, 1 / np.sqrt(D))
+            err = np.abs(got[i] - ref).max()
+            assert err <= ABS_O, (step, i, err)
+    # every written row's codes and scales, bit for bit
+    used = np.isfinite(ks)
+    got_k = k_pool.cpu().numpy().reshape(N, h_kv, 16, D)
+    got_v = v_pool.cpu().numpy().reshape(N, h_kv, D, 16)
+    exp_k, exp_v = k_physical(kc), v_physical(vc)
+    for b, h, r in zip(*np.nonzero(used)):
+        np.testing.assert_array_equal(got_k[b, h].reshape(-1)[r * 128:(r + 1) * 128],
+                                      exp_k[b, h].reshape(-1)[r * 128:(r + 1) * 128])
+        np.testing.assert_array_equal(got_v[b, h][:, r], exp_v[b, h][:, r])
+    np.testing.assert_array_equal(k_scale.cpu().numpy()[used], ks[used])
+    np.testing.assert_array_equal(v_scale.cpu().numpy()[used], vs[used])
+    a.close()

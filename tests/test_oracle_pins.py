@@ -453,3 +453,18 @@ def test_fp8_row_quantisation_bounds():
             assert s[i] == np.float32(np.float32(np.abs(x[i]).max()) / np.float32(448))
     codes, s = oracle.fp8.quantize_row(np.zeros(16, np.float32))
     assert (codes == 0).all() and s == 1.0
+
+
+def test_fp8_vectorised_forms_match_the_scalar_ones():
+    rng = np.random.default_rng(13)
+    x = (rng.standard_normal((40, 128)) * np.exp(rng.uniform(-8, 6, (40, 1)))).astype(np.float32)
+    x[3] = 0.0
+    x[5, :7] = 1e6                                       # saturating values
+    c1, s1 = oracle.fp8.quantize_rows(x)
+    c2, s2 = oracle.fp8.quantize_rows_fast(x)
+    np.testing.assert_array_equal(c1, c2)
+    np.testing.assert_array_equal(s1, s2)
+    enc1 = np.array([oracle.fp8.e4m3_encode_one(v) for v in x.ravel()[:2000]])
+    np.testing.assert_array_equal(enc1, oracle.fp8.e4m3_encode(x.ravel()[:2000]))
+    d1 = np.array([oracle.fp8.dequantize_row(c1[i], s1[i]) for i in range(40)])
+    np.testing.assert_array_equal(d1, oracle.fp8.dequantize_rows(c1, s1))
