@@ -63,6 +63,10 @@ constexpr int kMaxG = 16;
 constexpr int kMaxBatch = 2048;
 constexpr int kMaxStages = 8;
 constexpr float kLog2e = 1.4426950408889634f;
+// FP8 pools: P is multiplied by each token's V scale times kPvScale before the
+// f16 P.V product (keeping P' in f16's normal range down to p * |v| ~ 3e-5
+// and below its overflow for |v| < 28000), and the result by 1 / kPvScale.
+constexpr float kPvScale = 1024.0f;
 
 struct DecodeParams {
   const uint16_t* q;
@@ -220,7 +224,8 @@ __device__ __forceinline__ int fetch_chunk(const Piece& x, int base, int lane,
 // Each block's K and V codes and scales arrive by linear bulk copies; K and V
 // fragments are 4-byte shared-memory loads turned into f16 pairs (exact), the
 // products run on the f16 form of the same MMA, the K scales multiply the
-// logits and the V scales the value fragments (f16).  So that K and V need
+// logits and the V scales (times kPvScale) the probabilities that enter P.V
+// (the denominators use the unscaled ones).  So that K and V need
 // no byte transposes, the MMA's token order inside a block is permuted: row
 // rho of S^T (and k-slot rho of P^T V) is token tau(rho) = 4 (rho/2 % 4) +
 // rho % 2 + 2 (rho / 8), and q's d order follows the order of the K bytes a
@@ -556,11 +561,14 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
       const bool v0 = tok0 + tr0 < cur.len;
       const bool v1 = tok0 + tr1 < cur.len;
       float sc0 = p.scale_log2, sc1 = p.scale_log2;
+      float pv0 = 1.f, pv1 = 1.f;  // FP8: the V scale of each row's token, times kPvScale
       if constexpr (kF8) {
         const float* sks = reinterpret_cast<const float*>(my_stages + s * L::kStageBytes +
                                                           L::kScaleOff);
         sc0 *= sks[tr0];
         sc1 *= sks[tr1];
+        pv0 = v0 ? sks[KVS_BLOCK_TOKENS + tr0] * kPvScale : 0.f;
+        pv1 = v1 ? sks[KVS_BLOCK_TOKENS + tr1] * kPvScale : 0.f;
       }
       uint32_t pb0[NT], pb1[NT];
       bool rescale = false;
@@ -597,8 +605,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
         }
         // P^T (tokens x heads) -> B fragments (k = tokens, n = heads)
         if constexpr (kF8) {
-          pb0[nt] = movmatrix_t(pack_f16x2(s0[0], s0[1]));
-          pb1[nt] = movmatrix_t(pack_f16x2(s1[0], s1[1]));
+          pb0[nt] = movmatrix_t(pack_f16x2(s0[0] * pv0, s0[1] * pv0));
+          pb1[nt] = movmatrix_t(pack_f16x2(s1[0] * pv1, s1[1] * pv1));
         } else {
           pb0[nt] = movmatrix_t(pack_bf16x2(s0[0], s0[1]));
           pb1[nt] = movmatrix_t(pack_bf16x2(s1[0], s1[1]));
@@ -620,12 +628,6 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
         // transposed V codes: row d, bytes 4t .. 4t+3 = tokens of k-slots 2t, 2t+1, 2t+8, 2t+9
         const int gq = lane >> 2, t = lane & 3;
         const uint8_t* vt = my_stages + s * L::kStageBytes + L::kBlockBytes;
-        const float* svs = reinterpret_cast<const float*>(my_stages + s * L::kStageBytes +
-                                                          L::kScaleOff) + KVS_BLOCK_TOKENS;
-        float sv[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) sv[i] = tok0 + 4 * t + i < cur.len ? svs[4 * t + i] : 0.f;
-        const uint32_t sc_lo = pack_f16x2(sv[0], sv[1]), sc_hi = pack_f16x2(sv[2], sv[3]);
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt) {
           const uint32_t x0 =
@@ -635,10 +637,6 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
           uint32_t a[4];
           e4m3x4_to_f16x2(x0, a[0], a[2]);
           e4m3x4_to_f16x2(x1, a[1], a[3]);
-          a[0] = hmul2(a[0], sc_lo);
-          a[1] = hmul2(a[1], sc_lo);
-          a[2] = hmul2(a[2], sc_hi);
-          a[3] = hmul2(a[3], sc_hi);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) mma16816_f16(o[mt][nt], a, pb0[nt], pb1[nt]);
         }
@@ -678,7 +676,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
         for (int e = 0; e < 2; ++e) {
           const int hd = nt * 8 + (lane & 3) * 2 + e;
           if (hd < G) {
-            const float il = 1.0f / l_h[nt][e];
+            const float il = (kF8 ? 1.0f / kPvScale : 1.0f) / l_h[nt][e];
             if constexpr (kLogits)
               if (lane < 4) p.lse[out_row0 + hd] = m_h[nt][e] + log2f(l_h[nt][e]);
             uint16_t* orow = p.out + (out_row0 + hd) * D;
@@ -700,10 +698,11 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
         for (int e = 0; e < 2; ++e) {
           const int hd = nt * 8 + (lane & 3) * 2 + e;
           if (hd < G) {
+            const float os = kF8 ? 1.0f / kPvScale : 1.0f;
 #pragma unroll
             for (int mt = 0; mt < D / 16; ++mt) {
-              part[hd * D + mt * 16 + dr] = o[mt][nt][e];
-              part[hd * D + mt * 16 + dr + 8] = o[mt][nt][2 + e];
+              part[hd * D + mt * 16 + dr] = o[mt][nt][e] * os;
+              part[hd * D + mt * 16 + dr + 8] = o[mt][nt][2 + e] * os;
             }
             if (lane < 4) {
               part[G * D + hd] = m_h[nt][e];

@@ -52,12 +52,6 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
   return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-
 // two floats -> two e4m3 codes in a 16-bit value (lo in the low byte)
 __device__ __forceinline__ uint32_t e4m3x2_pack(float lo, float hi) {
   uint16_t d;
