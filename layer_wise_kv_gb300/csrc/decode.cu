@@ -10,9 +10,9 @@
 //
 // Design (HBM-bound: ~4 flop per byte of K/V):
 // * The work is the sequence of (item, KV head) segments, each a run of
-//   16-token blocks.  Persistent CTAs (one per SM, twelve warps) split the
-//   concatenated block sequence into equal contiguous ranges, one per warp
-//   (stream-K): every warp streams the same number of bytes, whatever the mix
+//   16-token blocks.  Persistent CTAs (one per SM; twelve warps, sixteen
+//   over FP8 pools) split the concatenated block sequence into equal
+//   contiguous ranges, one per warp (stream-K): every warp streams the same number of bytes, whatever the mix
 //   of lengths, and a segment is cut into at most a few pieces.  Segment
 //   offsets come from a prefix sum over `lens` in shared memory, so the launch
 //   needs no host knowledge of the lengths.
@@ -57,7 +57,11 @@ namespace {
 #define KVS_DECODE_WARPS 12
 #endif
 constexpr int kWarps = KVS_DECODE_WARPS;
-constexpr int kDecThreads = kWarps * 32;
+// FP8 pools: a block is half the bytes, so 16 warps fit two stages each, and
+// the kernel is latency-bound per warp (more warps, more chains in flight)
+constexpr int kWarpsF8 = 16;
+constexpr int kMaxWarps = kWarps > kWarpsF8 ? kWarps : kWarpsF8;
+__host__ __device__ constexpr int dec_warps(bool f8) { return f8 ? kWarpsF8 : kWarps; }
 constexpr int kMaxGrid = 256;
 constexpr int kMaxG = 16;
 constexpr int kMaxBatch = 2048;
@@ -231,11 +235,13 @@ __device__ __forceinline__ int fetch_chunk(const Piece& x, int base, int lane,
 // rho % 2 + 2 (rho / 8), and q's d order follows the order of the K bytes a
 // thread holds.
 template <int D, int NT, bool kLogits, bool kF8 = false>
-__global__ void __launch_bounds__(kDecThreads, 1)
+__global__ void __launch_bounds__(dec_warps(kF8) * 32, 1)
 paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
                     const __grid_constant__ CUtensorMap v_map, const DecodeParams p) {
   static_assert(!kF8 || (D == 128 && !kLogits), "FP8 pools: d = 128, no logits output");
   using L = DecodeLayout<D, kF8>;
+  constexpr int kWarps = dec_warps(kF8);
+  constexpr int kDecThreads = kWarps * 32;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -919,6 +925,7 @@ constexpr int kSmemLimit = 232448;
 template <int D, bool kF8>
 size_t plan_smem(DecodeParams& prm) {
   using L = DecodeLayout<D, kF8>;
+  constexpr int kWarps = dec_warps(kF8);
   prm.q_bytes = prm.group * D * 2;
   prm.q_stride = (prm.q_bytes + 127) / 128 * 128;
   for (int ns = kMaxStages; ns >= 1; --ns) {
@@ -963,6 +970,8 @@ kvs_status launch_decode(DecodeParams& prm, const CUtensorMap& km, const CUtenso
     configured = true;
   }
   const int grid = sm_count_dec() < kMaxGrid ? sm_count_dec() : kMaxGrid;
+  constexpr int kWarps = dec_warps(kF8);
+  constexpr int kDecThreads = kWarps * 32;
   if constexpr (kF8)
     paged_decode_kernel<D, NT, false, true><<<grid, kDecThreads, smem, stream>>>(km, vm, prm);
   else if (prm.logits != nullptr)
@@ -997,7 +1006,7 @@ size_t kvs_paged_decode_workspace_size(int32_t batch, int32_t h_q, int32_t h_kv,
   if (batch <= 0 || h_kv <= 0 || h_q <= 0 || d <= 0) return 0;
   const int64_t G = h_q / h_kv;
   // one partial slot per (warp, segment it touches): slot = warp + segment
-  const int64_t slots = static_cast<int64_t>(kvs::kMaxGrid) * kvs::kWarps +
+  const int64_t slots = static_cast<int64_t>(kvs::kMaxGrid) * kvs::kMaxWarps +
                         static_cast<int64_t>(batch) * h_kv;
   return static_cast<size_t>(slots * kvs::part_floats(static_cast<int>(G), d) * 4);
 }

@@ -217,3 +217,92 @@ def test_paged_decode_fp8_vs_oracle(h_q, h_kv):
     np.testing.assert_array_equal(k_scale.cpu().numpy()[used], ks[used])
     np.testing.assert_array_equal(v_scale.cpu().numpy()[used], vs[used])
     a.close()
+
+
+def test_engine_fp8_prefill_and_decode_vs_oracle_flow():
+    """The engine with FP8 pools, end to end: prefill + sparsify of a
+    600-token prompt at the Llama-3-8B head shapes over layers 0, 30 and 31
+    (one full-cache layer, two budgeted ones), the compaction into FP8 pools
+    and six eager decode steps.  Tables and kept sets against the oracle's
+    flow, every kept row's codes and scales bit for bit against the oracle's
+    quantiser, each step's outputs against the oracle's decode attention over
+    the stored values (the appended rows quantised the same way)."""
+    kvs_lib()
+    from layer_wise_kv_gb300.pipeline import DecodeBatch, Engine, Shape
+    from oracle import flow
+    from synth import decode_qkv, llama3_8b, prefill_qkv
+    from gpu_helpers import check_kept
+    w = llama3_8b()
+    n, steps, layers = 600, 6, [0, 30, 31]
+    shape = Shape(len(layers), w.h_q, w.h_kv, w.d, w.alpha, w.recent)
+    N = 256
+    eng = Engine(shape, N, poison=True, kv_dtype="fp8")
+    host = {l: prefill_qkv(w, 0, l, n) for l in layers}
+    ql, kl, vl = ([dev_bf16(host[l][i]) for l in layers] for i in range(3))
+    budgets = [[w.budget(l, n) for l in layers]]
+    res = eng.prefill_sparsify(ql, kl, vl, [n], budgets)
+    torch.cuda.synchronize()
+    eng.check_status()
+
+    pool = oracle.BlockPool(N)
+    recs, kdq, vdq = [], [], []
+    got_k = eng.k_pool.cpu().numpy().reshape(N, w.h_kv, 16, D)
+    got_v = eng.v_pool.cpu().numpy().reshape(N, w.h_kv, D, 16)
+    got_ks, got_vs = eng.k_scale.cpu().numpy(), eng.v_scale.cpu().numpy()
+    for li, l in enumerate(layers):
+        qb, kb, vb = host[l]
+        rec = flow.sparsify_layer(w, l, qb, kb, vb)
+        off = int(res.idx_off[0, li])
+        gidx = res.kept_idx[off:off + w.h_kv * rec.k_eff].cpu().numpy().reshape(w.h_kv, rec.k_eff)
+        if rec.budgeted:
+            for h in range(w.h_kv):
+                check_kept(gidx[h], rec.idx[h], rec.scores[h], n, w.budget(l, n), w.recent)
+        else:
+            np.testing.assert_array_equal(gidx, rec.idx)
+        rec.idx = gidx
+        flow.place_layer(rec, pool, kb, vb, None, None)
+        assert res.tables[0][li] == rec.table
+        recs.append(rec)
+        ks_l, vs_l = [], []
+        for h in range(w.h_kv):
+            ck, sk = oracle.fp8.quantize_rows_fast(bf16_to_f64(kb[gidx[h], h]).astype(np.float32))
+            cv, sv = oracle.fp8.quantize_rows_fast(bf16_to_f64(vb[gidx[h], h]).astype(np.float32))
+            for j in range(rec.k_eff):
+                b, r = rec.table[j // 16], j % 16
+                # the row as stored: row r of a 16-row tile (chunks swapped on odd rows)
+                phys = k_physical(np.pad(ck[j:j + 1], ((r, 15 - r), (0, 0))))[r]
+                np.testing.assert_array_equal(got_k[b, h, r], phys)
+                np.testing.assert_array_equal(got_v[b, h][:, r], cv[j])
+                assert got_ks[b, h, r] == sk[j] and got_vs[b, h, r] == sv[j]
+            ks_l.append(list(oracle.fp8.dequantize_rows(ck, sk)))
+            vs_l.append(list(oracle.fp8.dequantize_rows(cv, sv)))
+        kdq.append(ks_l)
+        vdq.append(vs_l)
+
+    dec = DecodeBatch(eng, 1, n + steps)
+    dec.set_stream(0, res.tables[0], res.k_eff[0])
+    st = flow.new_stream(recs)
+    dq = [decode_qkv(w, 0, l, steps) for l in layers]
+    for t in range(steps):
+        q = dev_bf16(np.stack([dq[li][0][t] for li in range(len(layers))]))
+        k = dev_bf16(np.stack([dq[li][1][t] for li in range(len(layers))]))
+        v = dev_bf16(np.stack([dq[li][2][t] for li in range(len(layers))]))
+        out = bf16_f64(dec.step(q, k, v))
+        for li in range(len(layers)):
+            flow.prepare_append(pool, st, li)
+            st.lens[li] += 1
+            for h in range(w.h_kv):
+                ck, sk = oracle.fp8.quantize_rows_fast(
+                    bf16_to_f64(dq[li][1][t][h:h + 1]).astype(np.float32))
+                cv, sv = oracle.fp8.quantize_rows_fast(
+                    bf16_to_f64(dq[li][2][t][h:h + 1]).astype(np.float32))
+                kdq[li][h].append(oracle.fp8.dequantize_rows(ck, sk)[0])
+                vdq[li][h].append(oracle.fp8.dequantize_rows(cv, sv)[0])
+            kk = np.stack([np.stack(kdq[li][h]) for h in range(w.h_kv)])
+            vv = np.stack([np.stack(vdq[li][h]) for h in range(w.h_kv)])
+            ref = oracle.decode_attention(bf16_to_f64(dq[li][0][t]), kk, vv, w.scale)
+            err = np.abs(out[li] - ref).max()
+            assert err <= ABS_O, (t, layers[li], err)
+    torch.cuda.synchronize()
+    eng.check_status()
+    assert dec.stream_tables(0) == st.tables
