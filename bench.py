@@ -194,6 +194,12 @@ def prefill_flops(w, n):
     return 2.0 * w.h_q * w.d * n * (n + 1)
 
 
+def prefill_exps(w, n):
+    """Softmax exponentials of the causal prefill of one layer: one per
+    (query head, query, key at or before it)."""
+    return w.h_q * n * (n + 1) / 2.0
+
+
 def decode_bytes(w, lens):
     """Algorithmic bytes of one decode launch: every cached K and V row of
     every item read once (the new row included), q read, out written, the new
@@ -329,6 +335,8 @@ def bench_gpu(args):
     k1_layers = rec["k1"].get("attn_layers") or [1] * len(k1_ms)
     flops_launch = prefill_flops(w, n) * (sum(k1_layers) / len(k1_layers))
     tflops = flops_launch / (k1_avg / 1e3) / 1e12
+    exps_launch = prefill_exps(w, n) * (sum(k1_layers) / len(k1_layers))
+    exp_rate = exps_launch / (k1_avg / 1e3)
     peak_t = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
     dk_ms = [a.elapsed_time(b) for a, b in rec["dk"]]
     dec_avg = sum(dk_ms) / len(dk_ms)            # the decode kernel alone
@@ -372,7 +380,12 @@ def bench_gpu(args):
                              "frac": round(tflops / peak_t, 4),
                              "traffic": traffic_for("prefill_attn"),
                              "peak_source": f"{peak_src} bf16 sustained",
-                             "per_launch_ms": round(k1_avg, 4), "flops_per_launch": flops_launch},
+                             "per_launch_ms": round(k1_avg, 4), "flops_per_launch": flops_launch,
+                             # the softmax's exponentials, the other unit the prefill leans
+                             # on (d = 128 puts them near the MMA rate); the kernel evaluates
+                             # part of them on the FMA pipe, so this is no MUFU bound
+                             "exp_per_launch": exps_launch,
+                             "exp_per_s": round(exp_rate, -6)},
         # one window-score launch per request covers the budgeted layers
         "scores_ms_per_launch": round(sum(k2_ms) / max(1, len(k2_ms)), 4),
         "scores_layers_per_launch": sum(1 for l in range(L) if w.budget(l, n) is not None
