@@ -229,6 +229,14 @@ kvs_status kvs_compact_blocks_fp8(const kvs_bf16* k, const kvs_bf16* v,
                                   float* v_scale, int32_t num_blocks, int32_t* status,
                                   kvs_stream stream);
 
+/* kvs_copy_blocks for FP8 pools (layout of kvs_compact_blocks_fp8; d = 128):
+ * each pair copies the block's K and V codes of every head and their row
+ * scales.  Two launches on `stream`. */
+kvs_status kvs_copy_blocks_fp8(const int32_t* src, const int32_t* dst, int32_t count,
+                               uint8_t* k_pool, uint8_t* v_pool, float* k_scale, float* v_scale,
+                               int32_t num_blocks, int32_t h_kv, int32_t d, int32_t* status,
+                               kvs_stream stream);
+
 /* Copy whole blocks src[i] -> dst[i] in both pools (the copy of
  * copy-on-write; Ultralytics glossary "PagedAttention", section "Block
  * sharing between sequences").  src, dst: device int32 [count]. */

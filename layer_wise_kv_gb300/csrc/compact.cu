@@ -331,6 +331,36 @@ kvs_status kvs_copy_blocks(const int32_t* src, const int32_t* dst, int32_t count
   return KVS_OK;
 }
 
+kvs_status kvs_copy_blocks_fp8(const int32_t* src, const int32_t* dst, int32_t count,
+                               uint8_t* k_pool, uint8_t* v_pool, float* k_scale, float* v_scale,
+                               int32_t num_blocks, int32_t h_kv, int32_t d, int32_t* status,
+                               kvs_stream stream) {
+  KVS_REQUIRE(count >= 0, "kvs_copy_blocks_fp8: negative count");
+  if (count == 0) return KVS_OK;
+  KVS_REQUIRE(src && dst && k_pool && v_pool && k_scale && v_scale,
+              "kvs_copy_blocks_fp8: NULL pointer");
+  KVS_SUPPORTED(d == 128, "kvs_copy_blocks_fp8: d = %d (supported: 128)", d);
+  KVS_REQUIRE(h_kv > 0 && num_blocks > 0, "kvs_copy_blocks_fp8: h_kv / num_blocks must be > 0");
+  KVS_REQUIRE(kvs::aligned16(k_pool) && kvs::aligned16(v_pool) && kvs::aligned16(k_scale) &&
+                  kvs::aligned16(v_scale),
+              "kvs_copy_blocks_fp8: pool and scale pointers must be 16-byte aligned");
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t cap = static_cast<int64_t>(kvs::sm_count()) * 8;
+  // the codes (16 x d bytes per head and pool), then the row scales (16 floats)
+  const int64_t chunk_counts[2] = {static_cast<int64_t>(h_kv) * KVS_BLOCK_TOKENS * d / 16,
+                                   static_cast<int64_t>(h_kv) * KVS_BLOCK_TOKENS * 4 / 16};
+  uint4* a_pools[2] = {reinterpret_cast<uint4*>(k_pool), reinterpret_cast<uint4*>(k_scale)};
+  uint4* b_pools[2] = {reinterpret_cast<uint4*>(v_pool), reinterpret_cast<uint4*>(v_scale)};
+  for (int i = 0; i < 2; ++i) {
+    int64_t grid = (chunk_counts[i] * 2 * count + 255) / 256;
+    if (grid > cap) grid = cap;
+    kvs::copy_blocks_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(
+        src, dst, count, a_pools[i], b_pools[i], num_blocks, chunk_counts[i], status);
+    KVS_CHECK_LAUNCH("kvs_copy_blocks_fp8");
+  }
+  return KVS_OK;
+}
+
 kvs_status kvs_workspace_zero(void* workspace, size_t bytes, kvs_stream stream) {
   if (bytes == 0) return KVS_OK;
   KVS_REQUIRE(workspace != nullptr, "kvs_workspace_zero: NULL workspace");

@@ -74,6 +74,8 @@ _SIGS = {
     "kvs_paged_decode_fp8": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I32, _VP, _I32, _VP, _VP,
                                     _VP, _I32, _I32, _I32, _I32, _F32, _VP, _VP, _SZ, _VP, _VP]),
     "kvs_copy_blocks": (_I32, [_VP, _VP, _I32, _VP, _VP, _I32, _I32, _I32, _VP, _VP]),
+    "kvs_copy_blocks_fp8": (_I32, [_VP, _VP, _I32, _VP, _VP, _VP, _VP, _I32, _I32, _I32, _VP,
+                                   _VP]),
     "kvs_paged_decode_workspace_size": (_SZ, [_I32, _I32, _I32, _I32]),
     "kvs_workspace_zero": (_I32, [_VP, _SZ, _VP]),
     "kvs_paged_decode": (_I32, [_VP, _VP, _VP, _VP, _VP, _I32, _VP, _I32, _VP, _VP, _VP, _I32,
@@ -249,6 +251,15 @@ def kvs_paged_decode_fp8(q, k_new, v_new, k_pool, v_pool, k_scale, v_scale, num_
         _dev(lens, "i32", "lens"), None if lens_next is None else _dev(lens_next, "i32", "lens_next"),
         batch, h_q, h_kv, d, float(scale), _dev(out, "bf16", "out"),
         _dev(workspace, "u8", "workspace"), workspace_bytes,
+        None if status is None else _dev(status, "i32", "status"), _stream(stream)))
+
+
+def kvs_copy_blocks_fp8(src, dst, count, k_pool, v_pool, k_scale, v_scale, num_blocks, h_kv, d,
+                        status=None, stream=None):
+    _check(library().kvs_copy_blocks_fp8(
+        _dev(src, "i32", "src"), _dev(dst, "i32", "dst"), count, _dev(k_pool, "u8", "k_pool"),
+        _dev(v_pool, "u8", "v_pool"), _dev(k_scale, "f32", "k_scale"),
+        _dev(v_scale, "f32", "v_scale"), num_blocks, h_kv, d,
         None if status is None else _dev(status, "i32", "status"), _stream(stream)))
 
 

@@ -624,16 +624,20 @@ class DecodeBatch:
             with torch.cuda.stream(cur_stream):
                 self.patch_d.copy_(patch_t, non_blocking=True)
                 patch_arg = self.patch_d
-                if n_cow and eng.kv_fp8:
-                    raise NotImplementedError("copy-on-write of shared FP8 blocks")
                 if n_cow:
                     cow = self._cow_np[slot]
                     cow[:n_cow] = self.cow_src[:n_cow]
                     cow[n_cow:2 * n_cow] = self.cow_dst[:n_cow]
                     self.cow_d[:2 * n_cow].copy_(cow_t[:2 * n_cow], non_blocking=True)
-                    kvs.kvs_copy_blocks(self.cow_d[:n_cow], self.cow_d[n_cow:2 * n_cow], n_cow,
-                                        eng.k_pool, eng.v_pool, eng.num_blocks, s.h_kv, s.d,
-                                        eng.status, cur_stream)
+                    if eng.kv_fp8:
+                        kvs.kvs_copy_blocks_fp8(self.cow_d[:n_cow], self.cow_d[n_cow:2 * n_cow],
+                                                n_cow, eng.k_pool, eng.v_pool, eng.k_scale,
+                                                eng.v_scale, eng.num_blocks, s.h_kv, s.d,
+                                                eng.status, cur_stream)
+                    else:
+                        kvs.kvs_copy_blocks(self.cow_d[:n_cow], self.cow_d[n_cow:2 * n_cow],
+                                            n_cow, eng.k_pool, eng.v_pool, eng.num_blocks,
+                                            s.h_kv, s.d, eng.status, cur_stream)
                 ev = torch.cuda.Event()
                 ev.record(cur_stream)
                 self._ev[slot] = ev

@@ -102,6 +102,12 @@ def test_invalid_arguments_rejected_before_launch(kvs):
                                       4, None, None) == kvs.KVS_ERR_UNSUPPORTED
     assert lib.kvs_compact_blocks_fp8(256, 256, 256, 2, 64, 8, 128, 256, 256, 256, 256, None, 256,
                                       4, None, None) == kvs.KVS_ERR_INVALID
+    assert lib.kvs_copy_blocks_fp8(256, 256, 0, 256, 256, 256, 256, 4, 8, 128, None,
+                                   None) == kvs.KVS_OK
+    assert lib.kvs_copy_blocks_fp8(256, 256, 2, 256, 256, None, 256, 4, 8, 128, None,
+                                   None) == kvs.KVS_ERR_INVALID
+    assert lib.kvs_copy_blocks_fp8(256, 256, 2, 256, 256, 256, 256, 4, 8, 64, None,
+                                   None) == kvs.KVS_ERR_UNSUPPORTED
     df = [256, None, None, 256, 256, 256, 256, 4, 256, 1, None, 256, None, 2, 32, 8, 128, 0.1, 256,
           256, 1 << 26, None, None]
     df[16] = 64

@@ -306,3 +306,103 @@ def test_engine_fp8_prefill_and_decode_vs_oracle_flow():
     torch.cuda.synchronize()
     eng.check_status()
     assert dec.stream_tables(0) == st.tables
+
+
+def test_copy_blocks_fp8_bit_exact():
+    kvs = kvs_lib()
+    rng = np.random.default_rng(5)
+    N, h_kv = 12, 8
+    kp = rng.integers(0, 256, (N, h_kv, 16 * D), dtype=np.uint8)
+    vp = rng.integers(0, 256, (N, h_kv, 16 * D), dtype=np.uint8)
+    ks = rng.standard_normal((N, h_kv, 16)).astype(np.float32)
+    vs = rng.standard_normal((N, h_kv, 16)).astype(np.float32)
+    dev = [_cuda(x) for x in (kp, vp, ks, vs)]
+    src, dst = np.array([3, 7, 0], np.int32), np.array([9, 1, 11], np.int32)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvs.kvs_copy_blocks_fp8(_cuda(src), _cuda(dst), 3, *dev, N, h_kv, D, status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    for x in (kp, vp, ks, vs):
+        x[dst] = x[src]
+    for got, want in zip(dev, (kp, vp, ks, vs)):
+        np.testing.assert_array_equal(got.cpu().numpy(), want)
+
+
+def test_engine_fp8_shared_prefix_copy_on_write():
+    """Three parallel samples share a 600-token prompt's FP8 blocks (Llama-3-8B
+    head shapes, layers 0 and 31): the partial last block of the full-cache
+    layer is copied, codes and scales, on the first write of samples 0 and 1;
+    every sample's outputs against the oracle's attention over its own stored
+    values; tables and reference counts against the oracle's allocator."""
+    kvs_lib()
+    from layer_wise_kv_gb300.pipeline import DecodeBatch, Engine, Shape
+    from oracle import flow
+    from synth import decode_qkv, llama3_8b, prefill_qkv
+    w = llama3_8b()
+    n, steps, layers, S = 600, 8, [0, 31], 3
+    L = len(layers)
+    N = 160
+    eng = Engine(Shape(L, w.h_q, w.h_kv, w.d, w.alpha, w.recent), N, poison=True,
+                 kv_dtype="fp8")
+    host = {l: prefill_qkv(w, 0, l, n) for l in layers}
+    ql, kl, vl = ([dev_bf16(host[l][i]) for l in layers] for i in range(3))
+    res = eng.prefill_sparsify(ql, kl, vl, [n], [[w.budget(l, n) for l in layers]])
+    torch.cuda.synchronize()
+    eng.check_status()
+    pool = oracle.BlockPool(N)
+    recs, rows_k, rows_v = [], [], []
+    for li, l in enumerate(layers):
+        qb, kb, vb = host[l]
+        rec = flow.sparsify_layer(w, l, qb, kb, vb)
+        off = int(res.idx_off[0, li])
+        rec.idx = res.kept_idx[off:off + w.h_kv * rec.k_eff].cpu().numpy().reshape(w.h_kv, -1)
+        flow.place_layer(rec, pool, kb, vb, None, None)
+        assert res.tables[0][li] == rec.table
+        recs.append(rec)
+        kq = [oracle.fp8.quantize_rows_fast(bf16_to_f64(kb[rec.idx[h], h]).astype(np.float32))
+              for h in range(w.h_kv)]
+        vq = [oracle.fp8.quantize_rows_fast(bf16_to_f64(vb[rec.idx[h], h]).astype(np.float32))
+              for h in range(w.h_kv)]
+        rows_k.append([list(oracle.fp8.dequantize_rows(*x)) for x in kq])
+        rows_v.append([list(oracle.fp8.dequantize_rows(*x)) for x in vq])
+    assert recs[0].k_eff % 16 != 0          # the full-cache layer ends in a partial block
+    dec = DecodeBatch(eng, S, n + steps)
+    streams = [flow.new_stream(recs)]
+    dec.set_stream(0, res.tables[0], res.k_eff[0])
+    for s in range(1, S):
+        streams.append(flow.share_stream(pool, streams[0]))
+        for t in res.tables[0]:
+            for b in t:
+                eng.alloc.incref(b)
+        dec.set_stream(s, res.tables[0], res.k_eff[0])
+    # per sample, per layer, per head: the stored values the sample attends over
+    kval = [[[list(r) for r in rows_k[li]] for li in range(L)] for _ in range(S)]
+    vval = [[[list(r) for r in rows_v[li]] for li in range(L)] for _ in range(S)]
+    dq = {(s, li): decode_qkv(w, 0, l, steps, sample=s) for s in range(S)
+          for li, l in enumerate(layers)}
+    for t in range(steps):
+        q, k, v = (dev_bf16(np.stack([dq[(s, li)][i][t] for s in range(S) for li in range(L)]))
+                   for i in range(3))
+        out = bf16_f64(dec.step(q, k, v))
+        copies = 0
+        for s in range(S):
+            for li in range(L):
+                copies += flow.prepare_append(pool, streams[s], li) is not None
+                streams[s].lens[li] += 1
+                for h in range(w.h_kv):
+                    kval[s][li][h].append(oracle.fp8.dequantize_rows(*oracle.fp8.quantize_rows_fast(
+                        bf16_to_f64(dq[(s, li)][1][t][h:h + 1]).astype(np.float32)))[0])
+                    vval[s][li][h].append(oracle.fp8.dequantize_rows(*oracle.fp8.quantize_rows_fast(
+                        bf16_to_f64(dq[(s, li)][2][t][h:h + 1]).astype(np.float32)))[0])
+                kk = np.stack([np.stack(kval[s][li][h]) for h in range(w.h_kv)])
+                vv = np.stack([np.stack(vval[s][li][h]) for h in range(w.h_kv)])
+                ref = oracle.decode_attention(bf16_to_f64(dq[(s, li)][0][t]), kk, vv, w.scale)
+                err = np.abs(out[s * L + li] - ref).max()
+                assert err <= ABS_O, (t, s, layers[li], err)
+        if t == 0:
+            assert copies == 2
+    torch.cuda.synchronize()
+    eng.check_status()
+    for s in range(S):
+        assert dec.stream_tables(s) == streams[s].tables
+    assert [eng.alloc.refcount(b) for b in range(N)] == pool.ref
