@@ -498,6 +498,20 @@ class DecodeBatch:
         return self.out
 
     # ------------------------------------------------------------ CUDA graphs
+    def _decode_launch(self, q, k_new, v_new, patch, lens, lens_next, stream=None):
+        """One decode call over every item, on the engine's pool type."""
+        eng, s = self.eng, self.eng.shape
+        if eng.kv_fp8:
+            kvs.kvs_paged_decode_fp8(q, k_new, v_new, eng.k_pool, eng.v_pool, eng.k_scale,
+                                     eng.v_scale, eng.num_blocks, self.tables_d, self.max_blocks,
+                                     patch, lens, lens_next, self.n_items, s.h_q, s.h_kv, s.d,
+                                     s.scale, self.out, self.ws, self.ws_bytes, eng.status, stream)
+        else:
+            kvs.kvs_paged_decode(q, k_new, v_new, eng.k_pool, eng.v_pool, eng.num_blocks,
+                                 self.tables_d, self.max_blocks, patch, lens, lens_next,
+                                 self.n_items, s.h_q, s.h_kv, s.d, s.scale, self.out, self.ws,
+                                 self.ws_bytes, eng.status, stream)
+
     def capture_graphs(self):
         """Capture the decode step as CUDA graphs, so that a step costs the host
         one graph launch instead of the library's launches (the method's
@@ -509,8 +523,6 @@ class DecodeBatch:
         the step's inputs from the fixed buffers self.q_in, self.k_in,
         self.v_in (step() copies other tensors into them) and the patch from
         two pinned buffers, one per direction."""
-        if self.eng.kv_fp8:
-            raise NotImplementedError("graph capture of the FP8 decode step")
         s, dev = self.eng.shape, self.eng.device
         n = self.n_items
         self.q_in = torch.zeros((n, s.h_q, s.d), dtype=torch.bfloat16, device=dev)
@@ -519,14 +531,10 @@ class DecodeBatch:
         self._patch_g = [torch.full((n,), -1, dtype=torch.int32).pin_memory() for _ in range(2)]
         self._patch_g_np = [t.numpy() for t in self._patch_g]
         self._gev = [None, None]
-        eng = self.eng
         # one-time library set-up (kernel attributes, tensor maps) outside the
         # capture: a call that appends nothing and writes only out and the
         # workspace leaves the caches as they are
-        kvs.kvs_paged_decode(self.q_in, None, None, eng.k_pool, eng.v_pool, eng.num_blocks,
-                             self.tables_d, self.max_blocks, None, self.lens_d[self.cur], None, n,
-                             s.h_q, s.h_kv, s.d, s.scale, self.out, self.ws, self.ws_bytes,
-                             eng.status)
+        self._decode_launch(self.q_in, None, None, None, self.lens_d[self.cur], None)
         torch.cuda.synchronize()
         graphs = {}
         for cur in (0, 1):
@@ -535,11 +543,9 @@ class DecodeBatch:
                 with torch.cuda.graph(g):
                     if with_patch:
                         self.patch_d.copy_(self._patch_g[cur], non_blocking=True)
-                    kvs.kvs_paged_decode(self.q_in, self.k_in, self.v_in, eng.k_pool, eng.v_pool,
-                                         eng.num_blocks, self.tables_d, self.max_blocks,
-                                         self.patch_d if with_patch else None, self.lens_d[cur],
-                                         self.lens_d[1 - cur], n, s.h_q, s.h_kv, s.d, s.scale,
-                                         self.out, self.ws, self.ws_bytes, eng.status)
+                    self._decode_launch(self.q_in, self.k_in, self.v_in,
+                                        self.patch_d if with_patch else None, self.lens_d[cur],
+                                        self.lens_d[1 - cur])
                 graphs[(cur, with_patch)] = g
         self._graphs = graphs
 
@@ -647,18 +653,8 @@ class DecodeBatch:
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(cur_stream)
-        if eng.kv_fp8:
-            kvs.kvs_paged_decode_fp8(q, k_new, v_new, eng.k_pool, eng.v_pool, eng.k_scale,
-                                     eng.v_scale, eng.num_blocks, self.tables_d, self.max_blocks,
-                                     patch_arg, self.lens_d[self.cur], self.lens_d[nxt], n,
-                                     s.h_q, s.h_kv, s.d, s.scale, self.out, self.ws,
-                                     self.ws_bytes, eng.status, cur_stream)
-        else:
-            kvs.kvs_paged_decode(q, k_new, v_new, eng.k_pool, eng.v_pool, eng.num_blocks,
-                                 self.tables_d, self.max_blocks, patch_arg,
-                                 self.lens_d[self.cur], self.lens_d[nxt], n, s.h_q, s.h_kv, s.d,
-                                 s.scale, self.out, self.ws, self.ws_bytes, eng.status,
-                                 cur_stream)
+        self._decode_launch(q, k_new, v_new, patch_arg, self.lens_d[self.cur],
+                            self.lens_d[nxt], cur_stream)
         if timing is not None:
             b.record(cur_stream)
             timing.append((a, b))

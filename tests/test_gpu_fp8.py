@@ -406,3 +406,54 @@ def test_engine_fp8_shared_prefix_copy_on_write():
     for s in range(S):
         assert dec.stream_tables(s) == streams[s].tables
     assert [eng.alloc.refcount(b) for b in range(N)] == pool.ref
+
+
+def test_engine_fp8_graphs_match_eager():
+    """DecodeBatch.capture_graphs() over FP8 pools: steps replayed from CUDA
+    graphs give, bit for bit, the outputs, tables, lengths, reference counts,
+    codes and scales of eager steps.  Three samples share a prompt (the first
+    step copies blocks on write, launched eagerly); later steps cross block
+    boundaries (graphs that upload a table patch) and stay inside blocks."""
+    kvs_lib()
+    from layer_wise_kv_gb300.pipeline import DecodeBatch, Engine, Shape
+    from synth import decode_qkv, llama3_8b, prefill_qkv
+    w = llama3_8b()
+    n, steps, layers, S, N = 600, 24, [0, 31], 3, 160
+    L = len(layers)
+    host = {l: prefill_qkv(w, 0, l, n) for l in layers}
+    ql, kl, vl = ([dev_bf16(host[l][i]) for l in layers] for i in range(3))
+    dq = {(s, li): decode_qkv(w, 0, l, steps, sample=s) for s in range(S)
+          for li, l in enumerate(layers)}
+    runs = []
+    for graphs in (False, True):
+        eng = Engine(Shape(L, w.h_q, w.h_kv, w.d, w.alpha, w.recent), N, poison=True,
+                     kv_dtype="fp8")
+        res = eng.prefill_sparsify(ql, kl, vl, [n], [[w.budget(l, n) for l in layers]])
+        dec = DecodeBatch(eng, S, n + steps)
+        dec.set_stream(0, res.tables[0], res.k_eff[0])
+        for s in range(1, S):
+            for t in res.tables[0]:
+                for b in t:
+                    eng.alloc.incref(b)
+            dec.set_stream(s, res.tables[0], res.k_eff[0])
+        if graphs:
+            dec.capture_graphs()
+        outs = []
+        for t in range(steps):
+            q, k, v = (dev_bf16(np.stack([dq[(s, li)][i][t] for s in range(S) for li in range(L)]))
+                       for i in range(3))
+            outs.append(dec.step(q, k, v).clone())
+        torch.cuda.synchronize()
+        eng.check_status()
+        runs.append((eng, dec, outs))
+    (ea, da, oa), (eb, db, ob) = runs
+    for t in range(steps):
+        assert torch.equal(oa[t].view(torch.int16), ob[t].view(torch.int16)), t
+    for s in range(S):
+        assert da.stream_tables(s) == db.stream_tables(s)
+    assert torch.equal(da.tables_d, db.tables_d)
+    assert torch.equal(da.lens_d[da.cur], db.lens_d[db.cur])
+    assert [ea.alloc.refcount(b) for b in range(N)] == [eb.alloc.refcount(b) for b in range(N)]
+    for x, y in ((ea.k_pool, eb.k_pool), (ea.v_pool, eb.v_pool), (ea.k_scale, eb.k_scale),
+                 (ea.v_scale, eb.v_scale)):
+        assert torch.equal(x.view(torch.uint8), y.view(torch.uint8))
