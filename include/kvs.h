@@ -406,6 +406,19 @@ kvs_status kvs_decode_step(kvs_allocator* a, int32_t* tables_h, int32_t* lens_h,
                            size_t workspace_bytes, int32_t* status, int32_t* n_cow,
                            int32_t* n_patch, kvs_stream stream);
 
+/* kvs_decode_step over FP8 pools (kvs_copy_blocks_fp8 for the copies,
+ * kvs_paged_decode_fp8 for the decode; d = 128). */
+kvs_status kvs_decode_step_fp8(kvs_allocator* a, int32_t* tables_h, int32_t* lens_h,
+                               int32_t* patch_h, int32_t* cow_h, int32_t* patch_d,
+                               int32_t* cow_d, const kvs_bf16* q, const kvs_bf16* k_new,
+                               const kvs_bf16* v_new, uint8_t* k_pool, uint8_t* v_pool,
+                               float* k_scale, float* v_scale, int32_t num_blocks,
+                               int32_t* block_tables, int32_t max_blocks, const int32_t* lens,
+                               int32_t* lens_next, int32_t n_items, int32_t h_q, int32_t h_kv,
+                               int32_t d, float scale, kvs_bf16* out, void* workspace,
+                               size_t workspace_bytes, int32_t* status, int32_t* n_cow,
+                               int32_t* n_patch, kvs_stream stream);
+
 /* ------------------------------------------------------------------------
  * 7. Decode-time scoring and fixed-budget replacement (budgeted layers).
  * Source: Novita article, section "Key techniques 1" (after the first three

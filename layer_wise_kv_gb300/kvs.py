@@ -67,6 +67,9 @@ _SIGS = {
     "kvs_decode_step": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I32,
                                _VP, _I32, _VP, _VP, _I32, _I32, _I32, _I32, _F32, _VP, _VP, _SZ,
                                _VP, _VP, _VP, _VP]),
+    "kvs_decode_step_fp8": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                   _VP, _VP, _I32, _VP, _I32, _VP, _VP, _I32, _I32, _I32, _I32,
+                                   _F32, _VP, _VP, _SZ, _VP, _VP, _VP, _VP]),
     "kvs_compact_blocks": (_I32, [_VP, _VP, _VP, _I32, _I64, _I32, _I32, _VP, _VP, _VP, _VP,
                                   _I32, _VP, _VP]),
     "kvs_compact_blocks_fp8": (_I32, [_VP, _VP, _VP, _I32, _I64, _I32, _I32, _VP, _VP, _VP, _VP,

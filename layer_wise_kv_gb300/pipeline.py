@@ -482,12 +482,21 @@ class DecodeBatch:
          lens_d, out, ws, status) = self._nat
         raw_stream = _raw_stream(stream, self._dev_index)
         n_cow, n_patch = self._counts
-        kvs._check(self._lib.kvs_decode_step(
-            alloc, tables_h, lens_h, patch_h[slot], cow_h[slot], patch_d, cow_d, q.data_ptr(),
-            k_new.data_ptr(), v_new.data_ptr(), k_pool, v_pool, self.eng.num_blocks, tables_d,
-            self.max_blocks, lens_d[self.cur], lens_d[1 - self.cur], self.n_items, s.h_q, s.h_kv,
-            s.d, s.scale, out, ws, self.ws_bytes, status, self._count_refs[0],
-            self._count_refs[1], raw_stream))
+        if self.eng.kv_fp8:
+            kvs._check(self._lib.kvs_decode_step_fp8(
+                alloc, tables_h, lens_h, patch_h[slot], cow_h[slot], patch_d, cow_d,
+                q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), k_pool, v_pool,
+                self.eng.k_scale.data_ptr(), self.eng.v_scale.data_ptr(), self.eng.num_blocks,
+                tables_d, self.max_blocks, lens_d[self.cur], lens_d[1 - self.cur], self.n_items,
+                s.h_q, s.h_kv, s.d, s.scale, out, ws, self.ws_bytes, status,
+                self._count_refs[0], self._count_refs[1], raw_stream))
+        else:
+            kvs._check(self._lib.kvs_decode_step(
+                alloc, tables_h, lens_h, patch_h[slot], cow_h[slot], patch_d, cow_d,
+                q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), k_pool, v_pool,
+                self.eng.num_blocks, tables_d, self.max_blocks, lens_d[self.cur],
+                lens_d[1 - self.cur], self.n_items, s.h_q, s.h_kv, s.d, s.scale, out, ws,
+                self.ws_bytes, status, self._count_refs[0], self._count_refs[1], raw_stream))
         if n_patch.value or n_cow.value:
             # this slot's staging buffers are read by copies queued above
             ev = torch.cuda.Event()
@@ -584,7 +593,7 @@ class DecodeBatch:
         timing: optional list receiving a (start, end) event pair around the
         decode kernel.  Without graphs or timing, the step is one native call
         (kvs_decode_step: host preparation, uploads and decode)."""
-        if self._graphs is None and timing is None and not self.eng.kv_fp8:
+        if self._graphs is None and timing is None:
             return self._native_step(q, k_new, v_new, stream)
         eng, s = self.eng, self.eng.shape
         n = self.n_items

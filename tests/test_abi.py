@@ -140,6 +140,12 @@ def test_invalid_arguments_rejected_before_launch(kvs):
     assert lib.kvs_decode_step(*args) == kvs.KVS_OK
     args[17] = 4
     assert lib.kvs_decode_step(*args) == kvs.KVS_ERR_INVALID
+    # the FP8 step: the same checks, with the two scale arrays after the pools
+    args8 = args[:12] + [None, None] + args[12:]
+    args8[19] = 0                                   # n_items
+    assert lib.kvs_decode_step_fp8(*args8) == kvs.KVS_OK
+    args8[19] = 4
+    assert lib.kvs_decode_step_fp8(*args8) == kvs.KVS_ERR_INVALID
 
 
 def test_worked_example_allocator(kvs, golden_dir):
