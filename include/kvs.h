@@ -12,6 +12,12 @@
  *      tracked by a block allocator (free list, reference counts,
  *      copy-on-write)                                   -> kvs_alloc_*, kvs_copy_blocks
  *   5. decode attention gathering K/V through block tables -> kvs_paged_decode
+ *      (one whole step with the host allocator's work   -> kvs_decode_step)
+ * Beyond them:
+ *   - decode-time replacement in budgeted layers -> kvs_evict_place,
+ *     kvs_paged_decode_logits, kvs_decode_scores_from_logits (section 7)
+ *   - FP8 (e4m3, per-row scale) pools -> kvs_compact_blocks_fp8,
+ *     kvs_copy_blocks_fp8, kvs_paged_decode_fp8, kvs_decode_step_fp8
  *
  * Conventions (all entry points)
  *   - bf16 tensors are passed as raw 16-bit patterns (kvs_bf16).
