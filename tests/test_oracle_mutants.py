@@ -1,0 +1,223 @@
+"""The pins catch plausible mistakes: each test here plants one mistake in the
+oracle (a mutated copy of one function, patched in on the CPU for the length
+of the test) and checks that the pin meant to catch it then fails.  Nothing
+here touches a GPU or the CUDA library."""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import eviction, flow
+import test_oracle_pins as pins
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _fails(fn, *args):
+    with pytest.raises(AssertionError):
+        fn(*args)
+
+
+# --------------------------------------------------------------------------- selection
+def _select_ties_high(scores, n, k, recent):
+    if k is None or k >= n:
+        return np.arange(n, dtype=np.int64)
+    cand = np.arange(0, n - recent)
+    order = cand[np.lexsort((-cand, -np.asarray(scores)[cand].astype(np.float64)))]
+    return np.sort(np.concatenate([order[: k - recent], np.arange(n - recent, n)]))
+
+
+def _select_one_too_many(scores, n, k, recent):
+    if k is None or k >= n:
+        return np.arange(n, dtype=np.int64)
+    cand = np.arange(0, n - recent)
+    order = cand[np.lexsort((cand, -np.asarray(scores)[cand].astype(np.float64)))]
+    return np.sort(np.concatenate([order[: k - recent + 1], np.arange(n - recent, n)]))
+
+
+def _select_recent_short(scores, n, k, recent):
+    if k is None or k >= n:
+        return np.arange(n, dtype=np.int64)
+    r = max(recent - 1, 0)
+    cand = np.arange(0, n - r)
+    order = cand[np.lexsort((cand, -np.asarray(scores)[cand].astype(np.float64)))]
+    return np.sort(np.concatenate([order[: k - r], np.arange(n - r, n)]))
+
+
+@pytest.mark.parametrize("mutant", [_select_ties_high, _select_one_too_many, _select_recent_short])
+def test_selection_mutants_fail_the_pins(monkeypatch, mutant):
+    monkeypatch.setattr(oracle, "select_kept", mutant)
+    with pytest.raises(AssertionError):
+        pins.test_selection_all_equal_keeps_lowest_positions_and_recent()
+        for trial in range(12):
+            pins.test_selection_brute_force(trial)
+
+
+# --------------------------------------------------------------------------- prefill
+def _prefill_gqa_modulo(q, k, v, scale, rows=None, heads=None):
+    n, h_q, d = q.shape
+    h_kv = k.shape[1]
+    rows = np.arange(n) if rows is None else np.asarray(rows)
+    out = np.zeros((rows.size, h_q, d))
+    visible = np.arange(n)[None, :] <= rows[:, None]
+    m_out, l_out = np.zeros((h_q, rows.size)), np.zeros((h_q, rows.size))
+    for g in range(h_q):
+        h = g % h_kv                                    # the mistake: interleaved groups
+        s = np.where(visible, (q[rows, g] @ k[:, h].T) * scale, -np.inf)
+        m = s.max(axis=1)
+        e = np.exp(s - m[:, None])
+        out[:, g] = (e / e.sum(axis=1)[:, None]) @ v[:, h]
+        m_out[g], l_out[g] = m, e.sum(axis=1)
+    return out, m_out, l_out
+
+
+def _prefill_strict_causal(q, k, v, scale, rows=None, heads=None):
+    n, h_q, d = q.shape
+    group = h_q // k.shape[1]
+    rows = np.arange(n) if rows is None else np.asarray(rows)
+    out = np.zeros((rows.size, h_q, d))
+    visible = np.arange(n)[None, :] < rows[:, None]      # the mistake: < for <=
+    m_out, l_out = np.zeros((h_q, rows.size)), np.zeros((h_q, rows.size))
+    with np.errstate(invalid="ignore", divide="ignore"):
+        for g in range(h_q):
+            h = g // group
+            s = np.where(visible, (q[rows, g] @ k[:, h].T) * scale, -np.inf)
+            m = s.max(axis=1)
+            e = np.exp(s - m[:, None])
+            out[:, g] = (e / e.sum(axis=1)[:, None]) @ v[:, h]
+            m_out[g], l_out[g] = m, e.sum(axis=1)
+    return out, m_out, l_out
+
+
+@pytest.mark.parametrize("mutant", [_prefill_gqa_modulo, _prefill_strict_causal])
+def test_prefill_mutants_fail_the_pins(monkeypatch, mutant):
+    monkeypatch.setattr(oracle, "prefill_rows", mutant)
+    _fails(pins.test_prefill_O_equals_sdpa, 67, 4, 2, 16)
+
+
+# --------------------------------------------------------------------------- window scores
+def _scores_window_shifted(q, k, m, l, alpha, scale):
+    n, h_q, _ = q.shape
+    h_kv = k.shape[1]
+    group = h_q // h_kv
+    win = np.arange(n - alpha - 1, n - 1)               # the mistake: one row early
+    visible = np.arange(n)[None, :] <= win[:, None]
+    S = np.zeros((h_kv, n))
+    for g in range(h_q):
+        s = (q[win, g] @ k[:, g // group].T) * scale
+        S[g // group] += (np.exp(np.where(visible, s, -np.inf) - m[g][:, None]) /
+                          l[g][:, None]).sum(axis=0)
+    return S
+
+
+def _scores_no_group_sum(q, k, m, l, alpha, scale):
+    n, h_q, _ = q.shape
+    h_kv = k.shape[1]
+    group = h_q // h_kv
+    win = np.arange(n - alpha, n)
+    visible = np.arange(n)[None, :] <= win[:, None]
+    S = np.zeros((h_kv, n))
+    for h in range(h_kv):
+        g = h * group                                   # the mistake: one query head per group
+        s = (q[win, g] @ k[:, h].T) * scale
+        S[h] += (np.exp(np.where(visible, s, -np.inf) - m[g][:, None]) /
+                 l[g][:, None]).sum(axis=0)
+    return S
+
+
+@pytest.mark.parametrize("mutant", [_scores_window_shifted, _scores_no_group_sum])
+def test_window_score_mutants_fail_the_pins(monkeypatch, mutant):
+    monkeypatch.setattr(oracle, "window_scores", mutant)
+    _fails(pins.test_window_scores_equal_sdpa_probability_column_sums)
+
+
+# --------------------------------------------------------------------------- paging
+class _LifoPool(oracle.BlockPool):
+    def alloc(self):
+        if not self.free:
+            raise oracle.OutOfBlocks()
+        b = self.free.pop()                             # the mistake: pop the tail
+        self.ref[b] = 1
+        return b
+
+
+def test_lifo_pool_fails_the_worked_example(monkeypatch):
+    monkeypatch.setattr(oracle, "BlockPool", _LifoPool)
+    _fails(pins.test_paging_worked_example, GOLDEN)
+
+
+# --------------------------------------------------------------------------- decode
+def _decode_values_reversed(q, k_cache, v_cache, scale):
+    return oracle.attention.decode_attention(q, k_cache, v_cache[:, ::-1], scale)
+
+
+def test_decode_mutant_fails_the_dense_pin(monkeypatch):
+    monkeypatch.setattr(flow, "decode_attention", _decode_values_reversed)
+    _fails(pins.test_decode_full_cache_equals_dense_attention)
+
+
+# --------------------------------------------------------------------------- eviction
+def _replace_highest(score, pos, new_pos, recent):
+    best = None
+    for i in range(len(pos)):
+        if pos[i] > new_pos - recent:
+            continue
+        if best is None or (score[i], -pos[i]) > (score[best], -pos[best]):
+            best = i
+    return best
+
+
+def _replace_ignores_window(score, pos, new_pos, recent):
+    return int(np.lexsort((pos, score))[0])             # the mistake: recent tokens eligible
+
+
+@pytest.mark.parametrize("mutant", [_replace_highest, _replace_ignores_window])
+def test_eviction_mutants_fail_the_pins(monkeypatch, mutant):
+    monkeypatch.setattr(eviction, "replace_slot", mutant)
+    _fails(pins.test_eviction_replaces_lowest_outside_recent_window_brute_force)
+
+
+# --------------------------------------------------------------------------- FP8
+def _encode_ties_away(x):
+    x = np.asarray(x, dtype=np.float64)
+    vals = oracle.fp8.E4M3_TABLE[:0x7F]
+    sign = np.where(np.signbit(x), 0x80, 0)
+    a = np.minimum(np.abs(x), 448.0)
+    lo = np.clip(np.searchsorted(vals, a, side="right") - 1, 0, 126)
+    hi = np.minimum(lo + 1, 126)
+    pick_lo = (a - vals[lo]) < (vals[hi] - a)           # the mistake: ties go up
+    return (sign | np.where(pick_lo, lo, hi)).astype(np.uint8)
+
+
+def _value_bias_8(code):
+    code = int(code) & 0xFF
+    if code in (0x7F, 0xFF):
+        return float("nan")
+    sign = -1.0 if code & 0x80 else 1.0
+    e, m = (code >> 3) & 0xF, code & 0x7
+    if e == 0:
+        return sign * (m / 8.0) * 2.0 ** -6
+    return sign * (1.0 + m / 8.0) * 2.0 ** (e - 8)      # the mistake: bias 8
+
+
+def _quantize_scale_447(x):
+    x32 = np.asarray(x, dtype=np.float32)
+    amax = np.float32(np.abs(x32).max())
+    scale = np.float32(amax / np.float32(447.0)) if amax > 0 else np.float32(1.0)
+    return oracle.fp8.e4m3_encode((x32 / scale).astype(np.float32)), scale
+
+
+def test_fp8_encode_mutant_fails_the_torch_pin(monkeypatch):
+    monkeypatch.setattr(oracle.fp8, "e4m3_encode", _encode_ties_away)
+    _fails(pins.test_fp8_encode_matches_torch_round_to_nearest_even)
+
+
+def test_fp8_decode_mutant_fails_the_torch_pin(monkeypatch):
+    monkeypatch.setattr(oracle.fp8, "e4m3_value", _value_bias_8)
+    _fails(pins.test_fp8_decode_matches_torch_for_every_code)
+
+
+def test_fp8_scale_mutant_fails_the_bound_pin(monkeypatch):
+    monkeypatch.setattr(oracle.fp8, "quantize_row", _quantize_scale_447)
+    _fails(pins.test_fp8_row_quantisation_bounds)
