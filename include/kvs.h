@@ -270,8 +270,11 @@ kvs_status kvs_copy_blocks(const int32_t* src, const int32_t* dst, int32_t count
  *   lens_next    [batch] int32, nullable, must not alias lens: receives
  *                lens[i] + (k_new != NULL).
  *   workspace    scratch of kvs_paged_decode_workspace_size(batch, h_q, h_kv,
- *                d) bytes (split partials); needs no initialisation.  Calls
- *                sharing a workspace must not overlap in time.
+ *                d) bytes (split partials; the size covers the bf16 and the
+ *                FP8 decode, whose launches differ in warps per CTA, so the
+ *                bf16 decode alone accepts a little less); needs no
+ *                initialisation.  Calls sharing a workspace must not overlap
+ *                in time.
  *   q, out, the pools and the workspace must be 16-byte aligned
  *   (KVS_ERR_INVALID otherwise).
  * Two launches on `stream`: the split decode, then a merge of the splits (a

@@ -908,6 +908,16 @@ bool pool_map(MapCache& c, const void* pool, int num_blocks, int h_kv, int d) {
 }
 
 
+// Partial slots one launch may touch: one per (warp, segment it touches),
+// slot = warp + segment, for `warps` warps per CTA.
+size_t workspace_need(int32_t batch, int32_t h_q, int32_t h_kv, int32_t d, int warps) {
+  if (batch <= 0 || h_kv <= 0 || h_q <= 0 || d <= 0) return 0;
+  const int64_t G = h_q / h_kv;
+  const int64_t slots = static_cast<int64_t>(kMaxGrid) * warps +
+                        static_cast<int64_t>(batch) * h_kv;
+  return static_cast<size_t>(slots * part_floats(static_cast<int>(G), d) * 4);
+}
+
 int sm_count_dec() {
   static int n = 0;
   if (n == 0) {
@@ -1003,12 +1013,8 @@ kvs_status launch_decode(DecodeParams& prm, const CUtensorMap& km, const CUtenso
 extern "C" {
 
 size_t kvs_paged_decode_workspace_size(int32_t batch, int32_t h_q, int32_t h_kv, int32_t d) {
-  if (batch <= 0 || h_kv <= 0 || h_q <= 0 || d <= 0) return 0;
-  const int64_t G = h_q / h_kv;
-  // one partial slot per (warp, segment it touches): slot = warp + segment
-  const int64_t slots = static_cast<int64_t>(kvs::kMaxGrid) * kvs::kMaxWarps +
-                        static_cast<int64_t>(batch) * h_kv;
-  return static_cast<size_t>(slots * kvs::part_floats(static_cast<int>(G), d) * 4);
+  // enough for either pool type's decode
+  return kvs::workspace_need(batch, h_q, h_kv, d, kvs::kMaxWarps);
 }
 
 }  // extern "C"
@@ -1048,7 +1054,7 @@ kvs_status paged_decode_impl(const kvs_bf16* q, const kvs_bf16* k_new, const kvs
                   (reinterpret_cast<uintptr_t>(workspace) & 15) == 0,
               "kvs_paged_decode: q, out, pools and workspace must be 16-byte aligned");
   const int64_t G = h_q / h_kv;
-  const size_t need = kvs_paged_decode_workspace_size(batch, h_q, h_kv, d);
+  const size_t need = kvs::workspace_need(batch, h_q, h_kv, d, kvs::dec_warps(fp8));
   KVS_REQUIRE(workspace_bytes >= need, "kvs_paged_decode: workspace %zu bytes < %zu needed",
               workspace_bytes, need);
   static thread_local kvs::MapCache kc, vc;
@@ -1188,7 +1194,7 @@ extern "C" kvs_status kvs_paged_decode_static(const kvs_bf16* q, const kvs_bf16*
   KVS_REQUIRE(batch >= 0, "kvs_paged_decode_static: negative batch");
   if (batch == 0) return KVS_OK;
   KVS_REQUIRE(h_kv > 0 && h_q > 0 && h_q % h_kv == 0, "kvs_paged_decode_static: bad head counts");
-  const size_t need = kvs_paged_decode_workspace_size(batch, h_q, h_kv, d);
+  const size_t need = kvs::workspace_need(batch, h_q, h_kv, d, kvs::dec_warps(false));
   if (need > KVS_DECODE_STATIC_SCRATCH_BYTES)
     return kvs::fail(KVS_ERR_UNSUPPORTED,
                      "kvs_paged_decode_static: this batch needs %zu bytes of scratch; the "
