@@ -677,7 +677,9 @@ class EvictingDecode:
     of each keeps exactly its k_l slots per KV head; each step's new token
     takes the slot of the lowest-scoring token outside the recent window, the
     step attends over the k_l slots, and its attention probabilities are added
-    to the scores (kvs_evict_place, kvs_paged_decode, kvs_decode_scores).
+    to the scores (kvs_evict_place, then kvs_paged_decode_logits and
+    kvs_decode_scores_from_logits; or kvs_paged_decode and kvs_decode_scores,
+    which recompute the logits from K).
 
     Sources: Novita AI, "How KV Sparsity achieves 1.5x acceleration for vLLM",
     section "Key techniques 1" (later layers replace their lowest-scoring KVs
