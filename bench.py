@@ -390,7 +390,11 @@ def bench_gpu(args):
         "scores_ms_per_launch": round(sum(k2_ms) / max(1, len(k2_ms)), 4),
         "scores_layers_per_launch": sum(1 for l in range(L) if w.budget(l, n) is not None
                                         and w.budget(l, n) < n),
-        "gpu_launches": args.steps * (2 * L - 3 + 2 + 2 * steps),
+        # per timed request: the prefill launch(es), the window-score launch(es)
+        # (one event pair around each), selection, compaction, and each decode
+        # step's decode + merge
+        "gpu_launches": args.steps * ((1 if all(x == L for x in k1_layers) else L)
+                                      + len(k2_ms) // max(1, args.steps) + 2 + 2 * steps),
         "clocks": clk,
         "wall_s": round(t_wall, 2),
     }
