@@ -147,6 +147,40 @@ def test_lifo_pool_fails_the_worked_example(monkeypatch):
     _fails(pins.test_paging_worked_example, GOLDEN)
 
 
+def _compact_ignores_idx(k, v, idx, table, pool_k, pool_v, block=16):
+    h_kv, k_eff = idx.shape
+    for h in range(h_kv):
+        for j in range(k_eff):
+            b = table[j // block]
+            pool_k[b, h, j % block] = k[j, h]              # the mistake: slot j <- row j
+            pool_v[b, h, j % block] = v[j, h]
+
+
+def _compact_head0_idx(k, v, idx, table, pool_k, pool_v, block=16):
+    h_kv, k_eff = idx.shape
+    for h in range(h_kv):
+        for j in range(k_eff):
+            b = table[j // block]
+            pool_k[b, h, j % block] = k[idx[0, j], h]      # the mistake: head 0's index
+            pool_v[b, h, j % block] = v[idx[0, j], h]
+
+
+def _compact_sorted_idx(k, v, idx, table, pool_k, pool_v, block=16):
+    h_kv, k_eff = idx.shape
+    for h in range(h_kv):
+        order = np.sort(idx[h])                            # the mistake: index order dropped
+        for j in range(k_eff):
+            b = table[j // block]
+            pool_k[b, h, j % block] = k[order[j], h]
+            pool_v[b, h, j % block] = v[order[j], h]
+
+
+@pytest.mark.parametrize("mutant", [_compact_ignores_idx, _compact_head0_idx, _compact_sorted_idx])
+def test_compaction_mutants_fail_the_selected_set_pin(monkeypatch, mutant):
+    monkeypatch.setattr(oracle, "compact", mutant)
+    _fails(pins.test_compaction_of_a_selected_set_follows_the_index_per_head)
+
+
 # --------------------------------------------------------------------------- decode
 def _decode_values_reversed(q, k_cache, v_cache, scale):
     return oracle.attention.decode_attention(q, k_cache, v_cache[:, ::-1], scale)

@@ -66,6 +66,41 @@ def test_paging_worked_example(golden_dir):
     assert pool.free == g["free_list"][nb:]
 
 
+def test_compaction_of_a_selected_set_follows_the_index_per_head():
+    """Compaction of a selected (not identity) set, read back two ways.
+
+    Every row carries its own coordinates (position and KV head in its first two
+    entries), so each pool slot tells where its bytes came from.  The kept index
+    differs per head, is not sorted by position, and 37 kept slots leave a
+    partial last block.  The worked example's write and gather lines (Ultralytics
+    glossary "PagedAttention", section "How paging works") fix what must hold:
+    reading the table's blocks slot by slot gives the kept rows in index order,
+    the gather returns exactly those rows, and nothing outside the table's
+    blocks or past the last kept slot is touched."""
+    n, h_kv, d, k_eff, nb_pool = 90, 3, 6, 37, 12
+    k = RNG.standard_normal((n, h_kv, d))
+    k[:, :, 0] = np.arange(n)[:, None]
+    k[:, :, 1] = np.arange(h_kv)[None, :]
+    v = k + 1000.0
+    idx = np.stack([RNG.permutation(n)[:k_eff] for _ in range(h_kv)])
+    assert not all(np.array_equal(idx[0], idx[h]) for h in range(1, h_kv))
+    assert not (np.diff(idx, axis=1) > 0).all()
+    table = [9, 2, 6]                                    # scattered, ceil(37/16) = 3
+    sentinel = -7.0
+    pk = np.full((nb_pool, h_kv, 16, d), sentinel)
+    pv = np.full_like(pk, sentinel)
+    oracle.compact(k, v, idx, table, pk, pv)
+    for h in range(h_kv):
+        slots = [pk[table[b], h, s] for b in range(len(table)) for s in range(16)]
+        tags = [(int(r[0]), int(r[1])) for r in slots[:k_eff]]
+        assert tags == [(int(p), h) for p in idx[h]]
+        assert all((r == sentinel).all() for r in slots[k_eff:])
+        np.testing.assert_array_equal(oracle.gather_rows(pk, table, k_eff, h), k[idx[h], h])
+        np.testing.assert_array_equal(oracle.gather_rows(pv, table, k_eff, h), v[idx[h], h])
+    untouched = [b for b in range(nb_pool) if b not in table]
+    assert (pk[untouched] == sentinel).all() and (pv[untouched] == sentinel).all()
+
+
 def test_pool_fifo_refcount_cow():
     pool = oracle.BlockPool(6)
     a, b, c = pool.alloc(), pool.alloc(), pool.alloc()
