@@ -294,6 +294,23 @@ kvs_status kvs_paged_decode(const kvs_bf16* q, const kvs_bf16* k_new, const kvs_
                             int32_t h_kv, int32_t d, float scale, kvs_bf16* out, void* workspace,
                             size_t workspace_bytes, int32_t* status, kvs_stream stream);
 
+/* Test hook for the bounded waits (no counterpart in the method: failure
+ * detection of the library itself).  Same arguments and checks as
+ * kvs_paged_decode without an append, but the decode's copy-issuing lane
+ * arms each stage's barrier and starts none of the copies it announced, and
+ * every barrier wait gives up after wait_ns (0 < wait_ns <= 1.5 s) instead
+ * of the usual 1.5 s.  So every wait runs out: the kernel stores
+ * KVS_ERR_DEVICE_TIMEOUT in `status` (nullable) and returns, nothing is left
+ * in flight, and the context stays usable.  `out` rows are undefined
+ * afterwards; the pools are not written.  Exists so that tests can drive the
+ * timeout path without a fault; serving code has no reason to call it. */
+kvs_status kvs_test_paged_decode_stalled(const kvs_bf16* q, kvs_bf16* k_pool, kvs_bf16* v_pool,
+                                         int32_t num_blocks, int32_t* block_tables,
+                                         int32_t max_blocks, const int32_t* lens, int32_t batch,
+                                         int32_t h_q, int32_t h_kv, int32_t d, float scale,
+                                         kvs_bf16* out, void* workspace, size_t workspace_bytes,
+                                         uint32_t wait_ns, int32_t* status, kvs_stream stream);
+
 /* ------------------------------------------------------------------------
  * Paged decode that allocates nothing (no counterpart in the method's
  * sources: this is a calling convention, not a step of the method).
@@ -308,13 +325,21 @@ kvs_status kvs_paged_decode(const kvs_bf16* q, const kvs_bf16* k_new, const kvs_
  * KVS_DECODE_STATIC_SCRATCH_BYTES; every GPU that loads the library holds
  * that array until the process exits.  It calls no cudaMalloc, cudaFree or
  * allocating library routine.
- *   - Sizes whose workspace (kvs_paged_decode_workspace_size) exceeds the
- *     array are rejected with KVS_ERR_UNSUPPORTED before any launch.  With
- *     h_q = 32, h_kv = 8, d = 128 the array serves up to 624 items (one
- *     32-layer sequence is 32 items and needs about 7 MB).
+ *   - Sizes whose partials (the bf16 decode's share of
+ *     kvs_paged_decode_workspace_size, which also covers the FP8 decode's
+ *     larger launch) exceed the array are rejected with KVS_ERR_UNSUPPORTED
+ *     before any launch.  With h_q = 32, h_kv = 8, d = 128 the array serves
+ *     up to 624 items (one 32-layer sequence is 32 items and needs about
+ *     7 MB); 625 are rejected.
  *   - The first call on a device looks up the array's device address on that
  *     device (the current one); make that first call before any stream
  *     capture.
+ *   - The CUDA runtime creates the array when it first loads the library's
+ *     decode code on a device (under lazy module loading, the default: the
+ *     first decode call of any kind there, or the first call of this entry
+ *     point).  A caller that means to reserve the rest of device memory for
+ *     its pool should make one such call first, or that first call may find
+ *     no room for the array and fail with KVS_ERR_CUDA.
  *   - All calls share the one array and it keeps the last call's contents;
  *     nothing in it needs to start at zero (each call writes its partials
  *     before reading them).  Calls that overlap on the GPU (on

@@ -90,6 +90,8 @@ struct DecodeParams {
   float* k_scale;  // FP8 pools: per-row scales [num_blocks][h_kv][16]
   float* v_scale;
   int32_t* status;
+  uint64_t wait_ns;  // limit of every mbarrier wait
+  int stall;         // test hook: issue no copies, so that every wait runs out
   int batch, max_blocks, num_blocks, h_q, h_kv, group, append, n_stages;
   int q_bytes, q_stride, q_off, bar_off, idx_off;
   float scale_log2;
@@ -158,6 +160,16 @@ __device__ __forceinline__ uint32_t sw_off(int r, int c) {
 // aligned (the merge reads records as float4; G*(D+2) floats alone are not a
 // multiple of four when G is odd)
 __host__ __device__ constexpr int part_floats(int G, int D) { return (G * (D + 2) + 3) & ~3; }
+
+// An item's length as the decode uses it: lens[i] clamped to [0, max_blocks *
+// 16 - append], so that its blocks (appended token included) stay inside its
+// table row and the block counts stay small enough for 32-bit prefix sums.
+// Returns whether the given length was already in range.
+__device__ __forceinline__ bool clamp_len(int v, int max_blocks, int append, int& out) {
+  const int64_t hi = static_cast<int64_t>(max_blocks) * KVS_BLOCK_TOKENS - append;
+  out = v < 0 ? 0 : (static_cast<int64_t>(v) > hi ? static_cast<int>(hi) : v);
+  return out == v;
+}
 
 // owner warp of global block b when T blocks are split evenly over W warps
 // (warp w owns [w*T/W, (w+1)*T/W))
@@ -266,7 +278,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
     for (int i = 0; i < kWarps * NS; ++i) mbar_init(reinterpret_cast<uint64_t*>(smem + p.bar_off) + i, 1);
     fence_mbar_init();
   }
-  for (int b = threadIdx.x; b < p.batch; b += kDecThreads) lens_s[b] = p.lens[b];
+  for (int b = threadIdx.x; b < p.batch; b += kDecThreads)
+    if (!clamp_len(p.lens[b], p.max_blocks, p.append, lens_s[b]))
+      flag_status(p.status, KVS_ERR_INVALID);
   __syncthreads();
   // prefix over items of (blocks x heads); one warp, each lane a contiguous range
   if (warp == 0) {
@@ -320,6 +334,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
       const int s = g_iss % NS;
       uint8_t* st = my_stages + s * L::kStageBytes;
       mbar_arrive_expect_tx(&my_full[s], L::kStageBytes + (j == 0 ? p.q_bytes : 0));
+      if (p.stall) {  // test hook: the copies this stage expects never start
+        ++g_iss;
+        return;
+      }
       const int row = (pb * p.h_kv + x.h) * KVS_BLOCK_TOKENS;
       if constexpr (kF8) {
         const int64_t off = static_cast<int64_t>(row) * D;
@@ -385,7 +403,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
 
     for (int j = 0; j < cur.nblk; ++j) {
       const int s = g_cons % NS;
-      if (!__all_sync(0xffffffffu, mbar_wait(&my_full[s], (g_cons / NS) & 1))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&my_full[s], (g_cons / NS) & 1, p.wait_ns))) {
         flag_status(p.status, KVS_ERR_DEVICE_TIMEOUT);
         aborted = true;
         break;
@@ -741,7 +759,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
   // leave no load of ours landing in shared memory after we return
   if (lane == 0)
     for (int g = g_cons; g < g_iss; ++g)
-      if (!mbar_wait(&my_full[g % NS], (g / NS) & 1)) break;
+      if (!mbar_wait(&my_full[g % NS], (g / NS) & 1, p.wait_ns)) break;
   __syncwarp();
 }
 
@@ -763,7 +781,7 @@ constexpr int kMergeBatch = 6;
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads, 2)
 decode_merge_kernel(const float* __restrict__ ws_part, const int32_t* __restrict__ lens, int batch,
-                    int append, int h_q, int h_kv, int G, int n_warps,
+                    int max_blocks, int append, int h_q, int h_kv, int G, int n_warps,
                     uint16_t* __restrict__ out, float* __restrict__ lse) {
   __shared__ float4 s_acc[kMergeGroups][kMergeGroupThreads];
   __shared__ float2 s_ml[kMergeGroups][kMergeGroupThreads];
@@ -778,7 +796,9 @@ decode_merge_kernel(const float* __restrict__ ws_part, const int32_t* __restrict
     const int b0 = threadIdx.x * per, b1 = min(batch, b0 + per);
     int sum = 0, before = 0;
     for (int b = b0; b < b1; ++b) {
-      const int nbk = (lens[b] + append + KVS_BLOCK_TOKENS - 1) / KVS_BLOCK_TOKENS * h_kv;
+      int lb;
+      clamp_len(lens[b], max_blocks, append, lb);  // as the decode kernel clamps it
+      const int nbk = (lb + append + KVS_BLOCK_TOKENS - 1) / KVS_BLOCK_TOKENS * h_kv;
       if (b < item) before += nbk;
       sum += nbk;
     }
@@ -789,7 +809,9 @@ decode_merge_kernel(const float* __restrict__ ws_part, const int32_t* __restrict
     __syncthreads();
   }
   const int64_t T = s_total;
-  const int nb = (lens[item] + append + KVS_BLOCK_TOKENS - 1) / KVS_BLOCK_TOKENS;
+  int len_item;
+  clamp_len(lens[item], max_blocks, append, len_item);
+  const int nb = (len_item + append + KVS_BLOCK_TOKENS - 1) / KVS_BLOCK_TOKENS;
   if (nb == 0) return;  // no tokens: no output row
   const int64_t seg_lo = s_before + static_cast<int64_t>(h) * nb;
   const int W = static_cast<int>(T < n_warps ? T : n_warps);
@@ -1001,7 +1023,8 @@ kvs_status launch_decode(DecodeParams& prm, const CUtensorMap& km, const CUtenso
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   KVS_CUDA(cudaLaunchKernelEx(&cfg, decode_merge_kernel<D>, static_cast<const float*>(prm.ws_part),
-                              prm.lens, prm.batch, prm.append, prm.h_q, prm.h_kv, prm.group,
+                              prm.lens, prm.batch, prm.max_blocks, prm.append, prm.h_q, prm.h_kv,
+                              prm.group,
                               grid * kWarps, prm.out, prm.logits != nullptr ? prm.lse : nullptr),
            "kvs_paged_decode (merge launch)");
   return KVS_OK;
@@ -1029,7 +1052,8 @@ kvs_status paged_decode_impl(const kvs_bf16* q, const kvs_bf16* k_new, const kvs
                              size_t workspace_bytes, int32_t* status, kvs_stream stream,
                              float* logits, int32_t logit_ld, float* lse,
                              float* k_scale = nullptr, float* v_scale = nullptr,
-                             bool fp8 = false) {
+                             bool fp8 = false, uint64_t wait_ns = kvs::kWaitLimitNs,
+                             bool stall = false) {
   KVS_REQUIRE(batch >= 0, "kvs_paged_decode: negative batch");
   if (batch == 0) return KVS_OK;
   KVS_REQUIRE(q && k_pool && v_pool && block_tables && lens && out && workspace,
@@ -1045,6 +1069,9 @@ kvs_status paged_decode_impl(const kvs_bf16* q, const kvs_bf16* k_new, const kvs
   KVS_SUPPORTED(batch <= kvs::kMaxBatch, "kvs_paged_decode: batch %d > %d", batch,
                 kvs::kMaxBatch);
   KVS_REQUIRE(num_blocks > 0 && max_blocks > 0, "kvs_paged_decode: bad sizes");
+  // the kernels' block counts (lengths clamped to each table row) are 32-bit sums
+  KVS_REQUIRE(static_cast<int64_t>(batch) * max_blocks * h_kv < (1ll << 31),
+              "kvs_paged_decode: batch x max_blocks x h_kv must stay below 2^31");
   KVS_REQUIRE(static_cast<int64_t>(num_blocks) * h_kv * KVS_BLOCK_TOKENS < (1ll << 31),
               "kvs_paged_decode: pool too large for 32-bit TMA row coordinates");
   KVS_REQUIRE((reinterpret_cast<uintptr_t>(k_pool) & 15) == 0 &&
@@ -1086,6 +1113,8 @@ kvs_status paged_decode_impl(const kvs_bf16* q, const kvs_bf16* k_new, const kvs
   prm.k_scale = k_scale;
   prm.v_scale = v_scale;
   prm.status = status;
+  prm.wait_ns = wait_ns;
+  prm.stall = stall ? 1 : 0;
   prm.batch = batch;
   prm.max_blocks = max_blocks;
   prm.num_blocks = num_blocks;
@@ -1150,6 +1179,21 @@ kvs_status kvs_paged_decode_logits(const kvs_bf16* q, const kvs_bf16* k_new,
   return paged_decode_impl(q, k_new, v_new, k_pool, v_pool, num_blocks, block_tables, max_blocks,
                            table_patch, lens, lens_next, batch, h_q, h_kv, d, scale, out,
                            workspace, workspace_bytes, status, stream, logits, logit_ld, lse);
+}
+
+kvs_status kvs_test_paged_decode_stalled(const kvs_bf16* q, kvs_bf16* k_pool, kvs_bf16* v_pool,
+                                         int32_t num_blocks, int32_t* block_tables,
+                                         int32_t max_blocks, const int32_t* lens, int32_t batch,
+                                         int32_t h_q, int32_t h_kv, int32_t d, float scale,
+                                         kvs_bf16* out, void* workspace, size_t workspace_bytes,
+                                         uint32_t wait_ns, int32_t* status, kvs_stream stream) {
+  KVS_REQUIRE(wait_ns > 0 && wait_ns <= kvs::kWaitLimitNs,
+              "kvs_test_paged_decode_stalled: wait_ns must be in (0, %llu]",
+              static_cast<unsigned long long>(kvs::kWaitLimitNs));
+  return paged_decode_impl(q, nullptr, nullptr, k_pool, v_pool, num_blocks, block_tables,
+                           max_blocks, nullptr, lens, nullptr, batch, h_q, h_kv, d, scale, out,
+                           workspace, workspace_bytes, status, stream, nullptr, 0, nullptr,
+                           nullptr, nullptr, false, wait_ns, true);
 }
 
 }  // extern "C"

@@ -93,14 +93,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
 }
 
 // Wait until the phase with the given parity has completed.  Gives up after
-// kWaitLimitNs and returns false (the caller records a timeout and unwinds).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// limit_ns (kWaitLimitNs by default) and returns false (the caller records a
+// timeout and unwinds).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
     if (mbar_try_wait(a, parity)) return true;
-    if (globaltimer() - t0 > kWaitLimitNs) return false;
+    if (globaltimer() - t0 > limit_ns) return false;
   }
 }
 

@@ -85,6 +85,9 @@ _SIGS = {
                                 _I32, _I32, _I32, _F32, _VP, _VP, _SZ, _VP, _VP]),
     "kvs_paged_decode_static": (_I32, [_VP, _VP, _VP, _VP, _VP, _I32, _VP, _I32, _VP, _VP, _VP,
                                        _I32, _I32, _I32, _I32, _F32, _VP, _VP, _VP]),
+    "kvs_test_paged_decode_stalled": (_I32, [_VP, _VP, _VP, _I32, _VP, _I32, _VP, _I32, _I32,
+                                             _I32, _I32, _F32, _VP, _VP, _SZ, ctypes.c_uint32,
+                                             _VP, _VP]),
     "kvs_alloc_create": (_I32, [_I32, _VP, _I32, ctypes.POINTER(_VP)]),
     "kvs_alloc_destroy": (None, [_VP]),
     "kvs_alloc_block": (_I32, [_VP, _P32]),
@@ -295,6 +298,17 @@ def kvs_paged_decode(q, k_new, v_new, k_pool, v_pool, num_blocks, block_tables, 
         _dev(lens, "i32", "lens"), None if lens_next is None else _dev(lens_next, "i32", "lens_next"),
         batch, h_q, h_kv, d, float(scale), _dev(out, "bf16", "out"),
         _dev(workspace, "u8", "workspace"), workspace_bytes,
+        None if status is None else _dev(status, "i32", "status"), _stream(stream)))
+
+
+def kvs_test_paged_decode_stalled(q, k_pool, v_pool, num_blocks, block_tables, max_blocks, lens,
+                                  batch, h_q, h_kv, d, scale, out, workspace, workspace_bytes,
+                                  wait_ns, status=None, stream=None):
+    _check(library().kvs_test_paged_decode_stalled(
+        _dev(q, "bf16", "q"), _dev(k_pool, "bf16", "k_pool"), _dev(v_pool, "bf16", "v_pool"),
+        num_blocks, _dev(block_tables, "i32", "block_tables"), max_blocks,
+        _dev(lens, "i32", "lens"), batch, h_q, h_kv, d, float(scale), _dev(out, "bf16", "out"),
+        _dev(workspace, "u8", "workspace"), workspace_bytes, int(wait_ns),
         None if status is None else _dev(status, "i32", "status"), _stream(stream)))
 
 

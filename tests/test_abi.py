@@ -68,6 +68,20 @@ def test_invalid_arguments_rejected_before_launch(kvs):
     assert lib.kvs_prefill_attn_lse(1, 1, 1, 1, 1, 1, 1, 1, 16, 16, 6, 4, 128, 0.1, None,
                                     None) == kvs.KVS_ERR_INVALID  # 6 % 4 != 0
     assert kvs.kvs_paged_decode_workspace_size(0, 32, 8, 128) == 0
+    # block counts beyond 32-bit prefix sums (batch x max_blocks x h_kv >= 2^31)
+    rc = lib.kvs_paged_decode(256, None, None, 256, 256, 4, 256, 1 << 20, None, 256, None, 2048,
+                              32, 8, 128, 0.1, 256, 256, 1 << 40, None, None)
+    assert rc == kvs.KVS_ERR_INVALID and "2^31" in kvs.last_error()
+    # the allocation-free decode: 625 items at the Llama-3-8B head shapes exceed
+    # its built-in array and are refused before any CUDA call
+    rc = lib.kvs_paged_decode_static(None, None, None, None, None, 1, None, 1, None, None, None,
+                                     625, 32, 8, 128, 0.1, None, None, None)
+    assert rc == kvs.KVS_ERR_UNSUPPORTED and "built-in array" in kvs.last_error()
+    # the stalled-decode test hook checks its wait limit first
+    for wait_ns in (0, 2_000_000_000):
+        assert lib.kvs_test_paged_decode_stalled(256, 256, 256, 4, 256, 1, 256, 1, 32, 8, 128,
+                                                 0.1, 256, 256, 1 << 20, wait_ns, None,
+                                                 None) == kvs.KVS_ERR_INVALID
     # the multi-layer entries: zero layers is a no-op, a negative count an error,
     # both before any launch
     assert lib.kvs_prefill_attn_lse_layers(256, 256, 256, 256, 256, 256, 256, 1, 16, 16, 8, 2,

@@ -374,7 +374,9 @@ def test_layerwise_upload_matches_resident_inputs():
 def test_decode_graphs_match_eager():
     """DecodeBatch.capture_graphs(): steps replayed from CUDA graphs give, bit
     for bit, the outputs, block tables, lengths, refcounts and pool bytes of
-    eager steps.  Three samples share a prompt's blocks, so the first step
+    eager steps, and every replayed step's outputs match the oracle's flow
+    (its allocator, copy-on-write and decode attention) within the output
+    tolerance.  Three samples share a prompt's blocks, so the first step
     copies blocks on write (launched eagerly), and later steps cross block
     boundaries (graphs that upload a table patch) and stay inside blocks
     (graphs without one)."""
@@ -382,7 +384,7 @@ def test_decode_graphs_match_eager():
     from layer_wise_kv_gb300.pipeline import DecodeBatch, Engine
     w = tiny()
     n, L, N, S, steps = 100, w.n_layers, 64, 3, 24
-    ql, kl, vl, _ = _layers_to_device(w, [3], [n])
+    ql, kl, vl, host = _layers_to_device(w, [3], [n])
     budgets = [[w.budget(l, n) for l in range(L)]]
     dq = {(s, l): decode_qkv(w, 3, l, steps, sample=s) for s in range(S) for l in range(L)}
     runs = []
@@ -398,12 +400,35 @@ def test_decode_graphs_match_eager():
             dec.set_stream(s, res.tables[0], res.k_eff[0])
         if graphs:
             dec.capture_graphs()
+            # the oracle's flow over the same kept sets: allocator, pools, streams
+            torch.cuda.synchronize()
+            pool = oracle.BlockPool(N)
+            opk = np.zeros((N, w.h_kv, 16, w.d), np.uint16)
+            opv = np.zeros_like(opk)
+            recs = []
+            for l in range(L):
+                qb, kb, vb = host[(3, l)]
+                rec = flow.sparsify_layer(w, l, qb, kb, vb)
+                rec.idx = _gpu_idx(res, 0, l, w.h_kv, rec.k_eff)
+                flow.place_layer(rec, pool, kb, vb, opk, opv)
+                assert res.tables[0][l] == rec.table
+                recs.append(rec)
+            streams = [flow.new_stream(recs)]
+            streams += [flow.share_stream(pool, streams[0]) for _ in range(1, S)]
         outs = []
         for t in range(steps):
             q = dev_bf16(np.stack([dq[(s, l)][0][t] for s in range(S) for l in range(L)]))
             k = dev_bf16(np.stack([dq[(s, l)][1][t] for s in range(S) for l in range(L)]))
             v = dev_bf16(np.stack([dq[(s, l)][2][t] for s in range(S) for l in range(L)]))
             outs.append(dec.step(q, k, v).clone())
+            if graphs:
+                got = bf16_f64(outs[-1])
+                for s in range(S):
+                    for l in range(L):
+                        flow.prepare_append(pool, streams[s], l, opk, opv)
+                        ref = flow.append_and_attend(w, streams[s], l, dq[(s, l)][0][t],
+                                                     dq[(s, l)][1][t], dq[(s, l)][2][t], opk, opv)
+                        assert np.abs(got[s * L + l] - ref).max() <= ABS_O, (t, s, l)
         torch.cuda.synchronize()
         eng.check_status()
         runs.append((eng, dec, outs))
@@ -411,10 +436,11 @@ def test_decode_graphs_match_eager():
     for t in range(steps):
         assert torch.equal(oa[t].view(torch.int16), ob[t].view(torch.int16)), t
     for s in range(S):
-        assert da.stream_tables(s) == db.stream_tables(s)
+        assert da.stream_tables(s) == db.stream_tables(s) == streams[s].tables
     assert torch.equal(da.tables_d, db.tables_d)
     assert torch.equal(da.lens_d[da.cur], db.lens_d[db.cur])
-    assert [ea.alloc.refcount(b) for b in range(N)] == [eb.alloc.refcount(b) for b in range(N)]
+    assert [ea.alloc.refcount(b) for b in range(N)] == [eb.alloc.refcount(b) for b in range(N)] \
+        == pool.ref
     np.testing.assert_array_equal(host_bits(ea.k_pool), host_bits(eb.k_pool))
     np.testing.assert_array_equal(host_bits(ea.v_pool), host_bits(eb.v_pool))
 

@@ -408,12 +408,60 @@ def test_engine_fp8_shared_prefix_copy_on_write():
     assert [eng.alloc.refcount(b) for b in range(N)] == pool.ref
 
 
+class _Fp8SampleOracle:
+    """The oracle's side of S samples sharing one FP8-compacted prompt: its
+    allocator and streams (flow), and per sample, layer and KV head the stored
+    values (dequantised e4m3 codes times row scales) the sample attends over."""
+
+    def __init__(self, w, res, host, layers, S, N):
+        from oracle import flow
+        self.w, self.S, self.L = w, S, len(layers)
+        self.pool = oracle.BlockPool(N)
+        recs, rows_k, rows_v = [], [], []
+        for li, l in enumerate(layers):
+            qb, kb, vb = host[l]
+            rec = flow.sparsify_layer(w, l, qb, kb, vb)
+            off = int(res.idx_off[0, li])
+            rec.idx = res.kept_idx[off:off + w.h_kv * rec.k_eff].cpu().numpy().reshape(w.h_kv, -1)
+            flow.place_layer(rec, self.pool, kb, vb, None, None)
+            assert res.tables[0][li] == rec.table
+            recs.append(rec)
+            for rows, x in ((rows_k, kb), (rows_v, vb)):
+                rows.append([list(oracle.fp8.dequantize_rows(*oracle.fp8.quantize_rows_fast(
+                    bf16_to_f64(x[rec.idx[h], h]).astype(np.float32)))) for h in range(w.h_kv)])
+        self.streams = [flow.new_stream(recs)]
+        self.streams += [flow.share_stream(self.pool, self.streams[0]) for _ in range(1, S)]
+        self.kval = [[[list(r) for r in rows_k[li]] for li in range(self.L)] for _ in range(S)]
+        self.vval = [[[list(r) for r in rows_v[li]] for li in range(self.L)] for _ in range(S)]
+
+    def step(self, qs, ks, vs):
+        """One decode step of every (sample, layer): qs[(s, li)] etc. are the
+        step's bf16 rows.  Returns the expected outputs [(S * L), h_q, d]."""
+        from oracle import flow
+        w, outs = self.w, []
+        for s in range(self.S):
+            for li in range(self.L):
+                flow.prepare_append(self.pool, self.streams[s], li)
+                self.streams[s].lens[li] += 1
+                for h in range(w.h_kv):
+                    for vals, x in ((self.kval, ks), (self.vval, vs)):
+                        vals[s][li][h].append(oracle.fp8.dequantize_rows(
+                            *oracle.fp8.quantize_rows_fast(
+                                bf16_to_f64(x[(s, li)][h:h + 1]).astype(np.float32)))[0])
+                kk = np.stack([np.stack(self.kval[s][li][h]) for h in range(w.h_kv)])
+                vv = np.stack([np.stack(self.vval[s][li][h]) for h in range(w.h_kv)])
+                outs.append(oracle.decode_attention(bf16_to_f64(qs[(s, li)]), kk, vv, w.scale))
+        return np.stack(outs)
+
+
 def test_engine_fp8_graphs_match_eager():
     """DecodeBatch.capture_graphs() over FP8 pools: steps replayed from CUDA
     graphs give, bit for bit, the outputs, tables, lengths, reference counts,
-    codes and scales of eager steps.  Three samples share a prompt (the first
-    step copies blocks on write, launched eagerly); later steps cross block
-    boundaries (graphs that upload a table patch) and stay inside blocks."""
+    codes and scales of eager steps, and every replayed step's outputs match
+    the oracle's attention over the stored values within the output
+    tolerance.  Three samples share a prompt (the first step copies blocks on
+    write, launched eagerly); later steps cross block boundaries (graphs that
+    upload a table patch) and stay inside blocks."""
     kvs_lib()
     from layer_wise_kv_gb300.pipeline import DecodeBatch, Engine, Shape
     from synth import decode_qkv, llama3_8b, prefill_qkv
@@ -438,11 +486,17 @@ def test_engine_fp8_graphs_match_eager():
             dec.set_stream(s, res.tables[0], res.k_eff[0])
         if graphs:
             dec.capture_graphs()
+            torch.cuda.synchronize()
+            orc = _Fp8SampleOracle(w, res, host, layers, S, N)
         outs = []
         for t in range(steps):
             q, k, v = (dev_bf16(np.stack([dq[(s, li)][i][t] for s in range(S) for li in range(L)]))
                        for i in range(3))
             outs.append(dec.step(q, k, v).clone())
+            if graphs:
+                ref = orc.step(*({key: val[i][t] for key, val in dq.items()} for i in range(3)))
+                err = np.abs(bf16_f64(outs[-1]) - ref).max()
+                assert err <= ABS_O, (t, err)
         torch.cuda.synchronize()
         eng.check_status()
         runs.append((eng, dec, outs))
@@ -450,10 +504,11 @@ def test_engine_fp8_graphs_match_eager():
     for t in range(steps):
         assert torch.equal(oa[t].view(torch.int16), ob[t].view(torch.int16)), t
     for s in range(S):
-        assert da.stream_tables(s) == db.stream_tables(s)
+        assert da.stream_tables(s) == db.stream_tables(s) == orc.streams[s].tables
     assert torch.equal(da.tables_d, db.tables_d)
     assert torch.equal(da.lens_d[da.cur], db.lens_d[db.cur])
-    assert [ea.alloc.refcount(b) for b in range(N)] == [eb.alloc.refcount(b) for b in range(N)]
+    assert [ea.alloc.refcount(b) for b in range(N)] == [eb.alloc.refcount(b) for b in range(N)] \
+        == orc.pool.ref
     for x, y in ((ea.k_pool, eb.k_pool), (ea.v_pool, eb.v_pool), (ea.k_scale, eb.k_scale),
                  (ea.v_scale, eb.v_scale)):
         assert torch.equal(x.view(torch.uint8), y.view(torch.uint8))
