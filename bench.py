@@ -200,6 +200,36 @@ def prefill_exps(w, n):
     return w.h_q * n * (n + 1) / 2.0
 
 
+def window_score_flops(w, n, layers):
+    """QK^T of the alpha window rows against their visible keys, every query
+    head, over `layers` budgeted layers: 2 d (alpha n - alpha (alpha-1) / 2)
+    per head."""
+    a = min(w.alpha, n)
+    return 2.0 * w.h_q * w.d * (a * n - a * (a - 1) / 2.0) * layers
+
+
+def xu_exp_peak(peaks):
+    """Exponentials per second the XU (MUFU) pipes can issue: Blackwell's
+    documented rate for ex2 is 16 results per clock per SM, and Blackwell
+    Ultra (GB300) doubles the SFU rate of the attention exponential, so 32 per
+    clock per SM, times the 152 SMs at the maximum SM clock."""
+    return 32.0 * 152 * peaks.get("sm_max_mhz", 2070.0) * 1e6
+
+
+def prefill_scores_roofline(w, n, flops_launch, k1_avg_ms, k2_ms, peak_t, peak_src, L):
+    n_bud = sum(1 for l in range(L) if w.budget(l, n) is not None and w.budget(l, n) < n)
+    k2_avg = sum(k2_ms) / max(1, len(k2_ms))
+    # one window-score launch covers every budgeted layer when the inputs are
+    # resident; the prefill launch covers flops_launch
+    layers_per_k1 = flops_launch / prefill_flops(w, n)
+    sf = window_score_flops(w, n, n_bud) * layers_per_k1 / L
+    ach = (flops_launch + sf) / ((k1_avg_ms + k2_avg) / 1e3) / 1e12
+    return {"kernels": "prefill_attn + window_scores", "bound": "tensor",
+            "achieved": round(ach, 1), "peak": peak_t, "unit": "TFLOP/s",
+            "frac": round(ach / peak_t, 4), "peak_source": f"{peak_src} bf16 burst",
+            "flops": flops_launch + sf, "ms": round(k1_avg_ms + k2_avg, 4)}
+
+
 def decode_bytes(w, lens):
     """Algorithmic bytes of one decode launch: every cached K and V row of
     every item read once (the new row included), q read, out written, the new
@@ -337,7 +367,9 @@ def bench_gpu(args):
     tflops = flops_launch / (k1_avg / 1e3) / 1e12
     exps_launch = prefill_exps(w, n) * (sum(k1_layers) / len(k1_layers))
     exp_rate = exps_launch / (k1_avg / 1e3)
-    peak_t = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    # the prefill launch runs a few ms at the maximum clock inside a step, not
+    # a seconds-long power-capped loop: the burst figure is its peak
+    peak_t = peaks["bf16_tflops"]
     dk_ms = [a.elapsed_time(b) for a, b in rec["dk"]]
     dec_avg = sum(dk_ms) / len(dk_ms)            # the decode kernel alone
     lens = [w.k_eff(l, n) + steps // 2 for l in range(L)]   # mean length over the request
@@ -379,13 +411,19 @@ def bench_gpu(args):
                              "achieved": round(tflops, 1), "peak": peak_t, "unit": "TFLOP/s",
                              "frac": round(tflops / peak_t, 4),
                              "traffic": traffic_for("prefill_attn"),
-                             "peak_source": f"{peak_src} bf16 sustained",
+                             "peak_source": f"{peak_src} bf16 burst",
                              "per_launch_ms": round(k1_avg, 4), "flops_per_launch": flops_launch,
-                             # the softmax's exponentials, the other unit the prefill leans
-                             # on (d = 128 puts them near the MMA rate); the kernel evaluates
-                             # part of them on the FMA pipe, so this is no MUFU bound
+                             # the softmax's exponentials (every one an ex2 on the XU pipe)
+                             # against the XU peak derived in xu_exp_peak()
                              "exp_per_launch": exps_launch,
-                             "exp_per_s": round(exp_rate, -6)},
+                             "exp_per_s": round(exp_rate, -6),
+                             "exp_peak_per_s": round(xu_exp_peak(peaks), -6),
+                             "exp_frac": round(exp_rate / xu_exp_peak(peaks), 4)},
+        # prefill attention and window scores together, the benchmark spec's
+        # "prefill attention + scoring" bar: both launches' flops over both
+        # launches' event time
+        "roofline_prefill_scores": prefill_scores_roofline(w, n, flops_launch, k1_avg, k2_ms,
+                                                           peak_t, peak_src, L),
         # one window-score launch per request covers the budgeted layers
         "scores_ms_per_launch": round(sum(k2_ms) / max(1, len(k2_ms)), 4),
         "scores_layers_per_launch": sum(1 for l in range(L) if w.budget(l, n) is not None
@@ -407,9 +445,18 @@ def bench_gpu(args):
     if args.decode_fp8:
         out["decode_fp8"] = bench_decode_fp8(args, shape, blocks + 64, w, n, steps, q, k, v, dq,
                                              dk, dv, o_buf, ml_buf, flush, world, dist)
+    if args.decode_per_layer:
+        out["decode_per_layer"] = bench_decode_per_layer(args, eng, w, n, steps, q, k, v, dq, dk,
+                                                         dv, o_buf, ml_buf, flush, world, dist)
     if args.e2e:
         out["e2e"] = bench_e2e(args, eng, dec, w, n, steps, q, k, v, dq, dk, dv, o_buf, ml_buf,
                                flush, world, dist)
+    if args.c2:
+        out["c2_serving"] = bench_c2_serving(args, w, q, k, v, dq, dk, dv, dev, world, dist)
+    if args.c3:
+        del o_buf, ml_buf
+        torch.cuda.empty_cache()
+        out["c3_long_context"] = bench_c3_long_context(args, dev, world, dist)
     if rank == 0 and args.cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args)
     if rank == 0:
@@ -572,6 +619,301 @@ def bench_decode_fp8(args, shape, num_blocks, w, n, steps, q, k, v, dq, dk, dv, 
                     "before each"}
 
 
+def _step_bytes(w, lens_h):
+    """Algorithmic bytes of one decode step over items whose lengths before
+    the step are lens_h (each appends one token)."""
+    return decode_bytes(w, [int(x) for x in lens_h])
+
+
+def bench_decode_per_layer(args, eng, w, n, steps, q, k, v, dq, dk, dv, o_buf, ml_buf, flush,
+                           world, dist):
+    """The headline request's decode in model order: each step is one host
+    preparation and then one decode launch per layer (32 launches of one item,
+    each with its merge), as a model issues them (layer l + 1's query needs
+    layer l's output), replayed from a CUDA graph per step; events per step,
+    L2 flushed before each, bytes as the headline decode."""
+    import torch
+    from layer_wise_kv_gb300.pipeline import DecodeBatch
+    L = w.n_layers
+    budgets = [[w.budget(l, n) for l in range(L)]]
+    decl = DecodeBatch(eng, 1, n + steps, layer_order=True)
+    res = eng.prefill_sparsify(list(q), list(k), list(v), [n], budgets, o_buf=o_buf,
+                               ml_buf=ml_buf)
+    decl.set_stream(0, res.tables[0], res.k_eff[0])
+    decl.capture_graphs()
+    torch.cuda.synchronize()
+    pairs, nbytes = [], 0
+    gc.collect()
+    gc.disable()
+    for t in range(steps):
+        flush()
+        nbytes += _step_bytes(w, decl.lens_h)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        decl.step(dq[t], dk[t], dv[t])
+        b.record()
+        pairs.append((a, b))
+    torch.cuda.synchronize()
+    gc.enable()
+    eng.check_status()
+    decl.retire(0)
+    del decl
+    t_ms = sum(a.elapsed_time(b) for a, b in pairs)
+    (t_ms,) = max_over_ranks([t_ms], world, dist, q.device)
+    peaks, src = read_peaks()
+    ach = nbytes / (t_ms / 1e3) / 1e9
+    return {"value": round(world * steps / (t_ms / 1e3), 1), "unit": "tok/s",
+            "ms_per_token": round(t_ms / steps, 4), "launches_per_step": 2 * L,
+            "bytes_per_step": int(nbytes / steps), "achieved_gbs": round(ach, 1),
+            "frac_of_hbm": round(ach / peaks["hbm_gbs"], 4),
+            "what": "one decode launch (+ merge) per layer per step, 32 x 1 item, the step "
+                    "replayed from a CUDA graph after the host allocator's preparation; events "
+                    "per step, L2 flushed before each"}
+
+
+def device_prompts(w, lens, layers, seed, dev):
+    """Seeded synthetic prompt Q/K/V generated on the device (torch's Philox
+    generator), packed [L][T][h][d] bf16: N(0,1) with the sink construction of
+    the workloads (keys at positions 0 and 37 of each sequence + 6u, every
+    query + 0.5u, u the workload's seeded unit vector), for timing runs whose
+    inputs are too large to draw on the host in reasonable time."""
+    import torch
+    from synth import sink_direction
+    from synth.workloads import SINK_KEY_GAIN, SINK_POSITIONS, SINK_QUERY_GAIN
+    T = int(sum(lens))
+    u = torch.from_numpy(sink_direction(w)).to(dev)
+    g = torch.Generator(device=dev)
+    out = [torch.empty((layers, T, h, w.d), dtype=torch.bfloat16, device=dev)
+           for h in (w.h_q, w.h_kv, w.h_kv)]
+    starts = np.concatenate([[0], np.cumsum(lens)[:-1]]).astype(int)
+    for l in range(layers):
+        for kind, (buf, h) in enumerate(zip(out, (w.h_q, w.h_kv, w.h_kv))):
+            g.manual_seed(seed * 1000003 + l * 4 + kind)
+            x = torch.randn((T, h, w.d), generator=g, device=dev, dtype=torch.float32)
+            if kind == 0:
+                x += SINK_QUERY_GAIN * u
+            elif kind == 1:
+                for s0, nb in zip(starts, lens):
+                    for p in SINK_POSITIONS:
+                        if p < nb:
+                            x[s0 + p] += SINK_KEY_GAIN * u
+            buf[l].copy_(x)
+            del x
+    return out
+
+
+def bench_c2_serving(args, w1, q, k, v, dq, dk, dv, dev, world, dist):
+    """Continuous batching at the pages' serving point: 20 live 4000-token
+    sequences, 40 in all, output lengths drawn in [400, 600]; a finished
+    sequence's blocks go back to the free list (a seeded shuffle at the start)
+    and its slot is refilled by the next sequence at once (one prefill of one
+    prompt); the first 20 are admitted with one packed prefill of 20 prompts.
+    Every prompt is the headline request's 4000-token prompt (resident) and
+    every step's q/k/v the headline request's decode inputs for that layer,
+    replicated over the streams: the shapes and lengths are the workload's,
+    the values do not change the work.  Two passes: one decode launch per step
+    over all 640 items (stream-major), and model order (one launch per layer
+    over its 20 items, each step replayed from a CUDA graph).  Events around
+    every prefill call and every decode step; no L2 flush (a step reads about
+    4.4 GB).  Decode bytes: every live item's cached rows (+ the new one),
+    q, out and new rows, from the host mirror of the lengths."""
+    import torch
+    from layer_wise_kv_gb300.pipeline import DecodeBatch, Engine, Shape, blocks_for
+    from synth import continuous_batching, shuffled_block_order
+    wc = continuous_batching()
+    conc, prompts, outs = wc.concurrency, [int(x) for x in wc.prompt_lens], \
+        [int(x) for x in wc.out_lens]
+    n = prompts[0]
+    assert all(p == n for p in prompts) and n == q.shape[1]
+    L, steps_in = wc.n_layers, dq.shape[0]
+    shape = Shape(L, wc.h_q, wc.h_kv, wc.d, wc.alpha, wc.recent)
+    per_seq = sum(blocks_for(wc.k_eff(l, n) + max(outs) + 1) for l in range(L))
+    N = conc * per_seq + 64
+    budgets1 = [[wc.budget(l, n) for l in range(L)]]
+    q20, k20, v20 = (x.repeat(1, conc, 1, 1) for x in (q, k, v))
+    o20 = torch.empty((L, conc * n, wc.h_q, wc.d), dtype=torch.bfloat16, device=dev)
+    ml20 = (torch.empty((L, wc.h_q, conc * n), dtype=torch.float32, device=dev),
+            torch.empty((L, wc.h_q, conc * n), dtype=torch.float32, device=dev))
+    o1 = torch.empty((L, n, wc.h_q, wc.d), dtype=torch.bfloat16, device=dev)
+    ml1 = (torch.empty((L, wc.h_q, n), dtype=torch.float32, device=dev),
+           torch.empty((L, wc.h_q, n), dtype=torch.float32, device=dev))
+    # decode inputs per step for every item: [steps][S*L] stream-major and
+    # [steps][L*S] layer-major
+    sm = [x[:, None].expand(steps_in, conc, L, *x.shape[2:]).reshape(steps_in, conc * L,
+                                                                     *x.shape[2:]).contiguous()
+          for x in (dq, dk, dv)]
+    lm = [x[:, :, None].expand(steps_in, L, conc, *x.shape[2:]).reshape(steps_in, conc * L,
+                                                                       *x.shape[2:]).contiguous()
+          for x in (dq, dk, dv)]
+    peaks, src = read_peaks()
+    result = {}
+    for mode in ("batched", "layer_order"):
+        eng = Engine(shape, N, device=dev, initial_free=shuffled_block_order(N, 1))
+        dec = DecodeBatch(eng, conc, n + max(outs) + 1, layer_order=(mode == "layer_order"))
+        inputs = lm if mode == "layer_order" else sm
+        pre, stp, live = [], [], {}
+        nbytes = tokens = 0
+
+        def timed(fn):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            r = fn()
+            b.record()
+            return r, (a, b)
+
+        torch.cuda.synchronize()
+        gc.collect()
+        gc.disable()
+        res, ev = timed(lambda: eng.prefill_sparsify(list(q20), list(k20), list(v20),
+                                                     [n] * conc, budgets1 * conc, o_buf=o20,
+                                                     ml_buf=ml20))
+        pre.append(ev)
+        for s in range(conc):
+            dec.set_stream(s, res.tables[s], res.k_eff[s])
+            live[s] = [s, 0]
+        if mode == "layer_order":
+            dec.capture_graphs()
+        nxt, t = conc, 0
+        while True:
+            nbytes += _step_bytes(wc, dec.lens_h)
+            _, ev = timed(lambda: dec.step(inputs[0][t % steps_in], inputs[1][t % steps_in],
+                                           inputs[2][t % steps_in]))
+            stp.append(ev)
+            tokens += conc
+            t += 1
+            done = False
+            for s in range(conc):
+                live[s][1] += 1
+                if live[s][1] >= outs[live[s][0]]:
+                    dec.retire(s)
+                    if nxt >= len(prompts):
+                        done = True
+                        continue
+                    r1, ev = timed(lambda: eng.prefill_sparsify(list(q), list(k), list(v), [n],
+                                                                budgets1, o_buf=o1, ml_buf=ml1))
+                    pre.append(ev)
+                    dec.set_stream(s, r1.tables[0], r1.k_eff[0])
+                    live[s] = [nxt, 0]
+                    nxt += 1
+            if done:
+                break
+        torch.cuda.synchronize()
+        gc.enable()
+        eng.check_status()
+        t_pre = sum(a.elapsed_time(b) for a, b in pre)
+        t_dec = sum(a.elapsed_time(b) for a, b in stp)
+        t_pre, t_dec = max_over_ranks([t_pre, t_dec], world, dist, dev)
+        ach = nbytes / (t_dec / 1e3) / 1e9
+        entry = {"decode_tok_s": round(world * tokens / (t_dec / 1e3), 1),
+                 "decode_steps": t, "ms_per_step": round(t_dec / t, 4),
+                 "bytes_per_step": int(nbytes / t), "achieved_gbs": round(ach, 1),
+                 "frac_of_hbm": round(ach / peaks["hbm_gbs"], 4),
+                 "launches_per_step": 2 * (L if mode == "layer_order" else 1)}
+        if mode == "batched":
+            entry = {"prefill_sparsify_tok_s": round(world * len(prompts) * n / (t_pre / 1e3), 1),
+                     "prefill_calls": len(pre), **entry}
+        result[mode] = entry
+        for s in range(conc):
+            if dec.lens_h[dec._item(s, 0)] > 0:
+                dec.retire(s)
+        del dec, eng
+    del q20, k20, v20, o20, ml20, sm, lm
+    torch.cuda.empty_cache()
+    result["what"] = ("20 live of 40 sequences, 4000-token prompts, outputs U[400,600], seeded "
+                      "shuffled free list; prefill+sparsify = 40 prompts over all prefill calls; "
+                      "decode 'batched' = one launch over all 640 items per step, 'layer_order' "
+                      "= 32 launches of 20 items per step from a CUDA graph; no L2 flush "
+                      "(4.4 GB per step)")
+    result["peak_source"] = f"{src} copy bandwidth"
+    return result
+
+
+def bench_c3_long_context(args, dev, world, dist):
+    """Long context at >10x compression: one batch of four prompts of 7000,
+    12000, 20000 and 30000 tokens (Llama-3-8B head shapes; layers 0-2 full,
+    layers 3-31 keep floor(n/12) incl. the 32 most recent), prefill+sparsify
+    as one call (one prefill launch over all layers and sequences), then 64
+    decode steps over the 128 items.  Inputs drawn on the device (seeded) with
+    the workloads' distribution and sinks.  Events around the call and around
+    the prefill-attention launch (its roofline at these lengths) and each
+    decode step; no L2 flush (a step reads about 1.5 GB)."""
+    import torch
+    from layer_wise_kv_gb300.pipeline import DecodeBatch, Engine, Shape, blocks_for
+    from synth import long_context
+    wl = long_context()
+    lens = [int(x) for x in wl.prompt_lens]
+    L, steps, T = wl.n_layers, wl.decode_steps, sum(lens)
+    shape = Shape(L, wl.h_q, wl.h_kv, wl.d, wl.alpha, wl.recent)
+    q, k, v = device_prompts(wl, lens, L, 3, dev)
+    budgets = [[wl.budget(l, nb) for l in range(L)] for nb in lens]
+    N = sum(blocks_for(wl.k_eff(l, nb) + steps + 1) for nb in lens for l in range(L)) + 64
+    eng = Engine(shape, N, device=dev)
+    o_buf = torch.empty((L, T, wl.h_q, wl.d), dtype=torch.bfloat16, device=dev)
+    ml_buf = (torch.empty((L, wl.h_q, T), dtype=torch.float32, device=dev),
+              torch.empty((L, wl.h_q, T), dtype=torch.float32, device=dev))
+    g = torch.Generator(device=dev)
+    g.manual_seed(77)
+    dqs = [torch.randn((steps, len(lens) * L, h, wl.d), generator=g, device=dev).bfloat16()
+           for h in (wl.h_q, wl.h_kv, wl.h_kv)]
+    peaks, src = read_peaks()
+    pre, k1, stp, nbytes = [], [], [], 0
+    reps = 2
+    for rep in range(reps + 1):                      # the first pass is a warm-up
+        torch.cuda.synchronize()
+        tm = {"attn": [], "scores": []}
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        res = eng.prefill_sparsify(list(q), list(k), list(v), lens, budgets, o_buf=o_buf,
+                                   ml_buf=ml_buf, timing=tm)
+        b.record()
+        if rep > 0:
+            pre.append((a, b))
+            k1 += tm["attn"]
+        dec = DecodeBatch(eng, len(lens), max(lens) + steps + 1)
+        for s in range(len(lens)):
+            dec.set_stream(s, res.tables[s], res.k_eff[s])
+        for t in range(steps):
+            if rep > 0:
+                nbytes += _step_bytes(wl, dec.lens_h)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            dec.step(dqs[0][t], dqs[1][t], dqs[2][t])
+            b.record()
+            if rep > 0:
+                stp.append((a, b))
+        torch.cuda.synchronize()
+        eng.check_status()
+        for s in range(len(lens)):
+            dec.retire(s)
+        del dec
+    t_pre = sum(a.elapsed_time(b) for a, b in pre) / reps
+    t_k1 = sum(a.elapsed_time(b) for a, b in k1) / reps
+    t_dec = sum(a.elapsed_time(b) for a, b in stp) / reps
+    t_pre, t_k1, t_dec = max_over_ranks([t_pre, t_k1, t_dec], world, dist, dev)
+    flops = sum(prefill_flops(wl, nb) for nb in lens) * L
+    tf = flops / (t_k1 / 1e3) / 1e12
+    ach = nbytes / reps / (t_dec / 1e3) / 1e9
+    del q, k, v, o_buf, ml_buf, dqs, eng
+    torch.cuda.empty_cache()
+    return {"prefill_sparsify_tok_s": round(world * T / (t_pre / 1e3), 1),
+            "ms_prefill_sparsify": round(t_pre, 3),
+            "roofline_prefill": {"achieved": round(tf, 1), "peak": peaks["bf16_tflops"],
+                                 "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4),
+                                 "flops_per_launch": flops, "per_launch_ms": round(t_k1, 4),
+                                 "peak_source": f"{src} bf16 burst"},
+            "decode_tok_s": round(world * len(lens) * steps / (t_dec / 1e3), 1),
+            "decode_ms_per_step": round(t_dec / steps, 4),
+            "decode_bytes_per_step": int(nbytes / reps / steps),
+            "decode_frac_of_hbm": round(ach / peaks["hbm_gbs"], 4),
+            "what": "batch of 4 prompts (7000/12000/20000/30000), layers 3-31 keep n/12, one "
+                    "prefill+sparsify call, 64 decode steps (one launch over 128 items each); "
+                    "inputs drawn on the device; no L2 flush (1.5 GB per step)"}
+
+
 def bench_e2e(args, eng, dec, w, n, steps, q, k, v, dq, dk, dv, o_buf, ml_buf, flush, world,
               dist):
     """Same metric through host buffers: Q/K/V of the request and every decode
@@ -714,6 +1056,12 @@ def main():
                     help="skip the decode pass with decode-time replacement")
     ap.add_argument("--no-decode-fp8", dest="decode_fp8", action="store_false",
                     help="skip the decode pass over FP8 pools")
+    ap.add_argument("--no-decode-per-layer", dest="decode_per_layer", action="store_false",
+                    help="skip the model-order decode pass (one launch per layer)")
+    ap.add_argument("--no-c2", dest="c2", action="store_false",
+                    help="skip the continuous-batching serving pass")
+    ap.add_argument("--no-c3", dest="c3", action="store_false",
+                    help="skip the long-context pass")
     ap.add_argument("--cpu-rows", type=int, default=400,
                     help="prefill rows the CPU oracle evaluates (sample size)")
     args = ap.parse_args()

@@ -13,7 +13,10 @@ Step orders (the same ones the CPU oracle uses):
   launch over all items.
 * decode step: the host allocator prepares every (stream, layer) item in order
   (new block when the length is a multiple of 16, copy-on-write of a shared
-  last block), the copies run, then one paged-decode launch covers all items.
+  last block), the copies run, then one paged-decode launch covers all items
+  -- or, in layer order (the launches a model issues, since layer l + 1's
+  query depends on layer l's output), one launch per layer over that layer's
+  items.
 
 Sources: Novita AI, "How KV Sparsity achieves 1.5x acceleration for vLLM"
 (sections "Key techniques 1" and "Key techniques 2"); Ultralytics glossary
@@ -413,14 +416,24 @@ def _stacked(layers):
 class DecodeBatch:
     """Decode items (one per (stream, layer)) over an Engine's pools."""
 
-    def __init__(self, eng: Engine, n_streams: int, max_len: int, n_layers: Optional[int] = None):
+    def __init__(self, eng: Engine, n_streams: int, max_len: int, n_layers: Optional[int] = None,
+                 layer_order: bool = False):
         """n_layers: layers per stream (default: the engine's), e.g. only the
-        full-cache layers when the budgeted ones run in an EvictingDecode."""
+        full-cache layers when the budgeted ones run in an EvictingDecode.
+        layer_order: items are numbered layer-major (item = layer * n_streams
+        + stream; the step's q / k_new / v_new and its output follow that
+        order) and each step issues one decode launch per layer over that
+        layer's n_streams items, in layer order, after one host preparation
+        of every item (which therefore allocates blocks layer by layer).  This
+        is the launch sequence of a model, whose layer l + 1 query depends on
+        layer l's output; without it, one launch covers every item of the
+        step (stream-major numbering)."""
         s = eng.shape
         self.eng = eng
         self.n_streams = n_streams
         self.n_layers = s.n_layers if n_layers is None else int(n_layers)
         self.n_items = n_streams * self.n_layers
+        self.layer_order = bool(layer_order)
         self.shape_ = s
         self.max_len = max_len
         self.max_blocks = blocks_for(max_len)
@@ -507,19 +520,35 @@ class DecodeBatch:
         return self.out
 
     # ------------------------------------------------------------ CUDA graphs
+    def _item(self, slot: int, layer: int) -> int:
+        return layer * self.n_streams + slot if self.layer_order else slot * self.n_layers + layer
+
     def _decode_launch(self, q, k_new, v_new, patch, lens, lens_next, stream=None):
-        """One decode call over every item, on the engine's pool type."""
+        """The step's decode over every item, on the engine's pool type: one
+        call, or in layer order one call per layer over its rows (each call
+        reuses the workspace; the calls are ordered on the stream)."""
         eng, s = self.eng, self.eng.shape
-        if eng.kv_fp8:
-            kvs.kvs_paged_decode_fp8(q, k_new, v_new, eng.k_pool, eng.v_pool, eng.k_scale,
-                                     eng.v_scale, eng.num_blocks, self.tables_d, self.max_blocks,
-                                     patch, lens, lens_next, self.n_items, s.h_q, s.h_kv, s.d,
-                                     s.scale, self.out, self.ws, self.ws_bytes, eng.status, stream)
-        else:
-            kvs.kvs_paged_decode(q, k_new, v_new, eng.k_pool, eng.v_pool, eng.num_blocks,
-                                 self.tables_d, self.max_blocks, patch, lens, lens_next,
-                                 self.n_items, s.h_q, s.h_kv, s.d, s.scale, self.out, self.ws,
-                                 self.ws_bytes, eng.status, stream)
+        groups = ([slice(l * self.n_streams, (l + 1) * self.n_streams)
+                   for l in range(self.n_layers)] if self.layer_order else [slice(None)])
+
+        def part(t, r):
+            return None if t is None else t[r]
+
+        for r in groups:
+            n = self.n_streams if self.layer_order else self.n_items
+            if eng.kv_fp8:
+                kvs.kvs_paged_decode_fp8(q[r], part(k_new, r), part(v_new, r), eng.k_pool,
+                                         eng.v_pool, eng.k_scale, eng.v_scale, eng.num_blocks,
+                                         self.tables_d[r], self.max_blocks, part(patch, r),
+                                         lens[r], part(lens_next, r), n, s.h_q, s.h_kv, s.d,
+                                         s.scale, self.out[r], self.ws, self.ws_bytes, eng.status,
+                                         stream)
+            else:
+                kvs.kvs_paged_decode(q[r], part(k_new, r), part(v_new, r), eng.k_pool, eng.v_pool,
+                                     eng.num_blocks, self.tables_d[r], self.max_blocks,
+                                     part(patch, r), lens[r], part(lens_next, r), n, s.h_q,
+                                     s.h_kv, s.d, s.scale, self.out[r], self.ws, self.ws_bytes,
+                                     eng.status, stream)
 
     def capture_graphs(self):
         """Capture the decode step as CUDA graphs, so that a step costs the host
@@ -561,20 +590,24 @@ class DecodeBatch:
     def set_stream(self, slot: int, tables: List[List[int]], lens: List[int]):
         """Install a stream's per-layer tables (host copy + device rows)."""
         L = self.n_layers
-        for l in range(L):
-            i = slot * L + l
+        rows = [self._item(slot, l) for l in range(L)]
+        for l, i in enumerate(rows):
             self.tables_h[i, :] = -1
             self.tables_h[i, :len(tables[l])] = tables[l]
             self.lens_h[i] = lens[l]
-        rows = slice(slot * L, (slot + 1) * L)
-        self.tables_d[rows] = torch.from_numpy(self.tables_h[rows]).to(self.eng.device)
-        self.lens_d[self.cur][rows] = torch.from_numpy(self.lens_h[rows]).to(self.eng.device)
+        if self.layer_order:
+            idx = torch.tensor(rows, dtype=torch.long, device=self.eng.device)
+            self.tables_d[idx] = torch.from_numpy(self.tables_h[rows]).to(self.eng.device)
+            self.lens_d[self.cur][idx] = torch.from_numpy(self.lens_h[rows]).to(self.eng.device)
+        else:
+            r = slice(slot * L, (slot + 1) * L)
+            self.tables_d[r] = torch.from_numpy(self.tables_h[r]).to(self.eng.device)
+            self.lens_d[self.cur][r] = torch.from_numpy(self.lens_h[r]).to(self.eng.device)
 
     def stream_tables(self, slot: int) -> List[List[int]]:
-        L = self.n_layers
         out = []
-        for l in range(L):
-            i = slot * L + l
+        for l in range(self.n_layers):
+            i = self._item(slot, l)
             nb = blocks_for(int(self.lens_h[i]))
             out.append(self.tables_h[i, :nb].tolist())
         return out
@@ -583,17 +616,18 @@ class DecodeBatch:
         for t in self.stream_tables(slot):
             for b in t:
                 self.eng.alloc.decref(b)
-        L = self.n_layers
-        self.tables_h[slot * L:(slot + 1) * L] = -1
-        self.lens_h[slot * L:(slot + 1) * L] = 0
+        rows = [self._item(slot, l) for l in range(self.n_layers)]
+        self.tables_h[rows] = -1
+        self.lens_h[rows] = 0
 
     def step(self, q, k_new, v_new, stream=None, timing=None):
         """One decode step for every item: q [n_items][h_q][d], k_new/v_new
         [n_items][h_kv][d] bf16 on the device.  Returns the output tensor.
         timing: optional list receiving a (start, end) event pair around the
-        decode kernel.  Without graphs or timing, the step is one native call
-        (kvs_decode_step: host preparation, uploads and decode)."""
-        if self._graphs is None and timing is None:
+        decode kernel(s).  Without graphs or timing, and not in layer order,
+        the step is one native call (kvs_decode_step: host preparation,
+        uploads and decode)."""
+        if self._graphs is None and timing is None and not self.layer_order:
             return self._native_step(q, k_new, v_new, stream)
         eng, s = self.eng, self.eng.shape
         n = self.n_items

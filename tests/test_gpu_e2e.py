@@ -445,6 +445,69 @@ def test_decode_graphs_match_eager():
     np.testing.assert_array_equal(host_bits(ea.v_pool), host_bits(eb.v_pool))
 
 
+@pytest.mark.parametrize("graphs", [False, True])
+def test_decode_layer_order_vs_oracle(graphs):
+    """DecodeBatch(layer_order=True): items numbered layer-major, one host
+    preparation per step, then one decode launch per layer (the launch
+    sequence of a model), eager or replayed from CUDA graphs.  Three samples
+    share a prompt's blocks, so copy-on-write happens on the first step.  The
+    oracle's flow prepares the items in the same layer-major order: tables,
+    reference counts and every step's outputs must match it."""
+    kvs_lib()
+    from layer_wise_kv_gb300.pipeline import DecodeBatch, Engine
+    w = tiny()
+    n, L, N, S, steps = 100, w.n_layers, 64, 3, 24
+    ql, kl, vl, host = _layers_to_device(w, [3], [n])
+    budgets = [[w.budget(l, n) for l in range(L)]]
+    eng = Engine(_shape(w), N, poison=True)
+    res = eng.prefill_sparsify(ql, kl, vl, [n], budgets)
+    torch.cuda.synchronize()
+    pool = oracle.BlockPool(N)
+    opk = np.zeros((N, w.h_kv, 16, w.d), np.uint16)
+    opv = np.zeros_like(opk)
+    recs = []
+    for l in range(L):
+        qb, kb, vb = host[(3, l)]
+        rec = flow.sparsify_layer(w, l, qb, kb, vb)
+        rec.idx = _gpu_idx(res, 0, l, w.h_kv, rec.k_eff)
+        flow.place_layer(rec, pool, kb, vb, opk, opv)
+        recs.append(rec)
+    dec = DecodeBatch(eng, S, n + steps + 1, layer_order=True)
+    streams = [flow.new_stream(recs)]
+    dec.set_stream(0, res.tables[0], res.k_eff[0])
+    for s in range(1, S):
+        streams.append(flow.share_stream(pool, streams[0]))
+        for t in res.tables[0]:
+            for b in t:
+                eng.alloc.incref(b)
+        dec.set_stream(s, res.tables[0], res.k_eff[0])
+    if graphs:
+        dec.capture_graphs()
+    dq = {(s, l): decode_qkv(w, 3, l, steps, sample=s) for s in range(S) for l in range(L)}
+    for t in range(steps):
+        # layer-major inputs: item l * S + s
+        q, k, v = (dev_bf16(np.stack([dq[(s, l)][i][t] for l in range(L) for s in range(S)]))
+                   for i in range(3))
+        got = bf16_f64(dec.step(q, k, v))
+        for l in range(L):
+            for s in range(S):
+                flow.prepare_append(pool, streams[s], l, opk, opv)
+        for l in range(L):
+            for s in range(S):
+                ref = flow.append_and_attend(w, streams[s], l, dq[(s, l)][0][t], dq[(s, l)][1][t],
+                                             dq[(s, l)][2][t], opk, opv)
+                assert np.abs(got[l * S + s] - ref).max() <= ABS_O, (t, s, l)
+    torch.cuda.synchronize()
+    eng.check_status()
+    for s in range(S):
+        assert dec.stream_tables(s) == streams[s].tables
+    assert [eng.alloc.refcount(b) for b in range(N)] == pool.ref
+    for s in range(S):
+        dec.retire(s)
+        flow.retire(pool, streams[s])
+    assert eng.alloc.num_free() == pool.num_free()
+
+
 @pytest.mark.parametrize("fused", [True, False])
 def test_evicting_decode_vs_oracle(fused):
     """Decode-time replacement in the tiny workload's budgeted layer (k = 64,
