@@ -93,7 +93,7 @@ struct DecodeParams {
   uint64_t wait_ns;  // limit of every mbarrier wait
   int stall;         // test hook: issue no copies, so that every wait runs out
   int batch, max_blocks, num_blocks, h_q, h_kv, group, append, n_stages;
-  int q_bytes, q_stride, q_off, bar_off, idx_off;
+  int q_bytes, q_stride, q_off, bar_off, pb_off, idx_off;
   float scale_log2;
 };
 
@@ -181,6 +181,7 @@ __device__ __forceinline__ int owner_of(int64_t b, int64_t T, int W) {
 struct Piece {
   bool valid;
   int item, h, seg, blk0, nblk, lens0, len, first_slot, npieces;
+  int patch;    // the item's table patch (-1: none); loaded here, first used when issuing
   int64_t end;  // global block index just past the piece
 };
 
@@ -192,6 +193,7 @@ __device__ __forceinline__ Piece piece_at(int64_t pos, int64_t range_end, int64_
   x.valid = pos < range_end;
   if (!x.valid) {
     x.item = x.h = x.seg = x.blk0 = x.nblk = x.lens0 = x.len = x.first_slot = x.npieces = 0;
+    x.patch = -1;
     x.end = pos;
     return x;
   }
@@ -215,23 +217,31 @@ __device__ __forceinline__ Piece piece_at(int64_t pos, int64_t range_end, int64_
   const int w_lo = owner_of(seg_lo, T, W);
   x.npieces = owner_of(seg_hi - 1, T, W) - w_lo + 1;
   x.first_slot = w_lo + x.seg;
+  x.patch = (p.append && p.patch != nullptr) ? p.patch[x.item] : -1;
   return x;
 }
 
-// Physical block for block (base + lane) of the piece; 0 past its end.
+// Table entry of block (base + lane) of the piece, as stored (-1 past its end).
+// Nothing here reads the loaded value, so the load stays in flight until the
+// entry is issued (a chunk or a piece later); resolve_block checks it then.
 __device__ __forceinline__ int fetch_chunk(const Piece& x, int base, int lane,
                                            const DecodeParams& p) {
   const int j = base + lane;
-  if (!x.valid || j >= x.nblk) return 0;
   const int lb = x.blk0 + j;
-  int pb;
-  if (p.append && p.patch != nullptr && lb == x.lens0 / KVS_BLOCK_TOKENS && p.patch[x.item] >= 0)
-    pb = p.patch[x.item];
-  else
-    pb = lb < p.max_blocks ? p.tables[static_cast<int64_t>(x.item) * p.max_blocks + lb] : -1;
+  if (!x.valid || j >= x.nblk || lb >= p.max_blocks) return -1;
+  return p.tables[static_cast<int64_t>(x.item) * p.max_blocks + lb];
+}
+
+// Physical block of block j of the piece from its table entry: the item's
+// patch replaces the entry of the block that receives the appended token.
+// Returns -1 (and flags the status) for an entry outside the pool.
+__device__ __forceinline__ int resolve_block(const Piece& x, int j, int entry,
+                                             const DecodeParams& p) {
+  int pb = entry;
+  if (p.append && x.patch >= 0 && x.blk0 + j == x.lens0 / KVS_BLOCK_TOKENS) pb = x.patch;
   if (pb < 0 || pb >= p.num_blocks) {
     flag_status(p.status, KVS_ERR_INVALID);
-    pb = 0;
+    return -1;
   }
   return pb;
 }
@@ -264,6 +274,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
   uint8_t* my_stages = smem + warp * NS * L::kStageBytes;
   uint8_t* my_q = smem + p.q_off + warp * 2 * p.q_stride;
   uint64_t* my_full = reinterpret_cast<uint64_t*>(smem + p.bar_off) + warp * NS;
+  // per stage: the physical block its copy reads (written by lane 0 when it
+  // issues the copy, read by the warp after the stage's barrier completes)
+  int* my_pb = reinterpret_cast<int*>(smem + p.pb_off) + warp * NS;
   int* prefix = reinterpret_cast<int*>(smem + p.idx_off);  // [batch + 1], in blocks
   int* lens_s = prefix + (p.batch + 1);
 
@@ -329,9 +342,14 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
   int k = 0;              // index of cur among this warp's pieces (q buffer parity)
   bool aborted = false;
 
-  auto issue = [&](const Piece& x, int j, int pb, int qpar) {
+  auto issue = [&](const Piece& x, int j, int entry, int qpar) {
     if (lane == 0) {
       const int s = g_iss % NS;
+      // the physical block (-1: corrupt entry; the copy then reads block 0 and
+      // the consumer writes nothing into the pool for it)
+      const int pbr = resolve_block(x, j, entry, p);
+      my_pb[s] = pbr;
+      const int pb = pbr < 0 ? 0 : pbr;
       uint8_t* st = my_stages + s * L::kStageBytes;
       mbar_arrive_expect_tx(&my_full[s], L::kStageBytes + (j == 0 ? p.q_bytes : 0));
       if (p.stall) {  // test hook: the copies this stage expects never start
@@ -379,8 +397,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
         tb_base += 32;
         tb_n = fetch_chunk(x, tb_base + 32, lane, p);
       }
-      const int pb = __shfl_sync(0xffffffffu, tb, iss_j - tb_base);
-      issue(x, iss_j, pb, (k + (iss_next ? 1 : 0)) & 1);
+      const int entry = __shfl_sync(0xffffffffu, tb, iss_j - tb_base);
+      issue(x, iss_j, entry, (k + (iss_next ? 1 : 0)) & 1);
       ++iss_j;
     }
   };
@@ -439,10 +457,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
       // and into the pool
       if (p.append && cur.lens0 >= tok0 && cur.lens0 < tok0 + KVS_BLOCK_TOKENS) {
         const int slot = cur.lens0 - tok0;
-        const int lb = cur.lens0 / KVS_BLOCK_TOKENS;
-        const int pb = (p.patch != nullptr && p.patch[cur.item] >= 0)
-                           ? p.patch[cur.item]
-                           : p.tables[static_cast<int64_t>(cur.item) * p.max_blocks + lb];
+        const int pb = my_pb[s];  // resolved when the stage was issued
         if constexpr (kF8) {
           // quantise the new rows (lane l holds d = 4l .. 4l+3) into the stage and the pool
           const int64_t nrow = (static_cast<int64_t>(cur.item) * p.h_kv + cur.h) * D + 4 * lane;
@@ -737,9 +752,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
     }
     // table patch and length bookkeeping, once per item (its head-0 segment start)
     if (lane == 0 && cur.blk0 == 0 && cur.h == 0) {
-      if (p.append && p.patch != nullptr && p.patch[cur.item] >= 0)
+      if (p.append && cur.patch >= 0)
         p.tables[static_cast<int64_t>(cur.item) * p.max_blocks + cur.lens0 / KVS_BLOCK_TOKENS] =
-            p.patch[cur.item];
+            cur.patch;
       if (p.lens_next != nullptr) p.lens_next[cur.item] = cur.len;
     }
 
@@ -966,6 +981,8 @@ size_t plan_smem(DecodeParams& prm) {
     off += static_cast<size_t>(kWarps) * 2 * prm.q_stride;
     const size_t bar_off = off;
     off += static_cast<size_t>(kWarps) * ns * 8;
+    const size_t pb_off = off;
+    off += static_cast<size_t>(kWarps) * ns * 4;
     const size_t idx_off = off;
     off += static_cast<size_t>(2 * prm.batch + 1) * 4;
     const size_t total = off + 1024;
@@ -973,6 +990,7 @@ size_t plan_smem(DecodeParams& prm) {
       prm.n_stages = ns;
       prm.q_off = static_cast<int>(q_off);
       prm.bar_off = static_cast<int>(bar_off);
+      prm.pb_off = static_cast<int>(pb_off);
       prm.idx_off = static_cast<int>(idx_off);
       return total;
     }
