@@ -52,6 +52,7 @@ class LayerRecord:
     m_rows: Optional[np.ndarray] = None
     l_rows: Optional[np.ndarray] = None
     table: List[int] = field(default_factory=list)
+    hits: List[int] = field(default_factory=list)  # prefix blocks found, not written
 
 
 def sparsify_layer(w, layer, q_bits, k_bits, v_bits, rows=None, scores_override=None):
@@ -84,11 +85,39 @@ def sparsify_layer(w, layer, q_bits, k_bits, v_bits, rows=None, scores_override=
     return rec
 
 
-def place_layer(rec, pool, k_bits, v_bits, pool_k, pool_v):
-    """Allocate ceil(k_eff/16) blocks and compact the kept rows into them."""
-    rec.table = [pool.alloc() for _ in range(blocks_for(rec.k_eff))]
+def place_layer(rec, pool, k_bits, v_bits, pool_k, pool_v, layer=None, tokens=None):
+    """Allocate ceil(k_eff/16) blocks and compact the kept rows into them.
+
+    With the prompt's token ids given (and the layer's index), a layer that
+    keeps every token looks its full blocks up as prefix blocks, in order,
+    each chained to the one before; blocks found hold that prefix's rows
+    already and are not written.  Its partial last block, and every block of a
+    budgeted layer, come from the free list.  rec.hits lists the blocks found."""
+    rec.hits = []
+    if tokens is not None and not rec.budgeted:
+        n_full = rec.k_eff // BLOCK
+        parent, table = -1, []
+        for i in range(n_full):
+            b, hit = pool.prefix_block(layer, parent, tokens[i * BLOCK:(i + 1) * BLOCK])
+            table.append(b)
+            if hit:
+                rec.hits.append(b)
+            parent = b
+        table += [pool.alloc() for _ in range(blocks_for(rec.k_eff) - n_full)]
+        rec.table = table
+    else:
+        rec.table = [pool.alloc() for _ in range(blocks_for(rec.k_eff))]
     if pool_k is not None:
-        compact(k_bits, v_bits, rec.idx, rec.table, pool_k, pool_v)
+        if rec.hits:
+            # only the blocks not found are written: compact into a scratch
+            # copy, then take the written blocks from it
+            sk, sv = pool_k.copy(), pool_v.copy()
+            compact(k_bits, v_bits, rec.idx, rec.table, sk, sv)
+            for b in rec.table:
+                if b not in rec.hits:
+                    pool_k[b], pool_v[b] = sk[b], sv[b]
+        else:
+            compact(k_bits, v_bits, rec.idx, rec.table, pool_k, pool_v)
     return rec.table
 
 

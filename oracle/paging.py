@@ -12,12 +12,25 @@ Source: Ultralytics glossary, "PagedAttention":
   write into a block others still use copies it first (copy-on-write).
 * section "Related techniques" (continuous batching): a finished sequence's
   blocks return to the free pool at once.
+* section "Block sharing between sequences", last paragraph: the sharing
+  extends across requests by hashing whole blocks (prompt caching): a request
+  whose prompt starts like one already held reuses that one's full blocks.
 
 Readings taken: allocation pops the head of the free list (as in the worked
 example), a block whose count drops to zero is appended to the tail; copy on
 write happens iff the block's count is above one at write time.  Pool layout
 is [num_blocks][H_kv][block][d]; the unused tail slots of a last block have
 undefined contents.
+
+Prefix blocks (whole-block hashing), readings taken: a full block of 16
+prompt tokens of one layer is identified by (layer, the physical block of
+the previous 16 tokens of that prefix or -1, the 16 token ids); since a
+request holding a block also holds its parent, the parent block stands for
+the whole prefix before it, so equal keys mean equal prefixes.  A block can
+be found while some request holds it; when its count drops to zero its key
+is forgotten.  A lookup that finds the key adds a reference to that block;
+one that does not pops a new block and records the key.  The hash of the key
+is only how an implementation finds it; equality of keys decides.
 """
 from __future__ import annotations
 
@@ -41,6 +54,8 @@ class BlockPool:
         self.num_blocks = int(num_blocks)
         self.free = list(range(self.num_blocks)) if free is None else [int(b) for b in free]
         self.ref = [0] * self.num_blocks
+        self.prefix = {}          # (layer, parent, tokens) -> block, for held prefix blocks
+        self.prefix_key = {}      # block -> its key
 
     def alloc(self):
         if not self.free:
@@ -59,7 +74,25 @@ class BlockPool:
             raise ValueError("decref of a free block")
         self.ref[b] -= 1
         if self.ref[b] == 0:
+            key = self.prefix_key.pop(b, None)
+            if key is not None:
+                del self.prefix[key]
             self.free.append(b)
+
+    def prefix_block(self, layer, parent, tokens):
+        """The block for 16 prompt tokens of `layer` after the prefix ending in
+        block `parent` (-1: none): (block, hit)."""
+        key = (int(layer), int(parent), tuple(int(t) for t in tokens))
+        if len(key[2]) != BLOCK:
+            raise ValueError("a prefix block holds exactly one block of tokens")
+        b = self.prefix.get(key)
+        if b is not None:
+            self.ref[b] += 1
+            return b, True
+        b = self.alloc()
+        self.prefix[key] = b
+        self.prefix_key[b] = key
+        return b, False
 
     def cow(self, b):
         """Returns (block to write into, copied?)."""

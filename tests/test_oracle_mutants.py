@@ -181,6 +181,34 @@ def test_compaction_mutants_fail_the_selected_set_pin(monkeypatch, mutant):
     _fails(pins.test_compaction_of_a_selected_set_follows_the_index_per_head)
 
 
+class _PrefixNoParent(oracle.BlockPool):
+    def prefix_block(self, layer, parent, tokens):
+        return super().prefix_block(layer, -1, tokens)   # the mistake: the prefix is ignored
+
+
+class _PrefixNoLayer(oracle.BlockPool):
+    def prefix_block(self, layer, parent, tokens):
+        return super().prefix_block(0, parent, tokens)   # the mistake: layers share keys
+
+
+class _PrefixNeverForgets(oracle.BlockPool):
+    def decref(self, b):
+        if self.ref[b] <= 0:
+            raise ValueError("decref of a free block")
+        self.ref[b] -= 1
+        if self.ref[b] == 0:                             # the mistake: the key stays
+            self.free.append(b)
+
+
+@pytest.mark.parametrize("mutant", [_PrefixNoParent, _PrefixNoLayer, _PrefixNeverForgets])
+def test_prefix_block_mutants_fail_the_pins(monkeypatch, mutant):
+    monkeypatch.setattr(oracle, "BlockPool", mutant)
+    with pytest.raises(AssertionError):
+        pins.test_prefix_blocks_forgotten_when_free_and_separate_per_layer()
+        for seed in range(6):
+            pins.test_prefix_blocks_shared_iff_prefixes_equal_brute_force(seed)
+
+
 # --------------------------------------------------------------------------- decode
 def _decode_values_reversed(q, k_cache, v_cache, scale):
     return oracle.attention.decode_attention(q, k_cache, v_cache[:, ::-1], scale)

@@ -124,6 +124,124 @@ def test_pool_fifo_refcount_cow():
         small.alloc()
 
 
+# ---------------------------------------------------------------------------
+# prefix blocks (whole-block hashing across requests)
+# ---------------------------------------------------------------------------
+def _prefix_requests(rng, n_req, vocab=3):
+    """Token sequences that share prefixes often: each request copies the
+    start of an earlier one (or of a common root) and then diverges."""
+    root = rng.integers(0, vocab, 200)
+    reqs = []
+    for _ in range(n_req):
+        src = reqs[rng.integers(len(reqs))] if reqs and rng.random() < 0.7 else root
+        cut = int(rng.integers(0, len(src) + 1))
+        tail = rng.integers(0, vocab, int(rng.integers(0, 60)))
+        reqs.append(np.concatenate([src[:cut], tail]).astype(np.int64))
+    return reqs
+
+
+def _place_prefix(pool, layer, toks):
+    parent, table, hits = -1, [], []
+    for i in range(len(toks) // 16):
+        b, hit = pool.prefix_block(layer, parent, toks[i * 16:(i + 1) * 16])
+        table.append(b)
+        hits.append(hit)
+        parent = b
+    return table, hits
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_prefix_blocks_shared_iff_prefixes_equal_brute_force(seed):
+    """Requests arrive and retire in a random order; every full block of a
+    layer's prompt is a prefix block.  By brute force over the requests held
+    at the time: block i of a new request is found iff some held request's
+    first 16 (i + 1) tokens are the same (and that request's block i is full),
+    and then it is that request's block i; the count of every block is the
+    number of held requests whose table holds it."""
+    rng = np.random.default_rng(seed)
+    reqs = _prefix_requests(rng, 40, vocab=2 + seed % 3)
+    pool = oracle.BlockPool(4000, free=rng.permutation(4000))
+    held = {}                                         # request -> (tokens, table)
+    order = list(range(len(reqs)))
+    for r in order:
+        if held and rng.random() < 0.35:              # retire someone first
+            victim = list(held)[rng.integers(len(held))]
+            for b in held.pop(victim)[1]:
+                pool.decref(b)
+        toks = reqs[r]
+        table, hits = _place_prefix(pool, 0, toks)
+        for i in range(len(table)):
+            end = 16 * (i + 1)
+            match = [q for q, (tq, bq) in held.items()
+                     if len(tq) >= end and np.array_equal(tq[:end], toks[:end])]
+            assert hits[i] == bool(match), (r, i)
+            if match:
+                assert all(held[q][1][i] == table[i] for q in match)
+        held[r] = (toks, table)
+        counts = {}
+        for _, tbl in held.values():
+            for b in tbl:
+                counts[b] = counts.get(b, 0) + 1
+        assert all(pool.ref[b] == c for b, c in counts.items())
+        assert sum(1 for b in range(4000) if pool.ref[b] > 0) == len(counts)
+        assert pool.num_free() + len(counts) == 4000
+
+
+def test_prefix_blocks_forgotten_when_free_and_separate_per_layer():
+    pool = oracle.BlockPool(64)
+    toks = np.arange(48) % 5
+    t0, h0 = _place_prefix(pool, 0, toks)
+    assert h0 == [False] * 3 and t0 == [0, 1, 2]
+    t1, h1 = _place_prefix(pool, 1, toks)             # another layer: its own blocks
+    assert h1 == [False] * 3 and t1 == [3, 4, 5]
+    t2, h2 = _place_prefix(pool, 0, toks)             # same layer, same prompt: all found
+    assert h2 == [True] * 3 and t2 == t0 and all(pool.ref[b] == 2 for b in t0)
+    other = toks.copy()
+    other[20] += 1                                    # differs inside block 1
+    t3, h3 = _place_prefix(pool, 0, other)
+    assert h3 == [True, False, False] and t3[0] == t0[0]
+    assert t3[2] != t0[2]                             # same tokens, another prefix: not found
+    for t in (t0, t1, t2, t3):
+        for b in t:
+            pool.decref(b)
+    assert pool.num_free() == 64 and not pool.prefix
+    t4, h4 = _place_prefix(pool, 0, toks)             # nothing held: nothing found
+    assert h4 == [False] * 3 and t4 == [8, 9, 10]     # the FIFO's head
+
+
+def test_place_layer_writes_only_blocks_not_found():
+    """A full-cache layer placed with its token ids: blocks found are left as
+    they are; the rest hold the kept rows; a budgeted layer finds nothing."""
+    w = tiny()
+    n = 40
+    qb, kb, vb = (bf16_bits(RNG.standard_normal(s).astype(np.float32))
+                  for s in ((n, w.h_q, w.d), (n, w.h_kv, w.d), (n, w.h_kv, w.d)))
+    toks = np.arange(n) % 7
+    pool = oracle.BlockPool(32)
+    pk = np.zeros((32, w.h_kv, 16, w.d), np.uint16)
+    pv = np.zeros_like(pk)
+    rec_a = flow.sparsify_layer(w, 0, qb, kb, vb)        # layer 0: full cache
+    flow.place_layer(rec_a, pool, kb, vb, pk, pv, layer=0, tokens=toks)
+    assert rec_a.hits == [] and len(rec_a.table) == 3
+    marked = pk[rec_a.table[0]].copy()
+    pk[rec_a.table[0]] ^= 0x1234                         # a write would restore it
+    rec_b = flow.sparsify_layer(w, 0, qb, kb, vb)
+    flow.place_layer(rec_b, pool, kb, vb, pk, pv, layer=0, tokens=toks)
+    assert rec_b.hits == rec_a.table[:2] and rec_b.table[:2] == rec_a.table[:2]
+    assert rec_b.table[2] != rec_a.table[2]              # the partial block is private
+    np.testing.assert_array_equal(pk[rec_a.table[0]], marked ^ 0x1234)
+    np.testing.assert_array_equal(oracle.gather_rows(pk, rec_b.table, n, 0)[32:], kb[32:, 0])
+    n2 = 256
+    qb2, kb2, vb2 = (bf16_bits(RNG.standard_normal(s).astype(np.float32))
+                     for s in ((n2, w.h_q, w.d), (n2, w.h_kv, w.d), (n2, w.h_kv, w.d)))
+    pool2 = oracle.BlockPool(64)
+    recs = [flow.sparsify_layer(w, 1, qb2, kb2, vb2) for _ in range(2)]   # layer 1: budgeted
+    assert recs[0].budgeted
+    for r in recs:
+        flow.place_layer(r, pool2, kb2, vb2, None, None, layer=1, tokens=np.zeros(n2, np.int64))
+        assert r.hits == []
+
+
 def test_pool_conservation_random_trace():
     pool = oracle.BlockPool(40, free=RNG.permutation(40))
     owned = []
