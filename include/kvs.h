@@ -192,7 +192,13 @@ kvs_status kvs_select_topk(const float* scores, int64_t head_stride, const kvs_s
  * copied together).  row_off is the item's first row in the flattened
  * (item, j) enumeration: row_off(i) = sum of k_eff over items before i;
  * total_rows = sum of all k_eff.  items: device array.
+ * A table entry of KVS_BLOCK_SKIP marks a block that already holds its rows
+ * (a prefix block found by kvs_alloc_prefix_blocks): its slots are neither
+ * read nor written.  Any other entry outside [0, num_blocks) skips the slot
+ * and flags KVS_ERR_INVALID in `status`.
  * ---------------------------------------------------------------------- */
+#define KVS_BLOCK_SKIP (-2)
+
 typedef struct {
   int64_t src_tok;   /* first token of the item's K/V in `k` / `v` */
   int64_t idx_off;   /* element offset of head 0's kept indices */
@@ -387,6 +393,27 @@ int32_t kvs_alloc_refcount(const kvs_allocator* a, int32_t block); /* -1 if out 
 int32_t kvs_alloc_num_free(const kvs_allocator* a);
 /* Copy up to cap free-list entries, head first, into buf (host); returns count. */
 int32_t kvs_alloc_free_list(const kvs_allocator* a, int32_t* buf, int32_t cap);
+
+/* Prefix blocks: prompt caching across requests by hashing whole blocks
+ * (Ultralytics glossary "PagedAttention", section "Block sharing between
+ * sequences", last paragraph).  For the n_tokens / 16 full blocks of a
+ * prompt's token ids (host int32, n_tokens of them) in one layer that keeps
+ * every token: block i is keyed by (layer, block i - 1 of this call or -1,
+ * tokens[16 i .. 16 i + 15]).  A key held by the allocator (its block in use)
+ * is a hit: that block gains a reference, hits[i] = 1.  Otherwise a block is
+ * popped from the free list (count 1) and recorded under the key, hits[i] = 0.
+ * A hit needs an equal key, not only an equal hash.  blocks, hits: host
+ * int32 [n_tokens / 16]; *n_hits (nullable) = blocks found, which always form
+ * a run from the first block.  A block's key is forgotten when its count
+ * drops to zero.  KVS_ERR_OOM_BLOCKS (nothing changed) when the free list
+ * cannot supply the blocks not found.  A caller that places a prompt this
+ * way need not write the blocks found (their slots already hold the rows of
+ * the same prefix): see KVS_BLOCK_SKIP. */
+kvs_status kvs_alloc_prefix_blocks(kvs_allocator* a, int32_t layer, const int32_t* tokens,
+                                   int32_t n_tokens, int32_t* blocks, int32_t* hits,
+                                   int32_t* n_hits);
+/* Number of blocks currently recorded as prefix blocks (-1 for NULL). */
+int32_t kvs_alloc_prefix_entries(const kvs_allocator* a);
 
 /* Host-side step preparation for a batch of decode items (one per (stream,
  * layer)), visited in order: for item i with length lens[i] (host) and table

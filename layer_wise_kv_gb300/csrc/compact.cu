@@ -53,6 +53,7 @@ compact_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
     if (j >= item.k_eff) continue;                // a row past a short item (cannot happen
                                                   // with consistent row_off)
     const int block = tables[item.table_off + j / KVS_BLOCK_TOKENS];
+    if (block == KVS_BLOCK_SKIP) continue;  // a prefix block already in place
     const bool block_ok = block >= 0 && block < num_blocks;
     if (!block_ok) {
       if (lane == 0) flag_status(status, KVS_ERR_INVALID);
@@ -171,6 +172,7 @@ compact_fp8_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ 
     const kvs_compact_item it = items[lo];
     const int jb = gb - pre[lo];
     const int b = tables[it.table_off + jb];
+    if (b == KVS_BLOCK_SKIP) continue;  // a prefix block already in place
     if (b < 0 || b >= num_blocks) {
       if (lane == 0) flag_status(status, KVS_ERR_INVALID);
       continue;

@@ -8,9 +8,17 @@
 // that other sequences still use).  The free list is a FIFO ring: a block
 // appears in it at most once, so a ring of num_blocks entries never
 // overflows, and pop-head / push-tail are O(1).
+//
+// Prefix blocks: the same glossary section's last paragraph (sharing extends
+// across requests by hashing whole blocks).  A held full block of a
+// full-cache layer's prompt is recorded under (layer, parent block, its 16
+// token ids) in a hash map; a lookup hits only on an equal key, so a hash
+// collision never aliases two prefixes.  The key is forgotten when the
+// block's count reaches zero.
 #include <cstdlib>
 #include <cstring>
 #include <new>
+#include <unordered_map>
 #include <vector>
 
 #include "host_common.h"
@@ -46,6 +54,38 @@ const char* last_error_cstr() { return g_last_error.c_str(); }
 
 }  // namespace kvs
 
+namespace {
+
+struct PrefixKey {
+  int32_t layer;
+  int32_t parent;
+  int32_t tok[KVS_BLOCK_TOKENS];
+  bool operator==(const PrefixKey& o) const {
+    return layer == o.layer && parent == o.parent &&
+           std::memcmp(tok, o.tok, sizeof(tok)) == 0;
+  }
+};
+
+// FNV-1a (64-bit) over the key's words, as bytes.
+struct PrefixKeyHash {
+  size_t operator()(const PrefixKey& k) const {
+    uint64_t h = 14695981039346656037ull;
+    auto mix = [&h](int32_t word) {
+      const uint32_t u = static_cast<uint32_t>(word);
+      for (int i = 0; i < 4; ++i) {
+        h ^= (u >> (8 * i)) & 0xFFu;
+        h *= 1099511628211ull;
+      }
+    };
+    mix(k.layer);
+    mix(k.parent);
+    for (int i = 0; i < KVS_BLOCK_TOKENS; ++i) mix(k.tok[i]);
+    return static_cast<size_t>(h);
+  }
+};
+
+}  // namespace
+
 struct kvs_allocator {
   int32_t num_blocks = 0;
   std::vector<int32_t> ring;  // free list, FIFO
@@ -53,6 +93,9 @@ struct kvs_allocator {
   int32_t count = 0;          // blocks in the free list
   std::vector<int32_t> ref;   // reference count per block
   std::vector<uint8_t> managed;
+  std::unordered_map<PrefixKey, int32_t, PrefixKeyHash> prefix;  // held prefix blocks
+  std::vector<PrefixKey> key_of;  // per block: its prefix key, if keyed[b]
+  std::vector<uint8_t> keyed;
 
   bool valid(int32_t b) const { return b >= 0 && b < num_blocks; }
 
@@ -86,6 +129,8 @@ kvs_status kvs_alloc_create(int32_t num_blocks, const int32_t* initial_free, int
   a->ring.assign(num_blocks, -1);
   a->ref.assign(num_blocks, 0);
   a->managed.assign(num_blocks, 0);
+  a->keyed.assign(num_blocks, 0);
+  a->key_of.resize(num_blocks);
   if (initial_free == nullptr) {
     for (int32_t b = 0; b < num_blocks; ++b) {
       a->managed[b] = 1;
@@ -150,8 +195,65 @@ kvs_status kvs_alloc_decref(kvs_allocator* a, int32_t block) {
   KVS_REQUIRE(a != nullptr, "kvs_alloc_decref: NULL allocator");
   KVS_REQUIRE(a->valid(block), "kvs_alloc_decref: block %d out of range", block);
   KVS_REQUIRE(a->ref[block] > 0, "kvs_alloc_decref: block %d is not in use", block);
-  if (--a->ref[block] == 0) a->push_tail(block);
+  if (--a->ref[block] == 0) {
+    if (a->keyed[block]) {
+      a->prefix.erase(a->key_of[block]);
+      a->keyed[block] = 0;
+    }
+    a->push_tail(block);
+  }
   return KVS_OK;
+}
+
+kvs_status kvs_alloc_prefix_blocks(kvs_allocator* a, int32_t layer, const int32_t* tokens,
+                                   int32_t n_tokens, int32_t* blocks, int32_t* hits,
+                                   int32_t* n_hits) {
+  KVS_REQUIRE(a != nullptr && n_tokens >= 0 && (tokens != nullptr || n_tokens == 0),
+              "kvs_alloc_prefix_blocks: bad argument");
+  const int32_t n_full = n_tokens / KVS_BLOCK_TOKENS;
+  KVS_REQUIRE(n_full == 0 || (blocks != nullptr && hits != nullptr),
+              "kvs_alloc_prefix_blocks: NULL output");
+  // the blocks found form a run from the start (the key after a new block
+  // names that block as its parent, which no key can hold yet): count it, so
+  // that a shortage of free blocks is known before anything changes
+  PrefixKey key;
+  key.layer = layer;
+  key.parent = -1;
+  int32_t run = 0;
+  for (; run < n_full; ++run) {
+    std::memcpy(key.tok, tokens + static_cast<int64_t>(run) * KVS_BLOCK_TOKENS, sizeof(key.tok));
+    const auto it = a->prefix.find(key);
+    if (it == a->prefix.end()) break;
+    key.parent = it->second;
+  }
+  if (n_full - run > a->count)
+    return kvs::fail(KVS_ERR_OOM_BLOCKS, "kvs_alloc_prefix_blocks: %d new blocks needed, %d free",
+                     n_full - run, a->count);
+  key.parent = -1;
+  for (int32_t i = 0; i < n_full; ++i) {
+    std::memcpy(key.tok, tokens + static_cast<int64_t>(i) * KVS_BLOCK_TOKENS, sizeof(key.tok));
+    int32_t b;
+    if (i < run) {
+      b = a->prefix.find(key)->second;
+      ++a->ref[b];
+      hits[i] = 1;
+    } else {
+      b = a->pop_head();
+      a->ref[b] = 1;
+      a->prefix.emplace(key, b);
+      a->key_of[b] = key;
+      a->keyed[b] = 1;
+      hits[i] = 0;
+    }
+    blocks[i] = b;
+    key.parent = b;
+  }
+  if (n_hits != nullptr) *n_hits = run;
+  return KVS_OK;
+}
+
+int32_t kvs_alloc_prefix_entries(const kvs_allocator* a) {
+  return a == nullptr ? -1 : static_cast<int32_t>(a->prefix.size());
 }
 
 kvs_status kvs_alloc_cow(kvs_allocator* a, int32_t block, int32_t* out, int32_t* copied) {

@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(HERE, "libkvs.so")
 KVS_OK, KVS_ERR_INVALID, KVS_ERR_OOM_BLOCKS, KVS_ERR_CUDA, KVS_ERR_UNSUPPORTED, \
     KVS_ERR_DEVICE_TIMEOUT = range(6)
 BLOCK_TOKENS = 16
+KVS_BLOCK_SKIP = -2
 
 SELECT_ITEM = np.dtype([("score_off", "<i8"), ("n", "<i4"), ("k", "<i4"), ("idx_off", "<i8")])
 COMPACT_ITEM = np.dtype([("src_tok", "<i8"), ("idx_off", "<i8"), ("row_off", "<i8"),
@@ -98,6 +99,8 @@ _SIGS = {
     "kvs_alloc_refcount": (_I32, [_VP, _I32]),
     "kvs_alloc_num_free": (_I32, [_VP]),
     "kvs_alloc_free_list": (_I32, [_VP, _VP, _I32]),
+    "kvs_alloc_prefix_blocks": (_I32, [_VP, _I32, _VP, _I32, _VP, _VP, _P32]),
+    "kvs_alloc_prefix_entries": (_I32, [_VP]),
     "kvs_decode_prepare": (_I32, [_VP, _VP, _I32, _VP, _I32, _VP, _VP, _VP, _P32, _P32, _P32]),
 }
 
@@ -464,6 +467,23 @@ class BlockAllocator:
 
     def num_free(self) -> int:
         return int(self._lib.kvs_alloc_num_free(self._h))
+
+    def prefix_blocks(self, layer: int, tokens):
+        """kvs_alloc_prefix_blocks: the blocks of the full 16-token blocks of a
+        prompt's token ids in one full-cache layer, found (hit) or new.
+        Returns (blocks int32, hits bool) arrays of len(tokens) // 16."""
+        toks = np.ascontiguousarray(tokens, dtype=np.int32)
+        n_full = toks.size // BLOCK_TOKENS
+        blocks = np.empty(max(n_full, 1), dtype=np.int32)
+        hits = np.empty(max(n_full, 1), dtype=np.int32)
+        _check(self._lib.kvs_alloc_prefix_blocks(self._h, int(layer),
+                                                 toks.ctypes.data if toks.size else None,
+                                                 toks.size, blocks.ctypes.data, hits.ctypes.data,
+                                                 None))
+        return blocks[:n_full], hits[:n_full].astype(bool)
+
+    def prefix_entries(self) -> int:
+        return int(self._lib.kvs_alloc_prefix_entries(self._h))
 
     def free_list(self) -> list:
         n = self.num_free()

@@ -74,6 +74,7 @@ class PrefillResult:
     m: Optional[List[torch.Tensor]] = None  # per layer [h_q][T] when kept
     l: Optional[List[torch.Tensor]] = None
     o: Optional[List[torch.Tensor]] = None
+    prefix_hits: int = 0                 # prefix blocks found (not written again)
 
 
 class Engine:
@@ -167,7 +168,8 @@ class Engine:
                          budgets: Sequence[Sequence[Optional[int]]], keep_outputs=False,
                          o_buf=None, ml_buf=None, select_scores: Optional[torch.Tensor] = None,
                          stream=None, timing=None, timing_layers=None,
-                         ready: Optional[Sequence[Sequence[torch.cuda.Event]]] = None
+                         ready: Optional[Sequence[Sequence[torch.cuda.Event]]] = None,
+                         prefix_tokens: Optional[Sequence[Optional[np.ndarray]]] = None
                          ) -> PrefillResult:
         """q_layers[l]: [T][h_q][d] bf16, k/v_layers[l]: [T][h_kv][d] (T = sum of
         seq_lens, sequences packed).  budgets[b][l]: k_l for sequence b (None =
@@ -189,7 +191,12 @@ class Engine:
         stream less.
         ready: optional per-layer lists of CUDA events (see upload_layers);
         layer l's launches wait for every event in ready[l], so the layers'
-        inputs may still be on their way to the device when this is called."""
+        inputs may still be on their way to the device when this is called.
+        prefix_tokens: optional per-sequence host arrays of the prompt's token
+        ids (None for a sequence: no prefix lookup): the full blocks of every
+        layer that keeps all its tokens are looked up as prefix blocks
+        (kvs_alloc_prefix_blocks, the layer's index as key); blocks found are
+        shared, not written again by the compaction."""
         s = self.shape
         dev = self.device
         L = s.n_layers
@@ -291,11 +298,23 @@ class Engine:
         tables: List[List[List[int]]] = []
         flat = np.empty(max(plan["n_tables"], 1), dtype=np.int32)
         toff = 0
+        n_hits = 0
         for b in range(B):
             per_layer = []
+            toks = None if prefix_tokens is None else prefix_tokens[b]
             for l in range(L):
-                ids = self.alloc.alloc_many(blocks_for(keff[b][l]))
-                flat[toff:toff + ids.size] = ids
+                nb = blocks_for(keff[b][l])
+                if toks is not None and not budgeted[b][l]:
+                    n_full = keff[b][l] // BLOCK
+                    pre, hit = self.alloc.prefix_blocks(l, np.asarray(toks)[:n_full * BLOCK])
+                    ids = np.concatenate([pre, self.alloc.alloc_many(nb - n_full)])
+                    # blocks found already hold these rows: the compaction skips them
+                    flat[toff:toff + ids.size] = ids
+                    flat[toff:toff + n_full][hit] = kvs.KVS_BLOCK_SKIP
+                    n_hits += int(hit.sum())
+                else:
+                    ids = self.alloc.alloc_many(nb)
+                    flat[toff:toff + ids.size] = ids
                 toff += ids.size
                 per_layer.append(ids.tolist())
             tables.append(per_layer)
@@ -314,7 +333,7 @@ class Engine:
                                    self.num_blocks, self.status, stream)
         idx_off = plan["idx_off"]
         res = PrefillResult(tables=tables, k_eff=keff, kept_idx=kept, idx_off=idx_off,
-                            scores=scores)
+                            scores=scores, prefix_hits=n_hits)
         if keep_outputs:
             res.m, res.l, res.o = list(m_all), list(l_all), list(o_all)
         return res

@@ -257,3 +257,59 @@ def test_decode_prepare_matches_oracle_flow(kvs):
         assert [a.refcount(b) for b in range(N)] == o.ref
     assert step == 39
     a.close()
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_prefix_blocks_match_the_oracle(kvs, seed):
+    """kvs_alloc_prefix_blocks against the oracle's prefix blocks over a random
+    trace of requests (shared prefixes, several layers, retirements): the same
+    blocks, hits, counts, free list order and number of recorded keys at every
+    step."""
+    rng = np.random.default_rng(100 + seed)
+    N = 3000
+    free = rng.permutation(N).astype(np.int32)
+    a = kvs.BlockAllocator(N, free)
+    pool = oracle.BlockPool(N, free=free)
+    root = rng.integers(0, 3, 300)
+    reqs, held = [], {}
+    for r in range(50):
+        if held and rng.random() < 0.4:
+            victim = list(held)[rng.integers(len(held))]
+            for b in held.pop(victim):
+                a.decref(b)
+                pool.decref(b)
+        src = reqs[rng.integers(len(reqs))] if reqs and rng.random() < 0.7 else root
+        toks = np.concatenate([src[:rng.integers(0, len(src) + 1)],
+                               rng.integers(0, 3, rng.integers(0, 50))]).astype(np.int32)
+        reqs.append(toks)
+        taken = []
+        for layer in range(3):
+            blocks, hits = a.prefix_blocks(layer, toks)
+            parent, want_b, want_h = -1, [], []
+            for i in range(len(toks) // 16):
+                b, hit = pool.prefix_block(layer, parent, toks[16 * i:16 * i + 16])
+                want_b.append(b)
+                want_h.append(hit)
+                parent = b
+            assert blocks.tolist() == want_b and hits.tolist() == want_h, (r, layer)
+            taken += want_b
+        held[r] = taken
+        assert a.free_list() == pool.free
+        assert [a.refcount(b) for b in range(N)] == pool.ref
+        assert a.prefix_entries() == len(pool.prefix)
+    a.close()
+
+
+def test_prefix_blocks_out_of_blocks_changes_nothing(kvs):
+    a = kvs.BlockAllocator(4)
+    toks = np.arange(64, dtype=np.int32)                  # 4 full blocks
+    blocks, hits = a.prefix_blocks(0, toks)
+    assert not hits.any() and a.num_free() == 0
+    longer = np.arange(80, dtype=np.int32)                # 4 found + 1 new: no room
+    with pytest.raises(kvs.KvsError) as e:
+        a.prefix_blocks(0, longer)
+    assert e.value.code == kvs.KVS_ERR_OOM_BLOCKS
+    assert [a.refcount(b) for b in range(4)] == [1, 1, 1, 1] and a.prefix_entries() == 4
+    again, hits2 = a.prefix_blocks(0, toks[:40])           # 2 full blocks, both found
+    assert hits2.all() and again.tolist() == blocks[:2].tolist()
+    a.close()
