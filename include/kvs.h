@@ -530,8 +530,11 @@ size_t kvs_decode_scores_workspace_size(int32_t n_items, int32_t h_q, int32_t h_
  * are quantised the same way into slot lens[i] (codes and scales).  The
  * result is the attention over the stored values e4m3(code) * s with q and
  * the probabilities (times each token's V scale and 2^10) rounded to fp16,
- * fp32 accumulation: q values must lie in fp16's range and |v| below 28000.
- * Workspace, status and every other argument as kvs_paged_decode. */
+ * fp32 accumulation.  Input range: every q entry must satisfy |q| <= 65504
+ * (a larger one turns into infinity in fp16 and the logits into NaN; entries
+ * below about 6.1e-5 in magnitude keep only fp16-subnormal precision), and
+ * |v| must stay below 28000.  Nothing checks these ranges.  Workspace, status
+ * and every other argument as kvs_paged_decode. */
 kvs_status kvs_paged_decode_fp8(const kvs_bf16* q, const kvs_bf16* k_new, const kvs_bf16* v_new,
                                 uint8_t* k_pool, uint8_t* v_pool, float* k_scale, float* v_scale,
                                 int32_t num_blocks, int32_t* block_tables, int32_t max_blocks,
