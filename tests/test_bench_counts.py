@@ -29,3 +29,14 @@ def test_kept_tokens_and_decode_bytes():
     kv = sum((L + 1) * row for L in lens)
     extra = w.n_layers * (w.h_q * w.d * 2 * 2 + w.h_kv * w.d * 2 * 2)
     assert bench.decode_bytes(w, lens) == kv + extra == 219545600
+
+
+def test_parallel_oracle_figure_runs_one_process_per_core():
+    """The per-core oracle figure spawns one process per host core (at most
+    the 29 budgeted layers), each on its own layer, and reports positive
+    rates; a small row sample keeps it to a few seconds."""
+    import argparse
+    import os
+    out = bench.cpu_baseline_parallel(argparse.Namespace(cpu_rows=40))
+    assert out["cores"] == max(1, min(len(os.sched_getaffinity(0)), 29))
+    assert out["kind"] == "oracle" and out["value"] > 0 and out["decode_tok_s"] > 0
