@@ -448,6 +448,9 @@ def bench_gpu(args):
     if args.decode_per_layer:
         out["decode_per_layer"] = bench_decode_per_layer(args, eng, w, n, steps, q, k, v, dq, dk,
                                                          dv, o_buf, ml_buf, flush, world, dist)
+    if args.prefill_per_layer:
+        out["prefill_per_layer"] = bench_prefill_per_layer(args, eng, dec, w, n, q, k, v, ml_buf,
+                                                           flush, world, dist)
     if args.e2e:
         out["e2e"] = bench_e2e(args, eng, dec, w, n, steps, q, k, v, dq, dk, dv, o_buf, ml_buf,
                                flush, world, dist)
@@ -671,6 +674,51 @@ def bench_decode_per_layer(args, eng, w, n, steps, q, k, v, dq, dk, dv, o_buf, m
             "what": "one decode launch (+ merge) per layer per step, 32 x 1 item, the step "
                     "replayed from a CUDA graph after the host allocator's preparation; events "
                     "per step, L2 flushed before each"}
+
+
+def bench_prefill_per_layer(args, eng, dec, w, n, q, k, v, ml_buf, flush, world, dist):
+    """The request's prefill+sparsify with one prefill-attention launch per
+    layer, the order a model issues them (layer l + 1's Q, K and V need layer
+    l's output): every layer overwrites one [n][h_q][d] output buffer; the
+    window scores, selection and compaction follow as in the headline.  Events
+    around the call (L2 flushed before each); the attention roofline from
+    event pairs around the launches of layers 5, 15 and 25."""
+    import torch
+    L = w.n_layers
+    budgets = [[w.budget(l, n) for l in range(L)]]
+    o_layer = torch.empty((n, w.h_q, w.d), dtype=torch.bfloat16, device=q.device)
+    totals, k1 = [], {}
+    for rep in range(1 + max(1, args.steps)):
+        flush()
+        tm = {} if rep == 0 else k1
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        res = eng.prefill_sparsify(list(q), list(k), list(v), [n], budgets, o_buf=o_layer,
+                                   ml_buf=ml_buf, timing=tm, timing_layers=TIMED_LAYERS)
+        e1.record()
+        torch.cuda.synchronize()
+        eng.check_status()
+        if rep > 0:
+            totals.append(e0.elapsed_time(e1))
+        dec.set_stream(0, res.tables[0], res.k_eff[0])
+        dec.retire(0)
+    attn = [a.elapsed_time(b) for a, b in k1.get("attn", [])]
+    t_ms = sum(totals) / len(totals)
+    a_ms = sum(attn) / max(1, len(attn))
+    t_ms, a_ms = max_over_ranks([t_ms, a_ms], world, dist, q.device)
+    peaks, peak_src = read_peaks()
+    tf = prefill_flops(w, n) / (a_ms / 1e3) / 1e12
+    return {"value": round(world * n / (t_ms / 1e3), 1), "unit": "tok/s",
+            "ms_prefill_sparsify": round(t_ms, 3),
+            "roofline_attn_layer": {"achieved": round(tf, 1), "peak": peaks["bf16_tflops"],
+                                    "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4),
+                                    "per_launch_ms": round(a_ms, 4),
+                                    "flops_per_launch": prefill_flops(w, n),
+                                    "peak_source": f"{peak_src} bf16 burst"},
+            "what": ("prefill+sparsify with 32 prefill-attention launches (one per layer, each "
+                     "overwriting one output buffer), then one window-score launch, selection "
+                     "and compaction; events around the call, L2 flushed before each")}
 
 
 def device_prompts(w, lens, layers, seed, dev):
@@ -1134,6 +1182,8 @@ def main():
                     help="skip the decode pass over FP8 pools")
     ap.add_argument("--no-decode-per-layer", dest="decode_per_layer", action="store_false",
                     help="skip the model-order decode pass (one launch per layer)")
+    ap.add_argument("--no-prefill-per-layer", dest="prefill_per_layer", action="store_false",
+                    help="skip the prefill pass with one attention launch per layer")
     ap.add_argument("--no-c2", dest="c2", action="store_false",
                     help="skip the continuous-batching serving pass")
     ap.add_argument("--no-c3", dest="c3", action="store_false",
