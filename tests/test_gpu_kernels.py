@@ -270,6 +270,48 @@ def test_window_scores_vs_oracle(lens, h_q, h_kv, d, alpha):
         np.testing.assert_allclose(got[:, s0:s0 + n].sum(axis=1), w * (h_q // h_kv), rtol=1e-4)
 
 
+def test_window_scores_beyond_the_persistent_batch_limit_vs_oracle():
+    """More sequences than the persistent form takes (2100 > 2048) go to the
+    one-CTA-per-tile form: lengths 1..48 (many shorter than the window), a
+    sample of sequences against the oracle, every sequence's total against
+    alpha * G (each window row's probabilities sum to one)."""
+    kvs = kvs_lib()
+    rng = np.random.default_rng(2100)
+    h_q, h_kv, d, alpha = 8, 2, 64, 16
+    lens = [int(x) for x in rng.integers(1, 49, 2100)]
+    T = sum(lens)
+    qb = _randn_bits(rng, (T, h_q, d), 1.5)
+    kb = _randn_bits(rng, (T, h_kv, d))
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    scale = 1 / np.sqrt(d)
+    m_in = np.zeros((h_q, T), np.float32)
+    l_in = np.ones((h_q, T), np.float32)
+    for b, n in enumerate(lens):
+        s0, w = cu[b], min(alpha, n)
+        q64, k64 = bf16_to_f64(qb[s0:s0 + n]), bf16_to_f64(kb[s0:s0 + n])
+        _, mw, lw = oracle.prefill_rows(q64, k64, k64, scale, np.arange(n - w, n))
+        m_in[:, s0 + n - w:s0 + n] = mw
+        l_in[:, s0 + n - w:s0 + n] = lw
+    scores = torch.full((h_kv, T), -1.0, dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvs.kvs_window_scores(dev_bf16(qb), dev_bf16(kb), torch.from_numpy(m_in).cuda(),
+                          torch.from_numpy(l_in).cuda(), scores, torch.from_numpy(cu).cuda(),
+                          len(lens), max(lens), T, h_q, h_kv, d, alpha, scale, status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    got = scores.cpu().numpy().astype(np.float64)
+    for b in rng.choice(len(lens), 150, replace=False):
+        n, s0 = lens[b], cu[b]
+        w = min(alpha, n)
+        q64, k64 = bf16_to_f64(qb[s0:s0 + n]), bf16_to_f64(kb[s0:s0 + n])
+        ref = oracle.window_scores(q64, k64, m_in[:, s0 + n - w:s0 + n].astype(np.float64),
+                                   l_in[:, s0 + n - w:s0 + n].astype(np.float64), w, scale)
+        check_rel(got[:, s0:s0 + n], ref, REL_S, ABS_S, what=f"S seq {b}")
+    tot = np.add.reduceat(got, cu[:-1], axis=1)
+    want = np.array([min(alpha, n) * (h_q // h_kv) for n in lens], np.float64)
+    np.testing.assert_allclose(tot, np.broadcast_to(want, tot.shape), rtol=1e-4)
+
+
 def test_window_scores_layers_match_per_layer_launches():
     """kvs_window_scores_layers over layers stacked in one buffer gives, bit
     for bit, what kvs_window_scores gives layer by layer (whose values the
