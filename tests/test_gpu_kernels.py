@@ -224,6 +224,8 @@ SCORE_CASES = [  # (lens, h_q, h_kv, d, alpha)
     ([0, 40, 0, 7], 8, 2, 64, 16),         # empty sequences; one shorter than alpha
     ([600, 200, 31], 64, 8, 128, 32),      # alpha * G = 256 columns (sixteen chunks)
     ([500, 33, 9], 12, 4, 64, 16),         # 48 columns: a width without its own kernel
+    ([300, 77], 32, 2, 64, 16),            # d = 64, 256 columns
+    ([129, 1000], 16, 2, 64, 16),          # d = 64, 128 columns
 ]
 
 
