@@ -1165,14 +1165,20 @@ def bench_reference(args):
     if rank != 0:
         return
     t0 = time.perf_counter()
-    cb = cpu_baseline(args)
+    # the oracle on the host's cores (one process per core over independent
+    # layers), with the single-core figure beside it
+    cb = cpu_baseline_parallel(args)
+    one = cpu_baseline(args)
     wall = time.perf_counter() - t0
     out = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "tok/s",
            "decode": {"value": cb["decode_tok_s"], "unit": "tok/s"},
            "n_gpus": 1, "steps": 1, "warmup": 0, "higher_is_better": True,
            "config": {"workload": WORKLOAD}, "dtype": "f64", "data": "synthetic",
            "cpu_baseline": {"value": cb["value"], "unit": "tok/s", "cores": cb["cores"],
-                            "kind": "oracle", "sample": cb["sample"]},
+                            "kind": "oracle", "sample": cb["sample"],
+                            "single_core": {"value": one["value"],
+                                            "decode_tok_s": one["decode_tok_s"],
+                                            "cores": 1, "sample": one["sample"]}},
            "e2e": {"value": cb["value"], "unit": "tok/s", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0},
            "wall_s": round(wall, 2)}
