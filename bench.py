@@ -460,6 +460,8 @@ def bench_gpu(args):
         del o_buf, ml_buf
         torch.cuda.empty_cache()
         out["c3_long_context"] = bench_c3_long_context(args, dev, world, dist)
+    if args.c4:
+        out["c4_shared_prefix"] = bench_c4_shared_prefix(args, dev, world, dist)
     if rank == 0 and args.cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args)
         out["cpu_baseline"]["parallel"] = cpu_baseline_parallel(args)
@@ -963,6 +965,106 @@ def bench_c3_long_context(args, dev, world, dist):
                     "inputs drawn on the device; no L2 flush (1.5 GB per step)"}
 
 
+def bench_c4_shared_prefix(args, dev, world, dist):
+    """Shared prefix: 16 prompts of 512 .. 16384 tokens (seeded), one
+    prefill+sparsify call over all 32 layers, then each prompt decoded as
+    three parallel samples that share its blocks through reference counts; a
+    sample's first write into a partially filled last block copies it
+    (copy-on-write).  256 decode steps over the 16 x 3 x 32 items.  Inputs
+    drawn on the device; events around the call and each decode step (one
+    warm-up pass first); no L2 flush (a step reads about 11 GB)."""
+    import torch
+    from layer_wise_kv_gb300.pipeline import DecodeBatch, Engine, Shape, blocks_for
+    from synth import shared_prefix
+    wl = shared_prefix()
+    lens = [int(x) for x in wl.prompt_lens]
+    P, S = len(lens), wl.samples
+    L, steps, T = wl.n_layers, wl.decode_steps, sum(lens)
+    shape = Shape(L, wl.h_q, wl.h_kv, wl.d, wl.alpha, wl.recent)
+    q, k, v = device_prompts(wl, lens, L, 4, dev)
+    budgets = [[wl.budget(l, nb) for l in range(L)] for nb in lens]
+    base = sum(blocks_for(wl.k_eff(l, nb)) for nb in lens for l in range(L))
+    growth = sum(blocks_for(wl.k_eff(l, nb) + steps) - blocks_for(wl.k_eff(l, nb)) + 1
+                 for nb in lens for l in range(L))
+    N = base + S * growth + 64
+    eng = Engine(shape, N, device=dev)
+    o_buf = torch.empty((L, T, wl.h_q, wl.d), dtype=torch.bfloat16, device=dev)
+    ml_buf = (torch.empty((L, wl.h_q, T), dtype=torch.float32, device=dev),
+              torch.empty((L, wl.h_q, T), dtype=torch.float32, device=dev))
+    g = torch.Generator(device=dev)
+    g.manual_seed(78)
+    dqs = [torch.randn((steps, P * S * L, h, wl.d), generator=g, device=dev).bfloat16()
+           for h in (wl.h_q, wl.h_kv, wl.h_kv)]
+    peaks, _ = read_peaks()
+    pre, stp, nbytes, ubytes = [], [], 0, 0
+    row = wl.h_kv * wl.d * 2 * 2                     # one token's K and V row, one head set
+    for rep in range(2):                             # the first pass is a warm-up
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        res = eng.prefill_sparsify(list(q), list(k), list(v), lens, budgets, o_buf=o_buf,
+                                   ml_buf=ml_buf)
+        b.record()
+        if rep > 0:
+            pre.append((a, b))
+        # layer-major numbering in one launch: a prompt's three samples sit
+        # side by side in the split, so their reads of shared blocks meet in L2
+        dec = DecodeBatch(eng, P * S, max(lens) + steps + 1, interleave=True)
+        for pi in range(P):
+            dec.set_stream(pi * S, res.tables[pi], res.k_eff[pi])
+            for si in range(1, S):
+                for t in res.tables[pi]:
+                    for blk in t:
+                        eng.alloc.incref(blk)
+                dec.set_stream(pi * S + si, res.tables[pi], res.k_eff[pi])
+        # the full blocks of a prompt's kept rows stay shared by its samples;
+        # each sample owns the rest (its copy of the partial last block and
+        # every appended row)
+        shared = [[(ke // 16) * 16 for ke in res.k_eff[pi]] for pi in range(P)]
+        for t in range(steps):
+            if rep > 0:
+                nbytes += _step_bytes(wl, dec.lens_h)
+                ubytes += sum(sh + S * (ke - sh + t + 1)
+                              for pi in range(P)
+                              for sh, ke in zip(shared[pi], res.k_eff[pi])) * row
+                ubytes += P * S * L * (wl.h_q * wl.d * 2 * 2 + row)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            dec.step(dqs[0][t], dqs[1][t], dqs[2][t])
+            b.record()
+            if rep > 0:
+                stp.append((a, b))
+        torch.cuda.synchronize()
+        eng.check_status()
+        for si in range(P * S):
+            dec.retire(si)
+        del dec
+    t_pre = sum(a.elapsed_time(b) for a, b in pre)
+    t_dec = sum(a.elapsed_time(b) for a, b in stp)
+    t_pre, t_dec = max_over_ranks([t_pre, t_dec], world, dist, dev)
+    ach = ubytes / (t_dec / 1e3) / 1e9
+    del q, k, v, o_buf, ml_buf, dqs, eng
+    torch.cuda.empty_cache()
+    return {"prefill_sparsify_tok_s": round(world * T / (t_pre / 1e3), 1),
+            "ms_prefill_sparsify": round(t_pre, 3),
+            "decode_tok_s": round(world * P * S * steps / (t_dec / 1e3), 1),
+            "decode_ms_per_step": round(t_dec / steps, 4),
+            # every sample's reads (the shared blocks once per sample, two of
+            # three then come from L2) and the bytes DRAM must supply (the
+            # shared blocks once per step): the roofline is on the second
+            "decode_read_bytes_per_step": int(nbytes / steps),
+            "decode_read_gbs": round(nbytes / (t_dec / 1e3) / 1e9, 1),
+            "decode_bytes_per_step": int(ubytes / steps),
+            "decode_frac_of_hbm": round(ach / peaks["hbm_gbs"], 4),
+            "what": (f"16 prompts ({T} tokens, 512..16384 each), one prefill+sparsify call, "
+                     "then three samples per prompt sharing its blocks (reference counts, "
+                     "copy-on-write of partial last blocks on the first step), 256 decode "
+                     "steps, one launch over the 1536 items numbered layer-major; inputs "
+                     "drawn on the device; no L2 flush")}
+
+
 def bench_e2e(args, eng, dec, w, n, steps, q, k, v, dq, dk, dv, o_buf, ml_buf, flush, world,
               dist):
     """Same metric through host buffers: Q/K/V of the request and every decode
@@ -1208,6 +1310,8 @@ def main():
                     help="skip the continuous-batching serving pass")
     ap.add_argument("--no-c3", dest="c3", action="store_false",
                     help="skip the long-context pass")
+    ap.add_argument("--no-c4", dest="c4", action="store_false",
+                    help="skip the shared-prefix pass")
     ap.add_argument("--cpu-rows", type=int, default=400,
                     help="prefill rows the CPU oracle evaluates (sample size)")
     args = ap.parse_args()

@@ -1142,17 +1142,54 @@ kvs_status paged_decode_impl(const kvs_bf16* q, const kvs_bf16* k_new, const kvs
   prm.append = k_new != nullptr ? 1 : 0;
   prm.scale_log2 = scale * kvs::kLog2e;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (fp8) {
-    static const CUtensorMap unused = {};  // FP8 blocks arrive by linear bulk copies
-    if (G <= 8) return kvs::launch_decode<128, 1, true>(prm, unused, unused, st);
-    return kvs::launch_decode<128, 2, true>(prm, unused, unused, st);
+  auto launch = [&](kvs::DecodeParams& pr) -> kvs_status {
+    if (fp8) {
+      static const CUtensorMap unused = {};  // FP8 blocks arrive by linear bulk copies
+      if (G <= 8) return kvs::launch_decode<128, 1, true>(pr, unused, unused, st);
+      return kvs::launch_decode<128, 2, true>(pr, unused, unused, st);
+    }
+    if (G <= 8) {
+      if (d == 128) return kvs::launch_decode<128, 1>(pr, kc.map, vc.map, st);
+      return kvs::launch_decode<64, 1>(pr, kc.map, vc.map, st);
+    }
+    if (d == 128) return kvs::launch_decode<128, 2>(pr, kc.map, vc.map, st);
+    return kvs::launch_decode<64, 2>(pr, kc.map, vc.map, st);
+  };
+  // stages per warp that the shared-memory plan leaves for nb items (their
+  // lengths and prefix take shared memory too); 0: it does not fit
+  auto stages = [&](int nb) -> int {
+    kvs::DecodeParams pr = prm;
+    pr.batch = nb;
+    const size_t sm = fp8 ? kvs::plan_smem<128, true>(pr)
+                          : (d == 128 ? kvs::plan_smem<128, false>(pr) : kvs::plan_smem<64, false>(pr));
+    return sm == 0 ? 0 : pr.n_stages;
+  };
+  // A batch whose per-item arrays would leave a single stage per warp (no
+  // load in flight while a block is computed) is decoded in consecutive
+  // chunks of items that keep two: each chunk a decode launch and its merge,
+  // in order on the stream, reusing the workspace (a chunk's decode is an
+  // ordinary launch, so it starts once the previous chunk's merge is done).
+  int chunk = batch;
+  while (chunk > 1 && stages(chunk) < 2) chunk = (chunk + 1) / 2;
+  if (chunk == batch) return launch(prm);
+  for (int b0 = 0; b0 < batch; b0 += chunk) {
+    const int nb = batch - b0 < chunk ? batch - b0 : chunk;
+    kvs::DecodeParams pc = prm;
+    pc.batch = nb;
+    pc.q = q + static_cast<int64_t>(b0) * h_q * d;
+    pc.k_new = k_new ? k_new + static_cast<int64_t>(b0) * h_kv * d : nullptr;
+    pc.v_new = v_new ? v_new + static_cast<int64_t>(b0) * h_kv * d : nullptr;
+    pc.tables = block_tables + static_cast<int64_t>(b0) * max_blocks;
+    pc.patch = table_patch ? table_patch + b0 : nullptr;
+    pc.lens = lens + b0;
+    pc.lens_next = lens_next ? lens_next + b0 : nullptr;
+    pc.out = out + static_cast<int64_t>(b0) * h_q * d;
+    pc.logits = logits ? logits + static_cast<int64_t>(b0) * h_kv * G * logit_ld : nullptr;
+    pc.lse = lse ? lse + static_cast<int64_t>(b0) * h_q : nullptr;
+    const kvs_status rc = launch(pc);
+    if (rc != KVS_OK) return rc;
   }
-  if (G <= 8) {
-    if (d == 128) return kvs::launch_decode<128, 1>(prm, kc.map, vc.map, st);
-    return kvs::launch_decode<64, 1>(prm, kc.map, vc.map, st);
-  }
-  if (d == 128) return kvs::launch_decode<128, 2>(prm, kc.map, vc.map, st);
-  return kvs::launch_decode<64, 2>(prm, kc.map, vc.map, st);
+  return KVS_OK;
 }
 
 }  // namespace

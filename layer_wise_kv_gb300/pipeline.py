@@ -436,7 +436,7 @@ class DecodeBatch:
     """Decode items (one per (stream, layer)) over an Engine's pools."""
 
     def __init__(self, eng: Engine, n_streams: int, max_len: int, n_layers: Optional[int] = None,
-                 layer_order: bool = False):
+                 layer_order: bool = False, interleave: bool = False):
         """n_layers: layers per stream (default: the engine's), e.g. only the
         full-cache layers when the budgeted ones run in an EvictingDecode.
         layer_order: items are numbered layer-major (item = layer * n_streams
@@ -446,13 +446,19 @@ class DecodeBatch:
         of every item (which therefore allocates blocks layer by layer).  This
         is the launch sequence of a model, whose layer l + 1 query depends on
         layer l's output; without it, one launch covers every item of the
-        step (stream-major numbering)."""
+        step (stream-major numbering).
+        interleave: the layer-major numbering with one launch over every item:
+        streams that share blocks (parallel samples of one prompt, in
+        consecutive slots) then have their items next to one another in the
+        launch's split, so their reads of the shared blocks fall together and
+        hit L2."""
         s = eng.shape
         self.eng = eng
         self.n_streams = n_streams
         self.n_layers = s.n_layers if n_layers is None else int(n_layers)
         self.n_items = n_streams * self.n_layers
         self.layer_order = bool(layer_order)
+        self.item_major = self.layer_order or bool(interleave)
         self.shape_ = s
         self.max_len = max_len
         self.max_blocks = blocks_for(max_len)
@@ -540,7 +546,7 @@ class DecodeBatch:
 
     # ------------------------------------------------------------ CUDA graphs
     def _item(self, slot: int, layer: int) -> int:
-        return layer * self.n_streams + slot if self.layer_order else slot * self.n_layers + layer
+        return layer * self.n_streams + slot if self.item_major else slot * self.n_layers + layer
 
     def _decode_launch(self, q, k_new, v_new, patch, lens, lens_next, stream=None):
         """The step's decode over every item, on the engine's pool type: one
@@ -614,7 +620,7 @@ class DecodeBatch:
             self.tables_h[i, :] = -1
             self.tables_h[i, :len(tables[l])] = tables[l]
             self.lens_h[i] = lens[l]
-        if self.layer_order:
+        if self.item_major:
             idx = torch.tensor(rows, dtype=torch.long, device=self.eng.device)
             self.tables_d[idx] = torch.from_numpy(self.tables_h[rows]).to(self.eng.device)
             self.lens_d[self.cur][idx] = torch.from_numpy(self.lens_h[rows]).to(self.eng.device)

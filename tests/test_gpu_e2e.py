@@ -445,14 +445,16 @@ def test_decode_graphs_match_eager():
     np.testing.assert_array_equal(host_bits(ea.v_pool), host_bits(eb.v_pool))
 
 
-@pytest.mark.parametrize("graphs", [False, True])
-def test_decode_layer_order_vs_oracle(graphs):
+@pytest.mark.parametrize("mode", ["layers", "layers_graphs", "interleave"])
+def test_decode_layer_order_vs_oracle(mode):
     """DecodeBatch(layer_order=True): items numbered layer-major, one host
     preparation per step, then one decode launch per layer (the launch
-    sequence of a model), eager or replayed from CUDA graphs.  Three samples
-    share a prompt's blocks, so copy-on-write happens on the first step.  The
-    oracle's flow prepares the items in the same layer-major order: tables,
-    reference counts and every step's outputs must match it."""
+    sequence of a model), eager or replayed from CUDA graphs; and
+    DecodeBatch(interleave=True): the same numbering with one launch over
+    every item.  Three samples share a prompt's blocks, so copy-on-write
+    happens on the first step.  The oracle's flow prepares the items in the
+    same layer-major order: tables, reference counts and every step's outputs
+    must match it."""
     kvs_lib()
     from layer_wise_kv_gb300.pipeline import DecodeBatch, Engine
     w = tiny()
@@ -472,7 +474,8 @@ def test_decode_layer_order_vs_oracle(graphs):
         rec.idx = _gpu_idx(res, 0, l, w.h_kv, rec.k_eff)
         flow.place_layer(rec, pool, kb, vb, opk, opv)
         recs.append(rec)
-    dec = DecodeBatch(eng, S, n + steps + 1, layer_order=True)
+    dec = DecodeBatch(eng, S, n + steps + 1, layer_order=mode != "interleave",
+                      interleave=mode == "interleave")
     streams = [flow.new_stream(recs)]
     dec.set_stream(0, res.tables[0], res.k_eff[0])
     for s in range(1, S):
@@ -481,7 +484,7 @@ def test_decode_layer_order_vs_oracle(graphs):
             for b in t:
                 eng.alloc.incref(b)
         dec.set_stream(s, res.tables[0], res.k_eff[0])
-    if graphs:
+    if mode == "layers_graphs":
         dec.capture_graphs()
     dq = {(s, l): decode_qkv(w, 3, l, steps, sample=s) for s in range(S) for l in range(L)}
     for t in range(steps):

@@ -423,6 +423,76 @@ def test_paged_decode_vs_oracle(h_q, h_kv, d):
 
 
 
+def test_paged_decode_large_batch_in_chunks_vs_oracle():
+    """1400 items at the Llama-3-8B head shape: their length and prefix arrays
+    leave a one-launch plan a single stage per warp, so the call decodes
+    consecutive chunks of items.  Two steps with appends (lengths 0 .. 70,
+    block boundaries crossed); every output against the oracle, the pools
+    and the next lengths exact."""
+    kvs = kvs_lib()
+    rng = np.random.default_rng(1400)
+    h_q, h_kv, d = 32, 8, 128
+    n_items, steps = 1400, 2
+    start_lens = [int(x) for x in rng.integers(0, 70, n_items)]
+    max_blocks = oracle.blocks_for(max(start_lens) + steps)
+    N = n_items * max_blocks + 8
+    a = kvs.BlockAllocator(N, rng.permutation(N))
+    pk = np.full((N, h_kv, 16, d), 0xFFFF, np.uint16)
+    pv = pk.copy()
+    tables = np.full((n_items, max_blocks), -1, np.int32)
+    for i, L0 in enumerate(start_lens):
+        ids = a.alloc_many(oracle.blocks_for(L0))
+        tables[i, :len(ids)] = ids
+        if L0:
+            rows_k = _randn_bits(rng, (L0, h_kv, d))
+            rows_v = _randn_bits(rng, (L0, h_kv, d))
+            for j in range(L0):
+                pk[ids[j // 16], :, j % 16] = rows_k[j]
+                pv[ids[j // 16], :, j % 16] = rows_v[j]
+    k_pool, v_pool = dev_bf16(pk), dev_bf16(pv)
+    tables_d = torch.from_numpy(tables).cuda()
+    lens_h = np.array(start_lens, np.int32)
+    lens_d = [torch.from_numpy(lens_h.copy()).cuda(), torch.zeros(n_items, dtype=torch.int32,
+                                                                  device="cuda")]
+    ws_bytes = kvs.kvs_paged_decode_workspace_size(n_items, h_q, h_kv, d)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
+    out = torch.empty((n_items, h_q, d), dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    patch = np.zeros(n_items, np.int32)
+    cs, cd = np.zeros(n_items, np.int32), np.zeros(n_items, np.int32)
+    for step in range(steps):
+        a.decode_prepare(tables, lens_h, patch, cs, cd)
+        q = _randn_bits(rng, (n_items, h_q, d))
+        kn = _randn_bits(rng, (n_items, h_kv, d))
+        vn = _randn_bits(rng, (n_items, h_kv, d))
+        cur = step % 2
+        kvs.kvs_paged_decode(dev_bf16(q), dev_bf16(kn), dev_bf16(vn), k_pool, v_pool, N,
+                             tables_d, max_blocks, torch.from_numpy(patch).cuda(), lens_d[cur],
+                             lens_d[1 - cur], n_items, h_q, h_kv, d, 1 / np.sqrt(d), out,
+                             ws, ws_bytes, status)
+        torch.cuda.synchronize()
+        assert status.item() == 0
+        for i in range(n_items):
+            L0 = lens_h[i]
+            b = tables[i, L0 // 16]
+            pk[b, :, L0 % 16] = kn[i]
+            pv[b, :, L0 % 16] = vn[i]
+        lens_h += 1
+        np.testing.assert_array_equal(tables_d.cpu().numpy(), tables)
+        np.testing.assert_array_equal(lens_d[1 - cur].cpu().numpy(), lens_h)
+        got = bf16_f64(out)
+        for i in range(n_items):
+            L1 = lens_h[i]
+            kc = np.stack([oracle.gather_rows(pk, tables[i], L1, h) for h in range(h_kv)])
+            vc = np.stack([oracle.gather_rows(pv, tables[i], L1, h) for h in range(h_kv)])
+            ref = oracle.decode_attention(bf16_to_f64(q[i]), bf16_to_f64(kc), bf16_to_f64(vc),
+                                          1 / np.sqrt(d))
+            assert np.abs(got[i] - ref).max() <= ABS_O, (step, i, np.abs(got[i] - ref).max())
+    np.testing.assert_array_equal(host_bits(k_pool), pk)
+    np.testing.assert_array_equal(host_bits(v_pool), pv)
+    a.close()
+
+
 # ---------------------------------------------------------------------------
 # decode that also writes its logits and softmax denominators, and the score
 # update that reads them (decode-time replacement)
