@@ -284,7 +284,11 @@ kvs_status kvs_copy_blocks(const int32_t* src, const int32_t* dst, int32_t count
  *   q, out, the pools and the workspace must be 16-byte aligned
  *   (KVS_ERR_INVALID otherwise).
  * Two launches on `stream`: the split decode, then a merge of the splits (a
- * programmatic dependent launch that waits for the decode's partials).
+ * programmatic dependent launch that waits for the decode's partials).  A
+ * batch whose per-item lengths and prefix would leave the kernel a single
+ * shared-memory stage per warp (about 1250 bf16 items at G = 4) is decoded
+ * in consecutive chunks of items, each chunk such a pair of launches, in
+ * order on `stream` and reusing the workspace.
  * An item with zero tokens to attend (lens[i] == 0 and no append) gets no
  * output row.
  * ---------------------------------------------------------------------- */
