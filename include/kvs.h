@@ -17,7 +17,9 @@
  *   - decode-time replacement in budgeted layers -> kvs_evict_place,
  *     kvs_paged_decode_logits, kvs_decode_scores_from_logits (section 7)
  *   - FP8 (e4m3, per-row scale) pools -> kvs_compact_blocks_fp8,
- *     kvs_copy_blocks_fp8, kvs_paged_decode_fp8, kvs_decode_step_fp8
+ *     kvs_copy_blocks_fp8, kvs_paged_decode_fp8, kvs_decode_step_fp8;
+ *     decode-time replacement over them -> kvs_evict_place_fp8,
+ *     kvs_paged_decode_logits_fp8, kvs_decode_scores_from_logits
  *
  * Conventions (all entry points)
  *   - bf16 tensors are passed as raw 16-bit patterns (kvs_bf16).
@@ -518,6 +520,21 @@ kvs_status kvs_evict_place(const kvs_bf16* k_new, const kvs_bf16* v_new, kvs_bf1
                            int32_t h_kv, int32_t d, int32_t recent, int32_t* status,
                            kvs_stream stream);
 
+/* kvs_evict_place over FP8 pools (layout and quantisation as
+ * kvs_compact_blocks_fp8; d = 128 only).  The claimed slot, positions and
+ * scores as kvs_evict_place; the new K and V rows are quantised the same way
+ * as the compaction (per-row scale from the row's maximum magnitude, e4m3
+ * codes) and written into the slot: K codes in the block's row layout, V
+ * codes transposed, the two scales into k_scale / v_scale.  k_new / v_new
+ * must be 8-byte aligned.  Errors as kvs_evict_place. */
+kvs_status kvs_evict_place_fp8(const kvs_bf16* k_new, const kvs_bf16* v_new, uint8_t* k_pool,
+                               uint8_t* v_pool, float* k_scale, float* v_scale,
+                               int32_t num_blocks, const int32_t* block_tables,
+                               int32_t max_blocks, const int32_t* lens, const int32_t* new_pos,
+                               float* score, int32_t* pos, int32_t max_slots, int32_t n_items,
+                               int32_t h_kv, int32_t d, int32_t recent, int32_t* status,
+                               kvs_stream stream);
+
 /* Add the step's attention probabilities to the scores: for each (item, KV
  * head), softmax over the lens[i] slots of scale * q_g . k_j for each query
  * head g of the group (q [n_items][h_q][d] bf16, K read from the pool), summed
@@ -563,6 +580,21 @@ kvs_status kvs_paged_decode_logits(const kvs_bf16* q, const kvs_bf16* k_new,
                                    int32_t d, float scale, kvs_bf16* out, void* workspace,
                                    size_t workspace_bytes, float* logits, int32_t logit_ld,
                                    float* lse, int32_t* status, kvs_stream stream);
+
+/* kvs_paged_decode_logits over FP8 pools: the decode of kvs_paged_decode_fp8
+ * (same arguments, the same input range), which also writes every attended
+ * slot's log2-scaled logit (the K row's scale included) and each query head's
+ * log2 softmax denominator, in the layouts of kvs_paged_decode_logits. */
+kvs_status kvs_paged_decode_logits_fp8(const kvs_bf16* q, const kvs_bf16* k_new,
+                                       const kvs_bf16* v_new, uint8_t* k_pool, uint8_t* v_pool,
+                                       float* k_scale, float* v_scale, int32_t num_blocks,
+                                       int32_t* block_tables, int32_t max_blocks,
+                                       const int32_t* table_patch, const int32_t* lens,
+                                       int32_t* lens_next, int32_t batch, int32_t h_q,
+                                       int32_t h_kv, int32_t d, float scale, kvs_bf16* out,
+                                       void* workspace, size_t workspace_bytes, float* logits,
+                                       int32_t logit_ld, float* lse, int32_t* status,
+                                       kvs_stream stream);
 
 /* The score update of kvs_decode_scores from those logits and denominators:
  * slot j of (item i, KV head h) gains sum_g exp2(logits[i][h][g][j] -

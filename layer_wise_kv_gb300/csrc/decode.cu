@@ -260,7 +260,7 @@ template <int D, int NT, bool kLogits, bool kF8 = false>
 __global__ void __launch_bounds__(dec_warps(kF8) * 32, 1)
 paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
                     const __grid_constant__ CUtensorMap v_map, const DecodeParams p) {
-  static_assert(!kF8 || (D == 128 && !kLogits), "FP8 pools: d = 128, no logits output");
+  static_assert(!kF8 || D == 128, "FP8 pools: d = 128");
   using L = DecodeLayout<D, kF8>;
   constexpr int kWarps = dec_warps(kF8);
   constexpr int kDecThreads = kWarps * 32;
@@ -1009,6 +1009,9 @@ kvs_status launch_decode(DecodeParams& prm, const CUtensorMap& km, const CUtenso
       KVS_CUDA(cudaFuncSetAttribute(paged_decode_kernel<D, NT, false, true>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit),
                "kvs_paged_decode: raising the shared-memory limit");
+      KVS_CUDA(cudaFuncSetAttribute(paged_decode_kernel<D, NT, true, true>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit),
+               "kvs_paged_decode: raising the shared-memory limit");
     } else {
       KVS_CUDA(cudaFuncSetAttribute(paged_decode_kernel<D, NT, false>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit),
@@ -1022,9 +1025,12 @@ kvs_status launch_decode(DecodeParams& prm, const CUtensorMap& km, const CUtenso
   const int grid = sm_count_dec() < kMaxGrid ? sm_count_dec() : kMaxGrid;
   constexpr int kWarps = dec_warps(kF8);
   constexpr int kDecThreads = kWarps * 32;
-  if constexpr (kF8)
-    paged_decode_kernel<D, NT, false, true><<<grid, kDecThreads, smem, stream>>>(km, vm, prm);
-  else if (prm.logits != nullptr)
+  if constexpr (kF8) {
+    if (prm.logits != nullptr)
+      paged_decode_kernel<D, NT, true, true><<<grid, kDecThreads, smem, stream>>>(km, vm, prm);
+    else
+      paged_decode_kernel<D, NT, false, true><<<grid, kDecThreads, smem, stream>>>(km, vm, prm);
+  } else if (prm.logits != nullptr)
     paged_decode_kernel<D, NT, true><<<grid, kDecThreads, smem, stream>>>(km, vm, prm);
   else
     paged_decode_kernel<D, NT, false><<<grid, kDecThreads, smem, stream>>>(km, vm, prm);
@@ -1234,6 +1240,25 @@ kvs_status kvs_paged_decode_logits(const kvs_bf16* q, const kvs_bf16* k_new,
   return paged_decode_impl(q, k_new, v_new, k_pool, v_pool, num_blocks, block_tables, max_blocks,
                            table_patch, lens, lens_next, batch, h_q, h_kv, d, scale, out,
                            workspace, workspace_bytes, status, stream, logits, logit_ld, lse);
+}
+
+kvs_status kvs_paged_decode_logits_fp8(const kvs_bf16* q, const kvs_bf16* k_new,
+                                       const kvs_bf16* v_new, uint8_t* k_pool, uint8_t* v_pool,
+                                       float* k_scale, float* v_scale, int32_t num_blocks,
+                                       int32_t* block_tables, int32_t max_blocks,
+                                       const int32_t* table_patch, const int32_t* lens,
+                                       int32_t* lens_next, int32_t batch, int32_t h_q,
+                                       int32_t h_kv, int32_t d, float scale, kvs_bf16* out,
+                                       void* workspace, size_t workspace_bytes, float* logits,
+                                       int32_t logit_ld, float* lse, int32_t* status,
+                                       kvs_stream stream) {
+  KVS_REQUIRE(logits != nullptr && logit_ld > 0 && lse != nullptr,
+              "kvs_paged_decode_logits_fp8: no logits or lse buffer");
+  return paged_decode_impl(q, k_new, v_new, reinterpret_cast<kvs_bf16*>(k_pool),
+                           reinterpret_cast<kvs_bf16*>(v_pool), num_blocks, block_tables,
+                           max_blocks, table_patch, lens, lens_next, batch, h_q, h_kv, d, scale,
+                           out, workspace, workspace_bytes, status, stream, logits, logit_ld, lse,
+                           k_scale, v_scale, true);
 }
 
 kvs_status kvs_test_paged_decode_stalled(const kvs_bf16* q, kvs_bf16* k_pool, kvs_bf16* v_pool,

@@ -23,6 +23,7 @@
 
 #include <cmath>
 
+#include "fp8.cuh"
 #include "host_common.h"
 #include "ptx.cuh"
 
@@ -48,25 +49,25 @@ __device__ __forceinline__ bool before(float s0, int p0, float s1, int p1) {
   return s0 < s1 || (s0 == s1 && p0 < p1);
 }
 
-__global__ void __launch_bounds__(kEvictThreads)
-evict_place_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
-                   uint4* __restrict__ k_pool, uint4* __restrict__ v_pool, int num_blocks,
-                   const int32_t* __restrict__ tables, int max_blocks,
-                   const int32_t* __restrict__ lens, const int32_t* __restrict__ new_pos,
-                   float* __restrict__ score, int32_t* __restrict__ pos, int max_slots, int h_kv,
-                   int chunks /* d * 2 / 16 */, int recent, int32_t* status) {
+// The slot (item, KV head h) gives its new token: the lowest (score,
+// position) among slots older than the recent window; its position becomes
+// new_pos[item] and its score 0.  Every thread of the CTA returns the slot,
+// -1 when there is none (empty or oversized length, every token recent: the
+// latter two flag KVS_ERR_INVALID).
+__device__ int claim_slot(int item, int h, const int32_t* __restrict__ lens,
+                          const int32_t* __restrict__ new_pos, float* __restrict__ score,
+                          int32_t* __restrict__ pos, int max_slots, int h_kv, int recent,
+                          int32_t* status) {
   __shared__ float s_sc[kEvictThreads / 32];
   __shared__ int s_ps[kEvictThreads / 32], s_ix[kEvictThreads / 32];
   __shared__ int s_best;
-  const int item = blockIdx.x, h = blockIdx.y;
   const int n = lens[item];
   const int np_ = new_pos[item];
   if (n <= 0 || n > max_slots) {
     if (threadIdx.x == 0 && n > max_slots) flag_status(status, KVS_ERR_INVALID);
-    return;
+    return -1;
   }
   const int64_t base = (static_cast<int64_t>(item) * h_kv + h) * max_slots;
-  // lowest (score, position) among slots older than the recent window
   float bs = INFINITY;
   int bp = 0x7fffffff, bi = -1;
   for (int j = threadIdx.x; j < n; j += kEvictThreads) {
@@ -116,7 +117,18 @@ evict_place_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_
     }
   }
   __syncthreads();
-  const int s = s_best;
+  return s_best;
+}
+
+__global__ void __launch_bounds__(kEvictThreads)
+evict_place_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
+                   uint4* __restrict__ k_pool, uint4* __restrict__ v_pool, int num_blocks,
+                   const int32_t* __restrict__ tables, int max_blocks,
+                   const int32_t* __restrict__ lens, const int32_t* __restrict__ new_pos,
+                   float* __restrict__ score, int32_t* __restrict__ pos, int max_slots, int h_kv,
+                   int chunks /* d * 2 / 16 */, int recent, int32_t* status) {
+  const int item = blockIdx.x, h = blockIdx.y;
+  const int s = claim_slot(item, h, lens, new_pos, score, pos, max_slots, h_kv, recent, status);
   if (s < 0) return;
   const int64_t row =
       slot_row(tables + static_cast<int64_t>(item) * max_blocks, max_blocks, num_blocks, h_kv, h, s);
@@ -130,6 +142,56 @@ evict_place_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_
       k_pool[row * chunks + c] = k_new[src + c];
     else
       v_pool[row * chunks + (c - chunks)] = v_new[src + (c - chunks)];
+  }
+}
+
+// The same over FP8 pools (d = 128; layout of kvs_compact_blocks_fp8): the
+// new K and V rows are quantised as the compaction does (per-row scale from
+// the row's maximum magnitude, e4m3 codes) and written into the claimed
+// slot, K codes in the block's row layout, V codes transposed, and the scales.
+// One warp writes: lane l holds dimensions 4l .. 4l+3.
+__global__ void __launch_bounds__(kEvictThreads)
+evict_place_fp8_kernel(const uint2* __restrict__ k_new, const uint2* __restrict__ v_new,
+                       uint8_t* __restrict__ k_pool, uint8_t* __restrict__ v_pool,
+                       float* __restrict__ k_scale, float* __restrict__ v_scale, int num_blocks,
+                       const int32_t* __restrict__ tables, int max_blocks,
+                       const int32_t* __restrict__ lens, const int32_t* __restrict__ new_pos,
+                       float* __restrict__ score, int32_t* __restrict__ pos, int max_slots, int h_kv,
+                       int recent, int32_t* status) {
+  constexpr int D = 128;
+  const int item = blockIdx.x, h = blockIdx.y;
+  const int s = claim_slot(item, h, lens, new_pos, score, pos, max_slots, h_kv, recent, status);
+  if (s < 0) return;
+  const int64_t row =
+      slot_row(tables + static_cast<int64_t>(item) * max_blocks, max_blocks, num_blocks, h_kv, h, s);
+  if (row < 0) {
+    if (threadIdx.x == 0) flag_status(status, KVS_ERR_INVALID);
+    return;
+  }
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  const int slot = s % KVS_BLOCK_TOKENS;
+  const int64_t block_row = row - slot;  // the block's first row of this head
+  const int64_t src = (static_cast<int64_t>(item) * h_kv + h) * (D / 4) + lane;
+  const uint2 kw = __ldg(k_new + src);
+  const uint2 vw = __ldg(v_new + src);
+  const float k0 = bf16_lo(kw.x), k1 = bf16_hi(kw.x), k2 = bf16_lo(kw.y), k3 = bf16_hi(kw.y);
+  const float v0 = bf16_lo(vw.x), v1 = bf16_hi(vw.x), v2 = bf16_lo(vw.y), v3 = bf16_hi(vw.y);
+  const float sk =
+      f8_row_scale(warp_max(fmaxf(fmaxf(fabsf(k0), fabsf(k1)), fmaxf(fabsf(k2), fabsf(k3)))));
+  const float sv =
+      f8_row_scale(warp_max(fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)))));
+  const uint32_t kc = f8_quant4(k0, k1, k2, k3, sk);
+  const uint32_t vc = f8_quant4(v0, v1, v2, v3, sv);
+  uint8_t* kp = k_pool + block_row * D;
+  uint8_t* vp = v_pool + block_row * D;
+  *reinterpret_cast<uint32_t*>(kp + f8_k_off(slot, 4 * lane)) = kc;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    vp[(4 * lane + i) * KVS_BLOCK_TOKENS + slot] = static_cast<uint8_t>(vc >> (8 * i));
+  if (lane == 0) {
+    k_scale[row] = sk;
+    v_scale[row] = sv;
   }
 }
 
@@ -346,6 +408,35 @@ extern "C" kvs_status kvs_evict_place(const kvs_bf16* k_new, const kvs_bf16* v_n
       reinterpret_cast<uint4*>(k_pool), reinterpret_cast<uint4*>(v_pool), num_blocks, block_tables,
       max_blocks, lens, new_pos, score, pos, max_slots, h_kv, d * 2 / 16, recent, status);
   KVS_CHECK_LAUNCH("kvs_evict_place");
+  return KVS_OK;
+}
+
+extern "C" kvs_status kvs_evict_place_fp8(const kvs_bf16* k_new, const kvs_bf16* v_new,
+                                          uint8_t* k_pool, uint8_t* v_pool, float* k_scale,
+                                          float* v_scale, int32_t num_blocks,
+                                          const int32_t* block_tables, int32_t max_blocks,
+                                          const int32_t* lens, const int32_t* new_pos,
+                                          float* score, int32_t* pos, int32_t max_slots,
+                                          int32_t n_items, int32_t h_kv, int32_t d,
+                                          int32_t recent, int32_t* status, kvs_stream stream) {
+  KVS_REQUIRE(n_items >= 0, "kvs_evict_place_fp8: negative item count");
+  if (n_items == 0) return KVS_OK;
+  KVS_REQUIRE(k_new && v_new && k_pool && v_pool && k_scale && v_scale && block_tables && lens &&
+                  new_pos && score && pos,
+              "kvs_evict_place_fp8: NULL pointer");
+  KVS_SUPPORTED(d == 128, "kvs_evict_place_fp8: d = %d (supported: 128)", d);
+  KVS_REQUIRE(h_kv > 0 && num_blocks > 0 && max_blocks > 0 && max_slots > 0 && recent >= 1 &&
+                  n_items <= 65535 && h_kv <= 65535,
+              "kvs_evict_place_fp8: bad sizes");
+  KVS_REQUIRE(((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 7) == 0 &&
+                  ((reinterpret_cast<uintptr_t>(k_pool) | reinterpret_cast<uintptr_t>(v_pool)) & 3) == 0,
+              "kvs_evict_place_fp8: k_new / v_new must be 8-byte and the pools 4-byte aligned");
+  kvs::evict_place_fp8_kernel<<<dim3(n_items, h_kv), kvs::kEvictThreads, 0,
+                                static_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<const uint2*>(k_new), reinterpret_cast<const uint2*>(v_new), k_pool, v_pool,
+      k_scale, v_scale, num_blocks, block_tables, max_blocks, lens, new_pos, score, pos, max_slots,
+      h_kv, recent, status);
+  KVS_CHECK_LAUNCH("kvs_evict_place_fp8");
   return KVS_OK;
 }
 

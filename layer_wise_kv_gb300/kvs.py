@@ -57,6 +57,11 @@ _SIGS = {
     "kvs_select_topk": (_I32, [_VP, _I64, _VP, _I32, _I32, _I32, _VP, _VP, _VP]),
     "kvs_evict_place": (_I32, [_VP, _VP, _VP, _VP, _I32, _VP, _I32, _VP, _VP, _VP, _VP, _I32,
                                _I32, _I32, _I32, _I32, _VP, _VP]),
+    "kvs_evict_place_fp8": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _I32, _VP, _I32, _VP, _VP, _VP,
+                                   _VP, _I32, _I32, _I32, _I32, _I32, _VP, _VP]),
+    "kvs_paged_decode_logits_fp8": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I32, _VP, _I32,
+                                           _VP, _VP, _VP, _I32, _I32, _I32, _I32, _F32, _VP, _VP,
+                                           _SZ, _VP, _I32, _VP, _VP, _VP]),
     "kvs_decode_scores_workspace_size": (_SZ, [_I32, _I32, _I32, _I32]),
     "kvs_paged_decode_logits": (_I32, [_VP, _VP, _VP, _VP, _VP, _I32, _VP, _I32, _VP, _VP, _VP,
                                        _I32, _I32, _I32, _I32, _F32, _VP, _VP, _SZ, _VP, _I32,
@@ -370,6 +375,39 @@ def kvs_evict_place(k_new, v_new, k_pool, v_pool, num_blocks, block_tables, max_
         max_blocks, _dev(lens, "i32", "lens"), _dev(new_pos, "i32", "new_pos"),
         _dev(score, "f32", "score"), _dev(pos, "i32", "pos"), max_slots, n_items, h_kv, d, recent,
         None if status is None else _dev(status, "i32", "status"), _stream(stream)))
+
+
+def kvs_evict_place_fp8(k_new, v_new, k_pool, v_pool, k_scale, v_scale, num_blocks, block_tables,
+                        max_blocks, lens, new_pos, score, pos, max_slots, n_items, h_kv, d, recent,
+                        status=None, stream=None):
+    _check(library().kvs_evict_place_fp8(
+        _dev(k_new, "bf16", "k_new"), _dev(v_new, "bf16", "v_new"), _dev(k_pool, "u8", "k_pool"),
+        _dev(v_pool, "u8", "v_pool"), _dev(k_scale, "f32", "k_scale"),
+        _dev(v_scale, "f32", "v_scale"), num_blocks, _dev(block_tables, "i32", "block_tables"),
+        max_blocks, _dev(lens, "i32", "lens"), _dev(new_pos, "i32", "new_pos"),
+        _dev(score, "f32", "score"), _dev(pos, "i32", "pos"), max_slots, n_items, h_kv, d, recent,
+        None if status is None else _dev(status, "i32", "status"), _stream(stream)))
+
+
+def kvs_paged_decode_logits_fp8(q, k_new, v_new, k_pool, v_pool, k_scale, v_scale, num_blocks,
+                                block_tables, max_blocks, table_patch, lens, lens_next, batch, h_q,
+                                h_kv, d, scale, out, workspace, workspace_bytes, logits, logit_ld,
+                                lse, status=None, stream=None):
+    if logits.numel() < batch * h_kv * (h_q // h_kv) * logit_ld:
+        raise ValueError("logits must hold batch x h_kv x G x logit_ld floats")
+    if lse.numel() < batch * h_q:
+        raise ValueError("lse must hold batch x h_q floats")
+    _check(library().kvs_paged_decode_logits_fp8(
+        _dev(q, "bf16", "q"), None if k_new is None else _dev(k_new, "bf16", "k_new"),
+        None if v_new is None else _dev(v_new, "bf16", "v_new"), _dev(k_pool, "u8", "k_pool"),
+        _dev(v_pool, "u8", "v_pool"), _dev(k_scale, "f32", "k_scale"),
+        _dev(v_scale, "f32", "v_scale"), num_blocks, _dev(block_tables, "i32", "block_tables"),
+        max_blocks, None if table_patch is None else _dev(table_patch, "i32", "table_patch"),
+        _dev(lens, "i32", "lens"), None if lens_next is None else _dev(lens_next, "i32", "lens_next"),
+        batch, h_q, h_kv, d, float(scale), _dev(out, "bf16", "out"),
+        _dev(workspace, "u8", "workspace"), workspace_bytes, _dev(logits, "f32", "logits"),
+        logit_ld, _dev(lse, "f32", "lse"), None if status is None else _dev(status, "i32", "status"),
+        _stream(stream)))
 
 
 def kvs_paged_decode_logits(q, k_new, v_new, k_pool, v_pool, num_blocks, block_tables,

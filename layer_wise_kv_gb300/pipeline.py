@@ -752,10 +752,12 @@ class EvictingDecode:
         """fused: the decode launch writes the slots' logits and each query
         head's softmax denominator, and the score update reads them
         (kvs_paged_decode_logits); otherwise the update recomputes the logits
-        from K (kvs_decode_scores)."""
+        from K (kvs_decode_scores).  Over FP8 pools only the fused form is
+        built (kvs_evict_place_fp8, kvs_paged_decode_logits_fp8)."""
         s = eng.shape
-        if eng.kv_fp8:
-            raise NotImplementedError("decode-time replacement over FP8 pools")
+        if eng.kv_fp8 and not fused:
+            raise NotImplementedError("over FP8 pools the score update reads the decode's logits "
+                                      "(fused=True)")
         self.fused = fused
         dev = eng.device
         self.eng, self.layers = eng, list(layers)
@@ -798,6 +800,21 @@ class EvictingDecode:
         the order of `layers`).  Returns the attention output."""
         eng, s = self.eng, self.eng.shape
         n = self.n_items
+        if eng.kv_fp8:
+            kvs.kvs_evict_place_fp8(k_new, v_new, eng.k_pool, eng.v_pool, eng.k_scale, eng.v_scale,
+                                    eng.num_blocks, self.tables_d, self.max_blocks, self.lens_d,
+                                    self.new_pos, self.score, self.pos, self.max_slots, n, s.h_kv,
+                                    s.d, s.recent, eng.status, stream)
+            kvs.kvs_paged_decode_logits_fp8(q, None, None, eng.k_pool, eng.v_pool, eng.k_scale,
+                                            eng.v_scale, eng.num_blocks, self.tables_d,
+                                            self.max_blocks, None, self.lens_d, None, n, s.h_q,
+                                            s.h_kv, s.d, s.scale, self.out, self.ws, self.ws_bytes,
+                                            self.logits, self.logit_ld, self.lse, eng.status,
+                                            stream)
+            kvs.kvs_decode_scores_from_logits(self.logits, self.logit_ld, self.lse, self.lens_d,
+                                              self.score, self.new_pos, self.max_slots, n, s.h_q,
+                                              s.h_kv, eng.status, stream)
+            return self.out
         kvs.kvs_evict_place(k_new, v_new, eng.k_pool, eng.v_pool, eng.num_blocks, self.tables_d,
                             self.max_blocks, self.lens_d, self.new_pos, self.score, self.pos,
                             self.max_slots, n, s.h_kv, s.d, s.recent, eng.status, stream)

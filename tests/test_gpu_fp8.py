@@ -512,3 +512,86 @@ def test_engine_fp8_graphs_match_eager():
     for x, y in ((ea.k_pool, eb.k_pool), (ea.v_pool, eb.v_pool), (ea.k_scale, eb.k_scale),
                  (ea.v_scale, eb.v_scale)):
         assert torch.equal(x.view(torch.uint8), y.view(torch.uint8))
+
+
+def test_evicting_decode_fp8_vs_oracle():
+    """Decode-time replacement over FP8 pools at the Llama-3-8B head shapes:
+    a 600-token prompt, the budgeted layers 30 and 31 (320 and 256 slots per
+    KV head, recent window 32), both items in one launch per step, 24 steps,
+    each step reading the rows placed by the steps before it.  Every
+    step, for every KV head: the replaced slot must be a valid choice for the
+    oracle's fp64 scores (the oracle then follows it); the codes and scales
+    written into it must match the oracle's quantiser bit for bit; the output
+    must match the oracle's attention over the stored values; scores and
+    positions must track the oracle's."""
+    kvs_lib()
+    from layer_wise_kv_gb300.pipeline import Engine, EvictingDecode, Shape
+    from oracle import eviction, flow
+    from synth import decode_qkv, llama3_8b, prefill_qkv
+    w = llama3_8b()
+    n, steps, layers = 600, 24, [30, 31]
+    shape = Shape(len(layers), w.h_q, w.h_kv, w.d, w.alpha, w.recent)
+    N = 128
+    eng = Engine(shape, N, poison=True, kv_dtype="fp8")
+    host = {l: prefill_qkv(w, 0, l, n) for l in layers}
+    ql, kl, vl = ([dev_bf16(host[l][i]) for l in layers] for i in range(3))
+    res = eng.prefill_sparsify(ql, kl, vl, [n], [[w.budget(l, n) for l in layers]])
+    torch.cuda.synchronize()
+    eng.check_status()
+    heads, kes = [], []
+    for li, l in enumerate(layers):
+        qb, kb, vb = host[l]
+        rec = flow.sparsify_layer(w, l, qb, kb, vb)
+        off = int(res.idx_off[0, li])
+        gidx = res.kept_idx[off:off + w.h_kv * rec.k_eff].cpu().numpy().reshape(w.h_kv, rec.k_eff)
+        kes.append(rec.k_eff)
+        hl = []
+        for h in range(w.h_kv):
+            ck, sk = oracle.fp8.quantize_rows_fast(bf16_to_f64(kb[gidx[h], h]).astype(np.float32))
+            cv, sv = oracle.fp8.quantize_rows_fast(bf16_to_f64(vb[gidx[h], h]).astype(np.float32))
+            hl.append(eviction.HeadCache(oracle.fp8.dequantize_rows(ck, sk),
+                                         oracle.fp8.dequantize_rows(cv, sv),
+                                         rec.scores[h][gidx[h]].astype(np.float64),
+                                         gidx[h].astype(np.int64)))
+        heads.append(hl)
+    ev = EvictingDecode(eng, res, 0, 0, n, [0, 1])
+    dqkv = [decode_qkv(w, 0, l, steps) for l in layers]
+    for t in range(steps):
+        new_pos = n + t
+        q = dev_bf16(np.stack([dqkv[i][0][t] for i in range(2)]))
+        k = dev_bf16(np.stack([dqkv[i][1][t] for i in range(2)]))
+        v = dev_bf16(np.stack([dqkv[i][2][t] for i in range(2)]))
+        out = bf16_f64(ev.step(q, k, v))
+        torch.cuda.synchronize()
+        got_k = eng.k_pool.cpu().numpy().reshape(N, w.h_kv, 16, D)
+        got_v = eng.v_pool.cpu().numpy().reshape(N, w.h_kv, D, 16)
+        got_ks, got_vs = eng.k_scale.cpu().numpy(), eng.v_scale.cpu().numpy()
+        for i in range(2):
+            pos_g = ev.pos[i, :, :kes[i]].cpu().numpy()
+            slots, kval, vval = [], [], []
+            for h, hc in enumerate(heads[i]):
+                where = np.nonzero(pos_g[h] == new_pos)[0]
+                assert where.size == 1, (t, i, h)
+                s = int(where[0])
+                assert eviction.is_valid_choice(hc.score, hc.pos, new_pos, w.recent, s, 1e-3,
+                                                1e-6), (t, i, h, hc.score[s], hc.score.min())
+                slots.append(s)
+                ck, sk = oracle.fp8.quantize_rows_fast(
+                    bf16_to_f64(dqkv[i][1][t][h:h + 1]).astype(np.float32))
+                cv, sv = oracle.fp8.quantize_rows_fast(
+                    bf16_to_f64(dqkv[i][2][t][h:h + 1]).astype(np.float32))
+                b, r = int(ev.tables_h[i][s // 16]), s % 16
+                phys = k_physical(np.pad(ck, ((r, 15 - r), (0, 0))))[r]
+                np.testing.assert_array_equal(got_k[b, h, r], phys)
+                np.testing.assert_array_equal(got_v[b, h][:, r], cv[0])
+                assert got_ks[b, h, r] == sk[0] and got_vs[b, h, r] == sv[0], (t, i, h)
+                kval.append(oracle.fp8.dequantize_rows(ck, sk)[0])
+                vval.append(oracle.fp8.dequantize_rows(cv, sv)[0])
+            ref, _, _ = eviction.step(heads[i], bf16_to_f64(dqkv[i][0][t]), np.stack(kval),
+                                      np.stack(vval), new_pos, w.recent, w.scale, slots=slots)
+            assert np.abs(out[i] - ref).max() <= ABS_O, (t, i, np.abs(out[i] - ref).max())
+            sc_g = ev.score[i, :, :kes[i]].cpu().numpy().astype(np.float64)
+            for h, hc in enumerate(heads[i]):
+                np.testing.assert_array_equal(pos_g[h], hc.pos)
+                np.testing.assert_allclose(sc_g[h], hc.score, rtol=1e-3, atol=1e-5)
+    eng.check_status()
