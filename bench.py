@@ -518,7 +518,8 @@ def bench_decode_evicting(args, eng, w, n, steps, q, k, v, dq, dk, dv, o_buf, ml
     the request's 500 steps with the same L2 flush and per-step events as the
     headline decode.  Bytes per step: the K/V rows every step reads (full
     layers at the mean length, budgeted layers at k_l) plus the budgeted
-    layers' logits written by the decode launch and read by the score update."""
+    layers' logits written by the decode launch and read by the score update.
+    Over FP8 pools (eng.kv_fp8) a row is its d codes and 4-byte scale."""
     import torch
     from layer_wise_kv_gb300.pipeline import DecodeBatch, EvictingDecode
     L = w.n_layers
@@ -551,7 +552,7 @@ def bench_decode_evicting(args, eng, w, n, steps, q, k, v, dq, dk, dv, o_buf, ml
     ev.release()
     t_ms = sum(a.elapsed_time(b) for a, b in pairs)
     (t_ms,) = max_over_ranks([t_ms], world, dist, q.device)
-    row = w.h_kv * w.d * 2
+    row = w.h_kv * (w.d + 4) if eng.kv_fp8 else w.h_kv * w.d * 2
     kv_full = sum((w.k_eff(l, n) + steps // 2 + 1) * row * 2 for l in full)
     kv_bud = sum(w.k_eff(l, n) * row * 2 for l in bud)
     # the decode launch writes the budgeted slots' logits (fp32, per query
@@ -602,6 +603,11 @@ def bench_decode_fp8(args, shape, num_blocks, w, n, steps, q, k, v, dq, dk, dv, 
     gc.enable()
     eng8.check_status()
     dec8.retire(0)
+    # the same request with decode-time replacement over the FP8 pools
+    evicting = bench_decode_evicting(args, eng8, w, n, steps, q, k, v, dq, dk, dv, o_buf, ml_buf,
+                                     flush, world, dist)
+    evicting["what"] = ("over the FP8 pools: " + evicting["what"] + "; the new row is "
+                        "quantised into the replaced slot")
     t_ms = sum(a.elapsed_time(b) for a, b in pairs)
     k_ms = sum(a.elapsed_time(b) for a, b in kern)
     t_ms, k_ms = max_over_ranks([t_ms, k_ms], world, dist, q.device)
@@ -622,7 +628,8 @@ def bench_decode_fp8(args, shape, num_blocks, w, n, steps, q, k, v, dq, dk, dv, 
             "frac_of_hbm": round(ach / peaks["hbm_gbs"], 4),
             "what": "decode over e4m3 pools with per-row scales (codes + scales read), "
                     "eager steps with allocator preparation, events per step, L2 flushed "
-                    "before each"}
+                    "before each",
+            "evicting": evicting}
 
 
 def _step_bytes(w, lens_h):
