@@ -130,6 +130,27 @@ def test_invalid_arguments_rejected_before_launch(kvs):
     assert lib.kvs_paged_decode_fp8(*df) == kvs.KVS_ERR_INVALID
     df[5], df[13] = 256, 0
     assert lib.kvs_paged_decode_fp8(*df) == kvs.KVS_OK
+    # decode-time replacement over FP8 pools (d = 128 only; k_new / v_new 8-byte
+    # aligned): placement, then the FP8 decode that writes logits and lse
+    ef = [256, 256, 256, 256, 256, 256, 4, 256, 1, 256, 256, 256, 256, 16, 0, 8, 128, 32, None,
+          None]
+    assert lib.kvs_evict_place_fp8(*ef) == kvs.KVS_OK
+    ef[14] = 2
+    ef[16] = 64
+    assert lib.kvs_evict_place_fp8(*ef) == kvs.KVS_ERR_UNSUPPORTED
+    ef[16], ef[4] = 128, None
+    assert lib.kvs_evict_place_fp8(*ef) == kvs.KVS_ERR_INVALID
+    ef[4], ef[0] = 256, 260
+    assert lib.kvs_evict_place_fp8(*ef) == kvs.KVS_ERR_INVALID
+    dlf = [256, None, None, 256, 256, 256, 256, 4, 256, 1, None, 256, None, 0, 32, 8, 128, 0.1,
+           256, 256, 1 << 26, 256, 16, 256, None, None]
+    assert lib.kvs_paged_decode_logits_fp8(*dlf) == kvs.KVS_OK
+    dlf[21] = None
+    assert lib.kvs_paged_decode_logits_fp8(*dlf) == kvs.KVS_ERR_INVALID
+    dlf[21], dlf[13], dlf[16] = 256, 2, 64
+    assert lib.kvs_paged_decode_logits_fp8(*dlf) == kvs.KVS_ERR_UNSUPPORTED
+    dlf[16], dlf[5] = 128, None
+    assert lib.kvs_paged_decode_logits_fp8(*dlf) == kvs.KVS_ERR_INVALID
     # decode that writes its logits and denominators: both buffers are required
     dl = [256, None, None, 256, 256, 4, 256, 1, None, 256, None, 0, 32, 8, 128, 0.1, 256, 256,
           1 << 20, 256, 16, 256, None, None]
