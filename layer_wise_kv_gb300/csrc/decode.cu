@@ -291,6 +291,15 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap k_map,
     for (int i = 0; i < kWarps * NS; ++i) mbar_init(reinterpret_cast<uint64_t*>(smem + p.bar_off) + i, 1);
     fence_mbar_init();
   }
+  // The block tables are read right after the length prefix: start them
+  // towards L2 now, one 128-byte line per thread over the grid, so that the
+  // first table reads wait on L2 rather than on a second DRAM round trip.
+  {
+    const int64_t tbytes = static_cast<int64_t>(p.batch) * p.max_blocks * 4;
+    for (int64_t off = (static_cast<int64_t>(blockIdx.x) * kDecThreads + threadIdx.x) * 128;
+         off < tbytes; off += static_cast<int64_t>(gridDim.x) * kDecThreads * 128)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(p.tables) + off));
+  }
   for (int b = threadIdx.x; b < p.batch; b += kDecThreads)
     if (!clamp_len(p.lens[b], p.max_blocks, p.append, lens_s[b]))
       flag_status(p.status, KVS_ERR_INVALID);
