@@ -56,7 +56,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 NCU_TRAFFIC = {
     # the one prefill launch over all 32 layers: the bench's own launch shape
     "prefill_attn": {"bytes": 1694695936 + 1057856512, "alg_bytes": None},
-    "paged_decode": {"bytes": 188678656 + 3158784, "alg_bytes": 187432960},
+    "paged_decode": {"bytes": 188694528 + 3154432, "alg_bytes": 187432960},
 }
 
 
