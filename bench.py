@@ -419,9 +419,8 @@ def bench_gpu(args):
                              "exp_per_s": round(exp_rate, -6),
                              "exp_peak_per_s": round(xu_exp_peak(peaks), -6),
                              "exp_frac": round(exp_rate / xu_exp_peak(peaks), 4)},
-        # prefill attention and window scores together, the benchmark spec's
-        # "prefill attention + scoring" bar: both launches' flops over both
-        # launches' event time
+        # prefill attention and window scores together, as one tensor-bound
+        # stage: both launches' flops over both launches' event time
         "roofline_prefill_scores": prefill_scores_roofline(w, n, flops_launch, k1_avg, k2_ms,
                                                            peak_t, peak_src, L),
         # one window-score launch per request covers the budgeted layers

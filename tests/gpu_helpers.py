@@ -9,7 +9,7 @@ try:
 except Exception:  # pragma: no cover
     torch = None
 
-# Tolerances (the benchmark spec of the path): fp32 scores and m / l
+# Tolerances of the parity tests: fp32 scores and m / l
 # within 1e-3 relative; bf16 attention outputs within 2e-2 max-abs; block
 # tables, compacted bytes and selection on identical scores bit-exact.
 REL_ML = 1e-3
