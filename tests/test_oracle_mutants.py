@@ -240,6 +240,58 @@ def test_eviction_mutants_fail_the_pins(monkeypatch, mutant):
     _fails(pins.test_eviction_replaces_lowest_outside_recent_window_brute_force)
 
 
+def _step_variant(score_reset=True, group_sum=True, after_placement=True):
+    """A decode step with one of three mistakes: the replaced slot keeps its
+    old score, the step's probabilities are averaged over the query group
+    instead of summed, or the query attends over the cache as it was before
+    the new row was placed."""
+    def step(heads, q, k_new, v_new, new_pos, recent, scale, slots=None):
+        h_q, d = q.shape
+        group = h_q // len(heads)
+        before = [(hc.k.copy(), hc.v.copy()) for hc in heads]
+        used = []
+        for h, hc in enumerate(heads):
+            s = eviction.replace_slot(hc.score, hc.pos, new_pos, recent) if slots is None \
+                else int(slots[h])
+            hc.k[s], hc.v[s], hc.pos[s] = k_new[h], v_new[h], new_pos
+            if score_reset:
+                hc.score[s] = 0.0
+            used.append(s)
+        out = np.zeros((h_q, d))
+        probs = np.zeros((len(heads), heads[0].k.shape[0]))
+        for g in range(h_q):
+            hc = heads[g // group]
+            kc, vc = (hc.k, hc.v) if after_placement else before[g // group]
+            lg = (kc @ q[g]) * scale
+            e = np.exp(lg - lg.max())
+            pr = e / e.sum()
+            out[g] = pr @ vc
+            probs[g // group] += pr if group_sum else pr / group
+        for h, hc in enumerate(heads):
+            hc.score += probs[h]
+        return out, probs, used
+    return step
+
+
+@pytest.mark.parametrize("mutant,pin", [
+    (_step_variant(score_reset=False),
+     pins.test_eviction_replaces_lowest_outside_recent_window_brute_force),
+    (_step_variant(group_sum=False), pins.test_eviction_step_attention_is_sdpa_over_the_cache),
+    (_step_variant(after_placement=False),
+     pins.test_eviction_step_attention_is_sdpa_over_the_cache),
+])
+def test_eviction_step_mutants_fail_the_pins(monkeypatch, mutant, pin):
+    monkeypatch.setattr(eviction, "step", mutant)
+    _fails(pin)
+
+
+def test_eviction_step_variant_without_mistakes_passes_the_pins(monkeypatch):
+    # the variant itself, with no mistake switched on, is the oracle's step
+    monkeypatch.setattr(eviction, "step", _step_variant())
+    pins.test_eviction_step_attention_is_sdpa_over_the_cache()
+    pins.test_eviction_replaces_lowest_outside_recent_window_brute_force()
+
+
 # --------------------------------------------------------------------------- FP8
 def _encode_ties_away(x):
     x = np.asarray(x, dtype=np.float64)
