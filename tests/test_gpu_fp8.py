@@ -514,11 +514,13 @@ def test_engine_fp8_graphs_match_eager():
         assert torch.equal(x.view(torch.uint8), y.view(torch.uint8))
 
 
-def test_evicting_decode_fp8_vs_oracle():
+@pytest.mark.parametrize("n,layers,N", [(600, [30, 31], 128), (4000, [3, 31], 512)])
+def test_evicting_decode_fp8_vs_oracle(n, layers, N):
     """Decode-time replacement over FP8 pools at the Llama-3-8B head shapes:
-    a 600-token prompt, the budgeted layers 30 and 31 (320 and 256 slots per
-    KV head, recent window 32), both items in one launch per step, 24 steps,
-    each step reading the rows placed by the steps before it.  Every
+    a 600-token prompt with the budgeted layers 30 and 31 (320 and 256 slots
+    per KV head), and the full 4000-token prompt with layers 3 and 31 (2048
+    and 256 slots); recent window 32, both items in one launch per step, 24
+    steps, each step reading the rows placed by the steps before it.  Every
     step, for every KV head: the replaced slot must be a valid choice for the
     oracle's fp64 scores (the oracle then follows it); the codes and scales
     written into it must match the oracle's quantiser bit for bit; the output
@@ -529,9 +531,8 @@ def test_evicting_decode_fp8_vs_oracle():
     from oracle import eviction, flow
     from synth import decode_qkv, llama3_8b, prefill_qkv
     w = llama3_8b()
-    n, steps, layers = 600, 24, [30, 31]
+    steps = 24
     shape = Shape(len(layers), w.h_q, w.h_kv, w.d, w.alpha, w.recent)
-    N = 128
     eng = Engine(shape, N, poison=True, kv_dtype="fp8")
     host = {l: prefill_qkv(w, 0, l, n) for l in layers}
     ql, kl, vl = ([dev_bf16(host[l][i]) for l in layers] for i in range(3))
