@@ -584,7 +584,10 @@ kvs_status kvs_paged_decode_logits(const kvs_bf16* q, const kvs_bf16* k_new,
 /* kvs_paged_decode_logits over FP8 pools: the decode of kvs_paged_decode_fp8
  * (same arguments, the same input range), which also writes every attended
  * slot's log2-scaled logit (the K row's scale included) and each query head's
- * log2 softmax denominator, in the layouts of kvs_paged_decode_logits. */
+ * log2 softmax denominator, in the layouts of kvs_paged_decode_logits.
+ * Errors as kvs_paged_decode_fp8; a NULL logits or lse buffer, or logit_ld <=
+ * 0, is KVS_ERR_INVALID with nothing launched.  Slots at or past logit_ld get
+ * no logit. */
 kvs_status kvs_paged_decode_logits_fp8(const kvs_bf16* q, const kvs_bf16* k_new,
                                        const kvs_bf16* v_new, uint8_t* k_pool, uint8_t* v_pool,
                                        float* k_scale, float* v_scale, int32_t num_blocks,
